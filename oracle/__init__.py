@@ -1,0 +1,37 @@
+"""CPU oracle of the sparse MoE expert-layer forward.
+
+TEST INFRASTRUCTURE ONLY.  Only ``tests/``, ``__graft_entry__.smoke()`` and
+``bench.py``'s CPU-baseline / reference leg may import or run this package.
+The product (``moe_expert_layer_fwd_gb300``) never imports it, and this package
+imports nothing from the product: the two share no code.  The only module both
+sides use is ``moe_inputs`` (seeded inputs, none of the method's arithmetic).
+
+What it computes, step by step, each function citing the passage it follows:
+
+* ``gating``   -- top-k expert choice and weights (softmax, or sigmoid with a
+  selection-only correction bias and a routed scaling factor).
+* ``routing``  -- init-routing: stable sort of token-expert pairs by expert,
+  per-expert counts, offsets, the permutation and its inverse.
+* ``ffn``      -- the expert FFN down(SiLU(gate(x)) * up(x)) over the
+  concatenated [gate; up] weight, grouped per expert.
+* ``layer``    -- finalize-routing (unpermute, weighted sum, shared-expert add)
+  and the whole layer.
+
+Precision: float64 everywhere, except the expert *selection*, which is an
+integer decided by floating point and is therefore taken in float32 with the
+same pinned operations the GPU uses (``gating.exp_f32_pinned``).
+
+Every function is pinned by ``tests/test_oracle_*.py`` against closed forms,
+brute force and library routines (no function is "parity unpinned").
+"""
+from .gating import exp_f32_pinned, sigmoid_f32_pinned, selection_keys, gating_topk
+from .routing import init_routing, expand_rows
+from .ffn import swiglu, expert_ffn, grouped_gemm_swiglu, grouped_gemm, bf16_to_f64
+from .layer import finalize_routing, moe_layer_forward, moe_layer_forward_tokens, shared_expert
+
+__all__ = [
+    "exp_f32_pinned", "sigmoid_f32_pinned", "selection_keys", "gating_topk",
+    "init_routing", "expand_rows",
+    "swiglu", "expert_ffn", "grouped_gemm_swiglu", "grouped_gemm", "bf16_to_f64",
+    "finalize_routing", "moe_layer_forward", "moe_layer_forward_tokens", "shared_expert",
+]
