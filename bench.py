@@ -1,0 +1,461 @@
+#!/usr/bin/env python3
+"""Benchmark of the GB300 MoE expert-layer forward; rank 0 prints one JSON line.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl gb300|reference] [--workload NAME]
+
+A step is one full layer forward (gating top-k, init-routing, gate/up grouped
+GEMM + SwiGLU, down grouped GEMM + routing weight, finalize) through the C ABI
+(moe_layer_forward), on seeded synthetic inputs already resident in HBM.
+The default workload is the Qwen3-MoE-style decode layer (T=64, H=4096,
+E=128, k=8, I=1536).  Its 4.75 GB of active expert weights per step exceed the
+129 MB L2, so no L2 flush is needed between steps.
+
+Multi-GPU: the layer does not shard here; --gpus N (under torchrun) runs N
+independent replicas, one per GPU, and reports the whole-job throughput with
+the max time over ranks (weak scaling, no data-path collective).
+
+--impl reference times the CPU oracle (the only reference this path has) on a
+bounded sample of the same workload, on the host cores.
+"""
+from __future__ import annotations
+
+import argparse
+import datetime as _dt
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "MoE-layer tokens/s on 1 GB300; % of HBM BW (decode) / % BF16 TC peak (prefill)"
+DEFAULT_WORKLOAD = "qwen3_decode"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+def _peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return d, "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+def _args(argv=None):
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-baseline-child", action="store_true", help=argparse.SUPPRESS)
+    ap.add_argument("--sample-tokens", type=int, default=8)
+    ap.add_argument("--profile-steps", action="store_true",
+                    help="plain moe_layer_forward loop only (for ncu launch lists)")
+    a = ap.parse_args(argv)
+    if a.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    return a
+
+
+# ------------------------------------------------------------------ clocks
+class Clocks:
+    """nvidia-smi sampling of SM clock and throttle reasons every 200 ms."""
+
+    FIELDS = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_id: str):
+        self.device_id = device_id
+        self.proc = None
+        self.file = None
+        self.window = None
+
+    def start(self):
+        try:
+            self.file = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+            self.proc = subprocess.Popen(["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                                          "-lms", "200", "-i", self.device_id], stdout=self.file,
+                                         stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def mark(self, t0, t1):
+        self.window = (t0, t1)
+
+    def stop(self):
+        out = {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        if self.proc is None:
+            out["note"] = "nvidia-smi unavailable"
+            return out
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.file.flush()
+        self.file.seek(0)
+        rows = []
+        for line in self.file.read().splitlines():
+            c = [x.strip() for x in line.split(",")]
+            if len(c) < 10:
+                continue
+            try:
+                ts = _dt.datetime.strptime(c[0], "%Y/%m/%d %H:%M:%S.%f").timestamp()
+                rows.append((ts, float(c[2]), float(c[3]), c[4], c[6:10]))
+            except ValueError:
+                continue
+        os.unlink(self.file.name)
+        if not rows:
+            out["note"] = "no samples"
+            return out
+        inwin = [r for r in rows if self.window and self.window[0] - 0.2 <= r[0] <= self.window[1] + 0.2]
+        use = inwin if inwin else rows
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in use for i, v in enumerate(r[4]) if v.lower() == "active"})
+        out.update(sm_mhz=statistics.median(r[1] for r in use), sm_max_mhz=max(r[2] for r in use),
+                   reasons=reasons, samples=len(use), samples_in_timed_region=len(inwin))
+        try:
+            out["power_w_max"] = max(float(r[3]) for r in use)
+        except ValueError:
+            pass
+        return out
+
+
+# ------------------------------------------------------------------ distributed plumbing
+def _dist():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        if backend == "nccl":
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend=backend)
+    return rank, world, local
+
+
+def _barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def _max_over_ranks(v: float, world: int) -> float:
+    if world == 1:
+        return v
+    import torch
+    import torch.distributed as dist
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([v], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ------------------------------------------------------------------ work accounting
+def layer_work(cfg, counts):
+    """Algorithmic bytes and FLOPs of the two grouped GEMMs for one step."""
+    import numpy as np
+    A = int((np.asarray(counts) > 0).sum())
+    P = cfg.T * cfg.k
+    w13_b = A * 2 * cfg.I * cfg.H * 2 + (2 * cfg.I_s * cfg.H * 2 if cfg.n_shared else 0)
+    w2_b = A * cfg.H * cfg.I * 2 + (cfg.H * cfg.I_s * 2 if cfg.n_shared else 0)
+    f1 = 2 * P * cfg.H * 2 * cfg.I + (2 * cfg.T * cfg.H * 2 * cfg.I_s if cfg.n_shared else 0)
+    f2 = 2 * P * cfg.I * cfg.H + (2 * cfg.T * cfg.I_s * cfg.H if cfg.n_shared else 0)
+    return dict(active_experts=A, gemm_w13=dict(bytes=w13_b, flops=f1), gemm_down=dict(bytes=w2_b, flops=f2))
+
+
+def _traffic(workload, kernel):
+    """DRAM bytes per launch from the committed ncu summary, if it matches the current kernel source."""
+    p = os.path.join(ROOT, "profiles", "dram_traffic.json")
+    if not os.path.exists(p):
+        return None
+    with open(p) as f:
+        d = json.load(f)
+    e = d.get(workload, {}).get(kernel)
+    if not e:
+        return None
+    src = os.path.join(ROOT, "moe_expert_layer_fwd_gb300", "csrc", "grouped_gemm.cu")
+    with open(src, "rb") as f:
+        sha = hashlib.sha256(f.read()).hexdigest()[:16]
+    return e.get("bytes_per_launch") if e.get("src_sha") == sha else None
+
+
+# ------------------------------------------------------------------ CPU oracle timing
+def cpu_baseline_child(args):
+    """Runs in a subprocess with the BLAS thread count fixed: times the oracle on a token sample."""
+    import numpy as np
+    import moe_inputs as mi
+    import oracle
+    cfg = mi.CONFIGS[args.workload]
+    inp = mi.generate(cfg)
+    n = min(args.sample_tokens, cfg.T)
+    toks = np.arange(n)
+    t0 = time.perf_counter()
+    oracle.moe_layer_forward_tokens(toks, inp.x, inp.logits, cfg.k, cfg.gate, inp.w13, inp.w2, inp.bias,
+                                    cfg.routed_scaling_factor, cfg.eps, inp.w13_s, inp.w2_s)
+    dt = time.perf_counter() - t0
+    print(json.dumps({"tokens": n, "seconds": dt}))
+
+
+def cpu_baseline(args):
+    cores = len(os.sched_getaffinity(0))
+    env = dict(os.environ, OMP_NUM_THREADS=str(cores), OPENBLAS_NUM_THREADS=str(cores), MKL_NUM_THREADS=str(cores))
+    for k in ("RANK", "WORLD_SIZE", "LOCAL_RANK", "MASTER_ADDR", "MASTER_PORT"):
+        env.pop(k, None)
+    cmd = [sys.executable, os.path.join(ROOT, "bench.py"), "--cpu-baseline-child", "--workload", args.workload,
+           "--sample-tokens", str(args.sample_tokens)]
+    r = subprocess.run(cmd, env=env, capture_output=True, text=True, timeout=900)
+    if r.returncode != 0:
+        return {"value": None, "unit": "tokens/s", "cores": cores, "kind": "oracle",
+                "error": r.stderr.strip().splitlines()[-1:] }
+    d = json.loads(r.stdout.strip().splitlines()[-1])
+    return {"value": d["tokens"] / d["seconds"], "unit": "tokens/s", "cores": cores, "kind": "oracle",
+            "sample": f"{d['tokens']} tokens of the {args.workload} workload (routing of all tokens, expert FFNs of the "
+                      f"sampled tokens, float64 numpy with BLAS on {cores} threads): {d['seconds']:.2f} s"}
+
+
+# ------------------------------------------------------------------ reference arm (the oracle)
+def run_reference(args, rank, world):
+    if rank != 0:
+        return
+    import numpy as np
+    import moe_inputs as mi
+    import oracle
+    cfg = mi.CONFIGS[args.workload]
+    inp = mi.generate(cfg)
+    cores = len(os.sched_getaffinity(0))
+
+    def step(i):
+        oracle.moe_layer_forward_tokens(np.array([i % cfg.T]), inp.x, inp.logits, cfg.k, cfg.gate, inp.w13, inp.w2,
+                                        inp.bias, cfg.routed_scaling_factor, cfg.eps, inp.w13_s, inp.w2_s)
+
+    for i in range(args.warmup):
+        step(i)
+    t0 = time.perf_counter()
+    for i in range(args.steps):
+        step(i)
+    dt = time.perf_counter() - t0
+    v = args.steps / dt
+    line = {
+        "metric": METRIC, "value": v, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": dt / args.steps * 1e3, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded Philox inputs, random-init weights)",
+        "impl": "reference",
+        "config": _config(cfg, world),
+        "cpu_baseline": {"value": v, "unit": "tokens/s", "cores": cores, "kind": "oracle",
+                         "sample": f"1 token of the {args.workload} workload per step (routing of all tokens, its "
+                                   f"{cfg.k} expert FFNs in float64 numpy)"},
+        "e2e": {"value": v, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def _config(cfg, world):
+    return {"workload": cfg.name, "T": cfg.T, "H": cfg.H, "E": cfg.E, "k": cfg.k, "I": cfg.I, "gate": cfg.gate,
+            "routed_scaling_factor": cfg.routed_scaling_factor, "n_shared": cfg.n_shared, "I_s": cfg.I_s,
+            "zipf_s": cfg.zipf_s, "global_batch": cfg.T * world,
+            "l2": "inputs larger than L2 (the active expert weights read each step exceed 129 MB)",
+            "parallelism": f"replicas x{world}"}
+
+
+# ------------------------------------------------------------------ GB300 arm
+def run_gb300(args, rank, world, local):
+    import numpy as np
+    import torch
+
+    import moe_expert_layer_fwd_gb300 as moe
+    import moe_inputs as mi
+    from moe_expert_layer_fwd_gb300 import build as moe_build
+
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py needs a CUDA GPU for --impl gb300")
+    torch.cuda.set_device(local)
+    moe_build.build()
+    cfg = mi.CONFIGS[args.workload]
+    inp = mi.generate(cfg)
+
+    def d16(u):
+        return torch.from_numpy(np.ascontiguousarray(u).view(np.int16)).cuda().view(torch.bfloat16)
+
+    t = dict(x=d16(inp.x), logits=torch.from_numpy(inp.logits).cuda(), w13=d16(inp.w13), w2=d16(inp.w2),
+             bias=torch.from_numpy(inp.bias).cuda() if inp.bias is not None else None,
+             w13_s=d16(inp.w13_s) if inp.w13_s is not None else None,
+             w2_s=d16(inp.w2_s) if inp.w2_s is not None else None)
+    layer = moe.MoELayer(cfg.T, cfg.H, cfg.E, cfg.k, cfg.I, cfg.gate, cfg.routed_scaling_factor, cfg.eps,
+                         cfg.n_shared, cfg.I_s)
+    launches = moe.moe_layer_kernel_launches(layer.desc)
+    K, W = args.steps, args.warmup
+
+    if args.profile_steps:
+        for _ in range(W + K):
+            layer.forward(**t)
+        torch.cuda.synchronize()
+        return
+
+    dev_id = str(local)
+    try:
+        dev_id = "GPU-" + str(torch.cuda.get_device_properties(local).uuid)
+    except Exception:
+        pass
+    clocks = Clocks(dev_id) if rank == 0 else None
+    if clocks:
+        clocks.start()
+    for _ in range(W):
+        layer.forward(**t)
+    torch.cuda.synchronize()
+    status = moe.moe_get_device_status(layer.ws)
+    if status != moe.MOE_OK:
+        raise SystemExit(f"device status after warm-up: {moe.status_string(status)}")
+    counts = layer.counts.cpu().numpy()
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(6)] for _ in range(K)]
+    for row in evs:
+        for e in row:
+            e.record()
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    _barrier(world)
+    torch.cuda.synchronize()
+    w0 = time.time()
+    start.record()
+    for i in range(K):
+        layer.forward_events(evs[i], **t)
+    end.record()
+    torch.cuda.synchronize()
+    w1 = time.time()
+    if clocks:
+        clocks.mark(w0, w1)
+    _barrier(world)
+    ms_total = _max_over_ranks(start.elapsed_time(end), world)
+    status = moe.moe_get_device_status(layer.ws)
+    if status != moe.MOE_OK:
+        raise SystemExit(f"device status after the timed region: {moe.status_string(status)}")
+    names = ["gating", "init_routing", "gemm_w13_swiglu", "gemm_down", "finalize"]
+    kern_ms = {n: statistics.mean(evs[i][j].elapsed_time(evs[i][j + 1]) for i in range(K))
+               for j, n in enumerate(names)}
+
+    # end to end: pinned host inputs -> device, forward, result -> pinned host, every step
+    e2e = None
+    if not args.no_e2e:
+        hx = torch.from_numpy(np.ascontiguousarray(inp.x).view(np.int16)).pin_memory()
+        hl = torch.from_numpy(inp.logits).pin_memory()
+        hy = torch.empty((cfg.T, cfg.H), dtype=torch.int16).pin_memory()
+        dx = torch.empty((cfg.T, cfg.H), dtype=torch.int16, device="cuda")
+        dl = torch.empty_like(t["logits"])
+        te = dict(t)
+        te["x"] = dx.view(torch.bfloat16)
+        te["logits"] = dl
+        stream = torch.cuda.current_stream()
+
+        def e2e_step():
+            dx.copy_(hx, non_blocking=True)
+            dl.copy_(hl, non_blocking=True)
+            y = layer.forward(**te)
+            hy.copy_(y.view(torch.int16), non_blocking=True)
+            stream.synchronize()
+
+        for _ in range(W):
+            e2e_step()
+        _barrier(world)
+        c0 = time.perf_counter()
+        for _ in range(K):
+            e2e_step()
+        c1 = time.perf_counter()
+        _barrier(world)
+        e2e_s = _max_over_ranks(c1 - c0, world)
+        e2e = {"value": world * cfg.T * K / e2e_s, "unit": "tokens/s",
+               "h2d_bytes_per_step": hx.numel() * 2 + hl.numel() * 4, "d2h_bytes_per_step": hy.numel() * 2,
+               "ms_per_step": e2e_s / K * 1e3, "sync": "stream synchronised every step (result read on the host)"}
+        if not np.array_equal(hy.numpy().view(np.uint16), layer.y.view(torch.int16).cpu().numpy().view(np.uint16)):
+            raise SystemExit("end-to-end result differs from the device-resident run")
+
+    clk = clocks.stop() if clocks else None
+    if rank != 0:
+        return
+
+    peaks, src = _peaks()
+    work = layer_work(cfg, counts)
+    ms = ms_total / K
+    # dominant kernel: the gate/up grouped GEMM (2/3 of the weight bytes and FLOPs)
+    dom = "gemm_w13_swiglu"
+    dom_work = work["gemm_w13"]
+    t_dom = kern_ms[dom] * 1e-3
+    bw = dom_work["bytes"] / t_dom / 1e9
+    tf = dom_work["flops"] / t_dom / 1e12
+    ridge = peaks["bf16_tflops_sustained"] * 1e12 / (peaks["hbm_gbs"] * 1e9)
+    ai = dom_work["flops"] / dom_work["bytes"]
+    if ai < ridge:
+        roof = {"bound": "hbm", "achieved": bw, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                "frac": bw / peaks["hbm_gbs"]}
+    else:
+        roof = {"bound": "tensor", "achieved": tf, "peak": peaks["bf16_tflops_sustained"], "unit": "TFLOP/s",
+                "frac": tf / peaks["bf16_tflops_sustained"]}
+    roof["traffic"] = _traffic(cfg.name, dom)
+    roof.update(kernel=dom, peak_source=f"{src} ({'hbm_gbs' if roof['bound'] == 'hbm' else 'bf16_tflops_sustained'})",
+                algorithmic_bytes_per_launch=dom_work["bytes"], flops_per_launch=dom_work["flops"],
+                per_unit=f"{2 * cfg.I * cfg.H * 2} weight bytes per active expert "
+                         f"(x {work['active_experts']} active experts" + (" + the shared expert)" if cfg.n_shared else ")"),
+                launch_ms=kern_ms[dom])
+    tot_b = work["gemm_w13"]["bytes"] + work["gemm_down"]["bytes"]
+    tot_f = work["gemm_w13"]["flops"] + work["gemm_down"]["flops"]
+    layer_roof = {"weight_bytes": tot_b, "flops": tot_f,
+                  "hbm_frac_of_measured": tot_b / (ms * 1e-3) / 1e9 / peaks["hbm_gbs"],
+                  "tc_frac_of_measured_burst": tot_f / (ms * 1e-3) / 1e12 / peaks["bf16_tflops"]}
+    t_down = kern_ms["gemm_down"] * 1e-3
+    line = {
+        "metric": METRIC,
+        "value": world * cfg.T * K / (ms_total * 1e-3),
+        "unit": "tokens/s",
+        "n_gpus": world, "steps": K, "warmup": W, "ms_per_step": ms,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "bf16", "data": "synthetic (seeded Philox inputs, random-init weights)",
+        "config": _config(cfg, world),
+        "roofline": roof,
+        "roofline_layer": layer_roof,
+        "roofline_gemm_down": {"achieved_gbs": work["gemm_down"]["bytes"] / t_down / 1e9,
+                               "achieved_tflops": work["gemm_down"]["flops"] / t_down / 1e12},
+        "kernels_ms": kern_ms,
+        "routing": {"active_experts": work["active_experts"], "max_over_mean": float(counts.max() / counts.mean()),
+                    "empty_experts": int((counts == 0).sum())},
+        "gpu_launches": launches * K,
+        "clocks": clk,
+    }
+    if e2e:
+        line["e2e"] = e2e
+    if world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(args)
+    print(json.dumps(line), flush=True)
+
+
+def main(argv=None):
+    args = _args(argv)
+    if args.cpu_baseline_child:
+        cpu_baseline_child(args)
+        return
+    rank, world, local = _dist()
+    try:
+        if args.impl == "reference":
+            run_reference(args, rank, world)
+        else:
+            run_gb300(args, rank, world, local)
+    finally:
+        if world > 1:
+            import torch.distributed as dist
+            dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

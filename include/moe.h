@@ -1,0 +1,242 @@
+/*
+ * moe.h -- C ABI of the GB300 (sm_103a) sparse MoE expert-layer forward.
+ *
+ * The forward pass of a sparse Mixture-of-Experts expert layer as served for
+ * Qwen3-MoE and Hy3 models, split into the steps the serving pages name:
+ *
+ *   moe_gating_topk          top-k expert choice and routing weights
+ *   moe_init_routing         stable sort of token-expert pairs by expert,
+ *                            per-expert counts/offsets, permutation, row gather
+ *   moe_grouped_gemm_swiglu  all experts' gate/up projections in one launch,
+ *                            SwiGLU fused into the epilogue
+ *   moe_grouped_gemm         all experts' down projections in one launch,
+ *                            the routing weight fused into the epilogue
+ *   moe_finalize_routing     unpermute + weighted sum (+ shared expert)
+ *   moe_layer_forward        the whole path on one stream
+ *
+ * Sources (page titles and sections):
+ *  [Q3]  "Qwen3-MoE low-latency inference practice on Atlas A3/950 clusters"
+ *        (cann-recipes-infer), sections "MoE TP optimisation: computation
+ *        decomposition" and "GMM enablement and routing optimisation".
+ *  [HY3] "Hy3 295B MoE end-to-end inference optimisation practice on Atlas A3"
+ *        (cann-recipes-infer), sections 1.1-1.3, 5.1, 6.2, 8.1.
+ *
+ * Conventions shared by every entry point:
+ *  - All tensor pointers are DEVICE pointers owned by the caller; the library
+ *    never allocates, frees or keeps device memory.  `stream` is a cudaStream_t
+ *    (NULL = legacy default stream).  Every call only enqueues work on `stream`
+ *    and returns without synchronising (except moe_get_device_status).
+ *  - bf16 tensors are passed as uint16_t bit patterns; all matrices are dense
+ *    row-major; every pointer must be 16-byte aligned.
+ *  - Notation: T tokens, H hidden size, E routed experts, k experts per token,
+ *    I expert intermediate size, P = T*k token-expert pairs, pair p = t*k + j
+ *    (j = slot in the top-k order), pos = index in expert-sorted order.
+ *  - Arguments are validated on the host before anything is launched; a bad
+ *    argument returns a negative moe_status and launches nothing.  A failed
+ *    launch returns MOE_ERR_CUDA.  Problems seen on the device (a bounded
+ *    pipeline wait that ran out, an index outside its buffer) never trap: the
+ *    kernel skips the access, sets a bit in the sticky status word at the
+ *    start of the workspace and finishes; read it with moe_get_device_status.
+ *  - Limits: 1 <= k <= min(E, 32); 1 <= E <= 1024; H % 64 == 0; I % 64 == 0;
+ *    T*k < 2^31; T*k*max(H, I) < 2^40.
+ */
+#ifndef MOE_GB300_MOE_H_
+#define MOE_GB300_MOE_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define MOE_API __attribute__((visibility("default")))
+#else
+#define MOE_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  MOE_OK = 0,
+  MOE_ERR_INVALID_ARG = -1,   /* null pointer, bad size, misaligned pointer */
+  MOE_ERR_UNSUPPORTED = -2,   /* valid but outside the limits above */
+  MOE_ERR_WORKSPACE = -3,     /* workspace missing or smaller than *_workspace_size() */
+  MOE_ERR_CUDA = -4,          /* a CUDA runtime call or launch failed */
+  MOE_ERR_TIMEOUT = -5,       /* device status: a bounded wait ran out */
+  MOE_ERR_DEVICE_CHECK = -6   /* device status: an index check failed, access skipped */
+} moe_status;
+
+/* Gate function.  Values follow norm_type of the Hy3 router call ([HY3] 1.3):
+ * 0 = softmax, 1 = sigmoid. */
+typedef enum { MOE_GATE_SOFTMAX = 0, MOE_GATE_SIGMOID = 1 } moe_gate;
+
+/* Shape and gating parameters of one MoE layer. */
+typedef struct moe_layer_desc {
+  int32_t T;                    /* tokens */
+  int32_t H;                    /* hidden size */
+  int32_t E;                    /* routed experts */
+  int32_t k;                    /* experts per token */
+  int32_t I;                    /* routed expert intermediate size */
+  int32_t gate;                 /* moe_gate */
+  float routed_scaling_factor;  /* sigmoid only: weights are multiplied by it (Hy3: 2.826) */
+  float eps;                    /* sigmoid only: added to the weight normaliser (Hy3: 1e-20) */
+  int32_t n_shared;             /* 0 or 1 shared experts ([HY3] 1.1) */
+  int32_t I_s;                  /* shared expert intermediate size (ignored if n_shared == 0) */
+} moe_layer_desc;
+
+/* Human-readable name of a moe_status value (static string). */
+MOE_API const char* moe_status_string(int status);
+
+/* ABI version (major * 100 + minor). */
+MOE_API int moe_abi_version(void);
+
+/* Bytes of workspace header holding the sticky device status word; every
+ * workspace starts with it. */
+MOE_API size_t moe_status_bytes(void);
+
+/* Clears the sticky device status word of a workspace (async on `stream`).
+ * Call once after allocating a workspace, and after handling an error. */
+MOE_API int moe_workspace_init(void* ws, size_t ws_bytes, void* stream);
+
+/* Synchronises `stream`, then reads the sticky status word of `ws`.
+ * Returns MOE_OK, MOE_ERR_TIMEOUT or MOE_ERR_DEVICE_CHECK (or MOE_ERR_CUDA). */
+MOE_API int moe_get_device_status(const void* ws, void* stream);
+
+/*
+ * a1. Gating top-k.  [Q3] "GMM enablement and routing optimisation" (one fused
+ * op replaces top-k followed by softmax); [HY3] 1.3 (sigmoid router with
+ * correction bias, norm_type=1, routed_scaling_factor, eps) and 5.1 (the bias
+ * is added after the sigmoid and only changes which experts are chosen).
+ *
+ *  logits   [T,E] fp32 router logits.
+ *  bias     [E] fp32 correction bias, sigmoid only; NULL = none.  Must be NULL
+ *           for softmax.
+ *  gate     moe_gate.  Selection key: softmax -> the logit; sigmoid ->
+ *           sigmoid(logit) + bias[e], computed with a fixed sequence of IEEE
+ *           fp32 operations so the choice is reproducible bit for bit.
+ *           Ties go to the lower expert index.
+ *  topk_idx [T,k] int32 out: chosen experts, best first.
+ *  topk_w   [T,k] fp32 out: softmax -> softmax of the k chosen logits;
+ *           sigmoid -> sigmoid_j / (sum_j sigmoid_j + eps) * routed_scaling_factor.
+ */
+MOE_API int moe_gating_topk(const float* logits, const float* bias, int T, int E, int k, int gate,
+                    float routed_scaling_factor, float eps, float* topk_w, int32_t* topk_idx, void* stream);
+
+/*
+ * a2. Init-routing.  [Q3] "GMM enablement and routing optimisation"
+ * (init-routing gives the expert sort order; compute-expert-tokens gives the
+ * number of tokens per expert); [HY3] 6.2 (group_list = per-expert counts).
+ *
+ *  topk_idx    [T,k] int32 in, values in [0,E).
+ *  counts      [E] int32 out: pairs routed to each expert.
+ *  offsets     [E+1] int32 out: exclusive prefix sum of counts, offsets[E] = P.
+ *  sorted_pair [P] int32 out: pos -> p; expert-major, ascending p inside an expert.
+ *  pair_pos    [P] int32 out: p -> pos (inverse permutation).
+ *  x, x_exp    optional (both NULL or both set): x [T,H] bf16 in,
+ *              x_exp [P,H] bf16 out, x_exp[pos] = x[sorted_pair[pos] / k].
+ *  ws          workspace of at least moe_init_routing_workspace_size(T,E,k) bytes.
+ * Indices outside [0,E) are counted nowhere, flagged as MOE_ERR_DEVICE_CHECK
+ * in the status word, and leave the outputs unspecified.
+ */
+MOE_API size_t moe_init_routing_workspace_size(int T, int E, int k);
+MOE_API int moe_init_routing(const int32_t* topk_idx, int T, int E, int k, const uint16_t* x, int H, uint16_t* x_exp,
+                     int32_t* counts, int32_t* offsets, int32_t* sorted_pair, int32_t* pair_pos, void* ws,
+                     size_t ws_bytes, void* stream);
+
+/*
+ * a3. Grouped gate/up GEMM with fused SwiGLU.  [Q3] "MoE TP optimisation:
+ * computation decomposition" (w13 = [gate_proj; up_proj]; SwiGLU splits the
+ * last axis in two halves and returns SiLU(x[0]) * x[1]) and "GMM enablement"
+ * (all experts in one grouped matmul).
+ *
+ *  x_rows  [M,H] bf16: rows in expert-sorted order (x_exp of moe_init_routing).
+ *  w13     [E,2I,H] bf16: per expert, rows 0..I-1 = gate_proj, I..2I-1 = up_proj
+ *          (checkpoint [out_features, in_features] layout, [HY3] 6.2).
+ *  offsets [E+1] int32 device: expert e owns rows [offsets[e], offsets[e+1]);
+ *          offsets[E] <= M.
+ *  act     [M,I] bf16 out: act[pos] = SiLU(g) * u, (g, u) = x_rows[pos] . w13[e]^T,
+ *          accumulated in fp32, rounded once to bf16.  Rows >= offsets[E] untouched.
+ *  ws      at least moe_grouped_gemm_workspace_size() bytes.
+ */
+MOE_API size_t moe_grouped_gemm_workspace_size(void);
+MOE_API int moe_grouped_gemm_swiglu(const uint16_t* x_rows, const uint16_t* w13, const int32_t* offsets, int E, int M,
+                            int H, int I, uint16_t* act, void* ws, size_t ws_bytes, void* stream);
+
+/*
+ * a4. Grouped GEMM (down projection) with the routing weight fused.  [Q3]
+ * "MoE TP optimisation" (x = down(...)) and "GMM enablement"; [HY3] 6.2.
+ *
+ *  a           [M,K] bf16 rows in expert-sorted order (act of a3).
+ *  w           [E,N,K] bf16 (down_proj, [out_features, in_features]).
+ *  offsets     [E+1] int32 device, as in a3.
+ *  topk_w, sorted_pair  optional (both NULL or both set): row pos is scaled by
+ *              topk_w[sorted_pair[pos]] ([T,k] fp32 and [M] int32 from a1/a2).
+ *  out         [M,N] bf16 out = scale * (a[pos] . w[e]^T), fp32 accumulation,
+ *              rounded once.  Rows >= offsets[E] untouched.
+ */
+MOE_API int moe_grouped_gemm(const uint16_t* a, const uint16_t* w, const int32_t* offsets, const float* topk_w,
+                     const int32_t* sorted_pair, int E, int M, int N, int K, uint16_t* out, void* ws,
+                     size_t ws_bytes, void* stream);
+
+/*
+ * a6. Finalize-routing.  [Q3] "GMM enablement and routing optimisation"
+ * (expert outputs back to token order and weighted sum); [HY3] 8.1 (the
+ * shared-expert term belongs to this combine step).
+ *
+ *  y_perm   [P,H] bf16: per-pair outputs, already scaled by the routing weight.
+ *  pair_pos [P] int32: p -> pos.
+ *  shared   [T,H] bf16 shared-expert output or NULL.
+ *  y        [T,H] bf16 out: y[t] = sum_{j<k} y_perm[pair_pos[t*k+j]] (+ shared[t]),
+ *           summed in fp32 in slot order, rounded once.
+ */
+MOE_API int moe_finalize_routing(const uint16_t* y_perm, const int32_t* pair_pos, const uint16_t* shared, int T, int k,
+                         int H, uint16_t* y, void* stream);
+
+/*
+ * The whole layer: a1 -> a2 -> a3 (+ shared gate/up) -> a4 (+ shared down) -> a6,
+ * enqueued on one stream.  The shared expert ([HY3] 1.1) runs inside the same
+ * grouped-GEMM launches as one more segment covering all T rows, weight 1.
+ *
+ *  d        layer shape (host pointer).
+ *  x        [T,H] bf16; logits [T,E] fp32; bias [E] fp32 or NULL (sigmoid only).
+ *  w13      [E,2I,H] bf16; w2 [E,H,I] bf16.
+ *  w13_s    [2I_s,H] bf16; w2_s [H,I_s] bf16 (NULL when d->n_shared == 0).
+ *  y        [T,H] bf16 out.
+ *  topk_w   [T,k] fp32 out; topk_idx [T,k] int32 out; counts [E] int32 out.
+ *  ws       at least moe_layer_workspace_size(d) bytes; holds offsets, the
+ *           permutation, x_exp, act, y_perm and the shared-expert buffers.
+ *           moe_layer_workspace_offsets() gives where each one lives.
+ */
+MOE_API size_t moe_layer_workspace_size(const moe_layer_desc* d);
+MOE_API int moe_layer_forward(const moe_layer_desc* d, const uint16_t* x, const float* logits, const float* bias,
+                      const uint16_t* w13, const uint16_t* w2, const uint16_t* w13_s, const uint16_t* w2_s,
+                      uint16_t* y, float* topk_w, int32_t* topk_idx, int32_t* counts, void* ws, size_t ws_bytes,
+                      void* stream);
+
+/* Same as moe_layer_forward, and additionally records caller-created CUDA
+ * events (cudaEvent_t, passed as void*) on `stream` around the steps, for
+ * per-step device timing: events[0] before gating, [1] before init-routing,
+ * [2] before the gate/up grouped GEMM, [3] before the down grouped GEMM(s),
+ * [4] before finalize, [5] after finalize.  n_events must be 6; the events
+ * stay owned by the caller. */
+MOE_API int moe_layer_forward_events(const moe_layer_desc* d, const uint16_t* x, const float* logits,
+                                     const float* bias, const uint16_t* w13, const uint16_t* w2,
+                                     const uint16_t* w13_s, const uint16_t* w2_s, uint16_t* y, float* topk_w,
+                                     int32_t* topk_idx, int32_t* counts, void* ws, size_t ws_bytes, void* stream,
+                                     void* const* events, int n_events);
+
+/* Number of kernel launches one moe_layer_forward call makes for this shape
+ * (0 if the shape is invalid). */
+MOE_API int moe_layer_kernel_launches(const moe_layer_desc* d);
+
+/* Byte offsets, inside the moe_layer_forward workspace, of its intermediates
+ * (valid after a call on the same desc): index 0 offsets[E+1], 1 sorted_pair[P],
+ * 2 pair_pos[P], 3 x_exp[P,H], 4 act[P,I], 5 y_perm[P,H], 6 act_s[T,I_s],
+ * 7 shared[T,H].  Writes min(n, 8) values into out; returns 8. */
+MOE_API int moe_layer_workspace_offsets(const moe_layer_desc* d, size_t* out, int n);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MOE_GB300_MOE_H_ */

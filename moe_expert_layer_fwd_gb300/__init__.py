@@ -1,0 +1,324 @@
+"""GB300 (sm_103a) sparse MoE expert-layer forward: Python binding of ``libmoe_gb300.so``.
+
+Argument marshalling only: every step of the forward pass runs in the CUDA
+kernels behind the C ABI declared in ``include/moe.h``.  PyTorch supplies
+device memory and streams; there is no CPU fallback -- if the library is not
+built, every call raises.
+
+Functions carry the C names:
+
+    moe_gating_topk, moe_init_routing, moe_grouped_gemm_swiglu, moe_grouped_gemm,
+    moe_finalize_routing, moe_layer_forward (+ MoELayer, which owns a workspace).
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+from typing import Optional
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(HERE, "libmoe_gb300.so")
+
+MOE_OK = 0
+MOE_ERR_INVALID_ARG = -1
+MOE_ERR_UNSUPPORTED = -2
+MOE_ERR_WORKSPACE = -3
+MOE_ERR_CUDA = -4
+MOE_ERR_TIMEOUT = -5
+MOE_ERR_DEVICE_CHECK = -6
+GATES = {"softmax": 0, "sigmoid": 1}
+
+_lib = None
+_lock = threading.Lock()
+
+
+class MoEError(RuntimeError):
+    def __init__(self, status: int, what: str):
+        self.status = status
+        super().__init__(f"{what} failed: {status_string(status)} ({status})")
+
+
+class moe_layer_desc(ctypes.Structure):
+    _fields_ = [("T", ctypes.c_int32), ("H", ctypes.c_int32), ("E", ctypes.c_int32), ("k", ctypes.c_int32),
+                ("I", ctypes.c_int32), ("gate", ctypes.c_int32), ("routed_scaling_factor", ctypes.c_float),
+                ("eps", ctypes.c_float), ("n_shared", ctypes.c_int32), ("I_s", ctypes.c_int32)]
+
+
+_SIGS = {
+    "moe_status_string": (ctypes.c_char_p, [ctypes.c_int]),
+    "moe_abi_version": (ctypes.c_int, []),
+    "moe_status_bytes": (ctypes.c_size_t, []),
+    "moe_workspace_init": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_size_t, ctypes.c_void_p]),
+    "moe_get_device_status": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_void_p]),
+    "moe_gating_topk": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                                       ctypes.c_int, ctypes.c_float, ctypes.c_float, ctypes.c_void_p,
+                                       ctypes.c_void_p, ctypes.c_void_p]),
+    "moe_init_routing_workspace_size": (ctypes.c_size_t, [ctypes.c_int, ctypes.c_int, ctypes.c_int]),
+    "moe_init_routing": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_void_p,
+                                        ctypes.c_int, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
+                                        ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_size_t,
+                                        ctypes.c_void_p]),
+    "moe_grouped_gemm_workspace_size": (ctypes.c_size_t, []),
+    "moe_grouped_gemm_swiglu": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int,
+                                               ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_void_p,
+                                               ctypes.c_void_p, ctypes.c_size_t, ctypes.c_void_p]),
+    "moe_grouped_gemm": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
+                                        ctypes.c_void_p, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                                        ctypes.c_void_p, ctypes.c_void_p, ctypes.c_size_t, ctypes.c_void_p]),
+    "moe_finalize_routing": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int,
+                                            ctypes.c_int, ctypes.c_int, ctypes.c_void_p, ctypes.c_void_p]),
+    "moe_layer_workspace_size": (ctypes.c_size_t, [ctypes.POINTER(moe_layer_desc)]),
+    "moe_layer_workspace_offsets": (ctypes.c_int, [ctypes.POINTER(moe_layer_desc),
+                                                   ctypes.POINTER(ctypes.c_size_t), ctypes.c_int]),
+    "moe_layer_forward": (ctypes.c_int, [ctypes.POINTER(moe_layer_desc)] + [ctypes.c_void_p] * 11 +
+                          [ctypes.c_void_p, ctypes.c_size_t, ctypes.c_void_p]),
+    "moe_layer_forward_events": (ctypes.c_int, [ctypes.POINTER(moe_layer_desc)] + [ctypes.c_void_p] * 11 +
+                                 [ctypes.c_void_p, ctypes.c_size_t, ctypes.c_void_p,
+                                  ctypes.POINTER(ctypes.c_void_p), ctypes.c_int]),
+    "moe_layer_kernel_launches": (ctypes.c_int, [ctypes.POINTER(moe_layer_desc)]),
+}
+
+
+def lib() -> ctypes.CDLL:
+    """The loaded C library (raises if it has not been built)."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            if not os.path.exists(LIB_PATH):
+                raise RuntimeError(f"{LIB_PATH} is missing: build it with `python -m moe_expert_layer_fwd_gb300.build`"
+                                   " (there is no CPU fallback)")
+            l = ctypes.CDLL(LIB_PATH)
+            for name, (res, args) in _SIGS.items():
+                f = getattr(l, name)
+                f.restype = res
+                f.argtypes = args
+            _lib = l
+    return _lib
+
+
+def status_string(status: int) -> str:
+    return lib().moe_status_string(status).decode()
+
+
+def _check(status: int, what: str) -> None:
+    if status != MOE_OK:
+        raise MoEError(status, what)
+
+
+# ------------------------------------------------------------------ torch glue
+def _torch():
+    import torch
+    return torch
+
+
+def _ptr(t) -> Optional[int]:
+    if t is None:
+        return None
+    if not t.is_cuda:
+        raise ValueError("expected a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError("expected a contiguous tensor")
+    return t.data_ptr()
+
+
+def _stream(stream) -> Optional[int]:
+    torch = _torch()
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return s.cuda_stream
+
+
+def _ws(nbytes: int, device, ws=None):
+    torch = _torch()
+    nbytes = max(int(nbytes), 256)
+    if ws is None or ws.numel() < nbytes:
+        ws = torch.zeros(nbytes, dtype=torch.uint8, device=device)
+    return ws
+
+
+def moe_gating_topk(logits, k: int, gate: str = "softmax", bias=None, routed_scaling_factor: float = 1.0,
+                    eps: float = 1e-20, topk_w=None, topk_idx=None, stream=None):
+    """a1: returns (topk_w [T,k] fp32, topk_idx [T,k] int32)."""
+    torch = _torch()
+    T, E = logits.shape
+    if topk_w is None:
+        topk_w = torch.empty((T, k), dtype=torch.float32, device=logits.device)
+    if topk_idx is None:
+        topk_idx = torch.empty((T, k), dtype=torch.int32, device=logits.device)
+    _check(lib().moe_gating_topk(_ptr(logits), _ptr(bias), T, E, k, GATES[gate], routed_scaling_factor, eps,
+                                 _ptr(topk_w), _ptr(topk_idx), _stream(stream)), "moe_gating_topk")
+    return topk_w, topk_idx
+
+
+def moe_init_routing(topk_idx, E: int, x=None, ws=None, out: Optional[dict] = None, stream=None) -> dict:
+    """a2: returns dict(counts, offsets, sorted_pair, pair_pos, x_exp (if x given), ws)."""
+    torch = _torch()
+    T, k = topk_idx.shape
+    P = T * k
+    dev = topk_idx.device
+    o = dict(out or {})
+    o.setdefault("counts", torch.empty(E, dtype=torch.int32, device=dev))
+    o.setdefault("offsets", torch.empty(E + 1, dtype=torch.int32, device=dev))
+    o.setdefault("sorted_pair", torch.empty(P, dtype=torch.int32, device=dev))
+    o.setdefault("pair_pos", torch.empty(P, dtype=torch.int32, device=dev))
+    H = 0
+    if x is not None:
+        H = x.shape[1]
+        o.setdefault("x_exp", torch.empty((P, H), dtype=x.dtype, device=dev))
+    need = lib().moe_init_routing_workspace_size(T, E, k)
+    ws = _ws(need, dev, ws)
+    _check(lib().moe_init_routing(_ptr(topk_idx), T, E, k, _ptr(x), H, _ptr(o.get("x_exp")), _ptr(o["counts"]),
+                                  _ptr(o["offsets"]), _ptr(o["sorted_pair"]), _ptr(o["pair_pos"]), _ptr(ws),
+                                  ws.numel(), _stream(stream)), "moe_init_routing")
+    o["ws"] = ws
+    return o
+
+
+def moe_grouped_gemm_swiglu(x_rows, w13, offsets, act=None, ws=None, stream=None):
+    """a3: act[M,I] = SwiGLU(x_rows . w13[e]^T) per expert segment."""
+    torch = _torch()
+    M, H = x_rows.shape
+    E, twoI, _ = w13.shape
+    I = twoI // 2
+    if act is None:
+        act = torch.empty((M, I), dtype=torch.bfloat16, device=x_rows.device)
+    ws = _ws(lib().moe_grouped_gemm_workspace_size(), x_rows.device, ws)
+    _check(lib().moe_grouped_gemm_swiglu(_ptr(x_rows), _ptr(w13), _ptr(offsets), E, M, H, I, _ptr(act), _ptr(ws),
+                                         ws.numel(), _stream(stream)), "moe_grouped_gemm_swiglu")
+    return act
+
+
+def moe_grouped_gemm(a, w, offsets, topk_w=None, sorted_pair=None, out=None, ws=None, stream=None):
+    """a4: out[M,N] = scale * (a . w[e]^T) per expert segment."""
+    torch = _torch()
+    M, K = a.shape
+    E, N, _ = w.shape
+    if out is None:
+        out = torch.empty((M, N), dtype=torch.bfloat16, device=a.device)
+    ws = _ws(lib().moe_grouped_gemm_workspace_size(), a.device, ws)
+    _check(lib().moe_grouped_gemm(_ptr(a), _ptr(w), _ptr(offsets), _ptr(topk_w), _ptr(sorted_pair), E, M, N, K,
+                                  _ptr(out), _ptr(ws), ws.numel(), _stream(stream)), "moe_grouped_gemm")
+    return out
+
+
+def moe_finalize_routing(y_perm, pair_pos, T: int, k: int, shared=None, y=None, stream=None):
+    """a6: y[t] = sum_j y_perm[pair_pos[t*k+j]] (+ shared[t])."""
+    torch = _torch()
+    H = y_perm.shape[1]
+    if y is None:
+        y = torch.empty((T, H), dtype=torch.bfloat16, device=y_perm.device)
+    _check(lib().moe_finalize_routing(_ptr(y_perm), _ptr(pair_pos), _ptr(shared), T, k, H, _ptr(y),
+                                      _stream(stream)), "moe_finalize_routing")
+    return y
+
+
+def make_desc(T, H, E, k, I, gate="softmax", routed_scaling_factor=1.0, eps=1e-20, n_shared=0, I_s=0):
+    return moe_layer_desc(T, H, E, k, I, GATES[gate] if isinstance(gate, str) else gate, routed_scaling_factor,
+                          eps, n_shared, I_s if n_shared else 0)
+
+
+def moe_layer_workspace_size(desc: moe_layer_desc) -> int:
+    n = lib().moe_layer_workspace_size(ctypes.byref(desc))
+    if n == 0:
+        raise MoEError(MOE_ERR_INVALID_ARG, "moe_layer_workspace_size")
+    return n
+
+
+def moe_layer_workspace_offsets(desc: moe_layer_desc) -> list:
+    arr = (ctypes.c_size_t * 8)()
+    lib().moe_layer_workspace_offsets(ctypes.byref(desc), arr, 8)
+    return list(arr)
+
+
+def moe_layer_forward(desc: moe_layer_desc, x, logits, w13, w2, bias=None, w13_s=None, w2_s=None, ws=None,
+                      y=None, topk_w=None, topk_idx=None, counts=None, stream=None):
+    """The whole layer; returns (y, topk_w, topk_idx, counts, ws)."""
+    torch = _torch()
+    dev = x.device
+    T, k, H, E = desc.T, desc.k, desc.H, desc.E
+    y = y if y is not None else torch.empty((T, H), dtype=torch.bfloat16, device=dev)
+    topk_w = topk_w if topk_w is not None else torch.empty((T, k), dtype=torch.float32, device=dev)
+    topk_idx = topk_idx if topk_idx is not None else torch.empty((T, k), dtype=torch.int32, device=dev)
+    counts = counts if counts is not None else torch.empty(E, dtype=torch.int32, device=dev)
+    ws = _ws(moe_layer_workspace_size(desc), dev, ws)
+    _check(lib().moe_layer_forward(ctypes.byref(desc), _ptr(x), _ptr(logits), _ptr(bias), _ptr(w13), _ptr(w2),
+                                   _ptr(w13_s), _ptr(w2_s), _ptr(y), _ptr(topk_w), _ptr(topk_idx), _ptr(counts),
+                                   _ptr(ws), ws.numel(), _stream(stream)), "moe_layer_forward")
+    return y, topk_w, topk_idx, counts, ws
+
+
+def moe_layer_forward_events(desc: moe_layer_desc, events, x, logits, w13, w2, bias=None, w13_s=None, w2_s=None,
+                             ws=None, y=None, topk_w=None, topk_idx=None, counts=None, stream=None):
+    """moe_layer_forward that also records six torch.cuda.Event objects around its steps
+    (before gating, routing, gate/up GEMM, down GEMM, finalize; after finalize)."""
+    handles = (ctypes.c_void_p * 6)()
+    for i, ev in enumerate(events):
+        if ev.cuda_event == 0:  # torch creates the event lazily on its first record
+            ev.record()
+        handles[i] = ev.cuda_event
+    _check(lib().moe_layer_forward_events(ctypes.byref(desc), _ptr(x), _ptr(logits), _ptr(bias), _ptr(w13),
+                                          _ptr(w2), _ptr(w13_s), _ptr(w2_s), _ptr(y), _ptr(topk_w), _ptr(topk_idx),
+                                          _ptr(counts), _ptr(ws), ws.numel(), _stream(stream), handles, 6),
+           "moe_layer_forward_events")
+    return y
+
+
+def moe_layer_kernel_launches(desc: moe_layer_desc) -> int:
+    return lib().moe_layer_kernel_launches(ctypes.byref(desc))
+
+
+def moe_get_device_status(ws, stream=None) -> int:
+    return lib().moe_get_device_status(_ptr(ws), _stream(stream))
+
+
+def moe_workspace_init(ws, stream=None) -> None:
+    _check(lib().moe_workspace_init(_ptr(ws), ws.numel(), _stream(stream)), "moe_workspace_init")
+
+
+class MoELayer:
+    """One MoE layer shape with its own workspace and output buffers (reused across calls)."""
+
+    def __init__(self, T, H, E, k, I, gate="softmax", routed_scaling_factor=1.0, eps=1e-20, n_shared=0, I_s=0,
+                 device="cuda"):
+        torch = _torch()
+        self.desc = make_desc(T, H, E, k, I, gate, routed_scaling_factor, eps, n_shared, I_s)
+        self.device = torch.device(device)
+        self.ws = torch.zeros(moe_layer_workspace_size(self.desc), dtype=torch.uint8, device=self.device)
+        self.y = torch.empty((T, H), dtype=torch.bfloat16, device=self.device)
+        self.topk_w = torch.empty((T, k), dtype=torch.float32, device=self.device)
+        self.topk_idx = torch.empty((T, k), dtype=torch.int32, device=self.device)
+        self.counts = torch.empty(E, dtype=torch.int32, device=self.device)
+        self.offsets_bytes = moe_layer_workspace_offsets(self.desc)
+
+    def forward(self, x, logits, w13, w2, bias=None, w13_s=None, w2_s=None, stream=None):
+        moe_layer_forward(self.desc, x, logits, w13, w2, bias, w13_s, w2_s, self.ws, self.y, self.topk_w,
+                          self.topk_idx, self.counts, stream)
+        return self.y
+
+    def forward_events(self, events, x, logits, w13, w2, bias=None, w13_s=None, w2_s=None, stream=None):
+        moe_layer_forward_events(self.desc, events, x, logits, w13, w2, bias, w13_s, w2_s, self.ws, self.y,
+                                 self.topk_w, self.topk_idx, self.counts, stream)
+        return self.y
+
+    def intermediate(self, name: str):
+        """View of an intermediate in the workspace: offsets, sorted_pair, pair_pos, x_exp, act, y_perm, act_s, shared."""
+        torch = _torch()
+        d = self.desc
+        P = d.T * d.k
+        spec = {
+            "offsets": (0, torch.int32, (d.E + 1,)),
+            "sorted_pair": (1, torch.int32, (P,)),
+            "pair_pos": (2, torch.int32, (P,)),
+            "x_exp": (3, torch.bfloat16, (P, d.H)),
+            "act": (4, torch.bfloat16, (P, d.I)),
+            "y_perm": (5, torch.bfloat16, (P, d.H)),
+            "act_s": (6, torch.bfloat16, (d.T, d.I_s)),
+            "shared": (7, torch.bfloat16, (d.T, d.H)),
+        }[name]
+        i, dt, shape = spec
+        n = 1
+        for s in shape:
+            n *= s
+        off = self.offsets_bytes[i]
+        nbytes = n * (4 if dt == torch.int32 else 2)
+        return self.ws[off:off + nbytes].view(dt).view(shape)

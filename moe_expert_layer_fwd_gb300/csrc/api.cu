@@ -1,0 +1,394 @@
+// C-ABI entry points: host-side validation, workspace carving and launches.
+// Declarations and full argument documentation are in include/moe.h.
+#include <cuda_runtime.h>
+#include <stdint.h>
+#include <string.h>
+
+#include "../../include/moe.h"
+#include "moe_common.cuh"
+#include "moe_internal.h"
+
+namespace {
+
+constexpr size_t kHeader = 256;  // status word + padding
+constexpr size_t kAlign = 256;
+constexpr int kAbiVersion = 100;
+
+inline size_t align_up(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
+
+inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+inline cudaStream_t as_stream(void* s) { return reinterpret_cast<cudaStream_t>(s); }
+
+inline int cuda_status(cudaError_t e) { return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA; }
+
+inline unsigned* status_word(void* ws) { return reinterpret_cast<unsigned*>(ws); }
+
+int check_common(int T, int E, int k) {
+  if (T < 0 || E < 1 || k < 1) return MOE_ERR_INVALID_ARG;
+  if (E > 1024 || k > 32 || k > E) return MOE_ERR_UNSUPPORTED;
+  if ((long long)T * k >= (1LL << 31)) return MOE_ERR_UNSUPPORTED;
+  return MOE_OK;
+}
+
+int check_dims(long long P, int H, int I) {
+  if (H <= 0 || I <= 0) return MOE_ERR_INVALID_ARG;
+  if (H % 64 != 0 || I % 64 != 0) return MOE_ERR_UNSUPPORTED;
+  const long long mx = H > I ? H : I;
+  if (P * mx >= (1LL << 40)) return MOE_ERR_UNSUPPORTED;
+  return MOE_OK;
+}
+
+// Layout of the moe_layer_forward workspace.
+struct LayerWs {
+  size_t offsets, scratch, sorted_pair, pair_pos, x_exp, act, y_perm, act_s, shared, total;
+};
+
+LayerWs layer_ws(const moe_layer_desc* d) {
+  LayerWs w{};
+  const size_t P = (size_t)d->T * d->k;
+  size_t o = kHeader;
+  w.offsets = o;     o = align_up(o + (size_t)(d->E + 1) * 4);
+  w.scratch = o;     o = align_up(o + moe::routing_scratch_bytes((int)P, d->E));
+  w.sorted_pair = o; o = align_up(o + P * 4);
+  w.pair_pos = o;    o = align_up(o + P * 4);
+  w.x_exp = o;       o = align_up(o + P * d->H * 2);
+  w.act = o;         o = align_up(o + P * d->I * 2);
+  w.y_perm = o;      o = align_up(o + P * d->H * 2);
+  const bool sh = d->n_shared > 0;
+  w.act_s = o;       o = align_up(o + (sh ? (size_t)d->T * d->I_s * 2 : 0));
+  w.shared = o;      o = align_up(o + (sh ? (size_t)d->T * d->H * 2 : 0));
+  w.total = o;
+  return w;
+}
+
+int check_desc(const moe_layer_desc* d) {
+  if (!d) return MOE_ERR_INVALID_ARG;
+  int s = check_common(d->T, d->E, d->k);
+  if (s) return s;
+  if ((s = check_dims((long long)d->T * d->k, d->H, d->I))) return s;
+  if (d->gate != MOE_GATE_SOFTMAX && d->gate != MOE_GATE_SIGMOID) return MOE_ERR_INVALID_ARG;
+  if (d->n_shared < 0) return MOE_ERR_INVALID_ARG;
+  if (d->n_shared > 1) return MOE_ERR_UNSUPPORTED;
+  if (d->n_shared == 1) {
+    if (d->I_s <= 0) return MOE_ERR_INVALID_ARG;
+    if (d->I_s % 64 != 0) return MOE_ERR_UNSUPPORTED;
+  }
+  return MOE_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* moe_status_string(int status) {
+  switch (status) {
+    case MOE_OK: return "MOE_OK";
+    case MOE_ERR_INVALID_ARG: return "MOE_ERR_INVALID_ARG";
+    case MOE_ERR_UNSUPPORTED: return "MOE_ERR_UNSUPPORTED";
+    case MOE_ERR_WORKSPACE: return "MOE_ERR_WORKSPACE";
+    case MOE_ERR_CUDA: return "MOE_ERR_CUDA";
+    case MOE_ERR_TIMEOUT: return "MOE_ERR_TIMEOUT";
+    case MOE_ERR_DEVICE_CHECK: return "MOE_ERR_DEVICE_CHECK";
+    default: return "MOE_ERR_UNKNOWN";
+  }
+}
+
+int moe_abi_version(void) { return kAbiVersion; }
+
+size_t moe_status_bytes(void) { return kHeader; }
+
+int moe_workspace_init(void* ws, size_t ws_bytes, void* stream) {
+  if (!ws || !aligned16(ws)) return MOE_ERR_INVALID_ARG;
+  if (ws_bytes < kHeader) return MOE_ERR_WORKSPACE;
+  return cuda_status(cudaMemsetAsync(ws, 0, kHeader, as_stream(stream)));
+}
+
+int moe_get_device_status(const void* ws, void* stream) {
+  if (!ws || !aligned16(ws)) return MOE_ERR_INVALID_ARG;
+  unsigned word = 0;
+  if (cudaStreamSynchronize(as_stream(stream)) != cudaSuccess) return MOE_ERR_CUDA;
+  if (cudaMemcpy(&word, ws, sizeof(word), cudaMemcpyDeviceToHost) != cudaSuccess) return MOE_ERR_CUDA;
+  if (word & moe::DEV_ERR_TIMEOUT) return MOE_ERR_TIMEOUT;
+  if (word & (moe::DEV_ERR_BOUNDS | moe::DEV_ERR_CONFIG)) return MOE_ERR_DEVICE_CHECK;
+  return MOE_OK;
+}
+
+int moe_gating_topk(const float* logits, const float* bias, int T, int E, int k, int gate,
+                    float routed_scaling_factor, float eps, float* topk_w, int32_t* topk_idx, void* stream) {
+  int s = check_common(T, E, k);
+  if (s) return s;
+  if (gate != MOE_GATE_SOFTMAX && gate != MOE_GATE_SIGMOID) return MOE_ERR_INVALID_ARG;
+  if (gate == MOE_GATE_SOFTMAX && bias) return MOE_ERR_INVALID_ARG;
+  if (T == 0) return MOE_OK;
+  if (!logits || !topk_w || !topk_idx) return MOE_ERR_INVALID_ARG;
+  if (!aligned16(logits) || !aligned16(topk_w) || !aligned16(topk_idx) || (bias && !aligned16(bias)))
+    return MOE_ERR_INVALID_ARG;
+  return cuda_status(moe::launch_gating_topk(logits, bias, T, E, k, gate, routed_scaling_factor, eps, topk_w,
+                                             topk_idx, as_stream(stream)));
+}
+
+size_t moe_init_routing_workspace_size(int T, int E, int k) {
+  if (check_common(T, E, k)) return 0;
+  return align_up(kHeader + moe::routing_scratch_bytes(T * k, E));
+}
+
+int moe_init_routing(const int32_t* topk_idx, int T, int E, int k, const uint16_t* x, int H, uint16_t* x_exp,
+                     int32_t* counts, int32_t* offsets, int32_t* sorted_pair, int32_t* pair_pos, void* ws,
+                     size_t ws_bytes, void* stream) {
+  int s = check_common(T, E, k);
+  if (s) return s;
+  if (!counts || !offsets || !ws) return MOE_ERR_INVALID_ARG;
+  if ((x == nullptr) != (x_exp == nullptr)) return MOE_ERR_INVALID_ARG;
+  if (x) {
+    if ((s = check_dims((long long)T * k, H, 64))) return s;
+    if (!aligned16(x) || !aligned16(x_exp)) return MOE_ERR_INVALID_ARG;
+  }
+  if (!aligned16(counts) || !aligned16(offsets) || !aligned16(ws)) return MOE_ERR_INVALID_ARG;
+  if (ws_bytes < moe_init_routing_workspace_size(T, E, k)) return MOE_ERR_WORKSPACE;
+  if (T > 0 && (!topk_idx || !sorted_pair || !pair_pos || !aligned16(topk_idx) || !aligned16(sorted_pair) ||
+                !aligned16(pair_pos)))
+    return MOE_ERR_INVALID_ARG;
+  int32_t* scratch = reinterpret_cast<int32_t*>(static_cast<char*>(ws) + kHeader);
+  return cuda_status(moe::launch_init_routing(topk_idx, T * k, E, k, x, H, x_exp, counts, offsets, sorted_pair,
+                                              pair_pos, scratch, status_word(ws), as_stream(stream)));
+}
+
+size_t moe_grouped_gemm_workspace_size(void) { return kHeader; }
+
+int moe_grouped_gemm_swiglu(const uint16_t* x_rows, const uint16_t* w13, const int32_t* offsets, int E, int M,
+                            int H, int I, uint16_t* act, void* ws, size_t ws_bytes, void* stream) {
+  if (E < 1 || M < 0) return MOE_ERR_INVALID_ARG;
+  if (E > 1024) return MOE_ERR_UNSUPPORTED;
+  int s = check_dims(M, H, I);
+  if (s) return s;
+  if (!w13 || !offsets || !ws) return MOE_ERR_INVALID_ARG;
+  if (ws_bytes < kHeader) return MOE_ERR_WORKSPACE;
+  if (M == 0) return MOE_OK;
+  if (!x_rows || !act) return MOE_ERR_INVALID_ARG;
+  if (!aligned16(x_rows) || !aligned16(w13) || !aligned16(offsets) || !aligned16(act) || !aligned16(ws))
+    return MOE_ERR_INVALID_ARG;
+  moe::GroupedGemmProblem p{};
+  p.mode = 0;
+  p.a_rows = x_rows;
+  p.w = w13;
+  p.offsets = offsets;
+  p.E = E;
+  p.M = M;
+  p.K = H;
+  p.n_out = 2 * I;
+  p.out = act;
+  p.ld_out = I;
+  p.status = status_word(ws);
+  return cuda_status(moe::launch_grouped_gemm(p, as_stream(stream)));
+}
+
+int moe_grouped_gemm(const uint16_t* a, const uint16_t* w, const int32_t* offsets, const float* topk_w,
+                     const int32_t* sorted_pair, int E, int M, int N, int K, uint16_t* out, void* ws,
+                     size_t ws_bytes, void* stream) {
+  if (E < 1 || M < 0) return MOE_ERR_INVALID_ARG;
+  if (E > 1024) return MOE_ERR_UNSUPPORTED;
+  int s = check_dims(M, N, K);
+  if (s) return s;
+  if ((topk_w == nullptr) != (sorted_pair == nullptr)) return MOE_ERR_INVALID_ARG;
+  if (!w || !offsets || !ws) return MOE_ERR_INVALID_ARG;
+  if (ws_bytes < kHeader) return MOE_ERR_WORKSPACE;
+  if (M == 0) return MOE_OK;
+  if (!a || !out) return MOE_ERR_INVALID_ARG;
+  if (!aligned16(a) || !aligned16(w) || !aligned16(offsets) || !aligned16(out) || !aligned16(ws) ||
+      (topk_w && (!aligned16(topk_w) || !aligned16(sorted_pair))))
+    return MOE_ERR_INVALID_ARG;
+  moe::GroupedGemmProblem p{};
+  p.mode = 1;
+  p.a_rows = a;
+  p.w = w;
+  p.offsets = offsets;
+  p.E = E;
+  p.M = M;
+  p.K = K;
+  p.n_out = N;
+  p.out = out;
+  p.ld_out = N;
+  p.topk_w = topk_w;
+  p.sorted_pair = sorted_pair;
+  p.status = status_word(ws);
+  return cuda_status(moe::launch_grouped_gemm(p, as_stream(stream)));
+}
+
+int moe_finalize_routing(const uint16_t* y_perm, const int32_t* pair_pos, const uint16_t* shared, int T, int k,
+                         int H, uint16_t* y, void* stream) {
+  if (T < 0 || k < 1 || H <= 0) return MOE_ERR_INVALID_ARG;
+  if (k > 32 || H % 64 != 0 || (long long)T * k >= (1LL << 31)) return MOE_ERR_UNSUPPORTED;
+  if (T == 0) return MOE_OK;
+  if (!y_perm || !pair_pos || !y) return MOE_ERR_INVALID_ARG;
+  if (!aligned16(y_perm) || !aligned16(pair_pos) || !aligned16(y) || (shared && !aligned16(shared)))
+    return MOE_ERR_INVALID_ARG;
+  return cuda_status(moe::launch_finalize(y_perm, pair_pos, shared, T, k, H, y, as_stream(stream)));
+}
+
+size_t moe_layer_workspace_size(const moe_layer_desc* d) {
+  if (check_desc(d)) return 0;
+  return layer_ws(d).total;
+}
+
+int moe_layer_workspace_offsets(const moe_layer_desc* d, size_t* out, int n) {
+  if (check_desc(d) || !out || n < 0) return MOE_ERR_INVALID_ARG;
+  const LayerWs w = layer_ws(d);
+  const size_t v[8] = {w.offsets, w.sorted_pair, w.pair_pos, w.x_exp, w.act, w.y_perm, w.act_s, w.shared};
+  for (int i = 0; i < n && i < 8; ++i) out[i] = v[i];
+  return 8;
+}
+
+}  // extern "C"
+
+namespace {
+
+int layer_forward_impl(const moe_layer_desc* d, const uint16_t* x, const float* logits, const float* bias,
+                       const uint16_t* w13, const uint16_t* w2, const uint16_t* w13_s, const uint16_t* w2_s,
+                       uint16_t* y, float* topk_w, int32_t* topk_idx, int32_t* counts, void* ws, size_t ws_bytes,
+                       void* stream, void* const* events) {
+  int s = check_desc(d);
+  if (s) return s;
+  if (d->gate == MOE_GATE_SOFTMAX && bias) return MOE_ERR_INVALID_ARG;
+  if (!ws || !counts) return MOE_ERR_INVALID_ARG;
+  const LayerWs L = layer_ws(d);
+  if (ws_bytes < L.total) return MOE_ERR_WORKSPACE;
+  if (d->T == 0) return MOE_OK;
+  if (!x || !logits || !w13 || !w2 || !y || !topk_w || !topk_idx) return MOE_ERR_INVALID_ARG;
+  if (d->n_shared && (!w13_s || !w2_s)) return MOE_ERR_INVALID_ARG;
+  const void* ptrs[] = {x, logits, w13, w2, y, topk_w, topk_idx, counts, ws};
+  for (const void* p : ptrs)
+    if (!aligned16(p)) return MOE_ERR_INVALID_ARG;
+  if ((bias && !aligned16(bias)) || (w13_s && !aligned16(w13_s)) || (w2_s && !aligned16(w2_s)))
+    return MOE_ERR_INVALID_ARG;
+
+  cudaStream_t st = as_stream(stream);
+  char* base = static_cast<char*>(ws);
+  unsigned* status = status_word(ws);
+  int32_t* offsets = reinterpret_cast<int32_t*>(base + L.offsets);
+  int32_t* scratch = reinterpret_cast<int32_t*>(base + L.scratch);
+  int32_t* sorted_pair = reinterpret_cast<int32_t*>(base + L.sorted_pair);
+  int32_t* pair_pos = reinterpret_cast<int32_t*>(base + L.pair_pos);
+  uint16_t* x_exp = reinterpret_cast<uint16_t*>(base + L.x_exp);
+  uint16_t* act = reinterpret_cast<uint16_t*>(base + L.act);
+  uint16_t* y_perm = reinterpret_cast<uint16_t*>(base + L.y_perm);
+  uint16_t* act_s = reinterpret_cast<uint16_t*>(base + L.act_s);
+  uint16_t* shared = reinterpret_cast<uint16_t*>(base + L.shared);
+  const int T = d->T, E = d->E, k = d->k, H = d->H, I = d->I, P = T * k;
+  const bool sh = d->n_shared > 0;
+
+  auto mark = [&](int i) {
+    return events ? cudaEventRecord(reinterpret_cast<cudaEvent_t>(events[i]), st) : cudaSuccess;
+  };
+  if (mark(0) != cudaSuccess) return MOE_ERR_CUDA;
+  cudaError_t e = moe::launch_gating_topk(logits, bias, T, E, k, d->gate, d->routed_scaling_factor, d->eps,
+                                          topk_w, topk_idx, st);
+  if (e != cudaSuccess) return MOE_ERR_CUDA;
+  if (mark(1) != cudaSuccess) return MOE_ERR_CUDA;
+  e = moe::launch_init_routing(topk_idx, P, E, k, x, H, x_exp, counts, offsets, sorted_pair, pair_pos, scratch,
+                               status, st);
+  if (e != cudaSuccess) return MOE_ERR_CUDA;
+
+  moe::GroupedGemmProblem g1{};
+  g1.mode = 0;
+  g1.a_rows = x_exp;
+  g1.w = w13;
+  g1.offsets = offsets;
+  g1.E = E;
+  g1.M = P;
+  g1.K = H;
+  g1.n_out = 2 * I;
+  g1.out = act;
+  g1.ld_out = I;
+  if (sh) {
+    g1.s_rows = x;
+    g1.s_w = w13_s;
+    g1.T_s = T;
+    g1.n_out_s = 2 * d->I_s;
+    g1.s_out = act_s;
+    g1.ld_out_s = d->I_s;
+  }
+  g1.status = status;
+  if (mark(2) != cudaSuccess) return MOE_ERR_CUDA;
+  if (moe::launch_grouped_gemm(g1, st) != cudaSuccess) return MOE_ERR_CUDA;
+  if (mark(3) != cudaSuccess) return MOE_ERR_CUDA;
+
+  // The down projection's K is I for routed experts and I_s for the shared
+  // one; one launch covers both only when they agree.
+  moe::GroupedGemmProblem g2{};
+  g2.mode = 1;
+  g2.a_rows = act;
+  g2.w = w2;
+  g2.offsets = offsets;
+  g2.E = E;
+  g2.M = P;
+  g2.K = I;
+  g2.n_out = H;
+  g2.out = y_perm;
+  g2.ld_out = H;
+  g2.topk_w = topk_w;
+  g2.sorted_pair = sorted_pair;
+  g2.status = status;
+  moe::GroupedGemmProblem g2s{};
+  const bool fused_shared = sh && d->I_s == I;
+  if (sh) {
+    moe::GroupedGemmProblem& gs = fused_shared ? g2 : g2s;
+    gs.s_rows = act_s;
+    gs.s_w = w2_s;
+    gs.T_s = T;
+    gs.n_out_s = H;
+    gs.s_out = shared;
+    gs.ld_out_s = H;
+  }
+  if (moe::launch_grouped_gemm(g2, st) != cudaSuccess) return MOE_ERR_CUDA;
+  if (sh && !fused_shared) {
+    // separate launch for the shared expert's down projection (K = I_s)
+    g2s.mode = 1;
+    g2s.a_rows = nullptr;
+    g2s.w = w2_s;
+    g2s.offsets = nullptr;
+    g2s.E = 1;
+    g2s.M = 0;
+    g2s.K = d->I_s;
+    g2s.n_out = H;
+    g2s.status = status;
+    if (moe::launch_grouped_gemm(g2s, st) != cudaSuccess) return MOE_ERR_CUDA;
+  }
+  if (mark(4) != cudaSuccess) return MOE_ERR_CUDA;
+  if (moe::launch_finalize(y_perm, pair_pos, sh ? shared : nullptr, T, k, H, y, st) != cudaSuccess)
+    return MOE_ERR_CUDA;
+  return cuda_status(mark(5));
+}
+
+}  // namespace
+
+extern "C" {
+
+int moe_layer_forward(const moe_layer_desc* d, const uint16_t* x, const float* logits, const float* bias,
+                      const uint16_t* w13, const uint16_t* w2, const uint16_t* w13_s, const uint16_t* w2_s,
+                      uint16_t* y, float* topk_w, int32_t* topk_idx, int32_t* counts, void* ws, size_t ws_bytes,
+                      void* stream) {
+  return layer_forward_impl(d, x, logits, bias, w13, w2, w13_s, w2_s, y, topk_w, topk_idx, counts, ws, ws_bytes,
+                            stream, nullptr);
+}
+
+int moe_layer_forward_events(const moe_layer_desc* d, const uint16_t* x, const float* logits, const float* bias,
+                             const uint16_t* w13, const uint16_t* w2, const uint16_t* w13_s, const uint16_t* w2_s,
+                             uint16_t* y, float* topk_w, int32_t* topk_idx, int32_t* counts, void* ws,
+                             size_t ws_bytes, void* stream, void* const* events, int n_events) {
+  if (!events || n_events != 6) return MOE_ERR_INVALID_ARG;
+  for (int i = 0; i < 6; ++i)
+    if (!events[i]) return MOE_ERR_INVALID_ARG;
+  return layer_forward_impl(d, x, logits, bias, w13, w2, w13_s, w2_s, y, topk_w, topk_idx, counts, ws, ws_bytes,
+                            stream, events);
+}
+
+int moe_layer_kernel_launches(const moe_layer_desc* d) {
+  if (check_desc(d)) return 0;
+  if (d->T == 0) return 0;
+  // gating 1 + routing (hist, scan, scatter, gather) 4 + gate/up GEMM 1 + down GEMM 1
+  // (+1 when the shared expert's intermediate size differs) + finalize 1
+  return 8 + ((d->n_shared > 0 && d->I_s != d->I) ? 1 : 0);
+}
+
+}  // extern "C"

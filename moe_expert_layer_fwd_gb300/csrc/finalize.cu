@@ -1,0 +1,62 @@
+// a6. Finalize-routing on GB300: unpermute + weighted sum (+ shared expert).
+//
+// Source: Qwen3-MoE low-latency inference practice, "GMM enablement and
+// routing optimisation" (expert outputs are re-arranged back to token order
+// and summed with their weights); Hy3 295B MoE practice, section 8.1 (the
+// shared-expert term is added in this combine step).  The routing weight is
+// already applied by the down-projection epilogue, so this step only sums.
+//
+// One thread per 8 consecutive hidden columns of one token (16-byte loads and
+// stores): y[t, c:c+8] = sum_j y_perm[pair_pos[t*k+j], c:c+8] (+ shared[t]),
+// in fp32 in slot order, rounded once to bf16.  HBM-bound: reads P*H*2 +
+// T*H*2 bytes, writes T*H*2.
+#include "moe_common.cuh"
+#include "moe_internal.h"
+
+namespace moe {
+namespace {
+
+__device__ __forceinline__ void acc8(float (&a)[8], const uint4& v) {
+  a[0] += bf16_lo(v.x); a[1] += bf16_hi(v.x);
+  a[2] += bf16_lo(v.y); a[3] += bf16_hi(v.y);
+  a[4] += bf16_lo(v.z); a[5] += bf16_hi(v.z);
+  a[6] += bf16_lo(v.w); a[7] += bf16_hi(v.w);
+}
+
+__global__ void __launch_bounds__(256) finalize_kernel(const uint4* __restrict__ y_perm,
+                                                       const int32_t* __restrict__ pair_pos,
+                                                       const uint4* __restrict__ shared, int T, int k, int H8,
+                                                       uint4* __restrict__ y) {
+  const size_t gid = (size_t)blockIdx.x * blockDim.x + threadIdx.x;
+  if (gid >= (size_t)T * H8) return;
+  const int t = (int)(gid / H8);
+  const int c = (int)(gid % H8);
+  const int P = T * k;
+  float a[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+  for (int j = 0; j < k; ++j) {
+    const int pos = __ldg(pair_pos + (size_t)t * k + j);
+    if ((unsigned)pos < (unsigned)P) acc8(a, __ldg(y_perm + (size_t)pos * H8 + c));
+  }
+  if (shared) acc8(a, __ldg(shared + gid));
+  uint4 o;
+  o.x = pack_bf16x2(a[0], a[1]);
+  o.y = pack_bf16x2(a[2], a[3]);
+  o.z = pack_bf16x2(a[4], a[5]);
+  o.w = pack_bf16x2(a[6], a[7]);
+  y[gid] = o;
+}
+
+}  // namespace
+
+cudaError_t launch_finalize(const uint16_t* y_perm, const int32_t* pair_pos, const uint16_t* shared, int T, int k,
+                            int H, uint16_t* y, cudaStream_t stream) {
+  const size_t n = (size_t)T * (H / 8);
+  if (n == 0) return cudaSuccess;
+  const int threads = 256;
+  finalize_kernel<<<(unsigned)((n + threads - 1) / threads), threads, 0, stream>>>(
+      reinterpret_cast<const uint4*>(y_perm), pair_pos, reinterpret_cast<const uint4*>(shared), T, k, H / 8,
+      reinterpret_cast<uint4*>(y));
+  return cudaGetLastError();
+}
+
+}  // namespace moe

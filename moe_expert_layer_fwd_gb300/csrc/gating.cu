@@ -1,0 +1,143 @@
+// a1. Gating top-k on GB300: one warp per token.
+//
+// Source: Qwen3-MoE low-latency inference practice, "GMM enablement and
+// routing optimisation" (one fused op computes routing scores and the top-k
+// experts, replacing top-k then softmax); Hy3 295B MoE practice, section 1.3
+// (sigmoid router: sigmoid, top-k, gather, normalise with eps = 1e-20, scale by
+// routed_scaling_factor = 2.826) and section 5.1 (the correction bias is added
+// after the sigmoid and only decides which experts are chosen).
+//
+// Each lane holds experts e = lane + 32*i.  The selection key is turned into
+// an order-preserving 32-bit integer and packed with the complement of the
+// expert index, so one 64-bit max over the warp picks "largest key, then
+// lowest index"; k rounds pick the k experts in order.  The sigmoid key is
+// computed with a fixed sequence of IEEE fp32 operations (Cody-Waite reduced
+// exp with a degree-7 Taylor polynomial, each multiply and add rounded
+// separately), so the choice is reproducible bit for bit on any IEEE machine.
+#include "moe_common.cuh"
+#include "moe_internal.h"
+
+namespace moe {
+namespace {
+
+// e^x by the fixed operation sequence: n = rint(x*log2e); r = (x - n*C1) - n*C2
+// with ln2 = C1 + C2 (C1 = 355/512); p = Horner of sum r^m/m!, m <= 7, each
+// step one rounded multiply and one rounded add; result p * 2^n.  x is clamped
+// to [-87, 88] so 2^n is a normal float.
+__device__ __forceinline__ float exp_fixed_f32(float x) {
+  x = fminf(fmaxf(x, -87.0f), 88.0f);
+  const float n = rintf(__fmul_rn(x, 1.4426950408889634f));
+  const float r = __fsub_rn(__fsub_rn(x, __fmul_rn(n, 0.693359375f)), __fmul_rn(n, -2.12194440e-4f));
+  float p = 1.0f / 5040.0f;
+  p = __fadd_rn(__fmul_rn(p, r), 1.0f / 720.0f);
+  p = __fadd_rn(__fmul_rn(p, r), 1.0f / 120.0f);
+  p = __fadd_rn(__fmul_rn(p, r), 1.0f / 24.0f);
+  p = __fadd_rn(__fmul_rn(p, r), 1.0f / 6.0f);
+  p = __fadd_rn(__fmul_rn(p, r), 0.5f);
+  p = __fadd_rn(__fmul_rn(p, r), 1.0f);
+  p = __fadd_rn(__fmul_rn(p, r), 1.0f);
+  const float scale = __int_as_float(((int)n + 127) << 23);
+  return __fmul_rn(p, scale);
+}
+
+__device__ __forceinline__ float sigmoid_fixed_f32(float l) {
+  return __fdiv_rn(1.0f, __fadd_rn(1.0f, exp_fixed_f32(-l)));
+}
+
+// Order-preserving map float -> uint32 (larger float -> larger integer), with
+// -0 and +0 mapped to the same value.
+__device__ __forceinline__ uint32_t ordered_key(float f) {
+  if (f == 0.0f) f = 0.0f;
+  uint32_t u = __float_as_uint(f);
+  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+
+__device__ __forceinline__ unsigned long long warp_max_u64(unsigned long long v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    unsigned long long w = __shfl_xor_sync(0xffffffffu, v, o);
+    v = w > v ? w : v;
+  }
+  return v;
+}
+
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  return v;
+}
+
+// VPL = keys held per lane (E <= 32 * VPL); a compile-time bound keeps them in registers.
+template <int VPL>
+__global__ void __launch_bounds__(256) gating_topk_kernel(const float* __restrict__ logits,
+                                                          const float* __restrict__ bias, int T, int E, int k,
+                                                          int gate, float rsf, float eps,
+                                                          float* __restrict__ topk_w,
+                                                          int32_t* __restrict__ topk_idx) {
+  const int lane = threadIdx.x & 31;
+  const int t = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+  if (t >= T) return;
+  const float* row = logits + (size_t)t * E;
+  unsigned long long packed[VPL];
+#pragma unroll
+  for (int i = 0; i < VPL; ++i) {
+    packed[i] = 0ull;  // below every real key: never chosen
+    const int e = lane + 32 * i;
+    if (e < E) {
+      const float l = __ldg(row + e);
+      float key = l;
+      if (gate == MOE_GATE_SIGMOID) {
+        key = sigmoid_fixed_f32(l);
+        if (bias) key = __fadd_rn(key, __ldg(bias + e));
+      }
+      packed[i] = ((unsigned long long)ordered_key(key) << 32) | (unsigned long long)(0xFFFFFFFFu - (uint32_t)e);
+    }
+  }
+
+  int my_e = -1;  // lane j keeps the j-th chosen expert
+  for (int j = 0; j < k; ++j) {
+    unsigned long long best = 0ull;
+#pragma unroll
+    for (int i = 0; i < VPL; ++i) best = packed[i] > best ? packed[i] : best;
+    best = warp_max_u64(best);
+    const int e = (int)(0xFFFFFFFFu - (uint32_t)(best & 0xFFFFFFFFull));
+    const bool mine = lane == (e & 31);
+    const int slot = e >> 5;
+#pragma unroll
+    for (int i = 0; i < VPL; ++i) packed[i] = (mine && i == slot) ? 0ull : packed[i];
+    if (lane == j) my_e = e;
+  }
+
+  const float l = (lane < k) ? __ldg(row + my_e) : 0.0f;
+  const float l0 = __shfl_sync(0xffffffffu, l, 0);  // softmax: slot 0 holds the largest logit
+  float w = 0.0f;
+  if (lane < k) w = (gate == MOE_GATE_SOFTMAX) ? expf(l - l0) : sigmoid_fixed_f32(l);
+  const float s = warp_sum(w);
+  if (lane < k) {
+    w = (gate == MOE_GATE_SOFTMAX) ? w / s : w / (s + eps) * rsf;
+    topk_w[(size_t)t * k + lane] = w;
+    topk_idx[(size_t)t * k + lane] = my_e;
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_gating_topk(const float* logits, const float* bias, int T, int E, int k, int gate, float rsf,
+                               float eps, float* topk_w, int32_t* topk_idx, cudaStream_t stream) {
+  if (T == 0) return cudaSuccess;
+  const int warps = 8;
+  dim3 grid((T + warps - 1) / warps);
+  const int vpl = (E + 31) / 32;
+#define MOE_GATING_LAUNCH(V) \
+  gating_topk_kernel<V><<<grid, warps * 32, 0, stream>>>(logits, bias, T, E, k, gate, rsf, eps, topk_w, topk_idx)
+  if (vpl <= 1) MOE_GATING_LAUNCH(1);
+  else if (vpl <= 2) MOE_GATING_LAUNCH(2);
+  else if (vpl <= 4) MOE_GATING_LAUNCH(4);
+  else if (vpl <= 8) MOE_GATING_LAUNCH(8);
+  else if (vpl <= 16) MOE_GATING_LAUNCH(16);
+  else MOE_GATING_LAUNCH(32);
+#undef MOE_GATING_LAUNCH
+  return cudaGetLastError();
+}
+
+}  // namespace moe

@@ -1,0 +1,48 @@
+// Host-side launchers shared between the kernel files and the C-ABI layer.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+namespace moe {
+
+cudaError_t launch_gating_topk(const float* logits, const float* bias, int T, int E, int k, int gate, float rsf,
+                               float eps, float* topk_w, int32_t* topk_idx, cudaStream_t stream);
+
+// Init-routing scratch: per-chunk expert histograms and bases.
+int routing_chunk_pairs(int P);
+size_t routing_scratch_bytes(int P, int E);
+cudaError_t launch_init_routing(const int32_t* topk_idx, int P, int E, int k, const uint16_t* x, int H,
+                                uint16_t* x_exp, int32_t* counts, int32_t* offsets, int32_t* sorted_pair,
+                                int32_t* pair_pos, int32_t* scratch, unsigned* status, cudaStream_t stream);
+cudaError_t launch_expand_rows(const uint16_t* x, const int32_t* sorted_pair, int P, int k, int H,
+                               uint16_t* x_exp, cudaStream_t stream);
+
+// One grouped GEMM launch: routed experts (+ optionally one dense "shared" segment).
+struct GroupedGemmProblem {
+  int mode;                    // 0: SwiGLU epilogue (w13), 1: scaled epilogue (down)
+  // routed experts
+  const uint16_t* a_rows;      // [M,K] token rows in expert-sorted order
+  const uint16_t* w;           // [E, n_out, K]
+  const int32_t* offsets;      // [E+1] device
+  int E, M, K, n_out;          // n_out = 2I (mode 0) or N (mode 1)
+  uint16_t* out;               // [M, ld_out]
+  int ld_out;                  // I (mode 0) or N (mode 1)
+  const float* topk_w;         // mode 1: row scale topk_w[sorted_pair[pos]] (NULL: 1)
+  const int32_t* sorted_pair;
+  // optional shared segment (weight 1, rows 0..T_s-1 of s_rows)
+  const uint16_t* s_rows;      // [T_s, K] or NULL
+  const uint16_t* s_w;         // [n_out_s, K]
+  int T_s, n_out_s;
+  uint16_t* s_out;             // [T_s, ld_out_s]
+  int ld_out_s;
+  unsigned* status;
+};
+
+cudaError_t launch_grouped_gemm(const GroupedGemmProblem& p, cudaStream_t stream);
+
+cudaError_t launch_finalize(const uint16_t* y_perm, const int32_t* pair_pos, const uint16_t* shared, int T, int k,
+                            int H, uint16_t* y, cudaStream_t stream);
+
+}  // namespace moe

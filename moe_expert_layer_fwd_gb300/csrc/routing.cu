@@ -1,0 +1,218 @@
+// a2. Init-routing on GB300: per-expert counts, offsets, a stable sort of the
+// token-expert pairs by expert (and its inverse), and the row gather x_exp.
+//
+// Source: Qwen3-MoE low-latency inference practice, "GMM enablement and
+// routing optimisation" (init-routing gives the expert sort order;
+// compute-expert-tokens gives each expert's token count); Hy3 295B MoE
+// practice, section 6.2 (group_list = per-expert token counts).
+//
+// Design: the P = T*k pairs are cut into chunks of CH consecutive pairs, one
+// warp per chunk.
+//   1. hist:    each warp counts its chunk per expert (shared-memory atomics;
+//               counts do not depend on order).
+//   2. scan:    one CTA turns the chunk histograms into counts, offsets and,
+//               for every (chunk, expert), the first output position.
+//   3. scatter: each warp walks its chunk in ascending pair order, 32 pairs at
+//               a time; __match_any_sync groups lanes with the same expert and
+//               the rank inside the group is the number of lower lanes in it,
+//               so positions follow pair order exactly (a stable sort) with no
+//               atomics deciding the order.
+//   4. expand:  x_exp[pos] = x[sorted_pair[pos] / k], one warp per row, 16-byte
+//               vector copies.
+#include "moe_common.cuh"
+#include "moe_internal.h"
+
+namespace moe {
+namespace {
+
+constexpr int kWarps = 8;
+
+__global__ void __launch_bounds__(kWarps * 32) route_hist_kernel(const int32_t* __restrict__ idx, int P, int E,
+                                                                 int CH, int n_chunks, int32_t* __restrict__ hist,
+                                                                 unsigned* status) {
+  extern __shared__ int sh[];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int c = blockIdx.x * kWarps + warp;
+  if (c >= n_chunks) return;
+  int* h = sh + warp * E;
+  for (int e = lane; e < E; e += 32) h[e] = 0;
+  __syncwarp();
+  const int p0 = c * CH, p1 = min(P, p0 + CH);
+  bool bad = false;
+  for (int p = p0 + lane; p < p1; p += 32) {
+    const int e = __ldg(idx + p);
+    if ((unsigned)e < (unsigned)E)
+      atomicAdd(&h[e], 1);
+    else
+      bad = true;
+  }
+  if (bad) set_status(status, DEV_ERR_BOUNDS);
+  __syncwarp();
+  for (int e = lane; e < E; e += 32) hist[(size_t)c * E + e] = h[e];
+}
+
+// One CTA of 1024 threads: thread (seg, e) owns expert e over the seg-th slice of chunks.
+__global__ void __launch_bounds__(1024) route_scan_kernel(const int32_t* __restrict__ hist,
+                                                          int32_t* __restrict__ base, int n_chunks, int E,
+                                                          int32_t* __restrict__ counts,
+                                                          int32_t* __restrict__ offsets) {
+  __shared__ int part[1024];
+  __shared__ int excl_s[1024];
+  __shared__ int wsum[32];
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int S = max(1, 1024 / E);
+  const int e = tid % E, seg = tid / E;
+  const bool active = seg < S;
+  const int cps = (n_chunks + S - 1) / S;
+  const int c0 = min(n_chunks, seg * cps), c1 = min(n_chunks, c0 + cps);
+  if (active) {
+    int s = 0;
+    for (int c = c0; c < c1; ++c) s += hist[(size_t)c * E + e];
+    part[seg * E + e] = s;
+  }
+  __syncthreads();
+  int v = 0;
+  if (tid < E) {
+    for (int g = 0; g < S; ++g) v += part[g * E + tid];
+    counts[tid] = v;
+  }
+  // block-wide exclusive scan of v over tid (E <= 1024)
+  int x = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int y = __shfl_up_sync(0xffffffffu, x, o);
+    if (lane >= o) x += y;
+  }
+  if (lane == 31) wsum[warp] = x;
+  __syncthreads();
+  if (warp == 0) {
+    int w = wsum[lane];
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, w, o);
+      if (lane >= o) w += y;
+    }
+    wsum[lane] = w;
+  }
+  __syncthreads();
+  const int incl = x + (warp > 0 ? wsum[warp - 1] : 0);
+  if (tid < E) {
+    excl_s[tid] = incl - v;
+    offsets[tid] = incl - v;
+    if (tid == E - 1) offsets[E] = incl;
+  }
+  __syncthreads();
+  if (active) {
+    int run = excl_s[e];
+    for (int g = 0; g < seg; ++g) run += part[g * E + e];
+    for (int c = c0; c < c1; ++c) {
+      base[(size_t)c * E + e] = run;
+      run += hist[(size_t)c * E + e];
+    }
+  }
+}
+
+__global__ void __launch_bounds__(kWarps * 32) route_scatter_kernel(const int32_t* __restrict__ idx, int P,
+                                                                    int E, int CH, int n_chunks,
+                                                                    const int32_t* __restrict__ base,
+                                                                    int32_t* __restrict__ sorted_pair,
+                                                                    int32_t* __restrict__ pair_pos) {
+  extern __shared__ int sh[];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int c = blockIdx.x * kWarps + warp;
+  if (c >= n_chunks) return;
+  int* cnt = sh + warp * E;
+  for (int e = lane; e < E; e += 32) cnt[e] = base[(size_t)c * E + e];
+  __syncwarp();
+  const int p0 = c * CH, p1 = min(P, p0 + CH);
+  const unsigned lower = (1u << lane) - 1u;
+  for (int pb = p0; pb < p1; pb += 32) {
+    const int p = pb + lane;
+    const int e = (p < p1) ? __ldg(idx + p) : -1;
+    const bool ok = (unsigned)e < (unsigned)E;
+    const int key = ok ? e : -1 - lane;  // lanes without a valid expert form singleton groups
+    const unsigned peers = __match_any_sync(0xffffffffu, key);
+    const int rank = __popc(peers & lower);
+    const int b = ok ? cnt[e] : 0;
+    __syncwarp();
+    if (ok) {
+      const int pos = b + rank;
+      if ((unsigned)pos < (unsigned)P) {
+        sorted_pair[pos] = p;
+        pair_pos[p] = pos;
+      }
+      if ((peers >> lane) == 1u) cnt[e] = b + __popc(peers);  // highest lane of the group
+    }
+    __syncwarp();
+  }
+}
+
+__global__ void __launch_bounds__(kWarps * 32) expand_rows_kernel(const uint4* __restrict__ x,
+                                                                  const int32_t* __restrict__ sorted_pair,
+                                                                  int P, int k, int T, int H8,
+                                                                  uint4* __restrict__ x_exp) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int row = blockIdx.x * kWarps + warp;
+  if (row >= P) return;
+  const int t = __ldg(sorted_pair + row) / k;
+  if ((unsigned)t >= (unsigned)T) return;
+  const uint4* src = x + (size_t)t * H8;
+  uint4* dst = x_exp + (size_t)row * H8;
+  for (int i = lane; i < H8; i += 32) dst[i] = __ldg(src + i);
+}
+
+}  // namespace
+
+int routing_chunk_pairs(int P) {
+  int ch = (P + 255) / 256;
+  ch = (ch + 31) / 32 * 32;
+  return ch < 512 ? 512 : ch;
+}
+
+size_t routing_scratch_bytes(int P, int E) {
+  const int CH = routing_chunk_pairs(P);
+  const size_t n_chunks = (size_t)((P + CH - 1) / CH);
+  return 2 * n_chunks * (size_t)E * sizeof(int32_t);
+}
+
+cudaError_t launch_expand_rows(const uint16_t* x, const int32_t* sorted_pair, int P, int k, int H,
+                               uint16_t* x_exp, cudaStream_t stream) {
+  if (P == 0) return cudaSuccess;
+  const int T = P / k;
+  expand_rows_kernel<<<(P + kWarps - 1) / kWarps, kWarps * 32, 0, stream>>>(
+      reinterpret_cast<const uint4*>(x), sorted_pair, P, k, T, H / 8, reinterpret_cast<uint4*>(x_exp));
+  return cudaGetLastError();
+}
+
+cudaError_t launch_init_routing(const int32_t* topk_idx, int P, int E, int k, const uint16_t* x, int H,
+                                uint16_t* x_exp, int32_t* counts, int32_t* offsets, int32_t* sorted_pair,
+                                int32_t* pair_pos, int32_t* scratch, unsigned* status, cudaStream_t stream) {
+  const int CH = routing_chunk_pairs(P);
+  const int n_chunks = (P + CH - 1) / CH;
+  int32_t* hist = scratch;
+  int32_t* base = scratch + (size_t)n_chunks * E;
+  const size_t smem = (size_t)kWarps * E * sizeof(int);
+  const int blocks = (n_chunks + kWarps - 1) / kWarps;
+  cudaError_t err;
+  if (smem > 48 * 1024) {
+    err = cudaFuncSetAttribute(route_hist_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (err != cudaSuccess) return err;
+    err = cudaFuncSetAttribute(route_scatter_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (err != cudaSuccess) return err;
+  }
+  if (n_chunks > 0) {
+    route_hist_kernel<<<blocks, kWarps * 32, smem, stream>>>(topk_idx, P, E, CH, n_chunks, hist, status);
+    if ((err = cudaGetLastError()) != cudaSuccess) return err;
+  }
+  route_scan_kernel<<<1, 1024, 0, stream>>>(hist, base, n_chunks, E, counts, offsets);
+  if ((err = cudaGetLastError()) != cudaSuccess) return err;
+  if (n_chunks > 0) {
+    route_scatter_kernel<<<blocks, kWarps * 32, smem, stream>>>(topk_idx, P, E, CH, n_chunks, base, sorted_pair,
+                                                                pair_pos);
+    if ((err = cudaGetLastError()) != cudaSuccess) return err;
+  }
+  if (x != nullptr && x_exp != nullptr) return launch_expand_rows(x, sorted_pair, P, k, H, x_exp, stream);
+  return cudaSuccess;
+}
+
+}  // namespace moe

@@ -1,0 +1,130 @@
+"""The C-ABI library builds, loads and exports every symbol include/moe.h declares.
+
+No compute call here: only host-side queries and argument validation, which
+returns before anything touches a GPU.
+"""
+import ctypes
+import os
+import re
+import subprocess
+
+import pytest
+
+import moe_inputs as mi
+import moe_expert_layer_fwd_gb300 as moe
+from moe_expert_layer_fwd_gb300 import build as moe_build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "moe.h")
+
+
+@pytest.fixture(scope="module")
+def L():
+    moe_build.build()
+    return moe.lib()
+
+
+def _declared():
+    with open(HEADER) as f:
+        return re.findall(r"^MOE_API [^(]*?\b(moe_\w+)\(", f.read(), flags=re.M)
+
+
+def test_every_declared_symbol_is_exported(L):
+    names = _declared()
+    assert len(names) >= 15
+    out = subprocess.run(["nm", "-D", "--defined-only", moe.LIB_PATH], capture_output=True, text=True, check=True)
+    exported = set(re.findall(r"\bT (moe_\w+)", out.stdout))
+    assert set(names) <= exported, set(names) - exported
+    for n in names:
+        assert hasattr(L, n)
+    # the binding declares a signature for every symbol of the header
+    assert set(names) == set(moe._SIGS)
+
+
+def test_version_and_status_strings(L):
+    assert moe.lib().moe_abi_version() == 100
+    assert moe.status_string(0) == "MOE_OK"
+    assert moe.status_string(-1) == "MOE_ERR_INVALID_ARG"
+    assert moe.status_string(-5) == "MOE_ERR_TIMEOUT"
+    assert moe.status_string(123) == "MOE_ERR_UNKNOWN"
+    assert moe.lib().moe_status_bytes() == 256
+
+
+@pytest.mark.parametrize("name", list(mi.CONFIGS))
+def test_workspace_sizes(L, name):
+    c = mi.CONFIGS[name]
+    d = moe.make_desc(c.T, c.H, c.E, c.k, c.I, c.gate, c.routed_scaling_factor, c.eps, c.n_shared, c.I_s)
+    n = moe.moe_layer_workspace_size(d)
+    P = c.T * c.k
+    # at least x_exp, act, y_perm and the permutation
+    assert n >= P * (2 * c.H + c.I) * 2 + 2 * P * 4
+    offs = moe.moe_layer_workspace_offsets(d)
+    assert offs == sorted(offs) and all(o % 256 == 0 for o in offs)
+    assert L.moe_init_routing_workspace_size(c.T, c.E, c.k) >= 256
+
+
+def test_desc_validation(L):
+    bad = [moe.make_desc(16, 100, 8, 2, 128),      # H % 64
+           moe.make_desc(16, 256, 8, 9, 128),      # k > E
+           moe.make_desc(16, 256, 2000, 2, 128),   # E > 1024
+           moe.make_desc(16, 256, 8, 2, 96),       # I % 64
+           moe.make_desc(-1, 256, 8, 2, 128)]
+    for d in bad:
+        assert L.moe_layer_workspace_size(ctypes.byref(d)) == 0
+    d = moe.make_desc(16, 256, 8, 2, 128, gate=7)
+    assert L.moe_layer_workspace_size(ctypes.byref(d)) == 0
+
+
+def test_gating_validation_returns_before_launch(L):
+    P16 = 16  # an aligned non-null dummy address: never dereferenced since validation fails first
+    assert L.moe_gating_topk(P16, None, 4, 8, 9, 0, 1.0, 1e-20, P16, P16, None) == moe.MOE_ERR_UNSUPPORTED
+    assert L.moe_gating_topk(P16, None, 4, 8, 2, 5, 1.0, 1e-20, P16, P16, None) == moe.MOE_ERR_INVALID_ARG
+    assert L.moe_gating_topk(P16, P16, 4, 8, 2, 0, 1.0, 1e-20, P16, P16, None) == moe.MOE_ERR_INVALID_ARG
+    assert L.moe_gating_topk(None, None, 4, 8, 2, 0, 1.0, 1e-20, P16, P16, None) == moe.MOE_ERR_INVALID_ARG
+    assert L.moe_gating_topk(P16 + 4, None, 4, 8, 2, 0, 1.0, 1e-20, P16, P16, None) == moe.MOE_ERR_INVALID_ARG
+    assert L.moe_gating_topk(P16, None, 4, 0, 1, 0, 1.0, 1e-20, P16, P16, None) == moe.MOE_ERR_INVALID_ARG
+    # empty input: nothing to do
+    assert L.moe_gating_topk(None, None, 0, 8, 2, 0, 1.0, 1e-20, None, None, None) == moe.MOE_OK
+
+
+def test_routing_and_gemm_validation(L):
+    P16 = 16
+    small = L.moe_init_routing_workspace_size(4, 8, 2)
+    assert L.moe_init_routing(P16, 4, 8, 2, None, 0, None, P16, P16, P16, P16, P16, small - 1, None) == \
+        moe.MOE_ERR_WORKSPACE
+    assert L.moe_init_routing(P16, 4, 8, 2, P16, 0, None, P16, P16, P16, P16, P16, small, None) == \
+        moe.MOE_ERR_INVALID_ARG  # x without x_exp
+    assert L.moe_grouped_gemm_swiglu(P16, P16, P16, 8, 32, 100, 128, P16, P16, 256, None) == moe.MOE_ERR_UNSUPPORTED
+    assert L.moe_grouped_gemm_swiglu(P16, P16, P16, 8, 32, 256, 128, P16, P16, 255, None) == moe.MOE_ERR_WORKSPACE
+    assert L.moe_grouped_gemm(P16, P16, P16, P16, None, 8, 32, 256, 128, P16, P16, 256, None) == \
+        moe.MOE_ERR_INVALID_ARG  # topk_w without sorted_pair
+    assert L.moe_grouped_gemm(P16, P16, P16, None, None, 8, 0, 256, 128, P16, P16, 256, None) == moe.MOE_OK
+    assert L.moe_finalize_routing(P16, P16, None, 4, 33, 256, P16, None) == moe.MOE_ERR_UNSUPPORTED
+
+
+def test_layer_forward_validation(L):
+    d = moe.make_desc(16, 256, 8, 2, 128)
+    need = L.moe_layer_workspace_size(ctypes.byref(d))
+    P16 = 16
+    args = [P16] * 11
+    args[2] = None  # no bias (softmax)
+    assert L.moe_layer_forward(ctypes.byref(d), *args, P16, need - 1, None) == moe.MOE_ERR_WORKSPACE
+    a = list(args)
+    a[2] = P16  # bias given with softmax gating
+    assert L.moe_layer_forward(ctypes.byref(d), *a, P16, need, None) == moe.MOE_ERR_INVALID_ARG
+    a = list(args)
+    a[2] = None
+    a[3] = None  # w13 missing
+    assert L.moe_layer_forward(ctypes.byref(d), *a, P16, need, None) == moe.MOE_ERR_INVALID_ARG
+    ds = moe.make_desc(16, 256, 8, 2, 128, gate="sigmoid", n_shared=1, I_s=128)
+    need_s = L.moe_layer_workspace_size(ctypes.byref(ds))
+    a = list(args)
+    a[5] = None  # shared expert weights missing
+    assert L.moe_layer_forward(ctypes.byref(ds), *a, P16, need_s, None) == moe.MOE_ERR_INVALID_ARG
+
+
+def test_missing_library_fails_loudly(tmp_path, monkeypatch):
+    monkeypatch.setattr(moe, "LIB_PATH", str(tmp_path / "nope.so"))
+    monkeypatch.setattr(moe, "_lib", None)
+    with pytest.raises(RuntimeError, match="no CPU fallback"):
+        moe.lib()

@@ -1,0 +1,182 @@
+"""GPU parity: every step of the CUDA path, through the C ABI, against the oracle.
+
+Routing (expert choice, counts, offsets, permutation and its inverse, gathered
+rows) must be bit-exact; floating-point outputs must meet
+max|gpu-oracle|/max|oracle| <= 2e-2 and mean|gpu-oracle|/mean|oracle| <= 5e-3
+(single bf16 roundings are also checked element by element).
+"""
+import numpy as np
+import pytest
+
+import moe_inputs as mi
+import oracle
+from gpu_util import (assert_bf16_rounding_close, assert_close, dev, dev_bf16, host, host_bf16_f64)
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def moe():
+    from moe_expert_layer_fwd_gb300 import build
+    build.build()
+    import moe_expert_layer_fwd_gb300 as m
+    return m
+
+
+def _torch():
+    import torch
+    return torch
+
+
+# ---------------------------------------------------------------- a1 gating
+GATING_CASES = [
+    ("tiny", {}), ("qwen3_decode", {}), ("hy3_decode", {}), ("hy3_prefill", {}), ("long_prefill", {}),
+    ("tiny", dict(T=1, E=1, k=1)),
+    ("tiny", dict(T=37, E=1024, k=32)),
+    ("hy3_decode", dict(T=33, E=200, k=8, bias_std=0.0)),  # sigmoid without bias: many exact key ties
+]
+
+
+@pytest.mark.parametrize("name,over", GATING_CASES)
+def test_gating_topk_parity(moe, name, over):
+    cfg = mi.CONFIGS[name].with_(**over)
+    inp = mi.generate(cfg, weights=False)
+    w_ref, idx_ref = oracle.gating_topk(inp.logits, cfg.k, cfg.gate, inp.bias, cfg.routed_scaling_factor, cfg.eps)
+    w, idx = moe.moe_gating_topk(dev(inp.logits), cfg.k, cfg.gate, dev(inp.bias) if inp.bias is not None else None,
+                                 cfg.routed_scaling_factor, cfg.eps)
+    _torch().cuda.synchronize()
+    assert (host(idx) == idx_ref).all(), "expert choice differs"
+    np.testing.assert_allclose(host(w), w_ref, rtol=2e-6, atol=1e-7)
+
+
+def test_gating_ties_on_coarse_grid(moe):
+    rng = np.random.default_rng(0)
+    logits = (np.round(rng.normal(size=(300, 64)) * 4) / 4).astype(np.float32)
+    logits[:10] = 0.0
+    logits[10:20, :7] = -0.0
+    for gate in ("softmax", "sigmoid"):
+        w_ref, idx_ref = oracle.gating_topk(logits, 6, gate, None, 2.826 if gate == "sigmoid" else 1.0)
+        w, idx = moe.moe_gating_topk(dev(logits), 6, gate, None, 2.826 if gate == "sigmoid" else 1.0)
+        assert (host(idx) == idx_ref).all()
+        np.testing.assert_allclose(host(w), w_ref, rtol=2e-6, atol=1e-7)
+
+
+# ---------------------------------------------------------------- a2 routing
+ROUTING_CASES = [(16, 8, 2, 256), (64, 128, 8, 4096), (16, 192, 8, 4096), (4096, 192, 8, 64), (16384, 128, 8, 64),
+                 (1, 1, 1, 64), (3, 1024, 32, 128), (20000, 7, 3, 64)]
+
+
+@pytest.mark.parametrize("T,E,k,H", ROUTING_CASES)
+def test_init_routing_parity(moe, T, E, k, H):
+    rng = np.random.default_rng(T + E + k)
+    # skewed choice: some experts hot, some never chosen
+    p = rng.dirichlet(np.full(E, 0.3))
+    idx = np.stack([rng.choice(E, size=k, replace=False, p=p) for _ in range(T)]).astype(np.int32) \
+        if T * E <= 2_000_000 else rng.integers(0, E, size=(T, k)).astype(np.int32)
+    x = mi.normal_bf16(1, 1, (T, H))
+    counts, offsets, sp, pp = oracle.init_routing(idx, E)
+    o = moe.moe_init_routing(dev(idx), E, dev_bf16(x))
+    _torch().cuda.synchronize()
+    assert (host(o["counts"]) == counts).all()
+    assert (host(o["offsets"]) == offsets).all()
+    assert (host(o["sorted_pair"]) == sp).all()
+    assert (host(o["pair_pos"]) == pp).all()
+    xe = host(o["x_exp"].view(_torch().int16)).view(np.uint16)
+    assert (xe == oracle.expand_rows(x, sp, k)).all()
+    assert moe.moe_get_device_status(o["ws"]) == 0
+
+
+def test_init_routing_all_pairs_one_expert(moe):
+    T, E, k = 5000, 16, 1
+    idx = np.full((T, k), 11, np.int32)
+    counts, offsets, sp, pp = oracle.init_routing(idx, E)
+    o = moe.moe_init_routing(dev(idx), E)
+    assert (host(o["counts"]) == counts).all() and (host(o["sorted_pair"]) == sp).all()
+    assert (host(o["offsets"]) == offsets).all() and (host(o["pair_pos"]) == pp).all()
+
+
+def test_init_routing_flags_bad_index(moe):
+    idx = np.array([[0, 1], [2, 9]], np.int32)  # 9 >= E
+    o = moe.moe_init_routing(dev(idx), 4)
+    assert moe.moe_get_device_status(o["ws"]) == moe.MOE_ERR_DEVICE_CHECK
+
+
+# ---------------------------------------------------------------- a3 / a4 grouped GEMMs
+def _segments(counts):
+    return np.concatenate([[0], np.cumsum(counts)]).astype(np.int32)
+
+
+GEMM_CASES = [
+    # (counts per expert, H, I): narrow instance (few rows per expert) ...
+    ([3, 0, 1, 7, 16, 17, 0, 32], 256, 128),
+    ([1] * 40 + [0] * 24, 512, 192),
+    ([5, 2, 0, 9], 4096, 1536),
+    ([4, 0, 20, 3], 192, 64),
+    # ... and the 256-wide instance (many rows per expert, ragged tails)
+    ([300, 0, 1, 255, 256, 257, 40, 600], 256, 128),
+    ([513, 64, 0, 1000], 1024, 256),
+]
+
+
+@pytest.mark.parametrize("counts,H,I", GEMM_CASES)
+def test_grouped_gemm_swiglu_parity(moe, counts, H, I):
+    E = len(counts)
+    off = _segments(counts)
+    M = int(off[-1])
+    rng_seed = M + H + I
+    x = mi.normal_bf16(rng_seed, 1, (M, H))
+    w13 = mi.normal_bf16(rng_seed, 2, (E, 2 * I, H), 0.0, 0.02)
+    ref = oracle.grouped_gemm_swiglu(x, w13, off)
+    act = moe.moe_grouped_gemm_swiglu(dev_bf16(x), dev_bf16(w13), dev(off))
+    got = host_bf16_f64(act)
+    assert_close(got, ref, "act")
+    assert_bf16_rounding_close(got, ref, "act")
+
+
+@pytest.mark.parametrize("counts,H,I", GEMM_CASES)
+def test_grouped_gemm_down_parity(moe, counts, H, I):
+    E = len(counts)
+    off = _segments(counts)
+    M = int(off[-1])
+    seed = 7 + M + H
+    a = mi.normal_bf16(seed, 1, (M, I), 0.0, 0.5)
+    w2 = mi.normal_bf16(seed, 3, (E, H, I), 0.0, 0.02)
+    T = M
+    topk_w = (np.abs(mi.normal_f32(seed, 5, (T, 1))) + 0.1).astype(np.float32)
+    sorted_pair = np.random.default_rng(seed).permutation(M).astype(np.int32)
+    ref = oracle.grouped_gemm(a, w2, off, topk_w.reshape(-1)[sorted_pair])
+    out = moe.moe_grouped_gemm(dev_bf16(a), dev_bf16(w2), dev(off), dev(topk_w), dev(sorted_pair))
+    got = host_bf16_f64(out)
+    assert_close(got, ref, "y_perm")
+    assert_bf16_rounding_close(got, ref, "y_perm")
+    # without routing weights
+    ref1 = oracle.grouped_gemm(a, w2, off)
+    got1 = host_bf16_f64(moe.moe_grouped_gemm(dev_bf16(a), dev_bf16(w2), dev(off)))
+    assert_bf16_rounding_close(got1, ref1, "plain")
+
+
+def test_grouped_gemm_rejects_inconsistent_offsets(moe):
+    torch = _torch()
+    off = np.array([0, 5, 3, 8], np.int32)  # decreasing: invalid
+    x = mi.normal_bf16(0, 1, (8, 256))
+    w13 = mi.normal_bf16(0, 2, (3, 256, 256), 0.0, 0.02)
+    ws = torch.zeros(256, dtype=torch.uint8, device="cuda")
+    act = torch.full((8, 128), 7.0, dtype=torch.bfloat16, device="cuda")
+    moe.moe_grouped_gemm_swiglu(dev_bf16(x), dev_bf16(w13), dev(off), act=act, ws=ws)
+    assert moe.moe_get_device_status(ws) == moe.MOE_ERR_DEVICE_CHECK
+    assert (act.float() == 7.0).all()  # nothing written
+
+
+# ---------------------------------------------------------------- a6 finalize
+@pytest.mark.parametrize("T,k,H,shared", [(16, 2, 256, False), (64, 8, 4096, False), (16, 8, 4096, True),
+                                          (1000, 3, 192, True), (1, 1, 64, False)])
+def test_finalize_parity(moe, T, k, H, shared):
+    P = T * k
+    y_perm = mi.normal_bf16(T, 1, (P, H))
+    pair_pos = np.random.default_rng(T).permutation(P).astype(np.int32)
+    s = mi.normal_bf16(T, 2, (T, H)) if shared else None
+    ref = oracle.finalize_routing(y_perm, pair_pos, T, k, s)
+    y = moe.moe_finalize_routing(dev_bf16(y_perm), dev(pair_pos), T, k, dev_bf16(s) if shared else None)
+    got = host_bf16_f64(y)
+    assert_close(got, ref, "y")
+    assert_bf16_rounding_close(got, ref, "y")
