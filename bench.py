@@ -61,6 +61,8 @@ def _args(argv=None):
     ap.add_argument("--sample-tokens", type=int, default=8)
     ap.add_argument("--profile-steps", action="store_true",
                     help="plain moe_layer_forward loop only (for ncu launch lists)")
+    ap.add_argument("--override", default="",
+                    help="shape overrides of the workload for small profiling captures, e.g. E=32,T=16")
     a = ap.parse_args(argv)
     if a.warmup < 3:
         ap.error("--warmup must be >= 3")
@@ -195,12 +197,24 @@ def _traffic(workload, kernel):
 
 
 # ------------------------------------------------------------------ CPU oracle timing
+def workload(args):
+    import moe_inputs as mi
+    cfg = mi.CONFIGS[args.workload]
+    if args.override:
+        kw = {}
+        for item in args.override.split(","):
+            key, val = item.split("=")
+            kw[key.strip()] = type(getattr(cfg, key.strip()))(val)
+        cfg = cfg.with_(**kw)
+    return cfg
+
+
 def cpu_baseline_child(args):
     """Runs in a subprocess with the BLAS thread count fixed: times the oracle on a token sample."""
     import numpy as np
     import moe_inputs as mi
     import oracle
-    cfg = mi.CONFIGS[args.workload]
+    cfg = workload(args)
     inp = mi.generate(cfg)
     n = min(args.sample_tokens, cfg.T)
     toks = np.arange(n)
@@ -217,7 +231,7 @@ def cpu_baseline(args):
     for k in ("RANK", "WORLD_SIZE", "LOCAL_RANK", "MASTER_ADDR", "MASTER_PORT"):
         env.pop(k, None)
     cmd = [sys.executable, os.path.join(ROOT, "bench.py"), "--cpu-baseline-child", "--workload", args.workload,
-           "--sample-tokens", str(args.sample_tokens)]
+           "--sample-tokens", str(args.sample_tokens), "--override", args.override]
     r = subprocess.run(cmd, env=env, capture_output=True, text=True, timeout=900)
     if r.returncode != 0:
         return {"value": None, "unit": "tokens/s", "cores": cores, "kind": "oracle",
@@ -235,7 +249,7 @@ def run_reference(args, rank, world):
     import numpy as np
     import moe_inputs as mi
     import oracle
-    cfg = mi.CONFIGS[args.workload]
+    cfg = workload(args)
     inp = mi.generate(cfg)
     cores = len(os.sched_getaffinity(0))
 
@@ -265,7 +279,9 @@ def run_reference(args, rank, world):
 
 
 def _config(cfg, world):
-    return {"workload": cfg.name, "T": cfg.T, "H": cfg.H, "E": cfg.E, "k": cfg.k, "I": cfg.I, "gate": cfg.gate,
+    import moe_inputs as mi
+    name = cfg.name if cfg == mi.CONFIGS.get(cfg.name) else cfg.name + " (overridden shape)"
+    return {"workload": name, "T": cfg.T, "H": cfg.H, "E": cfg.E, "k": cfg.k, "I": cfg.I, "gate": cfg.gate,
             "routed_scaling_factor": cfg.routed_scaling_factor, "n_shared": cfg.n_shared, "I_s": cfg.I_s,
             "zipf_s": cfg.zipf_s, "global_batch": cfg.T * world,
             "l2": "inputs larger than L2 (the active expert weights read each step exceed 129 MB)",
@@ -285,7 +301,7 @@ def run_gb300(args, rank, world, local):
         raise SystemExit("bench.py needs a CUDA GPU for --impl gb300")
     torch.cuda.set_device(local)
     moe_build.build()
-    cfg = mi.CONFIGS[args.workload]
+    cfg = workload(args)
     inp = mi.generate(cfg)
 
     def d16(u):
