@@ -144,6 +144,31 @@ MOE_API int moe_init_routing(const int32_t* topk_idx, int T, int E, int k, const
                      size_t ws_bytes, void* stream);
 
 /*
+ * Init-routing without a workspace, for callers that cannot allocate device
+ * memory (code running inside an allocator or memory-pool callback, runtimes
+ * whose device memory is entirely pre-reserved by someone else, or host
+ * threads that must not take the allocator's locks).  The pages have no
+ * counterpart of this entry point: it is a deployment convenience.
+ *
+ * Same arguments, outputs and results as moe_init_routing, minus the
+ * workspace.  Its scratch is a fixed 1 MiB device array inside the library
+ * (held by every GPU that loads the library until the process exits), so the
+ * problem must satisfy 2 * n_chunks * E * 4 <= 1 MiB with n_chunks =
+ * ceil(T*k / max(512, ceil(T*k/256) rounded up to 32)) <= 256 -- so any E <= 512
+ * at any T*k, and T*k <= 65536 at E = 1024; larger problems return
+ * MOE_ERR_UNSUPPORTED and launch nothing.  Out-of-range expert indices are
+ * skipped without a status report.  The call allocates nothing.
+ *  - Every call on a device shares the array.  Each call overwrites all the
+ *    scratch it reads, so nothing has to be cleared between calls, but calls
+ *    whose kernels may overlap on the GPU (different streams or threads) race.
+ *  - The first call on a device resolves the array's device address with that
+ *    device current; make it before any stream capture starts.
+ */
+MOE_API int moe_init_routing_static_scratch(const int32_t* topk_idx, int T, int E, int k, const uint16_t* x, int H,
+                                            uint16_t* x_exp, int32_t* counts, int32_t* offsets, int32_t* sorted_pair,
+                                            int32_t* pair_pos, void* stream);
+
+/*
  * a3. Grouped gate/up GEMM with fused SwiGLU.  [Q3] "MoE TP optimisation:
  * computation decomposition" (w13 = [gate_proj; up_proj]; SwiGLU splits the
  * last axis in two halves and returns SiLU(x[0]) * x[1]) and "GMM enablement"

@@ -59,6 +59,10 @@ _SIGS = {
                                         ctypes.c_int, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
                                         ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_size_t,
                                         ctypes.c_void_p]),
+    "moe_init_routing_static_scratch": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                                                       ctypes.c_void_p, ctypes.c_int, ctypes.c_void_p,
+                                                       ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
+                                                       ctypes.c_void_p, ctypes.c_void_p]),
     "moe_grouped_gemm_workspace_size": (ctypes.c_size_t, []),
     "moe_grouped_gemm_swiglu": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int,
                                                ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_void_p,
@@ -171,6 +175,29 @@ def moe_init_routing(topk_idx, E: int, x=None, ws=None, out: Optional[dict] = No
                                   _ptr(o["offsets"]), _ptr(o["sorted_pair"]), _ptr(o["pair_pos"]), _ptr(ws),
                                   ws.numel(), _stream(stream)), "moe_init_routing")
     o["ws"] = ws
+    return o
+
+
+def moe_init_routing_static_scratch(topk_idx, E: int, x=None, out: Optional[dict] = None, stream=None) -> dict:
+    """a2 without a workspace (scratch in a fixed device array inside the library; see include/moe.h).
+    Only the output tensors passed in `out` are used as given; missing ones are created here."""
+    torch = _torch()
+    T, k = topk_idx.shape
+    P = T * k
+    dev = topk_idx.device
+    o = dict(out or {})
+    o.setdefault("counts", torch.empty(E, dtype=torch.int32, device=dev))
+    o.setdefault("offsets", torch.empty(E + 1, dtype=torch.int32, device=dev))
+    o.setdefault("sorted_pair", torch.empty(P, dtype=torch.int32, device=dev))
+    o.setdefault("pair_pos", torch.empty(P, dtype=torch.int32, device=dev))
+    H = 0
+    if x is not None:
+        H = x.shape[1]
+        o.setdefault("x_exp", torch.empty((P, H), dtype=x.dtype, device=dev))
+    _check(lib().moe_init_routing_static_scratch(_ptr(topk_idx), T, E, k, _ptr(x), H, _ptr(o.get("x_exp")),
+                                                 _ptr(o["counts"]), _ptr(o["offsets"]), _ptr(o["sorted_pair"]),
+                                                 _ptr(o["pair_pos"]), _stream(stream)),
+           "moe_init_routing_static_scratch")
     return o
 
 
