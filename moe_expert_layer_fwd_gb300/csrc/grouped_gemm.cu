@@ -22,15 +22,20 @@
 //   rows.  Tiles of one expert are numbered f-major so that the token tiles
 //   that reuse a weight tile run next to each other (L2 reuse).
 //
+// Few, large TMA boxes: the per-SM rate of TMA box operations, not their
+// bytes, limits a stream of small boxes, so each stage moves the weight rows
+// in 128-row boxes (16 KB) and the token rows in BBOX-row boxes.
+//
 // Warp roles (192 threads, 1 CTA/SM, static round-robin tile schedule):
-//   warp 0      TMA producer: per stage 8 boxes of 16 weight rows + up to 16
-//               boxes of 16 token rows, one lane per box.
+//   warp 0      TMA producer: per stage one 128-row weight box (two in mode 0:
+//               the gate rows and the matching up rows) + ceil(rows/BBOX)
+//               token boxes, one lane per box.
 //   warp 1      TMEM allocator + single-thread tcgen05.mma issuer
 //               (M=128, N=rows, K=16 x 4 per stage), double-buffered accumulator.
+//               Mode 0 keeps two accumulators, gate and up, so that TMEM lane l
+//               of both holds the same output feature.
 //   warps 2..5  epilogue: tcgen05.ld 32 lanes x 16 columns, then
-//               mode 0 (w13): SwiGLU.  The w13 tile is loaded so that in each
-//                 32-row quarter, rows 0-15 are gate features and rows 16-31 the
-//                 matching up features; a shfl_xor(16) pairs them in registers.
+//               mode 0 (w13): SwiGLU = SiLU(gate) * up, in fp32, per element.
 //               mode 1 (down): multiply by the routing weight of the row.
 // Every wait is bounded (default 2 s); on expiry the CTA raises an abort flag,
 // records DEV_ERR_TIMEOUT, drains its in-flight copies and MMAs and frees TMEM.
@@ -46,9 +51,9 @@ namespace {
 
 constexpr int kBM = 128;                     // weight rows per tile (UMMA M)
 constexpr int kBK = 64;                      // K per stage: one 128-byte swizzle row of bf16
-constexpr int kBoxRows = 16;                 // rows per TMA box
-constexpr int kBoxBytes = kBoxRows * kBK * 2;  // 2 KB
-constexpr int kABytes = kBM * kBK * 2;       // 16 KB
+constexpr int kRowBytes = kBK * 2;           // 128 B per operand row per stage
+constexpr int kABox = kBM * kRowBytes;       // one 128-row weight box: 16 KB
+constexpr int kMaxDynSmem = 232448;          // 227 KB per CTA
 constexpr int kThreads = 192;
 constexpr unsigned long long kTimeoutNs = 2000000000ull;
 
@@ -56,9 +61,10 @@ struct GemmParams {
   const int32_t* offsets;
   int E, M, K;
   int n_out, n_ftiles, half;        // routed: rows per expert, feature tiles, up-half row offset (mode 0)
+  int n_feat;                       // output features per row (I in mode 0, N in mode 1)
   uint16_t* out;
   int ld_out;
-  int has_shared, T_s, n_out_s, n_ftiles_s, half_s;
+  int has_shared, T_s, n_out_s, n_ftiles_s, half_s, n_feat_s;
   uint16_t* s_out;
   int ld_out_s;
   int NT;                           // token rows per tile (multiple of 16)
@@ -68,15 +74,23 @@ struct GemmParams {
   unsigned long long timeout_ns;
 };
 
-template <int NTMAX, int STAGES>
+template <int NTMAX, int STAGES, int MODE, int BBOX>
 struct Layout {
-  static constexpr int kBBytes = NTMAX * kBK * 2;
-  static constexpr int kStageBytes = kABytes + kBBytes;  // multiple of 1024
+  static constexpr int kAParts = MODE == 0 ? 2 : 1;            // gate + up boxes in mode 0
+  static constexpr int kABytes = kAParts * kABox;
+  static constexpr int kBBytes = NTMAX * kRowBytes;
+  static constexpr int kStageBytes = kABytes + kBBytes;        // multiple of 1024
   static constexpr int kBarOff = STAGES * kStageBytes;
   static constexpr int kNumBars = 2 * STAGES + 5;
   static constexpr int kMiscOff = kBarOff + kNumBars * 8;
-  static constexpr int kTabOff = kMiscOff + 16;
-  static constexpr uint32_t kTmemCols = (2 * NTMAX <= 32) ? 32 : (2 * NTMAX <= 64 ? 64 : (2 * NTMAX <= 128 ? 128 : (2 * NTMAX <= 256 ? 256 : 512)));
+  static constexpr int kScaleOff = kMiscOff + 16;                // mode 1: per-epilogue-warp row scales
+  static constexpr int kTabOff = kScaleOff + (MODE == 1 ? 4 * NTMAX * 4 : 0);
+  static constexpr int kAccCols = kAParts * NTMAX;             // TMEM columns of one accumulator buffer
+  static constexpr uint32_t kTmemCols = (2 * kAccCols <= 32) ? 32 : (2 * kAccCols <= 64 ? 64 : (2 * kAccCols <= 128 ? 128 : (2 * kAccCols <= 256 ? 256 : 512)));
+  static_assert(2 * kAccCols <= 512, "accumulators exceed TMEM");
+  static_assert(NTMAX % BBOX == 0 && NTMAX / BBOX <= 30, "token boxes");
+  static_assert(kStageBytes % 1024 == 0, "stage alignment");
+  static_assert(1024 + kTabOff + 2 * 1025 * 4 <= kMaxDynSmem, "shared memory");
   static size_t bytes(int E) { return 1024 + kTabOff + 2 * (size_t)(E + 1) * 4; }
 };
 
@@ -115,12 +129,12 @@ __device__ __forceinline__ Tile decode_tile(int tile, int routed_total, const in
   return t;
 }
 
-template <int NTMAX, int STAGES, int MODE>
+template <int NTMAX, int STAGES, int MODE, int BBOX>
 __global__ void __launch_bounds__(kThreads, 1)
     grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                         const __grid_constant__ CUtensorMap tmAs, const __grid_constant__ CUtensorMap tmBs,
                         const GemmParams p) {
-  using L = Layout<NTMAX, STAGES>;
+  using L = Layout<NTMAX, STAGES, MODE, BBOX>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + L::kBarOff);
@@ -131,6 +145,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::kMiscOff);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::kMiscOff + 4);
   volatile int* cfg_bad = reinterpret_cast<volatile int*>(smem + L::kMiscOff + 8);
+  float* s_scale = reinterpret_cast<float*>(smem + L::kScaleOff);
   int* s_off = reinterpret_cast<int*>(smem + L::kTabOff);
   int* s_tt = s_off + (p.E + 1);
 
@@ -212,14 +227,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       const Tile t = decode_tile(tile, routed_total, s_off, s_tt, p);
       const CUtensorMap* mA = t.shared ? &tmAs : &tmA;
       const CUtensorMap* mB = t.shared ? &tmBs : &tmB;
-      const int nbox = (t.rows + kBoxRows - 1) / kBoxRows;
-      const int a_row0 = t.shared ? 0 : t.e * p.n_out;
-      const int half = t.shared ? p.half_s : p.half;
-      int a_row;
-      if (MODE == 0)  // box i: quarter i/2, gate (i even) or up (i odd) half, 16 features
-        a_row = a_row0 + (lane & 1) * half + t.f * 64 + (lane >> 1) * kBoxRows;
-      else
-        a_row = a_row0 + t.f * kBM + lane * kBoxRows;
+      const int nbox = (t.rows + BBOX - 1) / BBOX;
+      // weight box `lane` (< kAParts): mode 0 lane 0 = gate rows, lane 1 = the matching up rows
+      const int a_row = (t.shared ? 0 : t.e * p.n_out) + (lane == 1 ? (t.shared ? p.half_s : p.half) : 0) +
+                        t.f * kBM;
       for (int kb = 0; kb < KB; ++kb) {
         bool w = (lane == 0) ? mbar_wait_bounded(&empty[stage], phase ^ 1u, abort_flag, p.timeout_ns, p.status)
                              : false;
@@ -228,15 +239,15 @@ __global__ void __launch_bounds__(kThreads, 1)
           ok = false;
           break;
         }
-        if (lane == 0) mbar_arrive_expect_tx(&full[stage], kABytes + nbox * kBoxBytes);
+        if (lane == 0) mbar_arrive_expect_tx(&full[stage], L::kABytes + nbox * BBOX * kRowBytes);
         __syncwarp();
         uint8_t* sA = smem + stage * L::kStageBytes;
-        uint8_t* sB = sA + kABytes;
-        if (lane < 8) {
-          tma_load_2d(sA + lane * kBoxBytes, mA, kb * kBK, a_row, &full[stage], pol_w);
-        } else if (lane < 8 + nbox) {
-          const int j = lane - 8;
-          tma_load_2d(sB + j * kBoxBytes, mB, kb * kBK, t.row_base + j * kBoxRows, &full[stage], pol_x);
+        uint8_t* sB = sA + L::kABytes;
+        if (lane < L::kAParts) {
+          tma_load_2d(sA + lane * kABox, mA, kb * kBK, a_row, &full[stage], pol_w);
+        } else if (lane >= 2 && lane < 2 + nbox) {
+          const int j = lane - 2;
+          tma_load_2d(sB + j * BBOX * kRowBytes, mB, kb * kBK, t.row_base + j * BBOX, &full[stage], pol_x);
         }
         __syncwarp();
         ++issued;
@@ -267,7 +278,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t aph = (uint32_t)(it >> 1) & 1u;
         if (!mbar_wait_bounded(&tempty[buf], aph ^ 1u, abort_flag, p.timeout_ns, p.status)) break;
         tc_fence_after();
-        const uint32_t d = tmem_base + (uint32_t)(buf * NTMAX);
+        const uint32_t d = tmem_base + (uint32_t)(buf * L::kAccCols);
         const int nmma = (t.rows + 15) & ~15;
         const uint32_t idesc = umma_idesc_bf16(kBM, nmma);
         for (int kb = 0; kb < KB; ++kb) {
@@ -277,10 +288,14 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           tc_fence_after();
           const uint32_t a = smem_u32(smem + stage * L::kStageBytes);
-          const uint32_t b = a + kABytes;
+          const uint32_t b = a + L::kABytes;
 #pragma unroll
-          for (int kk = 0; kk < kBK / 16; ++kk)
-            umma_bf16(d, umma_desc_sw128(a + kk * 32), umma_desc_sw128(b + kk * 32), idesc, (kb | kk) != 0);
+          for (int kk = 0; kk < kBK / 16; ++kk) {
+            const uint64_t bd = umma_desc_sw128(b + kk * 32);
+            umma_bf16(d, umma_desc_sw128(a + kk * 32), bd, idesc, (kb | kk) != 0);
+            if (MODE == 0)  // up rows into the second accumulator, same token columns
+              umma_bf16(d + NTMAX, umma_desc_sw128(a + kABox + kk * 32), bd, idesc, (kb | kk) != 0);
+          }
           umma_commit(&empty[stage]);
           if (++stage == STAGES) {
             stage = 0;
@@ -303,51 +318,55 @@ __global__ void __launch_bounds__(kThreads, 1)
       const Tile t = decode_tile(tile, routed_total, s_off, s_tt, p);
       const int buf = it & 1;
       const uint32_t aph = (uint32_t)(it >> 1) & 1u;
+      // Mode 1: fetch the routing weights of the tile's rows before waiting for
+      // the accumulator, so their latency overlaps the mainloop.
+      float* wsc = s_scale + (warp - 2) * NTMAX;
+      const bool scale = MODE == 1 && !t.shared && p.topk_w != nullptr;
+      if (scale) {
+        int pr[NTMAX / 32];
+#pragma unroll
+        for (int r = 0; r < NTMAX / 32; ++r) {
+          const int col = r * 32 + lane;
+          pr[r] = col < t.rows ? __ldg(p.sorted_pair + t.row_base + col) : -1;
+        }
+#pragma unroll
+        for (int r = 0; r < NTMAX / 32; ++r) wsc[r * 32 + lane] = pr[r] >= 0 ? __ldg(p.topk_w + pr[r]) : 0.0f;
+        __syncwarp();
+      }
       bool w = (lane == 0) ? mbar_wait_bounded(&tfull[buf], aph, abort_flag, p.timeout_ns, p.status) : false;
       w = __shfl_sync(0xffffffffu, w, 0);
       if (!w) break;
       tc_fence_after();
-      const uint32_t tb = tmem_base + ((uint32_t)(qw * 32) << 16) + (uint32_t)(buf * NTMAX);
+      const uint32_t tb = tmem_base + ((uint32_t)(qw * 32) << 16) + (uint32_t)(buf * L::kAccCols);
       const int nch = (t.rows + 15) >> 4;
       uint16_t* out = t.shared ? p.s_out : p.out;
       const size_t ld = (size_t)(t.shared ? p.ld_out_s : p.ld_out);
+      const int feat = t.f * kBM + qw * 32 + lane;  // this thread's output feature (TMEM lane)
+      const bool feat_ok = feat < (t.shared ? p.n_feat_s : p.n_feat);
       if (MODE == 0) {
-        const bool is_gate = lane < 16;
-        const int feat = t.f * 64 + qw * 16 + (lane & 15);
         for (int c = 0; c < nch; ++c) {
-          float v[16];
-          tmem_ld16(tb + (uint32_t)(c * 16), v);
-          const int col0 = c * 16 + (is_gate ? 0 : 8);
+          float g[16], u[16];
+          tmem_ld16(tb + (uint32_t)(c * 16), g);
+          tmem_ld16(tb + (uint32_t)(NTMAX + c * 16), u);
 #pragma unroll
-          for (int i = 0; i < 8; ++i) {
-            const float send = is_gate ? v[8 + i] : v[i];
-            const float recv = __shfl_xor_sync(0xffffffffu, send, 16);
-            const float g = is_gate ? v[i] : recv;
-            const float u = is_gate ? recv : v[8 + i];
-            const float a = g / (1.0f + expf(-g)) * u;
-            const int col = col0 + i;
-            if (col < t.rows) out[(size_t)(t.row_base + col) * ld + feat] = f32_to_bf16_rne(a);
+          for (int i = 0; i < 16; ++i) {
+            const int col = c * 16 + i;
+            const float a = g[i] / (1.0f + expf(-g[i])) * u[i];
+            if (col < t.rows && feat_ok) out[(size_t)(t.row_base + col) * ld + feat] = f32_to_bf16_rne(a);
           }
         }
       } else {
-        const int feat = t.f * kBM + qw * 32 + lane;
-        const int n_out = t.shared ? p.n_out_s : p.n_out;
-        const bool scale = !t.shared && p.topk_w != nullptr;
         for (int c = 0; c < nch; ++c) {
           float v[16];
           tmem_ld16(tb + (uint32_t)(c * 16), v);
-          float sc = 1.0f;
-          if (scale) {
-            const int col = c * 16 + (lane & 15);
-            if (col < t.rows) sc = __ldg(p.topk_w + __ldg(p.sorted_pair + t.row_base + col));
-          }
 #pragma unroll
           for (int i = 0; i < 16; ++i) {
-            const float s = scale ? __shfl_sync(0xffffffffu, sc, i) : 1.0f;
             const int col = c * 16 + i;
-            if (col < t.rows && feat < n_out) out[(size_t)(t.row_base + col) * ld + feat] = f32_to_bf16_rne(v[i] * s);
+            const float sv = scale ? wsc[col] : 1.0f;
+            if (col < t.rows && feat_ok) out[(size_t)(t.row_base + col) * ld + feat] = f32_to_bf16_rne(v[i] * sv);
           }
         }
+        __syncwarp();  // the next tile rewrites this warp's scales
       }
       tc_fence_before();
       __syncwarp();
@@ -378,14 +397,14 @@ PFN_cuTensorMapEncodeTiled_v12000 get_encode_fn() {
   return fn;
 }
 
-// Row-major bf16 matrix [rows, K] as a 2-D tensor map with 64 x 16 boxes and
-// the 128-byte swizzle; rows past the end read as zeros.
-bool make_map(CUtensorMap* m, const void* base, int K, long long rows) {
+// Row-major bf16 matrix [rows, K] as a 2-D tensor map with 64 x box_rows boxes
+// and the 128-byte swizzle; rows past the end read as zeros.
+bool make_map(CUtensorMap* m, const void* base, int K, long long rows, int box_rows) {
   auto fn = get_encode_fn();
   if (!fn) return false;
   cuuint64_t dims[2] = {(cuuint64_t)K, (cuuint64_t)rows};
   cuuint64_t strides[1] = {(cuuint64_t)K * 2};
-  cuuint32_t box[2] = {(cuuint32_t)kBK, (cuuint32_t)kBoxRows};
+  cuuint32_t box[2] = {(cuuint32_t)kBK, (cuuint32_t)box_rows};
   cuuint32_t estr[2] = {1, 1};
   CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
@@ -400,15 +419,33 @@ int num_sms() {
   return n > 0 ? n : 1;
 }
 
-template <int NTMAX, int STAGES, int MODE>
-cudaError_t launch_instance(const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& as,
-                            const CUtensorMap& bs, const GemmParams& gp, cudaStream_t stream) {
-  using L = Layout<NTMAX, STAGES>;
-  auto kern = grouped_gemm_kernel<NTMAX, STAGES, MODE>;
+template <int NTMAX, int STAGES, int MODE, int BBOX>
+cudaError_t launch_instance(const GroupedGemmProblem& pr, GemmParams gp, cudaStream_t stream) {
+  using L = Layout<NTMAX, STAGES, MODE, BBOX>;
+  const bool has_shared = gp.has_shared != 0;
+  gp.NT = NTMAX;
+  CUtensorMap ta, tb, tas, tbs;
+  if (pr.M > 0) {
+    if (!make_map(&ta, pr.w, pr.K, (long long)pr.E * pr.n_out, kBM)) return cudaErrorInvalidValue;
+    if (!make_map(&tb, pr.a_rows, pr.K, pr.M, BBOX)) return cudaErrorInvalidValue;
+  }
+  if (has_shared) {
+    if (!make_map(&tas, pr.s_w, pr.K, pr.n_out_s, kBM)) return cudaErrorInvalidValue;
+    if (!make_map(&tbs, pr.s_rows, pr.K, pr.T_s, BBOX)) return cudaErrorInvalidValue;
+  }
+  // With no routed rows the routed maps are never read (and vice versa): alias them.
+  if (pr.M <= 0) {
+    ta = tas;
+    tb = tbs;
+  } else if (!has_shared) {
+    tas = ta;
+    tbs = tb;
+  }
+  auto kern = grouped_gemm_kernel<NTMAX, STAGES, MODE, BBOX>;
   const size_t smem = L::bytes(gp.E);
   cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (err != cudaSuccess) return err;
-  kern<<<num_sms(), kThreads, smem, stream>>>(a, b, as, bs, gp);
+  kern<<<num_sms(), kThreads, smem, stream>>>(ta, tb, tas, tbs, gp);
   return cudaGetLastError();
 }
 
@@ -418,56 +455,37 @@ cudaError_t launch_grouped_gemm(const GroupedGemmProblem& pr, cudaStream_t strea
   const bool has_shared = pr.s_rows != nullptr && pr.T_s > 0;
   if (pr.M <= 0 && !has_shared) return cudaSuccess;
   GemmParams gp{};
-  gp.offsets = pr.offsets;
+  gp.offsets = pr.M > 0 ? pr.offsets : nullptr;
   gp.E = pr.E;
   gp.M = pr.M;
   gp.K = pr.K;
   gp.n_out = pr.n_out;
-  gp.n_ftiles = pr.mode == 0 ? pr.n_out / 128 : (pr.n_out + kBM - 1) / kBM;
   gp.half = pr.n_out / 2;
+  gp.n_feat = pr.mode == 0 ? pr.n_out / 2 : pr.n_out;
+  gp.n_ftiles = (gp.n_feat + kBM - 1) / kBM;
   gp.out = pr.out;
   gp.ld_out = pr.ld_out;
   gp.has_shared = has_shared ? 1 : 0;
-  gp.T_s = has_shared ? pr.T_s : 0;
-  gp.n_out_s = has_shared ? pr.n_out_s : 0;
-  gp.n_ftiles_s = has_shared ? (pr.mode == 0 ? pr.n_out_s / 128 : (pr.n_out_s + kBM - 1) / kBM) : 0;
-  gp.half_s = has_shared ? pr.n_out_s / 2 : 0;
+  if (has_shared) {
+    gp.T_s = pr.T_s;
+    gp.n_out_s = pr.n_out_s;
+    gp.half_s = pr.n_out_s / 2;
+    gp.n_feat_s = pr.mode == 0 ? pr.n_out_s / 2 : pr.n_out_s;
+    gp.n_ftiles_s = (gp.n_feat_s + kBM - 1) / kBM;
+  }
   gp.s_out = pr.s_out;
   gp.ld_out_s = pr.ld_out_s;
   gp.topk_w = pr.topk_w;
   gp.sorted_pair = pr.sorted_pair;
   gp.status = pr.status;
   gp.timeout_ns = kTimeoutNs;
-
-  // With no routed rows the routed maps are never read: alias the shared ones.
-  if (pr.M <= 0) gp.offsets = nullptr;
-  CUtensorMap ta, tb, tas, tbs;
-  if (pr.M > 0) {
-    if (!make_map(&ta, pr.w, pr.K, (long long)pr.E * pr.n_out)) return cudaErrorInvalidValue;
-    if (!make_map(&tb, pr.a_rows, pr.K, pr.M)) return cudaErrorInvalidValue;
-  }
-  if (has_shared) {
-    if (!make_map(&tas, pr.s_w, pr.K, pr.n_out_s)) return cudaErrorInvalidValue;
-    if (!make_map(&tbs, pr.s_rows, pr.K, pr.T_s)) return cudaErrorInvalidValue;
-  }
-  if (pr.M <= 0) {
-    ta = tas;
-    tb = tbs;
-  } else if (!has_shared) {
-    tas = ta;
-    tbs = tb;
-  }
-  // Token tile: decode-like problems (few rows per expert) use the narrow
-  // instance with deep pipelining; prefill-like ones the 256-column instance.
+  // Decode-like problems (a few rows per expert) take the 32-column instance
+  // with a deep pipeline; prefill-like ones the wide instances.
   const bool narrow = (long long)pr.M <= 32LL * pr.E && (!has_shared || pr.T_s <= 32);
-  if (narrow) {
-    gp.NT = 32;
-    return pr.mode == 0 ? launch_instance<32, 10, 0>(ta, tb, tas, tbs, gp, stream)
-                        : launch_instance<32, 10, 1>(ta, tb, tas, tbs, gp, stream);
-  }
-  gp.NT = 256;
-  return pr.mode == 0 ? launch_instance<256, 4, 0>(ta, tb, tas, tbs, gp, stream)
-                      : launch_instance<256, 4, 1>(ta, tb, tas, tbs, gp, stream);
+  if (narrow)
+    return pr.mode == 0 ? launch_instance<32, 5, 0, 16>(pr, gp, stream) : launch_instance<32, 10, 1, 16>(pr, gp, stream);
+  return pr.mode == 0 ? launch_instance<128, 4, 0, 64>(pr, gp, stream)
+                      : launch_instance<256, 4, 1, 64>(pr, gp, stream);
 }
 
 }  // namespace moe
