@@ -19,14 +19,16 @@
 //
 //   tile = (segment, feature tile f, token tile m); segments are the routed
 //   experts in order, then optionally one dense "shared" segment over all T
-//   rows.  Tiles of one expert are numbered f-major so that the token tiles
-//   that reuse a weight tile run next to each other (L2 reuse).
+//   rows.  Inside a segment tiles run f-major (the token tiles that reuse a
+//   weight tile run next to each other) unless the segment has more token rows
+//   than weight rows, then m-major (the feature tiles that reuse a token tile
+//   run together and the segment's weights stay in L2).
 //
 // Few, large TMA boxes: the per-SM rate of TMA box operations, not their
 // bytes, limits a stream of small boxes, so each stage moves the weight rows
 // in 128-row boxes (16 KB) and the token rows in BBOX-row boxes.
 //
-// Warp roles (192 threads, 1 CTA/SM, static round-robin tile schedule):
+// Warp roles (320 threads, 1 CTA/SM, static round-robin tile schedule):
 //   warp 0      TMA producer: per stage one 128-row weight box (two in mode 0:
 //               the gate rows and the matching up rows) + ceil(rows/BBOX)
 //               token boxes, one lane per box.
@@ -34,7 +36,8 @@
 //               (M=128, N=rows, K=16 x 4 per stage), double-buffered accumulator.
 //               Mode 0 keeps two accumulators, gate and up, so that TMEM lane l
 //               of both holds the same output feature.
-//   warps 2..5  epilogue: tcgen05.ld 32 lanes x 16 columns, then
+//   warps 2..9  epilogue, two warps per TMEM lane quarter taking alternate
+//               32-column chunks: tcgen05.ld 32 lanes x 32 columns, then
 //               mode 0 (w13): SwiGLU = SiLU(gate) * up, in fp32, per element.
 //               mode 1 (down): multiply by the routing weight of the row.
 // Every wait is bounded (default 2 s); on expiry the CTA raises an abort flag,
@@ -54,7 +57,8 @@ constexpr int kBK = 64;                      // K per stage: one 128-byte swizzl
 constexpr int kRowBytes = kBK * 2;           // 128 B per operand row per stage
 constexpr int kABox = kBM * kRowBytes;       // one 128-row weight box: 16 KB
 constexpr int kMaxDynSmem = 232448;          // 227 KB per CTA
-constexpr int kThreads = 192;
+constexpr int kEpiWarps = 8;                 // two epilogue warps per TMEM lane quarter
+constexpr int kThreads = 64 + 32 * kEpiWarps;
 constexpr unsigned long long kTimeoutNs = 2000000000ull;
 
 struct GemmParams {
@@ -84,7 +88,7 @@ struct Layout {
   static constexpr int kNumBars = 2 * STAGES + 5;
   static constexpr int kMiscOff = kBarOff + kNumBars * 8;
   static constexpr int kScaleOff = kMiscOff + 16;                // mode 1: per-epilogue-warp row scales
-  static constexpr int kTabOff = kScaleOff + (MODE == 1 ? 4 * NTMAX * 4 : 0);
+  static constexpr int kTabOff = kScaleOff + (MODE == 1 ? kEpiWarps * NTMAX * 4 : 0);
   static constexpr int kAccCols = kAParts * NTMAX;             // TMEM columns of one accumulator buffer
   static constexpr uint32_t kTmemCols = (2 * kAccCols <= 32) ? 32 : (2 * kAccCols <= 64 ? 64 : (2 * kAccCols <= 128 ? 128 : (2 * kAccCols <= 256 ? 256 : 512)));
   static_assert(2 * kAccCols <= 512, "accumulators exceed TMEM");
@@ -96,6 +100,7 @@ struct Layout {
 
 struct Tile {
   int shared, e, f, row_base, rows;
+  int nt;  // token tiles of this segment: how many tiles reuse this tile's weight rows
 };
 
 __device__ __forceinline__ Tile decode_tile(int tile, int routed_total, const int* s_off, const int* s_tt,
@@ -110,19 +115,26 @@ __device__ __forceinline__ Tile decode_tile(int tile, int routed_total, const in
     }
     const int nt = s_tt[lo + 1] - s_tt[lo];
     const int local = tile - s_tt[lo] * p.n_ftiles;
-    const int m = local % nt;
+    const int cnt = s_off[lo + 1] - s_off[lo];
+    // An expert with more token rows than weight rows walks token-tile-major so its
+    // weights stay in L2 while its token tiles stream; otherwise feature-tile-major.
+    const bool m_major = cnt > p.n_out;
+    const int m = m_major ? local / p.n_ftiles : local % nt;
     t.shared = 0;
     t.e = lo;
-    t.f = local / nt;
+    t.nt = nt;
+    t.f = m_major ? local - m * p.n_ftiles : local / nt;
     t.row_base = s_off[lo] + m * p.NT;
     t.rows = min(p.NT, s_off[lo + 1] - t.row_base);
   } else {
     const int local = tile - routed_total;
     const int nt = (p.T_s + p.NT - 1) / p.NT;
-    const int m = local % nt;
+    const bool m_major = p.T_s > p.n_out_s;
+    const int m = m_major ? local / p.n_ftiles_s : local % nt;
     t.shared = 1;
     t.e = -1;
-    t.f = local / nt;
+    t.nt = nt;
+    t.f = m_major ? local - m * p.n_ftiles_s : local / nt;
     t.row_base = m * p.NT;
     t.rows = min(p.NT, p.T_s - t.row_base);
   }
@@ -159,7 +171,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(&tfull[b], 1);
-      mbar_init(&tempty[b], 4);
+      mbar_init(&tempty[b], kEpiWarps);
     }
     mbar_init(done, 1);
     *abort_flag = 0;
@@ -231,6 +243,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       // weight box `lane` (< kAParts): mode 0 lane 0 = gate rows, lane 1 = the matching up rows
       const int a_row = (t.shared ? 0 : t.e * p.n_out) + (lane == 1 ? (t.shared ? p.half_s : p.half) : 0) +
                         t.f * kBM;
+      // Weight rows read by one tile only are streamed past L2 (evict first); weight rows that
+      // the segment's other token tiles read again are kept (evict last), like the token rows.
+      const uint64_t pol_a = t.nt > 1 ? pol_x : pol_w;
       for (int kb = 0; kb < KB; ++kb) {
         bool w = (lane == 0) ? mbar_wait_bounded(&empty[stage], phase ^ 1u, abort_flag, p.timeout_ns, p.status)
                              : false;
@@ -244,7 +259,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         uint8_t* sA = smem + stage * L::kStageBytes;
         uint8_t* sB = sA + L::kABytes;
         if (lane < L::kAParts) {
-          tma_load_2d(sA + lane * kABox, mA, kb * kBK, a_row, &full[stage], pol_w);
+          tma_load_2d(sA + lane * kABox, mA, kb * kBK, a_row, &full[stage], pol_a);
         } else if (lane >= 2 && lane < 2 + nbox) {
           const int j = lane - 2;
           tma_load_2d(sB + j * BBOX * kRowBytes, mB, kb * kBK, t.row_base + j * BBOX, &full[stage], pol_x);
@@ -312,7 +327,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncwarp();
   } else {
     // ------------------------------------------------------------ epilogue
-    const int qw = warp & 3;  // TMEM lane quarter this warp may access
+    const int qw = warp & 3;            // TMEM lane quarter this warp may access
+    const int half_c = (warp - 2) >> 2; // which alternate 32-column chunks this warp takes
     int it = 0;
     for (int tile = blockIdx.x; tile < total; tile += gridDim.x, ++it) {
       const Tile t = decode_tile(tile, routed_total, s_off, s_tt, p);
@@ -323,14 +339,18 @@ __global__ void __launch_bounds__(kThreads, 1)
       float* wsc = s_scale + (warp - 2) * NTMAX;
       const bool scale = MODE == 1 && !t.shared && p.topk_w != nullptr;
       if (scale) {
-        int pr[NTMAX / 32];
+        constexpr int kMine = (NTMAX / 32 + 1) / 2;  // chunks of 32 columns this warp handles
+        int pr[kMine];
 #pragma unroll
-        for (int r = 0; r < NTMAX / 32; ++r) {
-          const int col = r * 32 + lane;
-          pr[r] = col < t.rows ? __ldg(p.sorted_pair + t.row_base + col) : -1;
+        for (int r = 0; r < kMine; ++r) {
+          const int col = (2 * r + half_c) * 32 + lane;
+          pr[r] = (col < t.rows && col < NTMAX) ? __ldg(p.sorted_pair + t.row_base + col) : -1;
         }
 #pragma unroll
-        for (int r = 0; r < NTMAX / 32; ++r) wsc[r * 32 + lane] = pr[r] >= 0 ? __ldg(p.topk_w + pr[r]) : 0.0f;
+        for (int r = 0; r < kMine; ++r) {
+          const int col = (2 * r + half_c) * 32 + lane;
+          if (col < NTMAX) wsc[col] = pr[r] >= 0 ? __ldg(p.topk_w + pr[r]) : 0.0f;
+        }
         __syncwarp();
       }
       bool w = (lane == 0) ? mbar_wait_bounded(&tfull[buf], aph, abort_flag, p.timeout_ns, p.status) : false;
@@ -338,32 +358,36 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!w) break;
       tc_fence_after();
       const uint32_t tb = tmem_base + ((uint32_t)(qw * 32) << 16) + (uint32_t)(buf * L::kAccCols);
-      const int nch = (t.rows + 15) >> 4;
+      const int nch = (t.rows + 31) >> 5;  // 32-column chunks
       uint16_t* out = t.shared ? p.s_out : p.out;
       const size_t ld = (size_t)(t.shared ? p.ld_out_s : p.ld_out);
       const int feat = t.f * kBM + qw * 32 + lane;  // this thread's output feature (TMEM lane)
       const bool feat_ok = feat < (t.shared ? p.n_feat_s : p.n_feat);
+      uint16_t* orow = out + (size_t)t.row_base * ld + feat;
       if (MODE == 0) {
-        for (int c = 0; c < nch; ++c) {
-          float g[16], u[16];
-          tmem_ld16(tb + (uint32_t)(c * 16), g);
-          tmem_ld16(tb + (uint32_t)(NTMAX + c * 16), u);
+        for (int c = half_c; c < nch; c += 2) {
+          uint32_t g[32], u[32];
+          tmem_ld32_async(tb + (uint32_t)(c * 32), g);
+          tmem_ld32_async(tb + (uint32_t)(NTMAX + c * 32), u);
+          tmem_wait_ld();
 #pragma unroll
-          for (int i = 0; i < 16; ++i) {
-            const int col = c * 16 + i;
-            const float a = g[i] / (1.0f + expf(-g[i])) * u[i];
-            if (col < t.rows && feat_ok) out[(size_t)(t.row_base + col) * ld + feat] = f32_to_bf16_rne(a);
+          for (int i = 0; i < 32; ++i) {
+            const int col = c * 32 + i;
+            const float gv = __uint_as_float(g[i]);
+            const float a = gv / (1.0f + expf(-gv)) * __uint_as_float(u[i]);
+            if (col < t.rows && feat_ok) orow[(size_t)col * ld] = f32_to_bf16_rne(a);
           }
         }
       } else {
-        for (int c = 0; c < nch; ++c) {
-          float v[16];
-          tmem_ld16(tb + (uint32_t)(c * 16), v);
+        for (int c = half_c; c < nch; c += 2) {
+          uint32_t v[32];
+          tmem_ld32_async(tb + (uint32_t)(c * 32), v);
+          tmem_wait_ld();
 #pragma unroll
-          for (int i = 0; i < 16; ++i) {
-            const int col = c * 16 + i;
+          for (int i = 0; i < 32; ++i) {
+            const int col = c * 32 + i;
             const float sv = scale ? wsc[col] : 1.0f;
-            if (col < t.rows && feat_ok) out[(size_t)(t.row_base + col) * ld + feat] = f32_to_bf16_rne(v[i] * sv);
+            if (col < t.rows && feat_ok) orow[(size_t)col * ld] = f32_to_bf16_rne(__uint_as_float(v[i]) * sv);
           }
         }
         __syncwarp();  // the next tile rewrites this warp's scales
