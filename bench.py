@@ -6,6 +6,9 @@
 A step is one full layer forward (gating top-k, init-routing, gate/up grouped
 GEMM + SwiGLU, down grouped GEMM + routing weight, finalize) through the C ABI
 (moe_layer_forward), on seeded synthetic inputs already resident in HBM.
+`value` times K plain calls; a second timed loop of K moe_layer_forward_events
+calls gives each step's duration (CUDA events on the launching stream), from
+which the dominant kernel's roofline is computed.
 The default workload is the Qwen3-MoE-style decode layer (T=64, H=4096,
 E=128, k=8, I=1536).  Its 4.75 GB of active expert weights per step exceed the
 129 MB L2, so no L2 flush is needed between steps.
@@ -337,18 +340,15 @@ def run_gb300(args, rank, world, local):
     if status != moe.MOE_OK:
         raise SystemExit(f"device status after warm-up: {moe.status_string(status)}")
     counts = layer.counts.cpu().numpy()
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(6)] for _ in range(K)]
-    for row in evs:
-        for e in row:
-            e.record()
+    # timed region 1 (the headline value): K plain moe_layer_forward calls
     start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     torch.cuda.synchronize()
     _barrier(world)
     torch.cuda.synchronize()
     w0 = time.time()
     start.record()
-    for i in range(K):
-        layer.forward_events(evs[i], **t)
+    for _ in range(K):
+        layer.forward(**t)
     end.record()
     torch.cuda.synchronize()
     w1 = time.time()
@@ -359,6 +359,16 @@ def run_gb300(args, rank, world, local):
     status = moe.moe_get_device_status(layer.ws)
     if status != moe.MOE_OK:
         raise SystemExit(f"device status after the timed region: {moe.status_string(status)}")
+    # timed region 2 (per-kernel durations): K moe_layer_forward_events calls, six events
+    # recorded on the launching stream around the steps of every call
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(6)] for _ in range(K)]
+    for row in evs:
+        for e in row:
+            e.record()
+    torch.cuda.synchronize()
+    for i in range(K):
+        layer.forward_events(evs[i], **t)
+    torch.cuda.synchronize()
     names = ["gating", "init_routing", "gemm_w13_swiglu", "gemm_down", "finalize"]
     kern_ms = {n: statistics.mean(evs[i][j].elapsed_time(evs[i][j + 1]) for i in range(K))
                for j, n in enumerate(names)}

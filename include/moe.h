@@ -153,10 +153,12 @@ MOE_API int moe_init_routing(const int32_t* topk_idx, int T, int E, int k, const
  * Same arguments, outputs and results as moe_init_routing, minus the
  * workspace.  Its scratch is a fixed 1 MiB device array inside the library
  * (held by every GPU that loads the library until the process exits), so the
- * problem must satisfy 2 * n_chunks * E * 4 <= 1 MiB with n_chunks =
- * ceil(T*k / max(512, ceil(T*k/256) rounded up to 32)) <= 256 -- so any E <= 512
- * at any T*k, and T*k <= 65536 at E = 1024; larger problems return
- * MOE_ERR_UNSUPPORTED and launch nothing.  Out-of-range expert indices are
+ * problem must satisfy 2 * n_chunks * E * 4 <= 1 MiB, where n_chunks is the
+ * number of pair chunks init-routing uses: ceil(T*k / 32) when T*k <= 4096,
+ * else ceil(T*k / max(512, ceil(T*k/256) rounded up to 32)); never above 256,
+ * and at most 128 when T*k <= 65536 -- so any E <= 512 fits at any T*k, and
+ * E = 1024 fits for T*k <= 65536; larger problems return MOE_ERR_UNSUPPORTED
+ * and launch nothing.  Out-of-range expert indices are
  * skipped without a status report.  The call allocates nothing.
  *  - Every call on a device shares the array.  Each call overwrites all the
  *    scratch it reads, so nothing has to be cleared between calls, but calls

@@ -285,8 +285,11 @@ int layer_forward_impl(const moe_layer_desc* d, const uint16_t* x, const float* 
                                           topk_w, topk_idx, st);
   if (e != cudaSuccess) return MOE_ERR_CUDA;
   if (mark(1) != cudaSuccess) return MOE_ERR_CUDA;
+  // Every kernel after the first may start while its predecessor finishes (programmatic
+  // dependent launch); each waits for its inputs before touching them.
+  constexpr bool kPdl = true;
   e = moe::launch_init_routing(topk_idx, P, E, k, x, H, x_exp, counts, offsets, sorted_pair, pair_pos, scratch,
-                               status, st);
+                               status, st, kPdl);
   if (e != cudaSuccess) return MOE_ERR_CUDA;
 
   moe::GroupedGemmProblem g1{};
@@ -310,7 +313,7 @@ int layer_forward_impl(const moe_layer_desc* d, const uint16_t* x, const float* 
   }
   g1.status = status;
   if (mark(2) != cudaSuccess) return MOE_ERR_CUDA;
-  if (moe::launch_grouped_gemm(g1, st) != cudaSuccess) return MOE_ERR_CUDA;
+  if (moe::launch_grouped_gemm(g1, st, kPdl) != cudaSuccess) return MOE_ERR_CUDA;
   if (mark(3) != cudaSuccess) return MOE_ERR_CUDA;
 
   // The down projection's K is I for routed experts and I_s for the shared
@@ -340,7 +343,7 @@ int layer_forward_impl(const moe_layer_desc* d, const uint16_t* x, const float* 
     gs.s_out = shared;
     gs.ld_out_s = H;
   }
-  if (moe::launch_grouped_gemm(g2, st) != cudaSuccess) return MOE_ERR_CUDA;
+  if (moe::launch_grouped_gemm(g2, st, kPdl) != cudaSuccess) return MOE_ERR_CUDA;
   if (sh && !fused_shared) {
     // separate launch for the shared expert's down projection (K = I_s)
     g2s.mode = 1;
@@ -352,10 +355,10 @@ int layer_forward_impl(const moe_layer_desc* d, const uint16_t* x, const float* 
     g2s.K = d->I_s;
     g2s.n_out = H;
     g2s.status = status;
-    if (moe::launch_grouped_gemm(g2s, st) != cudaSuccess) return MOE_ERR_CUDA;
+    if (moe::launch_grouped_gemm(g2s, st, kPdl) != cudaSuccess) return MOE_ERR_CUDA;
   }
   if (mark(4) != cudaSuccess) return MOE_ERR_CUDA;
-  if (moe::launch_finalize(y_perm, pair_pos, sh ? shared : nullptr, T, k, H, y, st) != cudaSuccess)
+  if (moe::launch_finalize(y_perm, pair_pos, sh ? shared : nullptr, T, k, H, y, st, kPdl) != cudaSuccess)
     return MOE_ERR_CUDA;
   return cuda_status(mark(5));
 }

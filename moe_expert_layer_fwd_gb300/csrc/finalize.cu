@@ -27,6 +27,8 @@ __global__ void __launch_bounds__(256) finalize_kernel(const uint4* __restrict__
                                                        const int32_t* __restrict__ pair_pos,
                                                        const uint4* __restrict__ shared, int T, int k, int H8,
                                                        uint4* __restrict__ y) {
+  pdl_wait();
+  pdl_launch_dependents();
   const size_t gid = (size_t)blockIdx.x * blockDim.x + threadIdx.x;
   if (gid >= (size_t)T * H8) return;
   const int t = (int)(gid / H8);
@@ -49,14 +51,13 @@ __global__ void __launch_bounds__(256) finalize_kernel(const uint4* __restrict__
 }  // namespace
 
 cudaError_t launch_finalize(const uint16_t* y_perm, const int32_t* pair_pos, const uint16_t* shared, int T, int k,
-                            int H, uint16_t* y, cudaStream_t stream) {
+                            int H, uint16_t* y, cudaStream_t stream, bool pdl) {
   const size_t n = (size_t)T * (H / 8);
   if (n == 0) return cudaSuccess;
   const int threads = 256;
-  finalize_kernel<<<(unsigned)((n + threads - 1) / threads), threads, 0, stream>>>(
-      reinterpret_cast<const uint4*>(y_perm), pair_pos, reinterpret_cast<const uint4*>(shared), T, k, H / 8,
-      reinterpret_cast<uint4*>(y));
-  return cudaGetLastError();
+  return launch_kernel(finalize_kernel, dim3((unsigned)((n + threads - 1) / threads)), dim3(threads), 0, stream, pdl,
+                       reinterpret_cast<const uint4*>(y_perm), pair_pos, reinterpret_cast<const uint4*>(shared), T, k,
+                       H / 8, reinterpret_cast<uint4*>(y));
 }
 
 }  // namespace moe

@@ -74,6 +74,8 @@ __global__ void __launch_bounds__(256) gating_topk_kernel(const float* __restric
                                                           int gate, float rsf, float eps,
                                                           float* __restrict__ topk_w,
                                                           int32_t* __restrict__ topk_idx) {
+  pdl_wait();
+  pdl_launch_dependents();
   const int lane = threadIdx.x & 31;
   const int t = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
   if (t >= T) return;
@@ -123,21 +125,21 @@ __global__ void __launch_bounds__(256) gating_topk_kernel(const float* __restric
 }  // namespace
 
 cudaError_t launch_gating_topk(const float* logits, const float* bias, int T, int E, int k, int gate, float rsf,
-                               float eps, float* topk_w, int32_t* topk_idx, cudaStream_t stream) {
+                               float eps, float* topk_w, int32_t* topk_idx, cudaStream_t stream, bool pdl) {
   if (T == 0) return cudaSuccess;
   const int warps = 8;
   dim3 grid((T + warps - 1) / warps);
   const int vpl = (E + 31) / 32;
-#define MOE_GATING_LAUNCH(V) \
-  gating_topk_kernel<V><<<grid, warps * 32, 0, stream>>>(logits, bias, T, E, k, gate, rsf, eps, topk_w, topk_idx)
-  if (vpl <= 1) MOE_GATING_LAUNCH(1);
-  else if (vpl <= 2) MOE_GATING_LAUNCH(2);
-  else if (vpl <= 4) MOE_GATING_LAUNCH(4);
-  else if (vpl <= 8) MOE_GATING_LAUNCH(8);
-  else if (vpl <= 16) MOE_GATING_LAUNCH(16);
-  else MOE_GATING_LAUNCH(32);
+#define MOE_GATING_LAUNCH(V)                                                                                 \
+  launch_kernel(gating_topk_kernel<V>, grid, dim3(warps * 32), 0, stream, pdl, logits, bias, T, E, k, gate, rsf, \
+                eps, topk_w, topk_idx)
+  if (vpl <= 1) return MOE_GATING_LAUNCH(1);
+  if (vpl <= 2) return MOE_GATING_LAUNCH(2);
+  if (vpl <= 4) return MOE_GATING_LAUNCH(4);
+  if (vpl <= 8) return MOE_GATING_LAUNCH(8);
+  if (vpl <= 16) return MOE_GATING_LAUNCH(16);
+  return MOE_GATING_LAUNCH(32);
 #undef MOE_GATING_LAUNCH
-  return cudaGetLastError();
 }
 
 }  // namespace moe

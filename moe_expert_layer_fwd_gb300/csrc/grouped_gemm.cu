@@ -28,7 +28,7 @@
 // bytes, limits a stream of small boxes, so each stage moves the weight rows
 // in 128-row boxes (16 KB) and the token rows in BBOX-row boxes.
 //
-// Warp roles (320 threads, 1 CTA/SM, static round-robin tile schedule):
+// Warp roles (64 + 32*EPI threads, 1 CTA/SM, static round-robin tile schedule):
 //   warp 0      TMA producer: per stage one 128-row weight box (two in mode 0:
 //               the gate rows and the matching up rows) + ceil(rows/BBOX)
 //               token boxes, one lane per box.
@@ -36,8 +36,8 @@
 //               (M=128, N=rows, K=16 x 4 per stage), double-buffered accumulator.
 //               Mode 0 keeps two accumulators, gate and up, so that TMEM lane l
 //               of both holds the same output feature.
-//   warps 2..9  epilogue, two warps per TMEM lane quarter taking alternate
-//               32-column chunks: tcgen05.ld 32 lanes x 32 columns, then
+//   warps 2..   epilogue, EPI/4 warps per TMEM lane quarter (EPI = 8 or 16) taking
+//               interleaved 32-column chunks: tcgen05.ld 32 lanes x 32 columns, then
 //               mode 0 (w13): SwiGLU = SiLU(gate) * up, in fp32, per element.
 //               mode 1 (down): multiply by the routing weight of the row.
 // Every wait is bounded (default 2 s); on expiry the CTA raises an abort flag,
@@ -57,8 +57,6 @@ constexpr int kBK = 64;                      // K per stage: one 128-byte swizzl
 constexpr int kRowBytes = kBK * 2;           // 128 B per operand row per stage
 constexpr int kABox = kBM * kRowBytes;       // one 128-row weight box: 16 KB
 constexpr int kMaxDynSmem = 232448;          // 227 KB per CTA
-constexpr int kEpiWarps = 8;                 // two epilogue warps per TMEM lane quarter
-constexpr int kThreads = 64 + 32 * kEpiWarps;
 constexpr unsigned long long kTimeoutNs = 2000000000ull;
 
 struct GemmParams {
@@ -78,8 +76,9 @@ struct GemmParams {
   unsigned long long timeout_ns;
 };
 
-template <int NTMAX, int STAGES, int MODE, int BBOX>
+template <int NTMAX, int STAGES, int MODE, int BBOX, int EPI>
 struct Layout {
+  static constexpr int kThreads = 64 + 32 * EPI;                 // producer, MMA, EPI epilogue warps
   static constexpr int kAParts = MODE == 0 ? 2 : 1;            // gate + up boxes in mode 0
   static constexpr int kABytes = kAParts * kABox;
   static constexpr int kBBytes = NTMAX * kRowBytes;
@@ -88,7 +87,7 @@ struct Layout {
   static constexpr int kNumBars = 2 * STAGES + 5;
   static constexpr int kMiscOff = kBarOff + kNumBars * 8;
   static constexpr int kScaleOff = kMiscOff + 16;                // mode 1: per-epilogue-warp row scales
-  static constexpr int kTabOff = kScaleOff + (MODE == 1 ? kEpiWarps * NTMAX * 4 : 0);
+  static constexpr int kTabOff = kScaleOff + (MODE == 1 ? EPI * NTMAX * 4 : 0);
   static constexpr int kAccCols = kAParts * NTMAX;             // TMEM columns of one accumulator buffer
   static constexpr uint32_t kTmemCols = (2 * kAccCols <= 32) ? 32 : (2 * kAccCols <= 64 ? 64 : (2 * kAccCols <= 128 ? 128 : (2 * kAccCols <= 256 ? 256 : 512)));
   static_assert(2 * kAccCols <= 512, "accumulators exceed TMEM");
@@ -141,12 +140,12 @@ __device__ __forceinline__ Tile decode_tile(int tile, int routed_total, const in
   return t;
 }
 
-template <int NTMAX, int STAGES, int MODE, int BBOX>
-__global__ void __launch_bounds__(kThreads, 1)
+template <int NTMAX, int STAGES, int MODE, int BBOX, int EPI>
+__global__ void __launch_bounds__(64 + 32 * EPI, 1)
     grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                         const __grid_constant__ CUtensorMap tmAs, const __grid_constant__ CUtensorMap tmBs,
                         const GemmParams p) {
-  using L = Layout<NTMAX, STAGES, MODE, BBOX>;
+  using L = Layout<NTMAX, STAGES, MODE, BBOX, EPI>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + L::kBarOff);
@@ -171,7 +170,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(&tfull[b], 1);
-      mbar_init(&tempty[b], kEpiWarps);
+      mbar_init(&tempty[b], EPI);
     }
     mbar_init(done, 1);
     *abort_flag = 0;
@@ -187,7 +186,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   }
   if (warp == 1) tmem_alloc(tmem_slot, L::kTmemCols);
-  for (int i = threadIdx.x; i <= E; i += kThreads) s_off[i] = p.offsets ? __ldg(p.offsets + i) : 0;
+  for (int i = threadIdx.x; i <= E; i += L::kThreads) s_off[i] = p.offsets ? __ldg(p.offsets + i) : 0;
   __syncthreads();
   if (warp == 2) {
     // Validate offsets and build the prefix of token tiles per expert.
@@ -235,6 +234,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     int stage = 0;
     uint32_t phase = 0, issued = 0;
     bool ok = true;
+    // Inside moe_layer_forward this kernel may start while the previous one finishes
+    // (programmatic dependent launch): the token rows it loads may still be being
+    // written, so wait for that kernel first, then let the next kernel launch.
+    pdl_wait();
+    pdl_launch_dependents();
     for (int tile = blockIdx.x; ok && tile < total; tile += gridDim.x) {
       const Tile t = decode_tile(tile, routed_total, s_off, s_tt, p);
       const CUtensorMap* mA = t.shared ? &tmAs : &tmA;
@@ -328,7 +332,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else {
     // ------------------------------------------------------------ epilogue
     const int qw = warp & 3;            // TMEM lane quarter this warp may access
-    const int half_c = (warp - 2) >> 2; // which alternate 32-column chunks this warp takes
+    constexpr int kPerQ = EPI / 4;           // epilogue warps sharing one TMEM lane quarter
+    const int half_c = (warp - 2) >> 2;     // this warp takes 32-column chunks half_c, half_c + kPerQ, ...
     int it = 0;
     for (int tile = blockIdx.x; tile < total; tile += gridDim.x, ++it) {
       const Tile t = decode_tile(tile, routed_total, s_off, s_tt, p);
@@ -339,16 +344,16 @@ __global__ void __launch_bounds__(kThreads, 1)
       float* wsc = s_scale + (warp - 2) * NTMAX;
       const bool scale = MODE == 1 && !t.shared && p.topk_w != nullptr;
       if (scale) {
-        constexpr int kMine = (NTMAX / 32 + 1) / 2;  // chunks of 32 columns this warp handles
+        constexpr int kMine = (NTMAX / 32 + kPerQ - 1) / kPerQ;  // chunks of 32 columns this warp handles
         int pr[kMine];
 #pragma unroll
         for (int r = 0; r < kMine; ++r) {
-          const int col = (2 * r + half_c) * 32 + lane;
+          const int col = (kPerQ * r + half_c) * 32 + lane;
           pr[r] = (col < t.rows && col < NTMAX) ? __ldg(p.sorted_pair + t.row_base + col) : -1;
         }
 #pragma unroll
         for (int r = 0; r < kMine; ++r) {
-          const int col = (2 * r + half_c) * 32 + lane;
+          const int col = (kPerQ * r + half_c) * 32 + lane;
           if (col < NTMAX) wsc[col] = pr[r] >= 0 ? __ldg(p.topk_w + pr[r]) : 0.0f;
         }
         __syncwarp();
@@ -365,7 +370,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const bool feat_ok = feat < (t.shared ? p.n_feat_s : p.n_feat);
       uint16_t* orow = out + (size_t)t.row_base * ld + feat;
       if (MODE == 0) {
-        for (int c = half_c; c < nch; c += 2) {
+        for (int c = half_c; c < nch; c += kPerQ) {
           uint32_t g[32], u[32];
           tmem_ld32_async(tb + (uint32_t)(c * 32), g);
           tmem_ld32_async(tb + (uint32_t)(NTMAX + c * 32), u);
@@ -379,7 +384,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
       } else {
-        for (int c = half_c; c < nch; c += 2) {
+        for (int c = half_c; c < nch; c += kPerQ) {
           uint32_t v[32];
           tmem_ld32_async(tb + (uint32_t)(c * 32), v);
           tmem_wait_ld();
@@ -443,9 +448,9 @@ int num_sms() {
   return n > 0 ? n : 1;
 }
 
-template <int NTMAX, int STAGES, int MODE, int BBOX>
-cudaError_t launch_instance(const GroupedGemmProblem& pr, GemmParams gp, cudaStream_t stream) {
-  using L = Layout<NTMAX, STAGES, MODE, BBOX>;
+template <int NTMAX, int STAGES, int MODE, int BBOX, int EPI>
+cudaError_t launch_instance(const GroupedGemmProblem& pr, GemmParams gp, cudaStream_t stream, bool pdl) {
+  using L = Layout<NTMAX, STAGES, MODE, BBOX, EPI>;
   const bool has_shared = gp.has_shared != 0;
   gp.NT = NTMAX;
   CUtensorMap ta, tb, tas, tbs;
@@ -465,17 +470,16 @@ cudaError_t launch_instance(const GroupedGemmProblem& pr, GemmParams gp, cudaStr
     tas = ta;
     tbs = tb;
   }
-  auto kern = grouped_gemm_kernel<NTMAX, STAGES, MODE, BBOX>;
+  auto kern = grouped_gemm_kernel<NTMAX, STAGES, MODE, BBOX, EPI>;
   const size_t smem = L::bytes(gp.E);
   cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (err != cudaSuccess) return err;
-  kern<<<num_sms(), kThreads, smem, stream>>>(ta, tb, tas, tbs, gp);
-  return cudaGetLastError();
+  return launch_kernel(kern, dim3(num_sms()), dim3(L::kThreads), smem, stream, pdl, ta, tb, tas, tbs, gp);
 }
 
 }  // namespace
 
-cudaError_t launch_grouped_gemm(const GroupedGemmProblem& pr, cudaStream_t stream) {
+cudaError_t launch_grouped_gemm(const GroupedGemmProblem& pr, cudaStream_t stream, bool pdl) {
   const bool has_shared = pr.s_rows != nullptr && pr.T_s > 0;
   if (pr.M <= 0 && !has_shared) return cudaSuccess;
   GemmParams gp{};
@@ -507,9 +511,10 @@ cudaError_t launch_grouped_gemm(const GroupedGemmProblem& pr, cudaStream_t strea
   // with a deep pipeline; prefill-like ones the wide instances.
   const bool narrow = (long long)pr.M <= 32LL * pr.E && (!has_shared || pr.T_s <= 32);
   if (narrow)
-    return pr.mode == 0 ? launch_instance<32, 5, 0, 16>(pr, gp, stream) : launch_instance<32, 10, 1, 16>(pr, gp, stream);
-  return pr.mode == 0 ? launch_instance<128, 4, 0, 64>(pr, gp, stream)
-                      : launch_instance<256, 4, 1, 64>(pr, gp, stream);
+    return pr.mode == 0 ? launch_instance<32, 5, 0, 16, 8>(pr, gp, stream, pdl)
+                        : launch_instance<32, 10, 1, 16, 8>(pr, gp, stream, pdl);
+  return pr.mode == 0 ? launch_instance<128, 4, 0, 64, 8>(pr, gp, stream, pdl)
+                      : launch_instance<256, 4, 1, 64, 16>(pr, gp, stream, pdl);
 }
 
 }  // namespace moe

@@ -7,17 +7,20 @@
 
 namespace moe {
 
+// `pdl`: launch so the kernel may overlap its predecessor on the stream (only
+// between the library's own kernels inside moe_layer_forward).
 cudaError_t launch_gating_topk(const float* logits, const float* bias, int T, int E, int k, int gate, float rsf,
-                               float eps, float* topk_w, int32_t* topk_idx, cudaStream_t stream);
+                               float eps, float* topk_w, int32_t* topk_idx, cudaStream_t stream, bool pdl = false);
 
 // Init-routing scratch: per-chunk expert histograms and bases.
 int routing_chunk_pairs(int P);
 size_t routing_scratch_bytes(int P, int E);
 cudaError_t launch_init_routing(const int32_t* topk_idx, int P, int E, int k, const uint16_t* x, int H,
                                 uint16_t* x_exp, int32_t* counts, int32_t* offsets, int32_t* sorted_pair,
-                                int32_t* pair_pos, int32_t* scratch, unsigned* status, cudaStream_t stream);
+                                int32_t* pair_pos, int32_t* scratch, unsigned* status, cudaStream_t stream,
+                                bool pdl = false);
 cudaError_t launch_expand_rows(const uint16_t* x, const int32_t* sorted_pair, int P, int k, int H,
-                               uint16_t* x_exp, cudaStream_t stream);
+                               uint16_t* x_exp, cudaStream_t stream, bool pdl = false);
 
 // One grouped GEMM launch: routed experts (+ optionally one dense "shared" segment).
 struct GroupedGemmProblem {
@@ -40,9 +43,9 @@ struct GroupedGemmProblem {
   unsigned* status;
 };
 
-cudaError_t launch_grouped_gemm(const GroupedGemmProblem& p, cudaStream_t stream);
+cudaError_t launch_grouped_gemm(const GroupedGemmProblem& p, cudaStream_t stream, bool pdl = false);
 
 cudaError_t launch_finalize(const uint16_t* y_perm, const int32_t* pair_pos, const uint16_t* shared, int T, int k,
-                            int H, uint16_t* y, cudaStream_t stream);
+                            int H, uint16_t* y, cudaStream_t stream, bool pdl = false);
 
 }  // namespace moe

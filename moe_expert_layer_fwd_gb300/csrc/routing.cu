@@ -17,8 +17,8 @@
 //               the rank inside the group is the number of lower lanes in it,
 //               so positions follow pair order exactly (a stable sort) with no
 //               atomics deciding the order.
-//   4. expand:  x_exp[pos] = x[sorted_pair[pos] / k], one warp per row, 16-byte
-//               vector copies.
+//   4. expand:  x_exp[pos] = x[sorted_pair[pos] / k], a flat grid of 16-byte
+//               vector copies, several independent ones per thread.
 #include "moe_common.cuh"
 #include "moe_internal.h"
 
@@ -30,6 +30,8 @@ constexpr int kWarps = 8;
 __global__ void __launch_bounds__(kWarps * 32) route_hist_kernel(const int32_t* __restrict__ idx, int P, int E,
                                                                  int CH, int n_chunks, int32_t* __restrict__ hist,
                                                                  unsigned* status) {
+  pdl_wait();
+  pdl_launch_dependents();
   extern __shared__ int sh[];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int c = blockIdx.x * kWarps + warp;
@@ -39,6 +41,7 @@ __global__ void __launch_bounds__(kWarps * 32) route_hist_kernel(const int32_t* 
   __syncwarp();
   const int p0 = c * CH, p1 = min(P, p0 + CH);
   bool bad = false;
+#pragma unroll 8
   for (int p = p0 + lane; p < p1; p += 32) {
     const int e = __ldg(idx + p);
     if ((unsigned)e < (unsigned)E)
@@ -59,6 +62,8 @@ __global__ void __launch_bounds__(1024) route_scan_kernel(const int32_t* __restr
   __shared__ int part[1024];
   __shared__ int excl_s[1024];
   __shared__ int wsum[32];
+  pdl_wait();
+  pdl_launch_dependents();
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int S = max(1, 1024 / E);
   const int e = tid % E, seg = tid / E;
@@ -117,6 +122,8 @@ __global__ void __launch_bounds__(kWarps * 32) route_scatter_kernel(const int32_
                                                                     const int32_t* __restrict__ base,
                                                                     int32_t* __restrict__ sorted_pair,
                                                                     int32_t* __restrict__ pair_pos) {
+  pdl_wait();
+  pdl_launch_dependents();
   extern __shared__ int sh[];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int c = blockIdx.x * kWarps + warp;
@@ -126,44 +133,75 @@ __global__ void __launch_bounds__(kWarps * 32) route_scatter_kernel(const int32_
   __syncwarp();
   const int p0 = c * CH, p1 = min(P, p0 + CH);
   const unsigned lower = (1u << lane) - 1u;
-  for (int pb = p0; pb < p1; pb += 32) {
-    const int p = pb + lane;
-    const int e = (p < p1) ? __ldg(idx + p) : -1;
-    const bool ok = (unsigned)e < (unsigned)E;
-    const int key = ok ? e : -1 - lane;  // lanes without a valid expert form singleton groups
-    const unsigned peers = __match_any_sync(0xffffffffu, key);
-    const int rank = __popc(peers & lower);
-    const int b = ok ? cnt[e] : 0;
-    __syncwarp();
-    if (ok) {
-      const int pos = b + rank;
-      if ((unsigned)pos < (unsigned)P) {
-        sorted_pair[pos] = p;
-        pair_pos[p] = pos;
-      }
-      if ((peers >> lane) == 1u) cnt[e] = b + __popc(peers);  // highest lane of the group
+  constexpr int kBatch = 8;  // steps whose expert indices are loaded together
+  for (int pg = p0; pg < p1; pg += 32 * kBatch) {
+    int ev[kBatch];
+#pragma unroll
+    for (int b = 0; b < kBatch; ++b) {
+      const int p = pg + b * 32 + lane;
+      ev[b] = (p < p1) ? __ldg(idx + p) : -1;
     }
-    __syncwarp();
+#pragma unroll
+    for (int b = 0; b < kBatch; ++b) {
+      if (pg + b * 32 >= p1) break;  // warp-uniform
+      const int p = pg + b * 32 + lane;
+      const int e = ev[b];
+      const bool ok = (unsigned)e < (unsigned)E;
+      const int key = ok ? e : -1 - lane;  // lanes without a valid expert form singleton groups
+      const unsigned peers = __match_any_sync(0xffffffffu, key);
+      const int rank = __popc(peers & lower);
+      const int bs = ok ? cnt[e] : 0;
+      __syncwarp();
+      if (ok) {
+        const int pos = bs + rank;
+        if ((unsigned)pos < (unsigned)P) {
+          sorted_pair[pos] = p;
+          pair_pos[p] = pos;
+        }
+        if ((peers >> lane) == 1u) cnt[e] = bs + __popc(peers);  // highest lane of the group
+      }
+      __syncwarp();
+    }
   }
 }
 
-__global__ void __launch_bounds__(kWarps * 32) expand_rows_kernel(const uint4* __restrict__ x,
-                                                                  const int32_t* __restrict__ sorted_pair,
-                                                                  int P, int k, int T, int H8,
-                                                                  uint4* __restrict__ x_exp) {
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int row = blockIdx.x * kWarps + warp;
-  if (row >= P) return;
-  const int t = __ldg(sorted_pair + row) / k;
-  if ((unsigned)t >= (unsigned)T) return;
-  const uint4* src = x + (size_t)t * H8;
-  uint4* dst = x_exp + (size_t)row * H8;
-  for (int i = lane; i < H8; i += 32) dst[i] = __ldg(src + i);
+// x_exp[pos] = x[sorted_pair[pos] / k]: a flat grid over the 16-byte words of
+// x_exp, each thread moving kExpandILP independent words (loads first, then
+// stores) so that enough bytes are in flight to stream at HBM rate.
+constexpr int kExpandILP = 4;
+
+__global__ void __launch_bounds__(256) expand_rows_kernel(const uint4* __restrict__ x,
+                                                          const int32_t* __restrict__ sorted_pair, int P, int k,
+                                                          int T, int H8, uint4* __restrict__ x_exp) {
+  pdl_wait();
+  pdl_launch_dependents();
+  const size_t n = (size_t)P * H8;
+  const size_t base = (size_t)blockIdx.x * blockDim.x * kExpandILP + threadIdx.x;
+  uint4 v[kExpandILP];
+  bool ok[kExpandILP];
+#pragma unroll
+  for (int u = 0; u < kExpandILP; ++u) {
+    const size_t j = base + (size_t)u * blockDim.x;
+    ok[u] = false;
+    if (j < n) {
+      const int row = (int)(j / H8);
+      const int col = (int)(j - (size_t)row * H8);
+      const int t = __ldg(sorted_pair + row) / k;
+      if ((unsigned)t < (unsigned)T) {
+        v[u] = __ldg(x + (size_t)t * H8 + col);
+        ok[u] = true;
+      }
+    }
+  }
+#pragma unroll
+  for (int u = 0; u < kExpandILP; ++u)
+    if (ok[u]) x_exp[base + (size_t)u * blockDim.x] = v[u];
 }
 
 }  // namespace
 
 int routing_chunk_pairs(int P) {
+  if (P <= 4096) return 32;  // decode-sized: one 32-pair step per warp, up to 128 warps
   int ch = (P + 255) / 256;
   ch = (ch + 31) / 32 * 32;
   return ch < 512 ? 512 : ch;
@@ -176,17 +214,20 @@ size_t routing_scratch_bytes(int P, int E) {
 }
 
 cudaError_t launch_expand_rows(const uint16_t* x, const int32_t* sorted_pair, int P, int k, int H,
-                               uint16_t* x_exp, cudaStream_t stream) {
+                               uint16_t* x_exp, cudaStream_t stream, bool pdl) {
   if (P == 0) return cudaSuccess;
   const int T = P / k;
-  expand_rows_kernel<<<(P + kWarps - 1) / kWarps, kWarps * 32, 0, stream>>>(
-      reinterpret_cast<const uint4*>(x), sorted_pair, P, k, T, H / 8, reinterpret_cast<uint4*>(x_exp));
-  return cudaGetLastError();
+  const size_t n = (size_t)P * (H / 8);
+  const size_t per_block = (size_t)256 * kExpandILP;
+  return launch_kernel(expand_rows_kernel, dim3((unsigned)((n + per_block - 1) / per_block)), dim3(256), 0, stream,
+                       pdl, reinterpret_cast<const uint4*>(x), sorted_pair, P, k, T, H / 8,
+                       reinterpret_cast<uint4*>(x_exp));
 }
 
 cudaError_t launch_init_routing(const int32_t* topk_idx, int P, int E, int k, const uint16_t* x, int H,
                                 uint16_t* x_exp, int32_t* counts, int32_t* offsets, int32_t* sorted_pair,
-                                int32_t* pair_pos, int32_t* scratch, unsigned* status, cudaStream_t stream) {
+                                int32_t* pair_pos, int32_t* scratch, unsigned* status, cudaStream_t stream,
+                                bool pdl) {
   const int CH = routing_chunk_pairs(P);
   const int n_chunks = (P + CH - 1) / CH;
   int32_t* hist = scratch;
@@ -201,17 +242,19 @@ cudaError_t launch_init_routing(const int32_t* topk_idx, int P, int E, int k, co
     if (err != cudaSuccess) return err;
   }
   if (n_chunks > 0) {
-    route_hist_kernel<<<blocks, kWarps * 32, smem, stream>>>(topk_idx, P, E, CH, n_chunks, hist, status);
-    if ((err = cudaGetLastError()) != cudaSuccess) return err;
+    err = launch_kernel(route_hist_kernel, dim3(blocks), dim3(kWarps * 32), smem, stream, pdl, topk_idx, P, E, CH,
+                        n_chunks, hist, status);
+    if (err != cudaSuccess) return err;
   }
-  route_scan_kernel<<<1, 1024, 0, stream>>>(hist, base, n_chunks, E, counts, offsets);
-  if ((err = cudaGetLastError()) != cudaSuccess) return err;
+  err = launch_kernel(route_scan_kernel, dim3(1), dim3(1024), 0, stream, pdl, (const int32_t*)hist, base, n_chunks, E,
+                      counts, offsets);
+  if (err != cudaSuccess) return err;
   if (n_chunks > 0) {
-    route_scatter_kernel<<<blocks, kWarps * 32, smem, stream>>>(topk_idx, P, E, CH, n_chunks, base, sorted_pair,
-                                                                pair_pos);
-    if ((err = cudaGetLastError()) != cudaSuccess) return err;
+    err = launch_kernel(route_scatter_kernel, dim3(blocks), dim3(kWarps * 32), smem, stream, pdl, topk_idx, P, E, CH,
+                        n_chunks, (const int32_t*)base, sorted_pair, pair_pos);
+    if (err != cudaSuccess) return err;
   }
-  if (x != nullptr && x_exp != nullptr) return launch_expand_rows(x, sorted_pair, P, k, H, x_exp, stream);
+  if (x != nullptr && x_exp != nullptr) return launch_expand_rows(x, sorted_pair, P, k, H, x_exp, stream, pdl);
   return cudaSuccess;
 }
 
