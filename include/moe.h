@@ -171,14 +171,25 @@ MOE_API int moe_init_routing_static_scratch(const int32_t* topk_idx, int T, int 
                                             int32_t* pair_pos, void* stream);
 
 /*
+ * One-time weight layout for the gate/up GEMMs (the analogue of the pages'
+ * process-weights-after-loading step, [HY3] 6.2): w13 [E,2I,H] with rows
+ * [gate_proj; up_proj] per expert ([Q3] "MoE TP optimisation") is rewritten so
+ * that every group of 32 rows holds 16 gate rows followed by the up rows of the
+ * same 16 features: packed[e][32g + r] = w13[e][16g + r] (r < 16) and
+ * w13[e][I + 16g + r - 16] (r >= 16).  Same size; not in place (w13 != packed).
+ * The grouped gate/up GEMM and moe_layer_forward read this layout.
+ */
+MOE_API int moe_prepack_w13(const uint16_t* w13, int E, int I, int H, uint16_t* w13_packed, void* stream);
+
+/*
  * a3. Grouped gate/up GEMM with fused SwiGLU.  [Q3] "MoE TP optimisation:
  * computation decomposition" (w13 = [gate_proj; up_proj]; SwiGLU splits the
  * last axis in two halves and returns SiLU(x[0]) * x[1]) and "GMM enablement"
  * (all experts in one grouped matmul).
  *
  *  x_rows  [M,H] bf16: rows in expert-sorted order (x_exp of moe_init_routing).
- *  w13     [E,2I,H] bf16: per expert, rows 0..I-1 = gate_proj, I..2I-1 = up_proj
- *          (checkpoint [out_features, in_features] layout, [HY3] 6.2).
+ *  w13     [E,2I,H] bf16 in the packed layout of moe_prepack_w13 (made from the
+ *          checkpoint [out_features, in_features] rows [gate; up], [HY3] 6.2).
  *  offsets [E+1] int32 device: expert e owns rows [offsets[e], offsets[e+1]);
  *          offsets[E] <= M.
  *  act     [M,I] bf16 out: act[pos] = SiLU(g) * u, (g, u) = x_rows[pos] . w13[e]^T,
@@ -226,8 +237,9 @@ MOE_API int moe_finalize_routing(const uint16_t* y_perm, const int32_t* pair_pos
  *
  *  d        layer shape (host pointer).
  *  x        [T,H] bf16; logits [T,E] fp32; bias [E] fp32 or NULL (sigmoid only).
- *  w13      [E,2I,H] bf16; w2 [E,H,I] bf16.
- *  w13_s    [2I_s,H] bf16; w2_s [H,I_s] bf16 (NULL when d->n_shared == 0).
+ *  w13      [E,2I,H] bf16 packed by moe_prepack_w13; w2 [E,H,I] bf16.
+ *  w13_s    [2I_s,H] bf16 packed by moe_prepack_w13 (E = 1); w2_s [H,I_s] bf16
+ *           (both NULL when d->n_shared == 0).
  *  y        [T,H] bf16 out.
  *  topk_w   [T,k] fp32 out; topk_idx [T,k] int32 out; counts [E] int32 out.
  *  ws       at least moe_layer_workspace_size(d) bytes; holds offsets, the

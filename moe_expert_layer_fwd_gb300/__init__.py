@@ -63,6 +63,8 @@ _SIGS = {
                                                        ctypes.c_void_p, ctypes.c_int, ctypes.c_void_p,
                                                        ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
                                                        ctypes.c_void_p, ctypes.c_void_p]),
+    "moe_prepack_w13": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_void_p,
+                                       ctypes.c_void_p]),
     "moe_grouped_gemm_workspace_size": (ctypes.c_size_t, []),
     "moe_grouped_gemm_swiglu": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int,
                                                ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_void_p,
@@ -201,8 +203,19 @@ def moe_init_routing_static_scratch(topk_idx, E: int, x=None, out: Optional[dict
     return o
 
 
+def moe_prepack_w13(w13, out=None, stream=None):
+    """w13 [E,2I,H] (or [2I,H]) rows [gate; up] -> the packed gate/up layout the GEMMs read."""
+    torch = _torch()
+    shape = w13.shape
+    E, twoI, H = (1, shape[0], shape[1]) if w13.dim() == 2 else shape
+    if out is None:
+        out = torch.empty_like(w13)
+    _check(lib().moe_prepack_w13(_ptr(w13), E, twoI // 2, H, _ptr(out), _stream(stream)), "moe_prepack_w13")
+    return out
+
+
 def moe_grouped_gemm_swiglu(x_rows, w13, offsets, act=None, ws=None, stream=None):
-    """a3: act[M,I] = SwiGLU(x_rows . w13[e]^T) per expert segment."""
+    """a3: act[M,I] = SwiGLU(x_rows . w13[e]^T) per expert segment; w13 packed by moe_prepack_w13."""
     torch = _torch()
     M, H = x_rows.shape
     E, twoI, _ = w13.shape
@@ -318,6 +331,7 @@ class MoELayer:
         self.offsets_bytes = moe_layer_workspace_offsets(self.desc)
 
     def forward(self, x, logits, w13, w2, bias=None, w13_s=None, w2_s=None, stream=None):
+        """w13 / w13_s in the packed layout of moe_prepack_w13."""
         moe_layer_forward(self.desc, x, logits, w13, w2, bias, w13_s, w2_s, self.ws, self.y, self.topk_w,
                           self.topk_idx, self.counts, stream)
         return self.y

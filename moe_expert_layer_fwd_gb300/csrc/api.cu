@@ -154,6 +154,15 @@ int moe_init_routing(const int32_t* topk_idx, int T, int E, int k, const uint16_
                                               pair_pos, scratch, status_word(ws), as_stream(stream)));
 }
 
+int moe_prepack_w13(const uint16_t* w13, int E, int I, int H, uint16_t* w13_packed, void* stream) {
+  if (E < 1) return MOE_ERR_INVALID_ARG;
+  int s = check_dims(1, H, I);
+  if (s) return s;
+  if (!w13 || !w13_packed || w13 == w13_packed) return MOE_ERR_INVALID_ARG;
+  if (!aligned16(w13) || !aligned16(w13_packed)) return MOE_ERR_INVALID_ARG;
+  return cuda_status(moe::launch_prepack_w13(w13, E, I, H, w13_packed, as_stream(stream)));
+}
+
 size_t moe_grouped_gemm_workspace_size(void) { return kHeader; }
 
 int moe_grouped_gemm_swiglu(const uint16_t* x_rows, const uint16_t* w13, const int32_t* offsets, int E, int M,

@@ -9,13 +9,19 @@
 // grouped matmul walks per-expert token counts; expert weights keep the
 // checkpoint [out_features, in_features] layout) and 1.1 (one shared expert).
 //
-// Layout of the product: the WEIGHT rows are the UMMA M operand (128 output
-// features per tile) and the expert's TOKEN rows are the N operand (16..256
-// columns, chosen per tile as the rows actually present, rounded up to 16).
-// Decode has 1-8 rows per expert, so this keeps the tensor core work
-// proportional to the real rows while every weight byte is streamed once.
-// Both operands are K-major in global memory and land in shared memory as
-// 128-byte swizzled rows (64 bf16 of K per stage).
+// Layout of the product: the WEIGHT rows are the UMMA M operand and the
+// expert's TOKEN rows are the N operand (16..256 columns, chosen per tile as
+// the rows actually present, rounded up to 16).  Decode has 1-8 rows per
+// expert, so this keeps the tensor core work proportional to the real rows
+// while every weight byte is streamed once.  Both operands are K-major in
+// global memory and land in shared memory as 128-byte swizzled rows (64 bf16
+// of K per stage).
+//
+// The gate/up weight (mode 0) is read in the packed layout of
+// moe_prepack_w13: in every 32-row group the first 16 rows are gate rows and
+// the next 16 the up rows of the same 16 features, so a 128-row box holds 64
+// whole features and, in TMEM, lane l and lane l^16 of each warp hold the
+// gate and the up value of one feature: shfl_xor(16) pairs them for SwiGLU.
 //
 //   tile = (segment, feature tile f, token tile m); segments are the routed
 //   experts in order, then optionally one dense "shared" segment over all T
@@ -28,17 +34,24 @@
 // bytes, limits a stream of small boxes, so each stage moves the weight rows
 // in 128-row boxes (16 KB) and the token rows in BBOX-row boxes.
 //
-// Warp roles (64 + 32*EPI threads, 1 CTA/SM, static round-robin tile schedule):
-//   warp 0      TMA producer: per stage one 128-row weight box (two in mode 0:
-//               the gate rows and the matching up rows) + ceil(rows/BBOX)
-//               token boxes, one lane per box.
-//   warp 1      TMEM allocator + single-thread tcgen05.mma issuer
-//               (M=128, N=rows, K=16 x 4 per stage), double-buffered accumulator.
-//               Mode 0 keeps two accumulators, gate and up, so that TMEM lane l
-//               of both holds the same output feature.
-//   warps 2..   epilogue, EPI/4 warps per TMEM lane quarter (EPI = 8 or 16) taking
-//               interleaved 32-column chunks: tcgen05.ld 32 lanes x 32 columns, then
-//               mode 0 (w13): SwiGLU = SiLU(gate) * up, in fp32, per element.
+// Two instance families:
+//   PAIR = 1 (decode-like, 32 token columns): one CTA per tile, cta_group::1
+//     UMMA M=128; APARTS weight boxes per stage, each into its own accumulator.
+//   PAIR = 2 (prefill-like, 256 token columns): a cluster of two CTAs computes
+//     one tile with the 2-SM UMMA (cta_group::2, M=256): each CTA stages its
+//     own 128 weight rows and HALF of the token rows, so shared-memory traffic
+//     per FLOP is half that of a 1-SM 128x256 tile; the 1-SM kernel is bound by
+//     shared-memory bandwidth (operand reads plus TMA writes) at prefill sizes.
+//     The leader CTA (rank 0) issues the MMAs; both CTAs' TMA loads complete on
+//     the leader's barriers; MMA commits are multicast to both CTAs.
+//
+// Warp roles (64 + 32*EPI threads per CTA, 1 CTA/SM, static round-robin tiles):
+//   warp 0      TMA producer (one lane per box).
+//   warp 1      TMEM allocator + single-thread tcgen05.mma issuer (the leader's
+//               only, when PAIR = 2), double-buffered accumulator.
+//   warps 2..   epilogue, EPI/4 warps per TMEM lane quarter taking interleaved
+//               32-column chunks: tcgen05.ld 32 lanes x 32 columns, then
+//               mode 0 (w13): SwiGLU = SiLU(gate) * up in fp32;
 //               mode 1 (down): multiply by the routing weight of the row.
 // Every wait is bounded (default 2 s); on expiry the CTA raises an abort flag,
 // records DEV_ERR_TIMEOUT, drains its in-flight copies and MMAs and frees TMEM.
@@ -52,7 +65,7 @@
 namespace moe {
 namespace {
 
-constexpr int kBM = 128;                     // weight rows per tile (UMMA M)
+constexpr int kBM = 128;                     // weight rows per box (UMMA M per CTA)
 constexpr int kBK = 64;                      // K per stage: one 128-byte swizzle row of bf16
 constexpr int kRowBytes = kBK * 2;           // 128 B per operand row per stage
 constexpr int kABox = kBM * kRowBytes;       // one 128-row weight box: 16 KB
@@ -62,11 +75,11 @@ constexpr unsigned long long kTimeoutNs = 2000000000ull;
 struct GemmParams {
   const int32_t* offsets;
   int E, M, K;
-  int n_out, n_ftiles, half;        // routed: rows per expert, feature tiles, up-half row offset (mode 0)
+  int n_out, n_ftiles;              // routed: weight rows per expert, feature tiles per expert
   int n_feat;                       // output features per row (I in mode 0, N in mode 1)
   uint16_t* out;
   int ld_out;
-  int has_shared, T_s, n_out_s, n_ftiles_s, half_s, n_feat_s;
+  int has_shared, T_s, n_out_s, n_ftiles_s, n_feat_s;
   uint16_t* s_out;
   int ld_out_s;
   int NT;                           // token rows per tile (multiple of 16)
@@ -76,22 +89,25 @@ struct GemmParams {
   unsigned long long timeout_ns;
 };
 
-template <int NTMAX, int STAGES, int MODE, int BBOX, int EPI>
+template <int NTMAX, int STAGES, int MODE, int BBOX, int EPI, int APARTS, int PAIR>
 struct Layout {
   static constexpr int kThreads = 64 + 32 * EPI;                 // producer, MMA, EPI epilogue warps
-  static constexpr int kAParts = MODE == 0 ? 2 : 1;            // gate + up boxes in mode 0
-  static constexpr int kABytes = kAParts * kABox;
-  static constexpr int kBBytes = NTMAX * kRowBytes;
-  static constexpr int kStageBytes = kABytes + kBBytes;        // multiple of 1024
+  static constexpr int kBRows = NTMAX / PAIR;                    // token rows staged by one CTA
+  static constexpr int kABytes = APARTS * kABox;
+  static constexpr int kBBytes = kBRows * kRowBytes;
+  static constexpr int kStageBytes = kABytes + kBBytes;          // multiple of 1024
   static constexpr int kBarOff = STAGES * kStageBytes;
   static constexpr int kNumBars = 2 * STAGES + 5;
   static constexpr int kMiscOff = kBarOff + kNumBars * 8;
   static constexpr int kScaleOff = kMiscOff + 16;                // mode 1: per-epilogue-warp row scales
   static constexpr int kTabOff = kScaleOff + (MODE == 1 ? EPI * NTMAX * 4 : 0);
-  static constexpr int kAccCols = kAParts * NTMAX;             // TMEM columns of one accumulator buffer
+  static constexpr int kAccCols = APARTS * NTMAX;                // TMEM columns of one accumulator buffer
   static constexpr uint32_t kTmemCols = (2 * kAccCols <= 32) ? 32 : (2 * kAccCols <= 64 ? 64 : (2 * kAccCols <= 128 ? 128 : (2 * kAccCols <= 256 ? 256 : 512)));
+  static constexpr int kFeatPerBox = MODE == 0 ? 64 : 128;       // output features of one weight box
+  static constexpr int kFeatPerTile = kFeatPerBox * APARTS * PAIR;
+  static_assert(PAIR == 1 || APARTS == 1, "CTA pairs stage one weight box per CTA");
   static_assert(2 * kAccCols <= 512, "accumulators exceed TMEM");
-  static_assert(NTMAX % BBOX == 0 && NTMAX / BBOX <= 30, "token boxes");
+  static_assert(kBRows % BBOX == 0 && kBRows / BBOX <= 30, "token boxes");
   static_assert(kStageBytes % 1024 == 0, "stage alignment");
   static_assert(1024 + kTabOff + 2 * 1025 * 4 <= kMaxDynSmem, "shared memory");
   static size_t bytes(int E) { return 1024 + kTabOff + 2 * (size_t)(E + 1) * 4; }
@@ -140,12 +156,12 @@ __device__ __forceinline__ Tile decode_tile(int tile, int routed_total, const in
   return t;
 }
 
-template <int NTMAX, int STAGES, int MODE, int BBOX, int EPI>
+template <int NTMAX, int STAGES, int MODE, int BBOX, int EPI, int APARTS, int PAIR>
 __global__ void __launch_bounds__(64 + 32 * EPI, 1)
     grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                         const __grid_constant__ CUtensorMap tmAs, const __grid_constant__ CUtensorMap tmBs,
                         const GemmParams p) {
-  using L = Layout<NTMAX, STAGES, MODE, BBOX, EPI>;
+  using L = Layout<NTMAX, STAGES, MODE, BBOX, EPI, APARTS, PAIR>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + L::kBarOff);
@@ -156,12 +172,16 @@ __global__ void __launch_bounds__(64 + 32 * EPI, 1)
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::kMiscOff);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::kMiscOff + 4);
   volatile int* cfg_bad = reinterpret_cast<volatile int*>(smem + L::kMiscOff + 8);
+  volatile uint32_t* peer_issued = reinterpret_cast<volatile uint32_t*>(smem + L::kMiscOff + 12);
   float* s_scale = reinterpret_cast<float*>(smem + L::kScaleOff);
   int* s_off = reinterpret_cast<int*>(smem + L::kTabOff);
   int* s_tt = s_off + (p.E + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int E = p.E;
+  const uint32_t rank = PAIR == 2 ? cluster_ctarank() : 0u;  // 0 = leader of the CTA pair
+  const int group = PAIR == 2 ? (int)(blockIdx.x >> 1) : (int)blockIdx.x;
+  const int ngroups = PAIR == 2 ? (int)(gridDim.x >> 1) : (int)gridDim.x;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
@@ -170,11 +190,12 @@ __global__ void __launch_bounds__(64 + 32 * EPI, 1)
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(&tfull[b], 1);
-      mbar_init(&tempty[b], EPI);
+      mbar_init(&tempty[b], PAIR * EPI);  // every epilogue warp of the pair releases the buffer
     }
     mbar_init(done, 1);
     *abort_flag = 0;
     *cfg_bad = 0;
+    *peer_issued = 0;
     fence_mbar_init();
   }
   if (warp == 0 && lane == 0) {
@@ -185,7 +206,10 @@ __global__ void __launch_bounds__(64 + 32 * EPI, 1)
       tma_prefetch_desc(&tmBs);
     }
   }
-  if (warp == 1) tmem_alloc(tmem_slot, L::kTmemCols);
+  if (warp == 1) {
+    if (PAIR == 2) tmem_alloc_pair(tmem_slot, L::kTmemCols);
+    else tmem_alloc(tmem_slot, L::kTmemCols);
+  }
   for (int i = threadIdx.x; i <= E; i += L::kThreads) s_off[i] = p.offsets ? __ldg(p.offsets + i) : 0;
   __syncthreads();
   if (warp == 2) {
@@ -218,7 +242,8 @@ __global__ void __launch_bounds__(64 + 32 * EPI, 1)
     }
   }
   tc_fence_before();
-  __syncthreads();
+  if (PAIR == 2) cluster_sync();  // the pair's barriers are initialised before any cross-CTA signal
+  else __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
 
@@ -226,30 +251,35 @@ __global__ void __launch_bounds__(64 + 32 * EPI, 1)
   const int shared_total = (*cfg_bad || !p.has_shared) ? 0 : ((p.T_s + p.NT - 1) / p.NT) * p.n_ftiles_s;
   const int total = routed_total + shared_total;
   const int KB = p.K / kBK;
+  uint32_t issued = 0;  // producer: stages filled by this CTA
 
   if (warp == 0) {
     // ------------------------------------------------------------ TMA producer
     const uint64_t pol_w = policy_evict_first();
     const uint64_t pol_x = policy_evict_last();
     int stage = 0;
-    uint32_t phase = 0, issued = 0;
+    uint32_t phase = 0;
     bool ok = true;
     // Inside moe_layer_forward this kernel may start while the previous one finishes
     // (programmatic dependent launch): the token rows it loads may still be being
     // written, so wait for that kernel first, then let the next kernel launch.
     pdl_wait();
     pdl_launch_dependents();
-    for (int tile = blockIdx.x; ok && tile < total; tile += gridDim.x) {
+    for (int tile = group; ok && tile < total; tile += ngroups) {
       const Tile t = decode_tile(tile, routed_total, s_off, s_tt, p);
       const CUtensorMap* mA = t.shared ? &tmAs : &tmA;
       const CUtensorMap* mB = t.shared ? &tmBs : &tmB;
-      const int nbox = (t.rows + BBOX - 1) / BBOX;
-      // weight box `lane` (< kAParts): mode 0 lane 0 = gate rows, lane 1 = the matching up rows
-      const int a_row = (t.shared ? 0 : t.e * p.n_out) + (lane == 1 ? (t.shared ? p.half_s : p.half) : 0) +
-                        t.f * kBM;
+      const int nmma = (t.rows + 15) & ~15;
+      const int brows = nmma / PAIR;  // token rows this CTA stages (its half when PAIR = 2)
+      const int nbox = (brows + BBOX - 1) / BBOX;
+      const int b_row = t.row_base + (int)rank * brows;
+      // weight box `lane` (< APARTS) of this CTA
+      const int a_row = (t.shared ? 0 : t.e * p.n_out) + t.f * (kBM * APARTS * PAIR) +
+                        ((int)rank * APARTS + lane) * kBM;
       // Weight rows read by one tile only are streamed past L2 (evict first); weight rows that
       // the segment's other token tiles read again are kept (evict last), like the token rows.
       const uint64_t pol_a = t.nt > 1 ? pol_x : pol_w;
+      const uint32_t tx = (uint32_t)PAIR * (uint32_t)(L::kABytes + nbox * BBOX * kRowBytes);
       for (int kb = 0; kb < KB; ++kb) {
         bool w = (lane == 0) ? mbar_wait_bounded(&empty[stage], phase ^ 1u, abort_flag, p.timeout_ns, p.status)
                              : false;
@@ -258,15 +288,25 @@ __global__ void __launch_bounds__(64 + 32 * EPI, 1)
           ok = false;
           break;
         }
-        if (lane == 0) mbar_arrive_expect_tx(&full[stage], L::kABytes + nbox * BBOX * kRowBytes);
+        if (lane == 0 && rank == 0) mbar_arrive_expect_tx(&full[stage], tx);  // both CTAs' bytes
         __syncwarp();
         uint8_t* sA = smem + stage * L::kStageBytes;
         uint8_t* sB = sA + L::kABytes;
-        if (lane < L::kAParts) {
-          tma_load_2d(sA + lane * kABox, mA, kb * kBK, a_row, &full[stage], pol_a);
-        } else if (lane >= 2 && lane < 2 + nbox) {
-          const int j = lane - 2;
-          tma_load_2d(sB + j * BBOX * kRowBytes, mB, kb * kBK, t.row_base + j * BBOX, &full[stage], pol_x);
+        if (PAIR == 1 || rank == 0) {
+          if (lane < APARTS) {
+            tma_load_2d(sA + lane * kABox, mA, kb * kBK, a_row, &full[stage], pol_a);
+          } else if (lane >= 2 && lane < 2 + nbox) {
+            const int j = lane - 2;
+            tma_load_2d(sB + j * BBOX * kRowBytes, mB, kb * kBK, b_row + j * BBOX, &full[stage], pol_x);
+          }
+        } else {
+          const uint32_t lbar = mapa_shared(smem_u32(&full[stage]), 0);  // the leader's barrier
+          if (lane < APARTS) {
+            tma_load_2d_pair(sA + lane * kABox, mA, kb * kBK, a_row, lbar, pol_a);
+          } else if (lane >= 2 && lane < 2 + nbox) {
+            const int j = lane - 2;
+            tma_load_2d_pair(sB + j * BBOX * kRowBytes, mB, kb * kBK, b_row + j * BBOX, lbar, pol_x);
+          }
         }
         __syncwarp();
         ++issued;
@@ -276,22 +316,27 @@ __global__ void __launch_bounds__(64 + 32 * EPI, 1)
         }
       }
     }
-    // Drain: the last fill of every stage must have landed before the CTA exits.
-    if (lane == 0) {
-      for (int s = 0; s < STAGES; ++s) {
-        const uint32_t n = issued / STAGES + ((uint32_t)s < issued % STAGES ? 1u : 0u);
-        if (n) mbar_wait_bounded(&full[s], (n - 1u) & 1u, abort_flag, p.timeout_ns, p.status, false);
+    if (PAIR == 1) {
+      // Drain: the last fill of every stage must have landed before the CTA exits.
+      if (lane == 0) {
+        for (int s = 0; s < STAGES; ++s) {
+          const uint32_t n = issued / STAGES + ((uint32_t)s < issued % STAGES ? 1u : 0u);
+          if (n) mbar_wait_bounded(&full[s], (n - 1u) & 1u, abort_flag, p.timeout_ns, p.status, false);
+        }
       }
+    } else if (rank == 1 && lane == 0) {
+      // the follower's loads complete on the leader's barriers: tell the leader how many it issued
+      st_shared_cluster_u32(mapa_shared(smem_u32((const void*)peer_issued), 0), issued);
     }
     __syncwarp();
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
-    if (lane == 0) {
+    if (lane == 0 && rank == 0) {
       int stage = 0;
       uint32_t phase = 0;
       bool ok = true;
       int it = 0;
-      for (int tile = blockIdx.x; ok && tile < total; tile += gridDim.x, ++it) {
+      for (int tile = group; ok && tile < total; tile += ngroups, ++it) {
         const Tile t = decode_tile(tile, routed_total, s_off, s_tt, p);
         const int buf = it & 1;
         const uint32_t aph = (uint32_t)(it >> 1) & 1u;
@@ -299,7 +344,7 @@ __global__ void __launch_bounds__(64 + 32 * EPI, 1)
         tc_fence_after();
         const uint32_t d = tmem_base + (uint32_t)(buf * L::kAccCols);
         const int nmma = (t.rows + 15) & ~15;
-        const uint32_t idesc = umma_idesc_bf16(kBM, nmma);
+        const uint32_t idesc = umma_idesc_bf16(kBM * PAIR, nmma);
         for (int kb = 0; kb < KB; ++kb) {
           if (!mbar_wait_bounded(&full[stage], phase, abort_flag, p.timeout_ns, p.status)) {
             ok = false;
@@ -311,31 +356,38 @@ __global__ void __launch_bounds__(64 + 32 * EPI, 1)
 #pragma unroll
           for (int kk = 0; kk < kBK / 16; ++kk) {
             const uint64_t bd = umma_desc_sw128(b + kk * 32);
-            umma_bf16(d, umma_desc_sw128(a + kk * 32), bd, idesc, (kb | kk) != 0);
-            if (MODE == 0)  // up rows into the second accumulator, same token columns
-              umma_bf16(d + NTMAX, umma_desc_sw128(a + kABox + kk * 32), bd, idesc, (kb | kk) != 0);
+#pragma unroll
+            for (int part = 0; part < APARTS; ++part) {
+              const uint64_t ad = umma_desc_sw128(a + part * kABox + kk * 32);
+              if (PAIR == 2) umma_bf16_pair(d + part * NTMAX, ad, bd, idesc, (kb | kk) != 0);
+              else umma_bf16(d + part * NTMAX, ad, bd, idesc, (kb | kk) != 0);
+            }
           }
-          umma_commit(&empty[stage]);
+          if (PAIR == 2) umma_commit_pair(&empty[stage], 0x3);
+          else umma_commit(&empty[stage]);
           if (++stage == STAGES) {
             stage = 0;
             phase ^= 1u;
           }
         }
         if (!ok) break;
-        umma_commit(&tfull[buf]);
+        if (PAIR == 2) umma_commit_pair(&tfull[buf], 0x3);
+        else umma_commit(&tfull[buf]);
       }
       // Drain: every MMA issued by this thread must be complete before TMEM is freed.
-      umma_commit(done);
+      if (PAIR == 2) umma_commit_pair(done, 0x1);
+      else umma_commit(done);
       mbar_wait_bounded(done, 0, abort_flag, p.timeout_ns, p.status, false);
     }
     __syncwarp();
   } else {
     // ------------------------------------------------------------ epilogue
-    const int qw = warp & 3;            // TMEM lane quarter this warp may access
+    const int qw = warp & 3;                 // TMEM lane quarter this warp may access
     constexpr int kPerQ = EPI / 4;           // epilogue warps sharing one TMEM lane quarter
-    const int half_c = (warp - 2) >> 2;     // this warp takes 32-column chunks half_c, half_c + kPerQ, ...
+    const int half_c = (warp - 2) >> 2;      // this warp takes 32-column chunks half_c, half_c + kPerQ, ...
+    const uint32_t tempty_leader = PAIR == 2 ? mapa_shared(smem_u32(&tempty[0]), 0) : 0u;
     int it = 0;
-    for (int tile = blockIdx.x; tile < total; tile += gridDim.x, ++it) {
+    for (int tile = group; tile < total; tile += ngroups, ++it) {
       const Tile t = decode_tile(tile, routed_total, s_off, s_tt, p);
       const int buf = it & 1;
       const uint32_t aph = (uint32_t)(it >> 1) & 1u;
@@ -366,24 +418,38 @@ __global__ void __launch_bounds__(64 + 32 * EPI, 1)
       const int nch = (t.rows + 31) >> 5;  // 32-column chunks
       uint16_t* out = t.shared ? p.s_out : p.out;
       const size_t ld = (size_t)(t.shared ? p.ld_out_s : p.ld_out);
-      const int feat = t.f * kBM + qw * 32 + lane;  // this thread's output feature (TMEM lane)
-      const bool feat_ok = feat < (t.shared ? p.n_feat_s : p.n_feat);
-      uint16_t* orow = out + (size_t)t.row_base * ld + feat;
+      const int n_feat = t.shared ? p.n_feat_s : p.n_feat;
       if (MODE == 0) {
-        for (int c = half_c; c < nch; c += kPerQ) {
-          uint32_t g[32], u[32];
-          tmem_ld32_async(tb + (uint32_t)(c * 32), g);
-          tmem_ld32_async(tb + (uint32_t)(NTMAX + c * 32), u);
-          tmem_wait_ld();
+        // packed gate/up: lanes 0-15 hold gate rows, lanes 16-31 the matching up rows
+        const bool is_gate = lane < 16;
 #pragma unroll
-          for (int i = 0; i < 32; ++i) {
-            const int col = c * 32 + i;
-            const float gv = __uint_as_float(g[i]);
-            const float a = gv / (1.0f + expf(-gv)) * __uint_as_float(u[i]);
-            if (col < t.rows && feat_ok) orow[(size_t)col * ld] = f32_to_bf16_rne(a);
+        for (int part = 0; part < APARTS; ++part) {
+          const int feat = t.f * L::kFeatPerTile + ((int)rank * APARTS + part) * L::kFeatPerBox + qw * 16 +
+                           (lane & 15);
+          const bool feat_ok = feat < n_feat;
+          uint16_t* orow = out + (size_t)t.row_base * ld + feat;
+          for (int c = half_c; c < nch; c += kPerQ) {
+            uint32_t v[32];
+            tmem_ld32_async(tb + (uint32_t)(part * NTMAX + c * 32), v);
+            tmem_wait_ld();
+            // gate lanes finish columns 0-15 of the chunk, up lanes columns 16-31
+            const int col0 = c * 32 + (is_gate ? 0 : 16);
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+              const float send = __uint_as_float(is_gate ? v[16 + i] : v[i]);
+              const float recv = __shfl_xor_sync(0xffffffffu, send, 16);
+              const float g = is_gate ? __uint_as_float(v[i]) : recv;
+              const float u = is_gate ? recv : __uint_as_float(v[16 + i]);
+              const float a = g / (1.0f + expf(-g)) * u;
+              const int col = col0 + i;
+              if (col < t.rows && feat_ok) orow[(size_t)col * ld] = f32_to_bf16_rne(a);
+            }
           }
         }
       } else {
+        const int feat = t.f * L::kFeatPerTile + (int)rank * kBM + qw * 32 + lane;
+        const bool feat_ok = feat < n_feat;
+        uint16_t* orow = out + (size_t)t.row_base * ld + feat;
         for (int c = half_c; c < nch; c += kPerQ) {
           uint32_t v[32];
           tmem_ld32_async(tb + (uint32_t)(c * 32), v);
@@ -399,16 +465,53 @@ __global__ void __launch_bounds__(64 + 32 * EPI, 1)
       }
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&tempty[buf]);
+      if (lane == 0) {
+        if (PAIR == 2) mbar_arrive_cluster(tempty_leader + (uint32_t)(buf * 8));  // the leader's barrier
+        else mbar_arrive(&tempty[buf]);
+      }
     }
   }
 
   tc_fence_before();
-  __syncthreads();
-  if (warp == 1) {
-    tc_fence_after();
-    tmem_dealloc(tmem_base, L::kTmemCols);
+  if (PAIR == 2) {
+    cluster_sync();  // both CTAs have stopped issuing; the follower's load count has arrived
+    if (rank == 0 && warp == 0 && lane == 0) {
+      // Drain: every stage's last fill, by either CTA, must have landed before either CTA exits.
+      const uint32_t pi = *peer_issued;
+      const uint32_t n_all = issued > pi ? issued : pi;
+      for (int s = 0; s < STAGES; ++s) {
+        const uint32_t n = n_all / STAGES + ((uint32_t)s < n_all % STAGES ? 1u : 0u);
+        if (n) mbar_wait_bounded(&full[s], (n - 1u) & 1u, abort_flag, p.timeout_ns, p.status, false);
+      }
+    }
+    cluster_sync();
+    if (warp == 1) {
+      tc_fence_after();
+      tmem_dealloc_pair(tmem_base, L::kTmemCols);
+    }
+  } else {
+    __syncthreads();
+    if (warp == 1) {
+      tc_fence_after();
+      tmem_dealloc(tmem_base, L::kTmemCols);
+    }
   }
+}
+
+// Packed gate/up layout: w13p[e][32g + r] = w13[e][16g + r] for r < 16 (gate), and
+// w13[e][I + 16g + r - 16] for r >= 16 (up).  One thread per 16 bytes.
+__global__ void __launch_bounds__(256) prepack_w13_kernel(const uint4* __restrict__ w13, int E, int I, int H8,
+                                                          uint4* __restrict__ w13p) {
+  const size_t n = (size_t)E * 2 * I * H8;
+  const size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x;
+  if (i >= n) return;
+  const size_t row = i / H8;
+  const int col = (int)(i - row * H8);
+  const int e = (int)(row / (2 * I));
+  const int r = (int)(row - (size_t)e * 2 * I);
+  const int g = r >> 5, q = r & 31;
+  const int src = q < 16 ? g * 16 + q : I + g * 16 + (q - 16);
+  w13p[i] = __ldg(w13 + ((size_t)e * 2 * I + src) * H8 + col);
 }
 
 // ---------------------------------------------------------------- host side
@@ -448,11 +551,13 @@ int num_sms() {
   return n > 0 ? n : 1;
 }
 
-template <int NTMAX, int STAGES, int MODE, int BBOX, int EPI>
+template <int NTMAX, int STAGES, int MODE, int BBOX, int EPI, int APARTS, int PAIR>
 cudaError_t launch_instance(const GroupedGemmProblem& pr, GemmParams gp, cudaStream_t stream, bool pdl) {
-  using L = Layout<NTMAX, STAGES, MODE, BBOX, EPI>;
+  using L = Layout<NTMAX, STAGES, MODE, BBOX, EPI, APARTS, PAIR>;
   const bool has_shared = gp.has_shared != 0;
   gp.NT = NTMAX;
+  gp.n_ftiles = (gp.n_feat + L::kFeatPerTile - 1) / L::kFeatPerTile;
+  gp.n_ftiles_s = has_shared ? (gp.n_feat_s + L::kFeatPerTile - 1) / L::kFeatPerTile : 0;
   CUtensorMap ta, tb, tas, tbs;
   if (pr.M > 0) {
     if (!make_map(&ta, pr.w, pr.K, (long long)pr.E * pr.n_out, kBM)) return cudaErrorInvalidValue;
@@ -470,11 +575,12 @@ cudaError_t launch_instance(const GroupedGemmProblem& pr, GemmParams gp, cudaStr
     tas = ta;
     tbs = tb;
   }
-  auto kern = grouped_gemm_kernel<NTMAX, STAGES, MODE, BBOX, EPI>;
+  auto kern = grouped_gemm_kernel<NTMAX, STAGES, MODE, BBOX, EPI, APARTS, PAIR>;
   const size_t smem = L::bytes(gp.E);
   cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (err != cudaSuccess) return err;
-  return launch_kernel(kern, dim3(num_sms()), dim3(L::kThreads), smem, stream, pdl, ta, tb, tas, tbs, gp);
+  const int grid = PAIR == 2 ? (num_sms() & ~1) : num_sms();
+  return launch_kernel_cluster(kern, dim3(grid), dim3(L::kThreads), smem, stream, pdl, PAIR, ta, tb, tas, tbs, gp);
 }
 
 }  // namespace
@@ -488,18 +594,14 @@ cudaError_t launch_grouped_gemm(const GroupedGemmProblem& pr, cudaStream_t strea
   gp.M = pr.M;
   gp.K = pr.K;
   gp.n_out = pr.n_out;
-  gp.half = pr.n_out / 2;
   gp.n_feat = pr.mode == 0 ? pr.n_out / 2 : pr.n_out;
-  gp.n_ftiles = (gp.n_feat + kBM - 1) / kBM;
   gp.out = pr.out;
   gp.ld_out = pr.ld_out;
   gp.has_shared = has_shared ? 1 : 0;
   if (has_shared) {
     gp.T_s = pr.T_s;
     gp.n_out_s = pr.n_out_s;
-    gp.half_s = pr.n_out_s / 2;
     gp.n_feat_s = pr.mode == 0 ? pr.n_out_s / 2 : pr.n_out_s;
-    gp.n_ftiles_s = (gp.n_feat_s + kBM - 1) / kBM;
   }
   gp.s_out = pr.s_out;
   gp.ld_out_s = pr.ld_out_s;
@@ -507,14 +609,23 @@ cudaError_t launch_grouped_gemm(const GroupedGemmProblem& pr, cudaStream_t strea
   gp.sorted_pair = pr.sorted_pair;
   gp.status = pr.status;
   gp.timeout_ns = kTimeoutNs;
-  // Decode-like problems (a few rows per expert) take the 32-column instance
-  // with a deep pipeline; prefill-like ones the wide instances.
+  // Decode-like problems (a few rows per expert) take the 32-column single-CTA
+  // instances with a deep pipeline; prefill-like ones the 256-column CTA-pair
+  // instances.
   const bool narrow = (long long)pr.M <= 32LL * pr.E && (!has_shared || pr.T_s <= 32);
   if (narrow)
-    return pr.mode == 0 ? launch_instance<32, 5, 0, 16, 8>(pr, gp, stream, pdl)
-                        : launch_instance<32, 10, 1, 16, 8>(pr, gp, stream, pdl);
-  return pr.mode == 0 ? launch_instance<128, 4, 0, 64, 8>(pr, gp, stream, pdl)
-                      : launch_instance<256, 4, 1, 64, 16>(pr, gp, stream, pdl);
+    return pr.mode == 0 ? launch_instance<32, 5, 0, 16, 8, 2, 1>(pr, gp, stream, pdl)
+                        : launch_instance<32, 10, 1, 16, 8, 1, 1>(pr, gp, stream, pdl);
+  return pr.mode == 0 ? launch_instance<256, 6, 0, 64, 16, 1, 2>(pr, gp, stream, pdl)
+                      : launch_instance<256, 6, 1, 64, 16, 1, 2>(pr, gp, stream, pdl);
+}
+
+cudaError_t launch_prepack_w13(const uint16_t* w13, int E, int I, int H, uint16_t* w13p, cudaStream_t stream) {
+  const size_t n = (size_t)E * 2 * I * (H / 8);
+  if (n == 0) return cudaSuccess;
+  prepack_w13_kernel<<<(unsigned)((n + 255) / 256), 256, 0, stream>>>(reinterpret_cast<const uint4*>(w13), E, I,
+                                                                      H / 8, reinterpret_cast<uint4*>(w13p));
+  return cudaGetLastError();
 }
 
 }  // namespace moe

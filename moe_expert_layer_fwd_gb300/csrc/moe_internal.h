@@ -27,7 +27,7 @@ struct GroupedGemmProblem {
   int mode;                    // 0: SwiGLU epilogue (w13), 1: scaled epilogue (down)
   // routed experts
   const uint16_t* a_rows;      // [M,K] token rows in expert-sorted order
-  const uint16_t* w;           // [E, n_out, K]
+  const uint16_t* w;           // [E, n_out, K] (mode 0: packed gate/up layout of moe_prepack_w13)
   const int32_t* offsets;      // [E+1] device
   int E, M, K, n_out;          // n_out = 2I (mode 0) or N (mode 1)
   uint16_t* out;               // [M, ld_out]
@@ -44,6 +44,9 @@ struct GroupedGemmProblem {
 };
 
 cudaError_t launch_grouped_gemm(const GroupedGemmProblem& p, cudaStream_t stream, bool pdl = false);
+
+// w13 [E,2I,H] -> packed gate/up layout read by the mode-0 grouped GEMM.
+cudaError_t launch_prepack_w13(const uint16_t* w13, int E, int I, int H, uint16_t* w13p, cudaStream_t stream);
 
 cudaError_t launch_finalize(const uint16_t* y_perm, const int32_t* pair_pos, const uint16_t* shared, int T, int k,
                             int H, uint16_t* y, cudaStream_t stream, bool pdl = false);

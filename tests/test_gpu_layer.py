@@ -30,9 +30,9 @@ def _layer(moe, cfg):
 
 def _run(moe, cfg, inp, layer=None):
     layer = layer or _layer(moe, cfg)
-    t = dict(x=dev_bf16(inp.x), logits=dev(inp.logits), w13=dev_bf16(inp.w13), w2=dev_bf16(inp.w2),
-             bias=dev(inp.bias) if inp.bias is not None else None,
-             w13_s=dev_bf16(inp.w13_s) if inp.w13_s is not None else None,
+    t = dict(x=dev_bf16(inp.x), logits=dev(inp.logits), w13=moe.moe_prepack_w13(dev_bf16(inp.w13)),
+             w2=dev_bf16(inp.w2), bias=dev(inp.bias) if inp.bias is not None else None,
+             w13_s=moe.moe_prepack_w13(dev_bf16(inp.w13_s)) if inp.w13_s is not None else None,
              w2_s=dev_bf16(inp.w2_s) if inp.w2_s is not None else None)
     layer.forward(**t)
     return layer, t

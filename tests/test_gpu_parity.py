@@ -115,7 +115,25 @@ GEMM_CASES = [
     # ... and the 256-wide instance (many rows per expert, ragged tails)
     ([300, 0, 1, 255, 256, 257, 40, 600], 256, 128),
     ([513, 64, 0, 1000], 1024, 256),
+    ([400, 3, 0, 700, 17], 384, 192),  # feature tiles cut by I and by N
 ]
+
+
+def _pack_ref(w13):
+    """The packed gate/up layout written out from its definition (numpy indexing)."""
+    E, twoI, H = w13.shape
+    I = twoI // 2
+    r = np.arange(twoI)
+    g, q = r // 32, r % 32
+    src = np.where(q < 16, 16 * g + q, I + 16 * g + q - 16)
+    return w13[:, src, :]
+
+
+@pytest.mark.parametrize("E,I,H", [(3, 128, 256), (2, 1536, 64), (1, 64, 128)])
+def test_prepack_w13_is_the_packed_permutation(moe, E, I, H):
+    w13 = mi.normal_bf16(E + I, 2, (E, 2 * I, H), 0.0, 0.02)
+    got = moe.moe_prepack_w13(dev_bf16(w13))
+    assert (host(got.view(_torch().int16)).view(np.uint16) == _pack_ref(w13)).all()
 
 
 @pytest.mark.parametrize("counts,H,I", GEMM_CASES)
@@ -127,7 +145,7 @@ def test_grouped_gemm_swiglu_parity(moe, counts, H, I):
     x = mi.normal_bf16(rng_seed, 1, (M, H))
     w13 = mi.normal_bf16(rng_seed, 2, (E, 2 * I, H), 0.0, 0.02)
     ref = oracle.grouped_gemm_swiglu(x, w13, off)
-    act = moe.moe_grouped_gemm_swiglu(dev_bf16(x), dev_bf16(w13), dev(off))
+    act = moe.moe_grouped_gemm_swiglu(dev_bf16(x), moe.moe_prepack_w13(dev_bf16(w13)), dev(off))
     got = host_bf16_f64(act)
     assert_close(got, ref, "act")
     assert_bf16_rounding_close(got, ref, "act")
