@@ -156,6 +156,27 @@ __device__ __forceinline__ Tile decode_tile(int tile, int routed_total, const in
   return t;
 }
 
+// Stores 16 token columns [col0, col0+16) of this lane's output feature, two features per
+// 32-bit store.  Lanes l and l^1 hold adjacent features (the even lane the even feature),
+// so after one shfl_xor(1) per column pair the even lane holds both features of the even
+// column and the odd lane both features of the odd one.  `orow` points at this lane's
+// feature in token row 0 of the tile; `ok` says the feature exists (output widths are
+// multiples of 64, so both lanes of a pair agree on it).
+__device__ __forceinline__ void store_pairs16(const float* v, int lane, uint16_t* orow, size_t ld, int col0,
+                                              int rows, bool ok) {
+  const bool odd = lane & 1;
+  uint16_t* base = odd ? orow - 1 : orow;  // the pair's even feature
+#pragma unroll
+  for (int m = 0; m < 8; ++m) {
+    const float send = odd ? v[2 * m] : v[2 * m + 1];
+    const float recv = __shfl_xor_sync(0xffffffffu, send, 1);
+    const float lo = odd ? recv : v[2 * m];
+    const float hi = odd ? v[2 * m + 1] : recv;
+    const int col = col0 + 2 * m + (odd ? 1 : 0);
+    if (ok && col < rows) *reinterpret_cast<uint32_t*>(base + (size_t)col * ld) = pack_bf16x2(lo, hi);
+  }
+}
+
 template <int NTMAX, int STAGES, int MODE, int BBOX, int EPI, int APARTS, int PAIR>
 __global__ void __launch_bounds__(64 + 32 * EPI, 1)
     grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
@@ -434,16 +455,16 @@ __global__ void __launch_bounds__(64 + 32 * EPI, 1)
             tmem_wait_ld();
             // gate lanes finish columns 0-15 of the chunk, up lanes columns 16-31
             const int col0 = c * 32 + (is_gate ? 0 : 16);
+            float a[16];
 #pragma unroll
             for (int i = 0; i < 16; ++i) {
               const float send = __uint_as_float(is_gate ? v[16 + i] : v[i]);
               const float recv = __shfl_xor_sync(0xffffffffu, send, 16);
               const float g = is_gate ? __uint_as_float(v[i]) : recv;
               const float u = is_gate ? recv : __uint_as_float(v[16 + i]);
-              const float a = g / (1.0f + expf(-g)) * u;
-              const int col = col0 + i;
-              if (col < t.rows && feat_ok) orow[(size_t)col * ld] = f32_to_bf16_rne(a);
+              a[i] = g / (1.0f + expf(-g)) * u;
             }
+            store_pairs16(a, lane, orow, ld, col0, t.rows, feat_ok);
           }
         }
       } else {
@@ -454,12 +475,11 @@ __global__ void __launch_bounds__(64 + 32 * EPI, 1)
           uint32_t v[32];
           tmem_ld32_async(tb + (uint32_t)(c * 32), v);
           tmem_wait_ld();
+          float o[32];
 #pragma unroll
-          for (int i = 0; i < 32; ++i) {
-            const int col = c * 32 + i;
-            const float sv = scale ? wsc[col] : 1.0f;
-            if (col < t.rows && feat_ok) orow[(size_t)col * ld] = f32_to_bf16_rne(__uint_as_float(v[i]) * sv);
-          }
+          for (int i = 0; i < 32; ++i) o[i] = __uint_as_float(v[i]) * (scale ? wsc[c * 32 + i] : 1.0f);
+          store_pairs16(o, lane, orow, ld, c * 32, t.rows, feat_ok);
+          store_pairs16(o + 16, lane, orow, ld, c * 32 + 16, t.rows, feat_ok);
         }
         __syncwarp();  // the next tile rewrites this warp's scales
       }
