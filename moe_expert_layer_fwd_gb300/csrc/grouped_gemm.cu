@@ -66,8 +66,8 @@ namespace moe {
 namespace {
 
 constexpr int kBM = 128;                     // weight rows per box (UMMA M per CTA)
-constexpr int kBK = 64;                      // K per stage: one 128-byte swizzle row of bf16
-constexpr int kRowBytes = kBK * 2;           // 128 B per operand row per stage
+constexpr int kBK = 64;                      // K per chunk: one 128-byte swizzle row of bf16
+constexpr int kRowBytes = kBK * 2;           // 128 B per operand row per chunk
 constexpr int kABox = kBM * kRowBytes;       // one 128-row weight box: 16 KB
 constexpr int kMaxDynSmem = 232448;          // 227 KB per CTA
 constexpr unsigned long long kTimeoutNs = 2000000000ull;
@@ -89,12 +89,18 @@ struct GemmParams {
   unsigned long long timeout_ns;
 };
 
-template <int NTMAX, int STAGES, int MODE, int BBOX, int EPI, int APARTS, int PAIR>
+template <int NTMAX, int STAGES, int MODE, int BBOX, int EPI, int APARTS, int PAIR, int KC>
 struct Layout {
   static constexpr int kThreads = 64 + 32 * EPI;                 // producer, MMA, EPI epilogue warps
   static constexpr int kBRows = NTMAX / PAIR;                    // token rows staged by one CTA
-  static constexpr int kABytes = APARTS * kABox;
-  static constexpr int kBBytes = kBRows * kRowBytes;
+  // A stage holds KC chunks of K = 64 (one 128-byte swizzle row each): KC x [APARTS weight
+  // boxes], then KC x [kBRows token rows].  The tensor pipe only runs at full rate when the
+  // MMA thread issues about 8 MMAs between two waits, so CTA pairs (4 MMAs per chunk) use KC = 2.
+  static constexpr int kAChunk = APARTS * kABox;
+  static constexpr int kBChunk = kBRows * kRowBytes;
+  static constexpr int kABytes = KC * kAChunk;
+  static constexpr int kBBytes = KC * kBChunk;
+  static constexpr int kStageK = KC * kBK;
   static constexpr int kStageBytes = kABytes + kBBytes;          // multiple of 1024
   static constexpr int kBarOff = STAGES * kStageBytes;
   static constexpr int kNumBars = 2 * STAGES + 5;
@@ -107,7 +113,8 @@ struct Layout {
   static constexpr int kFeatPerTile = kFeatPerBox * APARTS * PAIR;
   static_assert(PAIR == 1 || APARTS == 1, "CTA pairs stage one weight box per CTA");
   static_assert(2 * kAccCols <= 512, "accumulators exceed TMEM");
-  static_assert(kBRows % BBOX == 0 && kBRows / BBOX <= 30, "token boxes");
+  static_assert(kBRows % BBOX == 0 && KC * (kBRows / BBOX) <= 24 && KC * APARTS <= 8, "boxes per stage");
+  static_assert(kAChunk % 1024 == 0 && kBChunk % 1024 == 0, "chunk alignment");
   static_assert(kStageBytes % 1024 == 0, "stage alignment");
   static_assert(1024 + kTabOff + 2 * 1025 * 4 <= kMaxDynSmem, "shared memory");
   static size_t bytes(int E) { return 1024 + kTabOff + 2 * (size_t)(E + 1) * 4; }
@@ -177,12 +184,12 @@ __device__ __forceinline__ void store_pairs16(const float* v, int lane, uint16_t
   }
 }
 
-template <int NTMAX, int STAGES, int MODE, int BBOX, int EPI, int APARTS, int PAIR>
+template <int NTMAX, int STAGES, int MODE, int BBOX, int EPI, int APARTS, int PAIR, int KC>
 __global__ void __launch_bounds__(64 + 32 * EPI, 1)
     grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                         const __grid_constant__ CUtensorMap tmAs, const __grid_constant__ CUtensorMap tmBs,
                         const GemmParams p) {
-  using L = Layout<NTMAX, STAGES, MODE, BBOX, EPI, APARTS, PAIR>;
+  using L = Layout<NTMAX, STAGES, MODE, BBOX, EPI, APARTS, PAIR, KC>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + L::kBarOff);
@@ -271,7 +278,7 @@ __global__ void __launch_bounds__(64 + 32 * EPI, 1)
   const int routed_total = *cfg_bad ? 0 : s_tt[E] * p.n_ftiles;
   const int shared_total = (*cfg_bad || !p.has_shared) ? 0 : ((p.T_s + p.NT - 1) / p.NT) * p.n_ftiles_s;
   const int total = routed_total + shared_total;
-  const int KB = p.K / kBK;
+  const int KB = (p.K + L::kStageK - 1) / L::kStageK;  // stages per tile; K is a multiple of kBK
   uint32_t issued = 0;  // producer: stages filled by this CTA
 
   if (warp == 0) {
@@ -294,14 +301,18 @@ __global__ void __launch_bounds__(64 + 32 * EPI, 1)
       const int brows = nmma / PAIR;  // token rows this CTA stages (its half when PAIR = 2)
       const int nbox = (brows + BBOX - 1) / BBOX;
       const int b_row = t.row_base + (int)rank * brows;
-      // weight box `lane` (< APARTS) of this CTA
+      // weight box `apart` (< APARTS) of this CTA
       const int a_row = (t.shared ? 0 : t.e * p.n_out) + t.f * (kBM * APARTS * PAIR) +
-                        ((int)rank * APARTS + lane) * kBM;
+                        ((int)rank * APARTS + (lane % APARTS)) * kBM;
       // Weight rows read by one tile only are streamed past L2 (evict first); weight rows that
       // the segment's other token tiles read again are kept (evict last), like the token rows.
       const uint64_t pol_a = t.nt > 1 ? pol_x : pol_w;
-      const uint32_t tx = (uint32_t)PAIR * (uint32_t)(L::kABytes + nbox * BBOX * kRowBytes);
+      // lanes 0..KC*APARTS-1 load weight boxes, lanes 8..8+KC*nbox-1 token boxes
+      const int ac = lane / APARTS, apart = lane % APARTS;
+      const int bc = (lane - 8) / max(nbox, 1), bj = (lane - 8) % max(nbox, 1);
       for (int kb = 0; kb < KB; ++kb) {
+        const int nch = min(KC, (p.K - kb * L::kStageK) / kBK);  // chunks in this stage
+        const uint32_t tx = (uint32_t)(PAIR * nch) * (uint32_t)(L::kAChunk + nbox * BBOX * kRowBytes);
         bool w = (lane == 0) ? mbar_wait_bounded(&empty[stage], phase ^ 1u, abort_flag, p.timeout_ns, p.status)
                              : false;
         w = __shfl_sync(0xffffffffu, w, 0);
@@ -313,21 +324,16 @@ __global__ void __launch_bounds__(64 + 32 * EPI, 1)
         __syncwarp();
         uint8_t* sA = smem + stage * L::kStageBytes;
         uint8_t* sB = sA + L::kABytes;
-        if (PAIR == 1 || rank == 0) {
-          if (lane < APARTS) {
-            tma_load_2d(sA + lane * kABox, mA, kb * kBK, a_row, &full[stage], pol_a);
-          } else if (lane >= 2 && lane < 2 + nbox) {
-            const int j = lane - 2;
-            tma_load_2d(sB + j * BBOX * kRowBytes, mB, kb * kBK, b_row + j * BBOX, &full[stage], pol_x);
-          }
-        } else {
-          const uint32_t lbar = mapa_shared(smem_u32(&full[stage]), 0);  // the leader's barrier
-          if (lane < APARTS) {
-            tma_load_2d_pair(sA + lane * kABox, mA, kb * kBK, a_row, lbar, pol_a);
-          } else if (lane >= 2 && lane < 2 + nbox) {
-            const int j = lane - 2;
-            tma_load_2d_pair(sB + j * BBOX * kRowBytes, mB, kb * kBK, b_row + j * BBOX, lbar, pol_x);
-          }
+        const bool a_op = lane < KC * APARTS && ac < nch;
+        const bool b_op = lane >= 8 && lane < 8 + KC * nbox && bc < nch;
+        uint8_t* dst = a_op ? sA + ac * L::kAChunk + apart * kABox : sB + bc * L::kBChunk + bj * BBOX * kRowBytes;
+        const CUtensorMap* map = a_op ? mA : mB;
+        const int x = kb * L::kStageK + (a_op ? ac : bc) * kBK;
+        const int y = a_op ? a_row : b_row + bj * BBOX;
+        const uint64_t pol = a_op ? pol_a : pol_x;
+        if (a_op || b_op) {
+          if (PAIR == 1 || rank == 0) tma_load_2d(dst, map, x, y, &full[stage], pol);
+          else tma_load_2d_pair(dst, map, x, y, mapa_shared(smem_u32(&full[stage]), 0), pol);  // leader's barrier
         }
         __syncwarp();
         ++issued;
@@ -357,6 +363,7 @@ __global__ void __launch_bounds__(64 + 32 * EPI, 1)
       uint32_t phase = 0;
       bool ok = true;
       int it = 0;
+      const uint64_t desc0 = umma_desc_sw128(smem_u32(smem));
       for (int tile = group; ok && tile < total; tile += ngroups, ++it) {
         const Tile t = decode_tile(tile, routed_total, s_off, s_tt, p);
         const int buf = it & 1;
@@ -372,16 +379,24 @@ __global__ void __launch_bounds__(64 + 32 * EPI, 1)
             break;
           }
           tc_fence_after();
-          const uint32_t a = smem_u32(smem + stage * L::kStageBytes);
-          const uint32_t b = a + L::kABytes;
+          // descriptors of the stage's first chunk; the address field (bits 0-13, in 16-byte
+          // units) of a later chunk or K step is reached by adding its offset / 16
+          const uint64_t ad0 = desc0 + (uint64_t)((stage * L::kStageBytes) >> 4);
+          const uint64_t bd0 = ad0 + (uint64_t)(L::kABytes >> 4);
+          const bool two = KC == 1 || kb * L::kStageK + kBK < p.K;  // false: last stage holds one chunk
 #pragma unroll
-          for (int kk = 0; kk < kBK / 16; ++kk) {
-            const uint64_t bd = umma_desc_sw128(b + kk * 32);
+          for (int c = 0; c < KC; ++c) {
+            if (c > 0 && !two) break;
 #pragma unroll
-            for (int part = 0; part < APARTS; ++part) {
-              const uint64_t ad = umma_desc_sw128(a + part * kABox + kk * 32);
-              if (PAIR == 2) umma_bf16_pair(d + part * NTMAX, ad, bd, idesc, (kb | kk) != 0);
-              else umma_bf16(d + part * NTMAX, ad, bd, idesc, (kb | kk) != 0);
+            for (int kk = 0; kk < kBK / 16; ++kk) {
+              const uint64_t bd = bd0 + (uint64_t)((c * L::kBChunk + kk * 32) >> 4);
+#pragma unroll
+              for (int part = 0; part < APARTS; ++part) {
+                const uint64_t ad = ad0 + (uint64_t)((c * L::kAChunk + part * kABox + kk * 32) >> 4);
+                const uint32_t acc = (kb | c | kk) != 0;
+                if (PAIR == 2) umma_bf16_pair(d + part * NTMAX, ad, bd, idesc, acc);
+                else umma_bf16(d + part * NTMAX, ad, bd, idesc, acc);
+              }
             }
           }
           if (PAIR == 2) umma_commit_pair(&empty[stage], 0x3);
@@ -431,7 +446,8 @@ __global__ void __launch_bounds__(64 + 32 * EPI, 1)
         }
         __syncwarp();
       }
-      bool w = (lane == 0) ? mbar_wait_bounded(&tfull[buf], aph, abort_flag, p.timeout_ns, p.status) : false;
+      // The epilogue has slack: it sleeps in the barrier instead of polling.
+      bool w = (lane == 0) ? mbar_wait_sleep(&tfull[buf], aph, abort_flag, p.timeout_ns, p.status) : false;
       w = __shfl_sync(0xffffffffu, w, 0);
       if (!w) break;
       tc_fence_after();
@@ -571,9 +587,9 @@ int num_sms() {
   return n > 0 ? n : 1;
 }
 
-template <int NTMAX, int STAGES, int MODE, int BBOX, int EPI, int APARTS, int PAIR>
+template <int NTMAX, int STAGES, int MODE, int BBOX, int EPI, int APARTS, int PAIR, int KC>
 cudaError_t launch_instance(const GroupedGemmProblem& pr, GemmParams gp, cudaStream_t stream, bool pdl) {
-  using L = Layout<NTMAX, STAGES, MODE, BBOX, EPI, APARTS, PAIR>;
+  using L = Layout<NTMAX, STAGES, MODE, BBOX, EPI, APARTS, PAIR, KC>;
   const bool has_shared = gp.has_shared != 0;
   gp.NT = NTMAX;
   gp.n_ftiles = (gp.n_feat + L::kFeatPerTile - 1) / L::kFeatPerTile;
@@ -595,7 +611,7 @@ cudaError_t launch_instance(const GroupedGemmProblem& pr, GemmParams gp, cudaStr
     tas = ta;
     tbs = tb;
   }
-  auto kern = grouped_gemm_kernel<NTMAX, STAGES, MODE, BBOX, EPI, APARTS, PAIR>;
+  auto kern = grouped_gemm_kernel<NTMAX, STAGES, MODE, BBOX, EPI, APARTS, PAIR, KC>;
   const size_t smem = L::bytes(gp.E);
   cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (err != cudaSuccess) return err;
@@ -631,13 +647,21 @@ cudaError_t launch_grouped_gemm(const GroupedGemmProblem& pr, cudaStream_t strea
   gp.timeout_ns = kTimeoutNs;
   // Decode-like problems (a few rows per expert) take the 32-column single-CTA
   // instances with a deep pipeline; prefill-like ones the 256-column CTA-pair
-  // instances.
+  // instances.  Among those, segments averaging fewer than 256 rows do fewer than
+  // 256 FLOPs per weight byte, below the GPU's ratio of tensor rate to HBM bandwidth:
+  // they stream weights, and six 64-deep stages keep more weight bytes in flight.
+  // Longer segments are compute-bound and take three 128-deep stages, which let the
+  // MMA thread issue 8 MMAs between two waits (the tensor pipe idles otherwise).
   const bool narrow = (long long)pr.M <= 32LL * pr.E && (!has_shared || pr.T_s <= 32);
   if (narrow)
-    return pr.mode == 0 ? launch_instance<32, 5, 0, 16, 8, 2, 1>(pr, gp, stream, pdl)
-                        : launch_instance<32, 10, 1, 16, 8, 1, 1>(pr, gp, stream, pdl);
-  return pr.mode == 0 ? launch_instance<256, 6, 0, 64, 16, 1, 2>(pr, gp, stream, pdl)
-                      : launch_instance<256, 6, 1, 64, 16, 1, 2>(pr, gp, stream, pdl);
+    return pr.mode == 0 ? launch_instance<32, 5, 0, 16, 8, 2, 1, 1>(pr, gp, stream, pdl)
+                        : launch_instance<32, 10, 1, 16, 8, 1, 1, 1>(pr, gp, stream, pdl);
+  const bool streaming = (long long)pr.M < 256LL * pr.E;
+  if (streaming)
+    return pr.mode == 0 ? launch_instance<256, 6, 0, 64, 16, 1, 2, 1>(pr, gp, stream, pdl)
+                        : launch_instance<256, 6, 1, 64, 16, 1, 2, 1>(pr, gp, stream, pdl);
+  return pr.mode == 0 ? launch_instance<256, 3, 0, 64, 16, 1, 2, 2>(pr, gp, stream, pdl)
+                      : launch_instance<256, 3, 1, 64, 16, 1, 2, 2>(pr, gp, stream, pdl);
 }
 
 cudaError_t launch_prepack_w13(const uint16_t* w13, int E, int I, int H, uint16_t* w13p, cudaStream_t stream) {

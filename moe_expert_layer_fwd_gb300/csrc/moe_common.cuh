@@ -75,6 +75,19 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
   return ok != 0;
 }
 
+// One try_wait that may suspend the thread until the phase completes or `hint_ns` passes.
+__device__ __forceinline__ bool mbar_try_wait_sleep(uint64_t* bar, uint32_t parity, uint32_t hint_ns) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity), "r"(hint_ns)
+      : "memory");
+  return ok != 0;
+}
+
 // Waits for the phase with the given parity to complete.  Gives up after
 // `timeout_ns` of waiting (or, if `honor_abort`, as soon as another role of the
 // CTA raised its abort flag): raises the abort flag, sets DEV_ERR_TIMEOUT and
@@ -92,6 +105,24 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity
         set_status(status, DEV_ERR_TIMEOUT);
         return false;
       }
+    }
+  }
+}
+
+// mbar_wait_bounded for a waiter with slack: each try_wait may suspend the thread for up to
+// 20 us (it wakes as soon as the phase completes), so the abort flag and the deadline are
+// checked every 20 us at most and the waiting thread takes no issue slots meanwhile.
+__device__ __forceinline__ bool mbar_wait_sleep(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
+                                                uint64_t timeout_ns, unsigned* status, bool honor_abort = true) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t deadline = globaltimer_ns() + timeout_ns;
+  for (;;) {
+    if (mbar_try_wait_sleep(bar, parity, 20000u)) return true;
+    if (honor_abort && *abort_flag) return false;
+    if (globaltimer_ns() > deadline) {
+      *abort_flag = 1;
+      set_status(status, DEV_ERR_TIMEOUT);
+      return false;
     }
   }
 }

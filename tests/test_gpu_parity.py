@@ -116,6 +116,9 @@ GEMM_CASES = [
     ([300, 0, 1, 255, 256, 257, 40, 600], 256, 128),
     ([513, 64, 0, 1000], 1024, 256),
     ([400, 3, 0, 700, 17], 384, 192),  # feature tiles cut by I and by N
+    # >= 256 rows per expert: compute-bound instance with 128-deep stages; K = 320 and 192
+    # leave a last stage holding a single 64-deep chunk
+    ([600, 0, 900, 257], 320, 192),
 ]
 
 
