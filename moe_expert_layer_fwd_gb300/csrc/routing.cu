@@ -165,37 +165,37 @@ __global__ void __launch_bounds__(kWarps * 32) route_scatter_kernel(const int32_
   }
 }
 
-// x_exp[pos] = x[sorted_pair[pos] / k]: a flat grid over the 16-byte words of
-// x_exp, each thread moving kExpandILP independent words (loads first, then
-// stores) so that enough bytes are in flight to stream at HBM rate.
-constexpr int kExpandILP = 4;
+// x_exp[pos] = x[sorted_pair[pos] / k].  A block moves kExpandRows consecutive rows of x_exp;
+// its threads stride over the 16-byte words of a row, and each thread loads its word of every
+// one of the block's rows before storing any, so kExpandRows independent loads per thread are
+// in flight.  Indices are 32-bit: row * H8 + column stays below 2^31 words per row block.
+constexpr int kExpandRows = 4;
 
-__global__ void __launch_bounds__(256) expand_rows_kernel(const uint4* __restrict__ x,
+__global__ void __launch_bounds__(512) expand_rows_kernel(const uint4* __restrict__ x,
                                                           const int32_t* __restrict__ sorted_pair, int P, int k,
                                                           int T, int H8, uint4* __restrict__ x_exp) {
   pdl_wait();
   pdl_launch_dependents();
-  const size_t n = (size_t)P * H8;
-  const size_t base = (size_t)blockIdx.x * blockDim.x * kExpandILP + threadIdx.x;
-  uint4 v[kExpandILP];
-  bool ok[kExpandILP];
+  const int r0 = blockIdx.x * kExpandRows;
+  const uint4* src[kExpandRows];
 #pragma unroll
-  for (int u = 0; u < kExpandILP; ++u) {
-    const size_t j = base + (size_t)u * blockDim.x;
-    ok[u] = false;
-    if (j < n) {
-      const int row = (int)(j / H8);
-      const int col = (int)(j - (size_t)row * H8);
-      const int t = __ldg(sorted_pair + row) / k;
-      if ((unsigned)t < (unsigned)T) {
-        v[u] = __ldg(x + (size_t)t * H8 + col);
-        ok[u] = true;
-      }
+  for (int u = 0; u < kExpandRows; ++u) {
+    src[u] = nullptr;
+    if (r0 + u < P) {
+      const int t = __ldg(sorted_pair + r0 + u) / k;
+      if ((unsigned)t < (unsigned)T) src[u] = x + (size_t)t * H8;
     }
   }
+  uint4* dst = x_exp + (size_t)r0 * H8;
+  for (int c = threadIdx.x; c < H8; c += blockDim.x) {
+    uint4 v[kExpandRows];
 #pragma unroll
-  for (int u = 0; u < kExpandILP; ++u)
-    if (ok[u]) x_exp[base + (size_t)u * blockDim.x] = v[u];
+    for (int u = 0; u < kExpandRows; ++u)
+      if (src[u]) v[u] = __ldg(src[u] + c);
+#pragma unroll
+    for (int u = 0; u < kExpandRows; ++u)
+      if (src[u]) dst[u * H8 + c] = v[u];
+  }
 }
 
 }  // namespace
@@ -217,10 +217,10 @@ cudaError_t launch_expand_rows(const uint16_t* x, const int32_t* sorted_pair, in
                                uint16_t* x_exp, cudaStream_t stream, bool pdl) {
   if (P == 0) return cudaSuccess;
   const int T = P / k;
-  const size_t n = (size_t)P * (H / 8);
-  const size_t per_block = (size_t)256 * kExpandILP;
-  return launch_kernel(expand_rows_kernel, dim3((unsigned)((n + per_block - 1) / per_block)), dim3(256), 0, stream,
-                       pdl, reinterpret_cast<const uint4*>(x), sorted_pair, P, k, T, H / 8,
+  const int H8 = H / 8;
+  const int threads = H8 >= 512 ? 512 : (H8 + 31) / 32 * 32;
+  return launch_kernel(expand_rows_kernel, dim3((unsigned)((P + kExpandRows - 1) / kExpandRows)), dim3(threads), 0,
+                       stream, pdl, reinterpret_cast<const uint4*>(x), sorted_pair, P, k, T, H8,
                        reinterpret_cast<uint4*>(x_exp));
 }
 
