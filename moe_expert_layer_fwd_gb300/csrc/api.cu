@@ -41,7 +41,7 @@ int check_dims(long long P, int H, int I) {
 
 // Layout of the moe_layer_forward workspace.
 struct LayerWs {
-  size_t offsets, scratch, sorted_pair, pair_pos, x_exp, act, y_perm, act_s, shared, total;
+  size_t offsets, scratch, sorted_pair, pair_pos, gflags, x_exp, act, y_perm, act_s, shared, total;
 };
 
 LayerWs layer_ws(const moe_layer_desc* d) {
@@ -52,6 +52,7 @@ LayerWs layer_ws(const moe_layer_desc* d) {
   w.scratch = o;     o = align_up(o + moe::routing_scratch_bytes((int)P, d->E));
   w.sorted_pair = o; o = align_up(o + P * 4);
   w.pair_pos = o;    o = align_up(o + P * 4);
+  w.gflags = o;      o = align_up(o + (P + 15) / 16 * 4);  // one flag per 16 gathered rows
   w.x_exp = o;       o = align_up(o + P * d->H * 2);
   w.act = o;         o = align_up(o + P * d->I * 2);
   w.y_perm = o;      o = align_up(o + P * d->H * 2);
@@ -279,6 +280,7 @@ int layer_forward_impl(const moe_layer_desc* d, const uint16_t* x, const float* 
   int32_t* sorted_pair = reinterpret_cast<int32_t*>(base + L.sorted_pair);
   int32_t* pair_pos = reinterpret_cast<int32_t*>(base + L.pair_pos);
   uint16_t* x_exp = reinterpret_cast<uint16_t*>(base + L.x_exp);
+  unsigned* gflags = reinterpret_cast<unsigned*>(base + L.gflags);
   uint16_t* act = reinterpret_cast<uint16_t*>(base + L.act);
   uint16_t* y_perm = reinterpret_cast<uint16_t*>(base + L.y_perm);
   uint16_t* act_s = reinterpret_cast<uint16_t*>(base + L.act_s);
@@ -297,8 +299,10 @@ int layer_forward_impl(const moe_layer_desc* d, const uint16_t* x, const float* 
   // Every kernel after the first may start while its predecessor finishes (programmatic
   // dependent launch); each waits for its inputs before touching them.
   constexpr bool kPdl = true;
-  e = moe::launch_init_routing(topk_idx, P, E, k, x, H, x_exp, counts, offsets, sorted_pair, pair_pos, scratch,
-                               status, st, kPdl);
+  // The gate/up GEMM gathers the token rows into x_exp itself (overlapping the gather with
+  // its matmuls), so routing only sorts; it also clears the GEMM's gather flags.
+  e = moe::launch_init_routing(topk_idx, P, E, k, nullptr, H, nullptr, counts, offsets, sorted_pair, pair_pos,
+                               scratch, status, st, kPdl, gflags, (P + 15) / 16);
   if (e != cudaSuccess) return MOE_ERR_CUDA;
 
   moe::GroupedGemmProblem g1{};
@@ -312,6 +316,11 @@ int layer_forward_impl(const moe_layer_desc* d, const uint16_t* x, const float* 
   g1.n_out = 2 * I;
   g1.out = act;
   g1.ld_out = I;
+  g1.g_x = x;
+  g1.g_sorted_pair = sorted_pair;
+  g1.g_k = k;
+  g1.g_T = T;
+  g1.g_flags = gflags;
   if (sh) {
     g1.s_rows = x;
     g1.s_w = w13_s;
@@ -398,9 +407,12 @@ int moe_layer_forward_events(const moe_layer_desc* d, const uint16_t* x, const f
 int moe_layer_kernel_launches(const moe_layer_desc* d) {
   if (check_desc(d)) return 0;
   if (d->T == 0) return 0;
-  // gating 1 + routing (hist, scan, scatter, gather) 4 + gate/up GEMM 1 + down GEMM 1
-  // (+1 when the shared expert's intermediate size differs) + finalize 1
-  return 8 + ((d->n_shared > 0 && d->I_s != d->I) ? 1 : 0);
+  // gating 1 + routing (hist, scan, scatter) 3 + row gather 1 (decode-sized problems only:
+  // otherwise the gate/up GEMM gathers) + gate/up GEMM 1 + down GEMM 1 (+1 when the shared
+  // expert's intermediate size differs) + finalize 1
+  const bool sh = d->n_shared > 0;
+  const bool gather_kernel = moe::grouped_gemm_narrow(d->T * d->k, d->E, sh, d->T);
+  return 7 + (gather_kernel ? 1 : 0) + ((sh && d->I_s != d->I) ? 1 : 0);
 }
 
 }  // extern "C"

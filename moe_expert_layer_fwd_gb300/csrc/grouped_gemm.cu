@@ -87,11 +87,36 @@ struct GemmParams {
   const int32_t* sorted_pair;
   unsigned* status;
   unsigned long long timeout_ns;
+  // In-kernel row gather (mode 0 with gather warps; g_flags == nullptr: off).  The routed token
+  // rows are then copied x -> a_rows (= g_xexp) by the gather warps while the GEMM runs:
+  // a_rows[pos] = x[sorted_pair[pos] / k], in chunks of kGatherRows rows whose flags
+  // (zeroed before the launch) are set once the chunk is written.
+  const uint4* g_x;
+  const int32_t* g_sp;
+  uint4* g_xexp;
+  int g_k, g_T, g_H8;
+  unsigned* g_flags;
 };
 
-template <int NTMAX, int STAGES, int MODE, int BBOX, int EPI, int APARTS, int PAIR, int KC>
+constexpr int kGatherRows = 16;  // rows per gather chunk (one flag each)
+
+// Acquire load of a flag written with release semantics by another CTA.
+__device__ __forceinline__ unsigned ld_acquire_gpu(const unsigned* p) {
+  unsigned v;
+  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+__device__ __forceinline__ void st_release_gpu(unsigned* p, unsigned v) {
+  asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+// Orders this thread's generic-proxy global accesses with its async-proxy (TMA) ones.
+__device__ __forceinline__ void fence_proxy_async_global() {
+  asm volatile("fence.proxy.async.global;" ::: "memory");
+}
+
+template <int NTMAX, int STAGES, int MODE, int BBOX, int EPI, int APARTS, int PAIR, int KC, int GW>
 struct Layout {
-  static constexpr int kThreads = 64 + 32 * EPI;                 // producer, MMA, EPI epilogue warps
+  static constexpr int kThreads = 64 + 32 * (EPI + GW);          // producer, MMA, EPI epilogue, GW gather warps
   static constexpr int kBRows = NTMAX / PAIR;                    // token rows staged by one CTA
   // A stage holds KC chunks of K = 64 (one 128-byte swizzle row each): KC x [APARTS weight
   // boxes], then KC x [kBRows token rows].  The tensor pipe only runs at full rate when the
@@ -184,12 +209,12 @@ __device__ __forceinline__ void store_pairs16(const float* v, int lane, uint16_t
   }
 }
 
-template <int NTMAX, int STAGES, int MODE, int BBOX, int EPI, int APARTS, int PAIR, int KC>
-__global__ void __launch_bounds__(64 + 32 * EPI, 1)
+template <int NTMAX, int STAGES, int MODE, int BBOX, int EPI, int APARTS, int PAIR, int KC, int GW>
+__global__ void __launch_bounds__(64 + 32 * (EPI + GW), 1)
     grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                         const __grid_constant__ CUtensorMap tmAs, const __grid_constant__ CUtensorMap tmBs,
                         const GemmParams p) {
-  using L = Layout<NTMAX, STAGES, MODE, BBOX, EPI, APARTS, PAIR, KC>;
+  using L = Layout<NTMAX, STAGES, MODE, BBOX, EPI, APARTS, PAIR, KC, GW>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + L::kBarOff);
@@ -310,6 +335,37 @@ __global__ void __launch_bounds__(64 + 32 * EPI, 1)
       // lanes 0..KC*APARTS-1 load weight boxes, lanes 8..8+KC*nbox-1 token boxes
       const int ac = lane / APARTS, apart = lane % APARTS;
       const int bc = (lane - 8) / max(nbox, 1), bj = (lane - 8) % max(nbox, 1);
+      if (GW > 0 && p.g_flags != nullptr && !t.shared) {
+        // The token rows this CTA stages must have been gathered: wait for the flags of the
+        // chunks holding rows [b_row, b_end), one lane per chunk, then order the TMA reads
+        // after the gathering CTAs' writes.
+        const int b_end = min(b_row + brows, t.row_base + t.rows);
+        const int q0 = b_row / kGatherRows;
+        const int nq = b_end > b_row ? (b_end - 1) / kGatherRows - q0 + 1 : 0;
+        bool fine = true;
+        if (lane < nq) {
+          const unsigned* f = p.g_flags + q0 + lane;
+          if (ld_acquire_gpu(f) == 0u) {
+            const uint64_t deadline = globaltimer_ns() + p.timeout_ns;
+            while (ld_acquire_gpu(f) == 0u) {
+              if (*abort_flag || globaltimer_ns() > deadline) {
+                fine = false;
+                break;
+              }
+              __nanosleep(64);
+            }
+          }
+        }
+        if (!__all_sync(0xffffffffu, fine)) {
+          if (lane == 0) {
+            *abort_flag = 1;
+            set_status(p.status, DEV_ERR_TIMEOUT);
+          }
+          ok = false;
+          break;
+        }
+        fence_proxy_async_global();
+      }
       for (int kb = 0; kb < KB; ++kb) {
         const int nch = min(KC, (p.K - kb * L::kStageK) / kBK);  // chunks in this stage
         const uint32_t tx = (uint32_t)(PAIR * nch) * (uint32_t)(L::kAChunk + nbox * BBOX * kRowBytes);
@@ -416,7 +472,7 @@ __global__ void __launch_bounds__(64 + 32 * EPI, 1)
       mbar_wait_bounded(done, 0, abort_flag, p.timeout_ns, p.status, false);
     }
     __syncwarp();
-  } else {
+  } else if (warp < 2 + EPI) {
     // ------------------------------------------------------------ epilogue
     const int qw = warp & 3;                 // TMEM lane quarter this warp may access
     constexpr int kPerQ = EPI / 4;           // epilogue warps sharing one TMEM lane quarter
@@ -508,6 +564,50 @@ __global__ void __launch_bounds__(64 + 32 * EPI, 1)
         else mbar_arrive(&tempty[buf]);
       }
     }
+  } else if (GW > 0 && p.g_flags != nullptr) {
+    // ------------------------------------------------------------ row gather
+    // Chunk q (rows [16q, 16q+16)) belongs to CTA (q / GW) % gridDim.x, warp q % GW; every warp
+    // walks its chunks in ascending order, so rows are gathered in the order the tiles need them
+    // (tiles are dealt out in expert order).  Nothing here waits on another CTA.
+    pdl_wait();  // sorted_pair comes from the previous kernel
+    const int gw = warp - 2 - EPI;
+    const int n_chunks = (p.M + kGatherRows - 1) / kGatherRows;
+    const int H8 = p.g_H8;
+    for (int q = GW * (int)blockIdx.x + gw; q < n_chunks; q += GW * (int)gridDim.x) {
+      const int r0 = q * kGatherRows, nrow = min(kGatherRows, p.M - r0);
+      int tl = -1;  // lane i < nrow: source token of row r0 + i
+      if (lane < nrow) {
+        tl = __ldg(p.g_sp + r0 + lane) / p.g_k;
+        if ((unsigned)tl >= (unsigned)p.g_T) tl = -1;
+      }
+      for (int i = 0; i < nrow; i += 4) {
+        int tr[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          tr[u] = __shfl_sync(0xffffffffu, tl, min(i + u, 31));
+          if (i + u >= nrow) tr[u] = -1;
+        }
+        for (int c = lane; c < H8; c += 2 * 32) {
+          uint4 v[4][2];
+#pragma unroll
+          for (int u = 0; u < 4; ++u)
+#pragma unroll
+            for (int w = 0; w < 2; ++w)
+              if (tr[u] >= 0 && c + 32 * w < H8) v[u][w] = __ldg(p.g_x + (size_t)tr[u] * H8 + c + 32 * w);
+#pragma unroll
+          for (int u = 0; u < 4; ++u)
+#pragma unroll
+            for (int w = 0; w < 2; ++w)
+              if (tr[u] >= 0 && c + 32 * w < H8) p.g_xexp[(size_t)(r0 + i + u) * H8 + c + 32 * w] = v[u][w];
+        }
+      }
+      __syncwarp();
+      if (lane == 0) {
+        fence_proxy_async_global();
+        __threadfence();
+        st_release_gpu(p.g_flags + q, 1u);
+      }
+    }
   }
 
   tc_fence_before();
@@ -589,9 +689,9 @@ int num_sms() {
   return n > 0 ? n : 1;
 }
 
-template <int NTMAX, int STAGES, int MODE, int BBOX, int EPI, int APARTS, int PAIR, int KC>
+template <int NTMAX, int STAGES, int MODE, int BBOX, int EPI, int APARTS, int PAIR, int KC, int GW>
 cudaError_t launch_instance(const GroupedGemmProblem& pr, GemmParams gp, cudaStream_t stream, bool pdl) {
-  using L = Layout<NTMAX, STAGES, MODE, BBOX, EPI, APARTS, PAIR, KC>;
+  using L = Layout<NTMAX, STAGES, MODE, BBOX, EPI, APARTS, PAIR, KC, GW>;
   const bool has_shared = gp.has_shared != 0;
   gp.NT = NTMAX;
   gp.n_ftiles = (gp.n_feat + L::kFeatPerTile - 1) / L::kFeatPerTile;
@@ -613,15 +713,39 @@ cudaError_t launch_instance(const GroupedGemmProblem& pr, GemmParams gp, cudaStr
     tas = ta;
     tbs = tb;
   }
-  auto kern = grouped_gemm_kernel<NTMAX, STAGES, MODE, BBOX, EPI, APARTS, PAIR, KC>;
+  auto kern = grouped_gemm_kernel<NTMAX, STAGES, MODE, BBOX, EPI, APARTS, PAIR, KC, GW>;
   const size_t smem = L::bytes(gp.E);
   cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (err != cudaSuccess) return err;
-  const int grid = PAIR == 2 ? (num_sms() & ~1) : num_sms();
+  int grid = PAIR == 2 ? (num_sms() & ~1) : num_sms();
+  if (PAIR == 2) {
+    // Persistent grid: no more CTA pairs than can be resident at once (the gather flags are
+    // waited on across CTAs, which needs every CTA of the grid running).
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(L::kThreads);
+    cfg.dynamicSmemBytes = smem;
+    cudaLaunchAttribute attr;
+    attr.id = cudaLaunchAttributeClusterDimension;
+    attr.val.clusterDim.x = 2;
+    attr.val.clusterDim.y = 1;
+    attr.val.clusterDim.z = 1;
+    cfg.attrs = &attr;
+    cfg.numAttrs = 1;
+    int clusters = 0;
+    if (cudaOccupancyMaxActiveClusters(&clusters, kern, &cfg) == cudaSuccess && clusters > 0 && 2 * clusters < grid)
+      grid = 2 * clusters;
+  }
   return launch_kernel_cluster(kern, dim3(grid), dim3(L::kThreads), smem, stream, pdl, PAIR, ta, tb, tas, tbs, gp);
 }
 
 }  // namespace
+
+bool grouped_gemm_narrow(int M, int E, bool has_shared, int T_s) {
+  // Decode-like problems (a few rows per expert) take the 32-column single-CTA instances with
+  // a deep pipeline; prefill-like ones the 256-column CTA-pair instances.
+  return (long long)M <= 32LL * E && (!has_shared || T_s <= 32);
+}
 
 cudaError_t launch_grouped_gemm(const GroupedGemmProblem& pr, cudaStream_t stream, bool pdl) {
   const bool has_shared = pr.s_rows != nullptr && pr.T_s > 0;
@@ -647,23 +771,39 @@ cudaError_t launch_grouped_gemm(const GroupedGemmProblem& pr, cudaStream_t strea
   gp.sorted_pair = pr.sorted_pair;
   gp.status = pr.status;
   gp.timeout_ns = kTimeoutNs;
-  // Decode-like problems (a few rows per expert) take the 32-column single-CTA
-  // instances with a deep pipeline; prefill-like ones the 256-column CTA-pair
-  // instances.  Among those, segments averaging fewer than 256 rows do fewer than
+  const bool gather = pr.mode == 0 && pr.g_x != nullptr && pr.M > 0;
+  // Among the CTA-pair instances, segments averaging fewer than 256 rows do fewer than
   // 256 FLOPs per weight byte, below the GPU's ratio of tensor rate to HBM bandwidth:
   // they stream weights, and six 64-deep stages keep more weight bytes in flight.
   // Longer segments are compute-bound and take three 128-deep stages, which let the
   // MMA thread issue 8 MMAs between two waits (the tensor pipe idles otherwise).
-  const bool narrow = (long long)pr.M <= 32LL * pr.E && (!has_shared || pr.T_s <= 32);
-  if (narrow)
-    return pr.mode == 0 ? launch_instance<32, 5, 0, 16, 8, 2, 1, 1>(pr, gp, stream, pdl)
-                        : launch_instance<32, 10, 1, 16, 8, 1, 1, 1>(pr, gp, stream, pdl);
+  // The 256-wide gate/up instances run 12 epilogue warps and 4 warps that gather the token
+  // rows while the GEMM runs (when asked to); the 32-wide ones have the rows gathered by a
+  // separate kernel first.
+  if (grouped_gemm_narrow(pr.M, pr.E, has_shared, pr.T_s)) {
+    if (gather) {
+      cudaError_t e = launch_expand_rows(pr.g_x, pr.g_sorted_pair, pr.M, pr.g_k, pr.K, const_cast<uint16_t*>(pr.a_rows),
+                                         stream, pdl);
+      if (e != cudaSuccess) return e;
+    }
+    return pr.mode == 0 ? launch_instance<32, 5, 0, 16, 8, 2, 1, 1, 0>(pr, gp, stream, pdl)
+                        : launch_instance<32, 10, 1, 16, 8, 1, 1, 1, 0>(pr, gp, stream, pdl);
+  }
+  if (gather) {
+    gp.g_x = reinterpret_cast<const uint4*>(pr.g_x);
+    gp.g_sp = pr.g_sorted_pair;
+    gp.g_xexp = reinterpret_cast<uint4*>(const_cast<uint16_t*>(pr.a_rows));
+    gp.g_k = pr.g_k;
+    gp.g_T = pr.g_T;
+    gp.g_H8 = pr.K / 8;
+    gp.g_flags = pr.g_flags;
+  }
   const bool streaming = (long long)pr.M < 256LL * pr.E;
   if (streaming)
-    return pr.mode == 0 ? launch_instance<256, 6, 0, 64, 16, 1, 2, 1>(pr, gp, stream, pdl)
-                        : launch_instance<256, 6, 1, 64, 16, 1, 2, 1>(pr, gp, stream, pdl);
-  return pr.mode == 0 ? launch_instance<256, 3, 0, 64, 16, 1, 2, 2>(pr, gp, stream, pdl)
-                      : launch_instance<256, 3, 1, 64, 16, 1, 2, 2>(pr, gp, stream, pdl);
+    return pr.mode == 0 ? launch_instance<256, 6, 0, 64, 12, 1, 2, 1, 4>(pr, gp, stream, pdl)
+                        : launch_instance<256, 6, 1, 64, 16, 1, 2, 1, 0>(pr, gp, stream, pdl);
+  return pr.mode == 0 ? launch_instance<256, 3, 0, 64, 12, 1, 2, 2, 4>(pr, gp, stream, pdl)
+                      : launch_instance<256, 3, 1, 64, 16, 1, 2, 2, 0>(pr, gp, stream, pdl);
 }
 
 cudaError_t launch_prepack_w13(const uint16_t* w13, int E, int I, int H, uint16_t* w13p, cudaStream_t stream) {

@@ -15,10 +15,12 @@ cudaError_t launch_gating_topk(const float* logits, const float* bias, int T, in
 // Init-routing scratch: per-chunk expert histograms and bases.
 int routing_chunk_pairs(int P);
 size_t routing_scratch_bytes(int P, int E);
+// `zero`, `n_zero`: optional words zeroed by the routing kernels (the gather flags of the
+// following gate/up GEMM).
 cudaError_t launch_init_routing(const int32_t* topk_idx, int P, int E, int k, const uint16_t* x, int H,
                                 uint16_t* x_exp, int32_t* counts, int32_t* offsets, int32_t* sorted_pair,
                                 int32_t* pair_pos, int32_t* scratch, unsigned* status, cudaStream_t stream,
-                                bool pdl = false);
+                                bool pdl = false, unsigned* zero = nullptr, int n_zero = 0);
 cudaError_t launch_expand_rows(const uint16_t* x, const int32_t* sorted_pair, int P, int k, int H,
                                uint16_t* x_exp, cudaStream_t stream, bool pdl = false);
 
@@ -41,7 +43,17 @@ struct GroupedGemmProblem {
   uint16_t* s_out;             // [T_s, ld_out_s]
   int ld_out_s;
   unsigned* status;
+  // Mode 0 only, optional: gather the routed rows while the GEMM runs, a_rows[pos] =
+  // g_x[g_sorted_pair[pos] / g_k] (a_rows is then written, not only read).  g_flags: one word
+  // per 16 rows of a_rows, zeroed before the launch.
+  const uint16_t* g_x;
+  const int32_t* g_sorted_pair;
+  int g_k, g_T;
+  unsigned* g_flags;
 };
+
+// Whether the problem takes the 32-column (decode) instances.
+bool grouped_gemm_narrow(int M, int E, bool has_shared, int T_s);
 
 cudaError_t launch_grouped_gemm(const GroupedGemmProblem& p, cudaStream_t stream, bool pdl = false);
 

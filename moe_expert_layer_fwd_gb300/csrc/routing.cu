@@ -58,13 +58,15 @@ __global__ void __launch_bounds__(kWarps * 32) route_hist_kernel(const int32_t* 
 __global__ void __launch_bounds__(1024) route_scan_kernel(const int32_t* __restrict__ hist,
                                                           int32_t* __restrict__ base, int n_chunks, int E,
                                                           int32_t* __restrict__ counts,
-                                                          int32_t* __restrict__ offsets) {
+                                                          int32_t* __restrict__ offsets,
+                                                          unsigned* __restrict__ zero, int n_zero) {
   __shared__ int part[1024];
   __shared__ int excl_s[1024];
   __shared__ int wsum[32];
   pdl_wait();
   pdl_launch_dependents();
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  for (int i = tid; i < n_zero; i += 1024) zero[i] = 0u;
   const int S = max(1, 1024 / E);
   const int e = tid % E, seg = tid / E;
   const bool active = seg < S;
@@ -227,7 +229,7 @@ cudaError_t launch_expand_rows(const uint16_t* x, const int32_t* sorted_pair, in
 cudaError_t launch_init_routing(const int32_t* topk_idx, int P, int E, int k, const uint16_t* x, int H,
                                 uint16_t* x_exp, int32_t* counts, int32_t* offsets, int32_t* sorted_pair,
                                 int32_t* pair_pos, int32_t* scratch, unsigned* status, cudaStream_t stream,
-                                bool pdl) {
+                                bool pdl, unsigned* zero, int n_zero) {
   const int CH = routing_chunk_pairs(P);
   const int n_chunks = (P + CH - 1) / CH;
   int32_t* hist = scratch;
@@ -247,7 +249,7 @@ cudaError_t launch_init_routing(const int32_t* topk_idx, int P, int E, int k, co
     if (err != cudaSuccess) return err;
   }
   err = launch_kernel(route_scan_kernel, dim3(1), dim3(1024), 0, stream, pdl, (const int32_t*)hist, base, n_chunks, E,
-                      counts, offsets);
+                      counts, offsets, zero, n_zero);
   if (err != cudaSuccess) return err;
   if (n_chunks > 0) {
     err = launch_kernel(route_scatter_kernel, dim3(blocks), dim3(kWarps * 32), smem, stream, pdl, topk_idx, P, E, CH,
