@@ -407,11 +407,11 @@ int moe_layer_forward_events(const moe_layer_desc* d, const uint16_t* x, const f
 int moe_layer_kernel_launches(const moe_layer_desc* d) {
   if (check_desc(d)) return 0;
   if (d->T == 0) return 0;
-  // gating 1 + routing (hist, scan, scatter) 3 + row gather 1 (decode-sized problems only:
-  // otherwise the gate/up GEMM gathers) + gate/up GEMM 1 + down GEMM 1 (+1 when the shared
-  // expert's intermediate size differs) + finalize 1
+  // gating 1 + routing (hist, scan, scatter) 3 + row gather 1 (unless the gate/up GEMM gathers
+  // its rows itself) + gate/up GEMM 1 + down GEMM 1 (+1 when the shared expert's intermediate
+  // size differs) + finalize 1
   const bool sh = d->n_shared > 0;
-  const bool gather_kernel = moe::grouped_gemm_narrow(d->T * d->k, d->E, sh, d->T);
+  const bool gather_kernel = !moe::grouped_gemm_gathers_inline(d->T * d->k, d->E, sh, d->T);
   return 7 + (gather_kernel ? 1 : 0) + ((sh && d->I_s != d->I) ? 1 : 0);
 }
 

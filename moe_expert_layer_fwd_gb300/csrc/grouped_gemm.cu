@@ -747,6 +747,18 @@ bool grouped_gemm_narrow(int M, int E, bool has_shared, int T_s) {
   return (long long)M <= 32LL * E && (!has_shared || T_s <= 32);
 }
 
+bool grouped_gemm_streaming(int M, int E) {
+  // Segments averaging fewer than 256 rows do fewer than 256 FLOPs per weight byte, below the
+  // GPU's ratio of tensor rate to HBM bandwidth: those GEMMs stream weights.
+  return (long long)M < 256LL * E;
+}
+
+bool grouped_gemm_gathers_inline(int M, int E, bool has_shared, int T_s) {
+  // Only a compute-bound gate/up GEMM hides the row gather's HBM traffic behind its matmuls; a
+  // weight-streaming one would only share its bandwidth with it.
+  return !grouped_gemm_narrow(M, E, has_shared, T_s) && !grouped_gemm_streaming(M, E);
+}
+
 cudaError_t launch_grouped_gemm(const GroupedGemmProblem& pr, cudaStream_t stream, bool pdl) {
   const bool has_shared = pr.s_rows != nullptr && pr.T_s > 0;
   if (pr.M <= 0 && !has_shared) return cudaSuccess;
@@ -777,18 +789,20 @@ cudaError_t launch_grouped_gemm(const GroupedGemmProblem& pr, cudaStream_t strea
   // they stream weights, and six 64-deep stages keep more weight bytes in flight.
   // Longer segments are compute-bound and take three 128-deep stages, which let the
   // MMA thread issue 8 MMAs between two waits (the tensor pipe idles otherwise).
-  // The 256-wide gate/up instances run 12 epilogue warps and 4 warps that gather the token
-  // rows while the GEMM runs (when asked to); the 32-wide ones have the rows gathered by a
+  // The compute-bound 256-wide gate/up instance runs 2 extra warps that gather the token rows
+  // while the GEMM runs (when asked to); the other instances have the rows gathered by a
   // separate kernel first.
-  if (grouped_gemm_narrow(pr.M, pr.E, has_shared, pr.T_s)) {
-    if (gather) {
-      cudaError_t e = launch_expand_rows(pr.g_x, pr.g_sorted_pair, pr.M, pr.g_k, pr.K, const_cast<uint16_t*>(pr.a_rows),
-                                         stream, pdl);
-      if (e != cudaSuccess) return e;
-    }
+  if (gather && !grouped_gemm_gathers_inline(pr.M, pr.E, has_shared, pr.T_s)) {
+    cudaError_t e = launch_expand_rows(pr.g_x, pr.g_sorted_pair, pr.M, pr.g_k, pr.K, const_cast<uint16_t*>(pr.a_rows),
+                                       stream, pdl);
+    if (e != cudaSuccess) return e;
+  }
+  if (grouped_gemm_narrow(pr.M, pr.E, has_shared, pr.T_s))
     return pr.mode == 0 ? launch_instance<32, 5, 0, 16, 8, 2, 1, 1, 0>(pr, gp, stream, pdl)
                         : launch_instance<32, 10, 1, 16, 8, 1, 1, 1, 0>(pr, gp, stream, pdl);
-  }
+  if (grouped_gemm_streaming(pr.M, pr.E))
+    return pr.mode == 0 ? launch_instance<256, 6, 0, 64, 16, 1, 2, 1, 0>(pr, gp, stream, pdl)
+                        : launch_instance<256, 6, 1, 64, 16, 1, 2, 1, 0>(pr, gp, stream, pdl);
   if (gather) {
     gp.g_x = reinterpret_cast<const uint4*>(pr.g_x);
     gp.g_sp = pr.g_sorted_pair;
@@ -798,11 +812,7 @@ cudaError_t launch_grouped_gemm(const GroupedGemmProblem& pr, cudaStream_t strea
     gp.g_H8 = pr.K / 8;
     gp.g_flags = pr.g_flags;
   }
-  const bool streaming = (long long)pr.M < 256LL * pr.E;
-  if (streaming)
-    return pr.mode == 0 ? launch_instance<256, 6, 0, 64, 12, 1, 2, 1, 4>(pr, gp, stream, pdl)
-                        : launch_instance<256, 6, 1, 64, 16, 1, 2, 1, 0>(pr, gp, stream, pdl);
-  return pr.mode == 0 ? launch_instance<256, 3, 0, 64, 12, 1, 2, 2, 4>(pr, gp, stream, pdl)
+  return pr.mode == 0 ? launch_instance<256, 3, 0, 64, 16, 1, 2, 2, 2>(pr, gp, stream, pdl)
                       : launch_instance<256, 3, 1, 64, 16, 1, 2, 2, 0>(pr, gp, stream, pdl);
 }
 

@@ -52,8 +52,12 @@ struct GroupedGemmProblem {
   unsigned* g_flags;
 };
 
-// Whether the problem takes the 32-column (decode) instances.
+// Whether the problem takes the 32-column (decode) instances; whether its CTA-pair instance
+// streams weights (under 256 rows per expert); whether a gate/up GEMM asked to gather its rows
+// does so inside the GEMM (else a separate gather kernel runs first).
 bool grouped_gemm_narrow(int M, int E, bool has_shared, int T_s);
+bool grouped_gemm_streaming(int M, int E);
+bool grouped_gemm_gathers_inline(int M, int E, bool has_shared, int T_s);
 
 cudaError_t launch_grouped_gemm(const GroupedGemmProblem& p, cudaStream_t stream, bool pdl = false);
 
