@@ -299,10 +299,13 @@ int layer_forward_impl(const moe_layer_desc* d, const uint16_t* x, const float* 
   // Every kernel after the first may start while its predecessor finishes (programmatic
   // dependent launch); each waits for its inputs before touching them.
   constexpr bool kPdl = true;
-  // The gate/up GEMM gathers the token rows into x_exp itself (overlapping the gather with
-  // its matmuls), so routing only sorts; it also clears the GEMM's gather flags.
-  e = moe::launch_init_routing(topk_idx, P, E, k, nullptr, H, nullptr, counts, offsets, sorted_pair, pair_pos,
-                               scratch, status, st, kPdl, gflags, (P + 15) / 16);
+  // A compute-bound gate/up GEMM gathers the token rows into x_exp itself (overlapping the
+  // gather with its matmuls): routing then only sorts, and clears the GEMM's gather flags.
+  // Otherwise routing ends with the row gather kernel.
+  const bool inline_gather = moe::grouped_gemm_gathers_inline(P, E, sh, T);
+  e = moe::launch_init_routing(topk_idx, P, E, k, inline_gather ? nullptr : x, H, inline_gather ? nullptr : x_exp,
+                               counts, offsets, sorted_pair, pair_pos, scratch, status, st, kPdl,
+                               inline_gather ? gflags : nullptr, inline_gather ? (P + 15) / 16 : 0);
   if (e != cudaSuccess) return MOE_ERR_CUDA;
 
   moe::GroupedGemmProblem g1{};
@@ -316,11 +319,13 @@ int layer_forward_impl(const moe_layer_desc* d, const uint16_t* x, const float* 
   g1.n_out = 2 * I;
   g1.out = act;
   g1.ld_out = I;
-  g1.g_x = x;
-  g1.g_sorted_pair = sorted_pair;
-  g1.g_k = k;
-  g1.g_T = T;
-  g1.g_flags = gflags;
+  if (inline_gather) {
+    g1.g_x = x;
+    g1.g_sorted_pair = sorted_pair;
+    g1.g_k = k;
+    g1.g_T = T;
+    g1.g_flags = gflags;
+  }
   if (sh) {
     g1.s_rows = x;
     g1.s_w = w13_s;
