@@ -68,7 +68,9 @@ typedef enum {
 
 /* Gate function.  Values follow norm_type of the Hy3 router call ([HY3] 1.3):
  * 0 = softmax, 1 = sigmoid. */
-typedef enum { MOE_GATE_SOFTMAX = 0, MOE_GATE_SIGMOID = 1 } moe_gate;
+/* MOE_GATE_SIGMOID_INNER_BIAS: the fused routing op's placement of the correction bias, inside
+ * the sigmoid ([HY3] 5.1, P1 precision note), where the model adds it after the sigmoid. */
+typedef enum { MOE_GATE_SOFTMAX = 0, MOE_GATE_SIGMOID = 1, MOE_GATE_SIGMOID_INNER_BIAS = 2 } moe_gate;
 
 /* Shape and gating parameters of one MoE layer. */
 typedef struct moe_layer_desc {
@@ -109,15 +111,19 @@ MOE_API int moe_get_device_status(const void* ws, void* stream);
  * is added after the sigmoid and only changes which experts are chosen).
  *
  *  logits   [T,E] fp32 router logits.
- *  bias     [E] fp32 correction bias, sigmoid only; NULL = none.  Must be NULL
- *           for softmax.
+ *  bias     [E] fp32 correction bias, sigmoid gates only; NULL = none.  Must be
+ *           NULL for softmax.
  *  gate     moe_gate.  Selection key: softmax -> the logit; sigmoid ->
- *           sigmoid(logit) + bias[e], computed with a fixed sequence of IEEE
- *           fp32 operations so the choice is reproducible bit for bit.
- *           Ties go to the lower expert index.
+ *           sigmoid(logit) + bias[e] (the model's placement, [HY3] 5.1);
+ *           sigmoid_inner_bias -> sigmoid(logit + bias[e]) (the fused op's
+ *           placement, [HY3] 5.1 P1 note; the fp32 sum rounded once).  The
+ *           sigmoid is a fixed sequence of IEEE fp32 operations so the choice
+ *           is reproducible bit for bit.  Ties go to the lower expert index.
  *  topk_idx [T,k] int32 out: chosen experts, best first.
  *  topk_w   [T,k] fp32 out: softmax -> softmax of the k chosen logits;
- *           sigmoid -> sigmoid_j / (sum_j sigmoid_j + eps) * routed_scaling_factor.
+ *           sigmoid -> s_j / (sum_j s_j + eps) * routed_scaling_factor with
+ *           s_j = sigmoid(logit_j) (sigmoid) or sigmoid(logit_j + bias_j)
+ *           (sigmoid_inner_bias).
  */
 MOE_API int moe_gating_topk(const float* logits, const float* bias, int T, int E, int k, int gate,
                     float routed_scaling_factor, float eps, float* topk_w, int32_t* topk_idx, void* stream);

@@ -27,7 +27,7 @@ MOE_ERR_WORKSPACE = -3
 MOE_ERR_CUDA = -4
 MOE_ERR_TIMEOUT = -5
 MOE_ERR_DEVICE_CHECK = -6
-GATES = {"softmax": 0, "sigmoid": 1}
+GATES = {"softmax": 0, "sigmoid": 1, "sigmoid_inner_bias": 2}
 
 _lib = None
 _lock = threading.Lock()

@@ -68,7 +68,8 @@ int check_desc(const moe_layer_desc* d) {
   int s = check_common(d->T, d->E, d->k);
   if (s) return s;
   if ((s = check_dims((long long)d->T * d->k, d->H, d->I))) return s;
-  if (d->gate != MOE_GATE_SOFTMAX && d->gate != MOE_GATE_SIGMOID) return MOE_ERR_INVALID_ARG;
+  if (d->gate != MOE_GATE_SOFTMAX && d->gate != MOE_GATE_SIGMOID && d->gate != MOE_GATE_SIGMOID_INNER_BIAS)
+    return MOE_ERR_INVALID_ARG;
   if (d->n_shared < 0) return MOE_ERR_INVALID_ARG;
   if (d->n_shared > 1) return MOE_ERR_UNSUPPORTED;
   if (d->n_shared == 1) {
@@ -119,7 +120,8 @@ int moe_gating_topk(const float* logits, const float* bias, int T, int E, int k,
                     float routed_scaling_factor, float eps, float* topk_w, int32_t* topk_idx, void* stream) {
   int s = check_common(T, E, k);
   if (s) return s;
-  if (gate != MOE_GATE_SOFTMAX && gate != MOE_GATE_SIGMOID) return MOE_ERR_INVALID_ARG;
+  if (gate != MOE_GATE_SOFTMAX && gate != MOE_GATE_SIGMOID && gate != MOE_GATE_SIGMOID_INNER_BIAS)
+    return MOE_ERR_INVALID_ARG;
   if (gate == MOE_GATE_SOFTMAX && bias) return MOE_ERR_INVALID_ARG;
   if (T == 0) return MOE_OK;
   if (!logits || !topk_w || !topk_idx) return MOE_ERR_INVALID_ARG;

@@ -5,7 +5,8 @@
 // experts, replacing top-k then softmax); Hy3 295B MoE practice, section 1.3
 // (sigmoid router: sigmoid, top-k, gather, normalise with eps = 1e-20, scale by
 // routed_scaling_factor = 2.826) and section 5.1 (the correction bias is added
-// after the sigmoid and only decides which experts are chosen).
+// after the sigmoid and only decides which experts are chosen; the fused op adds
+// it inside the sigmoid instead, MOE_GATE_SIGMOID_INNER_BIAS here).
 //
 // Each lane holds experts e = lane + 32*i.  The selection key is turned into
 // an order-preserving 32-bit integer and packed with the complement of the
@@ -91,6 +92,8 @@ __global__ void __launch_bounds__(256) gating_topk_kernel(const float* __restric
       if (gate == MOE_GATE_SIGMOID) {
         key = sigmoid_fixed_f32(l);
         if (bias) key = __fadd_rn(key, __ldg(bias + e));
+      } else if (gate == MOE_GATE_SIGMOID_INNER_BIAS) {
+        key = sigmoid_fixed_f32(bias ? __fadd_rn(l, __ldg(bias + e)) : l);
       }
       packed[i] = ((unsigned long long)ordered_key(key) << 32) | (unsigned long long)(0xFFFFFFFFu - (uint32_t)e);
     }
@@ -113,7 +116,11 @@ __global__ void __launch_bounds__(256) gating_topk_kernel(const float* __restric
   const float l = (lane < k) ? __ldg(row + my_e) : 0.0f;
   const float l0 = __shfl_sync(0xffffffffu, l, 0);  // softmax: slot 0 holds the largest logit
   float w = 0.0f;
-  if (lane < k) w = (gate == MOE_GATE_SOFTMAX) ? expf(l - l0) : sigmoid_fixed_f32(l);
+  if (lane < k) {
+    if (gate == MOE_GATE_SOFTMAX) w = expf(l - l0);
+    else if (gate == MOE_GATE_SIGMOID_INNER_BIAS && bias) w = sigmoid_fixed_f32(__fadd_rn(l, __ldg(bias + my_e)));
+    else w = sigmoid_fixed_f32(l);
+  }
   const float s = warp_sum(w);
   if (lane < k) {
     w = (gate == MOE_GATE_SOFTMAX) ? w / s : w / (s + eps) * rsf;

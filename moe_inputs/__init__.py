@@ -119,7 +119,7 @@ class MoEConfig:
     E: int
     k: int
     I: int
-    gate: str  # "softmax" | "sigmoid"
+    gate: str  # "softmax" | "sigmoid" | "sigmoid_inner_bias"
     routed_scaling_factor: float = 1.0
     eps: float = 1e-20
     n_shared: int = 0
@@ -193,7 +193,8 @@ def generate(cfg: MoEConfig, weights: bool = True) -> MoEInputs:
     off = zipf_offsets(cfg)
     x = normal_bf16(s, TID_X, (cfg.T, cfg.H))
     logits = grid_logits(s, TID_LOGITS, cfg.T, cfg.E, off)
-    bias = normal_f32(s, TID_BIAS, (cfg.E,), 0.0, cfg.bias_std) if cfg.gate == "sigmoid" and cfg.bias_std > 0 else None
+    bias = normal_f32(s, TID_BIAS, (cfg.E,), 0.0, cfg.bias_std) \
+        if cfg.gate in ("sigmoid", "sigmoid_inner_bias") and cfg.bias_std > 0 else None
     w13 = w2 = w13s = w2s = None
     if weights:
         w13 = normal_bf16(s, TID_W13, (cfg.E, 2 * cfg.I, cfg.H), 0.0, cfg.w_std)

@@ -9,7 +9,11 @@ Sources:
   norm_type=1, routed_scaling_factor, eps=1e-20)``; the seven small ops it
   replaces are sigmoid, top-k, gather, normalise, scale; top-k weights x2.826)
   and section 5.1 "P1 precision note" (in the model the correction bias is
-  added AFTER the sigmoid and only affects which experts are chosen).
+  added AFTER the sigmoid and only affects which experts are chosen; the fused
+  op adds it INSIDE the sigmoid -- gate "sigmoid_inner_bias" here).
+* For the fused op's placement the pages say only that the bias sits inside
+  the sigmoid; the reading taken: one sigmoid s_e = sigma(l_e + b_e) serves both
+  the choice and the weights (normalised with eps, scaled like "sigmoid").
 
 Readings (the pages are silent or garbled here):
 * ties between equal selection keys go to the lower expert index, and keys
@@ -65,6 +69,7 @@ def selection_keys(logits: np.ndarray, gate: str, bias=None) -> np.ndarray:
     softmax: softmax is strictly increasing in the logit, so the logit itself is
     the key (top-k of the probabilities == top-k of the logits).
     sigmoid: sigma(l) + bias, the bias added after the sigmoid (Hy3 section 5.1).
+    sigmoid_inner_bias: sigma(l + bias), the sum rounded once to float32.
     """
     logits = np.asarray(logits, np.float32)
     if gate == "softmax":
@@ -74,6 +79,9 @@ def selection_keys(logits: np.ndarray, gate: str, bias=None) -> np.ndarray:
         if bias is not None:
             s = (s + np.asarray(bias, np.float32)[None, :]).astype(np.float32)
         return s
+    if gate == "sigmoid_inner_bias":
+        z = logits if bias is None else (logits + np.asarray(bias, np.float32)[None, :]).astype(np.float32)
+        return sigmoid_f32_pinned(z)
     raise ValueError(f"unknown gate {gate!r}")
 
 
@@ -85,6 +93,7 @@ def gating_topk(logits, k: int, gate: str, bias=None, routed_scaling_factor: flo
       logits ("top-k then softmax" equals softmax over all E renormalised over k).
     sigmoid: w_j = sigma_j / (sum_j' sigma_j' + eps) * routed_scaling_factor, with
       sigma the plain sigmoid of the logit (bias excluded).
+    sigmoid_inner_bias: the same with sigma_j = sigmoid(l_j + b_j).
     """
     logits = np.asarray(logits, np.float32)
     T, E = logits.shape
@@ -100,6 +109,8 @@ def gating_topk(logits, k: int, gate: str, bias=None, routed_scaling_factor: flo
         z = np.exp(l - l.max(axis=1, keepdims=True))
         w = z / z.sum(axis=1, keepdims=True)
     else:
+        if gate == "sigmoid_inner_bias" and bias is not None:
+            l = l + np.asarray(bias, np.float64)[topk_idx]
         sig = 1.0 / (1.0 + np.exp(-l))
         rsf = float(np.float32(routed_scaling_factor))
         w = sig / (sig.sum(axis=1, keepdims=True) + float(np.float32(eps))) * rsf

@@ -79,6 +79,11 @@ def test_gating_validation_returns_before_launch(L):
     P16 = 16  # an aligned non-null dummy address: never dereferenced since validation fails first
     assert L.moe_gating_topk(P16, None, 4, 8, 9, 0, 1.0, 1e-20, P16, P16, None) == moe.MOE_ERR_UNSUPPORTED
     assert L.moe_gating_topk(P16, None, 4, 8, 2, 5, 1.0, 1e-20, P16, P16, None) == moe.MOE_ERR_INVALID_ARG
+    assert L.moe_gating_topk(P16, None, 4, 8, 2, 3, 1.0, 1e-20, P16, P16, None) == moe.MOE_ERR_INVALID_ARG
+    # the three gates pass validation (an empty batch then returns without a launch)
+    for gate in (0, 1, 2):
+        assert L.moe_gating_topk(None, None, 0, 8, 2, gate, 1.0, 1e-20, None, None, None) == moe.MOE_OK
+    assert L.moe_gating_topk(None, P16, 0, 8, 2, 2, 2.826, 1e-20, None, None, None) == moe.MOE_OK
     assert L.moe_gating_topk(P16, P16, 4, 8, 2, 0, 1.0, 1e-20, P16, P16, None) == moe.MOE_ERR_INVALID_ARG
     assert L.moe_gating_topk(None, None, 4, 8, 2, 0, 1.0, 1e-20, P16, P16, None) == moe.MOE_ERR_INVALID_ARG
     assert L.moe_gating_topk(P16 + 4, None, 4, 8, 2, 0, 1.0, 1e-20, P16, P16, None) == moe.MOE_ERR_INVALID_ARG

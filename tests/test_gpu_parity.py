@@ -34,6 +34,10 @@ GATING_CASES = [
     ("tiny", dict(T=1, E=1, k=1)),
     ("tiny", dict(T=37, E=1024, k=32)),
     ("hy3_decode", dict(T=33, E=200, k=8, bias_std=0.0)),  # sigmoid without bias: many exact key ties
+    # the fused op's bias placement (inside the sigmoid)
+    ("hy3_decode", dict(gate="sigmoid_inner_bias")),
+    ("hy3_prefill", dict(gate="sigmoid_inner_bias", bias_std=0.5)),
+    ("tiny", dict(T=37, E=1024, k=32, gate="sigmoid_inner_bias", bias_std=1.0, routed_scaling_factor=2.826)),
 ]
 
 
@@ -54,9 +58,13 @@ def test_gating_ties_on_coarse_grid(moe):
     logits = (np.round(rng.normal(size=(300, 64)) * 4) / 4).astype(np.float32)
     logits[:10] = 0.0
     logits[10:20, :7] = -0.0
-    for gate in ("softmax", "sigmoid"):
-        w_ref, idx_ref = oracle.gating_topk(logits, 6, gate, None, 2.826 if gate == "sigmoid" else 1.0)
-        w, idx = moe.moe_gating_topk(dev(logits), 6, gate, None, 2.826 if gate == "sigmoid" else 1.0)
+    # a bias on a coarse grid keeps l + b on the grid: exact ties inside the sigmoid too
+    bias = (np.round(rng.normal(size=64) * 2) / 4).astype(np.float32)
+    for gate, b in (("softmax", None), ("sigmoid", None), ("sigmoid_inner_bias", None),
+                    ("sigmoid_inner_bias", bias)):
+        rsf = 1.0 if gate == "softmax" else 2.826
+        w_ref, idx_ref = oracle.gating_topk(logits, 6, gate, b, rsf)
+        w, idx = moe.moe_gating_topk(dev(logits), 6, gate, dev(b) if b is not None else None, rsf)
         assert (host(idx) == idx_ref).all()
         np.testing.assert_allclose(host(w), w_ref, rtol=2e-6, atol=1e-7)
 

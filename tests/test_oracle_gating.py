@@ -3,7 +3,7 @@
 Passages pinned: Qwen3-MoE practice, "GMM enablement and routing optimisation"
 (fused gating replaces top-k then softmax); Hy3 practice section 1.3 (sigmoid
 router, eps 1e-20, weights normalised then x2.826) and section 5.1 P1 note
-(bias after the sigmoid, selection only).
+(bias after the sigmoid, selection only; the fused op's bias inside the sigmoid).
 """
 import math
 
@@ -139,3 +139,57 @@ def test_weight_invariants(gate, target):
         # sigmoid weights use sigma of the logit only (no bias): closed form per row
         sig = 1.0 / (1.0 + np.exp(-np.take_along_axis(logits, idx, 1).astype(np.float64)))
         np.testing.assert_allclose(w, sig / sig.sum(1, keepdims=True) * float(np.float32(2.826)), rtol=1e-12)
+
+
+# ---------------------------------------------------------------- bias inside the sigmoid
+def _golden_bias_placement():
+    import json, os
+    with open(os.path.join(os.path.dirname(__file__), "golden", "gating_bias_placement.json")) as f:
+        return json.load(f)
+
+
+def test_bias_placement_hand_example():
+    g = _golden_bias_placement()
+    logits = np.float32([g["logits"]])
+    bias = np.float32(g["bias"])
+    m = g["model_after_sigmoid"]
+    w, idx = oracle.gating_topk(logits, m["k"], "sigmoid", bias, g["routed_scaling_factor"], g["eps"])
+    assert list(idx[0]) == m["topk_idx"]
+    np.testing.assert_allclose(w[0], m["topk_w"], rtol=1e-6)
+    for case in g["fused_inside_sigmoid"]:
+        w, idx = oracle.gating_topk(logits, case["k"], "sigmoid_inner_bias", bias, g["routed_scaling_factor"],
+                                    g["eps"])
+        assert list(idx[0]) == case["topk_idx"]
+        np.testing.assert_allclose(w[0], case["topk_w"], rtol=1e-6)
+
+
+def test_inner_bias_without_bias_is_the_plain_sigmoid_gate():
+    rng = np.random.default_rng(21)
+    logits = (np.round(rng.normal(size=(200, 40)) * 256) / 256).astype(np.float32)
+    for bias in (None, np.zeros(40, np.float32)):
+        w0, i0 = oracle.gating_topk(logits, 6, "sigmoid", None, 2.826)
+        w1, i1 = oracle.gating_topk(logits, 6, "sigmoid_inner_bias", bias, 2.826)
+        assert (i0 == i1).all()
+        np.testing.assert_allclose(w1, w0, rtol=1e-12)
+
+
+def test_inner_bias_selection_is_the_order_of_logit_plus_bias():
+    """sigmoid is strictly increasing: away from float32 ties the choice is the top-k of l + b."""
+    rng = np.random.default_rng(23)
+    T, E, k = 200, 64, 8
+    logits = (np.round(rng.normal(size=(T, E)) * 256) / 256).astype(np.float32)
+    bias = rng.normal(0, 0.5, size=E).astype(np.float32)
+    w, idx = oracle.gating_topk(logits, k, "sigmoid_inner_bias", bias, 2.826)
+    checked = 0
+    for t in range(T):
+        z = [float(l) + float(b) for l, b in zip(logits[t], bias)]
+        keys = [1.0 / (1.0 + math.exp(-v)) for v in z]
+        srt = sorted(keys, reverse=True)
+        if srt[k - 1] - srt[k] < 1e-6:
+            continue
+        checked += 1
+        assert list(idx[t]) == _brute_select(z, k)
+        sel = [keys[e] for e in idx[t]]
+        np.testing.assert_allclose(w[t], np.array(sel) / sum(sel) * float(np.float32(2.826)), rtol=1e-9)
+    assert checked > 150
+    np.testing.assert_allclose(w.sum(1), float(np.float32(2.826)), rtol=1e-6)
