@@ -150,6 +150,34 @@ MOE_API int moe_init_routing(const int32_t* topk_idx, int T, int E, int k, const
                      size_t ws_bytes, void* stream);
 
 /*
+ * Init-routing restricted to a local expert range [e0, e1), the expert-parallel
+ * form of a2: [Q3] MoE EP with AllGather + ReduceScatter (W4A8 section) routes the
+ * gathered tokens with init_routing_v2 keeping only the tokens of the experts in
+ * this rank's range, runs the GMMs on those experts and finalises a partial sum
+ * that a reduce-scatter adds up across ranks.  On one device: the partial outputs
+ * of a partition of [0, E) into ranges sum to the whole layer's output.
+ *
+ *  e0, e1      0 <= e0 < e1 <= E; the local experts are l = e - e0, EL = e1 - e0.
+ *  counts      [EL] int32 out: pairs routed to each local expert.
+ *  offsets     [EL+1] int32 out: exclusive prefix of counts; offsets[EL] = the
+ *              number of local pairs P_loc.
+ *  sorted_pair [P] int32 out: positions 0..P_loc-1 hold the local pairs sorted by
+ *              local expert, ascending pair index inside an expert; the rest is
+ *              left alone.
+ *  pair_pos    [P] int32 out: pair_pos[p] = its position, or -1 when the pair's
+ *              expert is outside [e0, e1) (moe_finalize_routing skips those, which
+ *              gives the range's partial output).
+ *  x, x_exp    optional as for moe_init_routing; rows 0..P_loc-1 of x_exp are written.
+ *  ws          moe_init_routing_workspace_size(T, E, k) bytes suffice.
+ *  Expert indices outside [0, E) raise MOE_ERR_DEVICE_CHECK as in moe_init_routing.
+ *  Feed the GEMMs the local slice: weights w + e0 * (rows per expert) * K, E = EL,
+ *  these offsets, and M = P (rows past P_loc are never read).
+ */
+MOE_API int moe_init_routing_range(const int32_t* topk_idx, int T, int E, int k, int e0, int e1, const uint16_t* x,
+                                   int H, uint16_t* x_exp, int32_t* counts, int32_t* offsets, int32_t* sorted_pair,
+                                   int32_t* pair_pos, void* ws, size_t ws_bytes, void* stream);
+
+/*
  * Init-routing without a workspace, for callers that cannot allocate device
  * memory (code running inside an allocator or memory-pool callback, runtimes
  * whose device memory is entirely pre-reserved by someone else, or host

@@ -59,6 +59,10 @@ _SIGS = {
                                         ctypes.c_int, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
                                         ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_size_t,
                                         ctypes.c_void_p]),
+    "moe_init_routing_range": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                                              ctypes.c_int, ctypes.c_void_p, ctypes.c_int, ctypes.c_void_p,
+                                              ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
+                                              ctypes.c_void_p, ctypes.c_size_t, ctypes.c_void_p]),
     "moe_init_routing_static_scratch": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_int, ctypes.c_int, ctypes.c_int,
                                                        ctypes.c_void_p, ctypes.c_int, ctypes.c_void_p,
                                                        ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
@@ -176,6 +180,34 @@ def moe_init_routing(topk_idx, E: int, x=None, ws=None, out: Optional[dict] = No
     _check(lib().moe_init_routing(_ptr(topk_idx), T, E, k, _ptr(x), H, _ptr(o.get("x_exp")), _ptr(o["counts"]),
                                   _ptr(o["offsets"]), _ptr(o["sorted_pair"]), _ptr(o["pair_pos"]), _ptr(ws),
                                   ws.numel(), _stream(stream)), "moe_init_routing")
+    o["ws"] = ws
+    return o
+
+
+def moe_init_routing_range(topk_idx, E: int, e0: int, e1: int, x=None, ws=None, out: Optional[dict] = None,
+                           stream=None) -> dict:
+    """a2 restricted to the local experts [e0, e1): counts/offsets over e1-e0 experts, sorted_pair
+    holding the local pairs first (offsets[-1] of them), pair_pos -1 for pairs routed elsewhere."""
+    torch = _torch()
+    T, k = topk_idx.shape
+    P = T * k
+    EL = e1 - e0
+    dev = topk_idx.device
+    o = dict(out or {})
+    o.setdefault("counts", torch.empty(max(EL, 0), dtype=torch.int32, device=dev))
+    o.setdefault("offsets", torch.empty(max(EL, 0) + 1, dtype=torch.int32, device=dev))
+    o.setdefault("sorted_pair", torch.empty(P, dtype=torch.int32, device=dev))
+    o.setdefault("pair_pos", torch.empty(P, dtype=torch.int32, device=dev))
+    H = 0
+    if x is not None:
+        H = x.shape[1]
+        o.setdefault("x_exp", torch.empty((P, H), dtype=x.dtype, device=dev))
+    need = lib().moe_init_routing_workspace_size(T, E, k)
+    ws = _ws(need, dev, ws)
+    _check(lib().moe_init_routing_range(_ptr(topk_idx), T, E, k, e0, e1, _ptr(x), H, _ptr(o.get("x_exp")),
+                                        _ptr(o["counts"]), _ptr(o["offsets"]), _ptr(o["sorted_pair"]),
+                                        _ptr(o["pair_pos"]), _ptr(ws), ws.numel(), _stream(stream)),
+           "moe_init_routing_range")
     o["ws"] = ws
     return o
 

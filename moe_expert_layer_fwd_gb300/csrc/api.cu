@@ -136,11 +136,16 @@ size_t moe_init_routing_workspace_size(int T, int E, int k) {
   return align_up(kHeader + moe::routing_scratch_bytes(T * k, E));
 }
 
-int moe_init_routing(const int32_t* topk_idx, int T, int E, int k, const uint16_t* x, int H, uint16_t* x_exp,
-                     int32_t* counts, int32_t* offsets, int32_t* sorted_pair, int32_t* pair_pos, void* ws,
-                     size_t ws_bytes, void* stream) {
+}  // extern "C"
+
+namespace {
+
+int init_routing_impl(const int32_t* topk_idx, int T, int E, int k, int e0, int e1, const uint16_t* x, int H,
+                      uint16_t* x_exp, int32_t* counts, int32_t* offsets, int32_t* sorted_pair, int32_t* pair_pos,
+                      void* ws, size_t ws_bytes, void* stream) {
   int s = check_common(T, E, k);
   if (s) return s;
+  if (e0 < 0 || e1 <= e0 || e1 > E) return MOE_ERR_INVALID_ARG;
   if (!counts || !offsets || !ws) return MOE_ERR_INVALID_ARG;
   if ((x == nullptr) != (x_exp == nullptr)) return MOE_ERR_INVALID_ARG;
   if (x) {
@@ -154,7 +159,26 @@ int moe_init_routing(const int32_t* topk_idx, int T, int E, int k, const uint16_
     return MOE_ERR_INVALID_ARG;
   int32_t* scratch = reinterpret_cast<int32_t*>(static_cast<char*>(ws) + kHeader);
   return cuda_status(moe::launch_init_routing(topk_idx, T * k, E, k, x, H, x_exp, counts, offsets, sorted_pair,
-                                              pair_pos, scratch, status_word(ws), as_stream(stream)));
+                                              pair_pos, scratch, status_word(ws), as_stream(stream), false, nullptr,
+                                              0, e0, e1));
+}
+
+}  // namespace
+
+extern "C" {
+
+int moe_init_routing(const int32_t* topk_idx, int T, int E, int k, const uint16_t* x, int H, uint16_t* x_exp,
+                     int32_t* counts, int32_t* offsets, int32_t* sorted_pair, int32_t* pair_pos, void* ws,
+                     size_t ws_bytes, void* stream) {
+  return init_routing_impl(topk_idx, T, E, k, 0, E, x, H, x_exp, counts, offsets, sorted_pair, pair_pos, ws,
+                           ws_bytes, stream);
+}
+
+int moe_init_routing_range(const int32_t* topk_idx, int T, int E, int k, int e0, int e1, const uint16_t* x, int H,
+                           uint16_t* x_exp, int32_t* counts, int32_t* offsets, int32_t* sorted_pair,
+                           int32_t* pair_pos, void* ws, size_t ws_bytes, void* stream) {
+  return init_routing_impl(topk_idx, T, E, k, e0, e1, x, H, x_exp, counts, offsets, sorted_pair, pair_pos, ws,
+                           ws_bytes, stream);
 }
 
 int moe_prepack_w13(const uint16_t* w13, int E, int I, int H, uint16_t* w13_packed, void* stream) {

@@ -16,13 +16,17 @@ cudaError_t launch_gating_topk(const float* logits, const float* bias, int T, in
 int routing_chunk_pairs(int P);
 size_t routing_scratch_bytes(int P, int E);
 // `zero`, `n_zero`: optional words zeroed by the routing kernels (the gather flags of the
-// following gate/up GEMM).
+// following gate/up GEMM).  [e0, e1): the local expert range (e1 < 0: all E experts); counts
+// and offsets then have e1-e0 (+1) entries and pair_pos is -1 for pairs routed elsewhere.
 cudaError_t launch_init_routing(const int32_t* topk_idx, int P, int E, int k, const uint16_t* x, int H,
                                 uint16_t* x_exp, int32_t* counts, int32_t* offsets, int32_t* sorted_pair,
                                 int32_t* pair_pos, int32_t* scratch, unsigned* status, cudaStream_t stream,
-                                bool pdl = false, unsigned* zero = nullptr, int n_zero = 0);
+                                bool pdl = false, unsigned* zero = nullptr, int n_zero = 0, int e0 = 0,
+                                int e1 = -1);
+// n_rows: optional device count of the rows to gather (the rest of x_exp is left alone).
 cudaError_t launch_expand_rows(const uint16_t* x, const int32_t* sorted_pair, int P, int k, int H,
-                               uint16_t* x_exp, cudaStream_t stream, bool pdl = false);
+                               uint16_t* x_exp, cudaStream_t stream, bool pdl = false,
+                               const int32_t* n_rows = nullptr);
 
 // One grouped GEMM launch: routed experts (+ optionally one dense "shared" segment).
 struct GroupedGemmProblem {

@@ -17,8 +17,16 @@
 //               the rank inside the group is the number of lower lanes in it,
 //               so positions follow pair order exactly (a stable sort) with no
 //               atomics deciding the order.
-//   4. expand:  x_exp[pos] = x[sorted_pair[pos] / k], a flat grid of 16-byte
-//               vector copies, several independent ones per thread.
+//   4. expand:  x_exp[pos] = x[sorted_pair[pos] / k], 16-byte vector copies,
+//               several independent ones per thread.
+//
+// Expert range: with a local slice [e0, e0 + EL) of the E experts (routing that
+// keeps only the pairs whose expert this device owns, the expert-parallel form of
+// init-routing: Qwen3-MoE practice, W4A8 EP section, "init_routing_v2 ... only the
+// tokens in this rank's expert range"), the histograms, counts and offsets cover the
+// EL local experts, sorted_pair lists only local pairs (local expert order, then
+// pair order), and pair_pos is -1 for every other pair.  The whole range (e0 = 0,
+// EL = E) is ordinary init-routing.
 #include "moe_common.cuh"
 #include "moe_internal.h"
 
@@ -28,30 +36,30 @@ namespace {
 constexpr int kWarps = 8;
 
 __global__ void __launch_bounds__(kWarps * 32) route_hist_kernel(const int32_t* __restrict__ idx, int P, int E,
-                                                                 int CH, int n_chunks, int32_t* __restrict__ hist,
-                                                                 unsigned* status) {
+                                                                 int e0, int EL, int CH, int n_chunks,
+                                                                 int32_t* __restrict__ hist, unsigned* status) {
   pdl_wait();
   pdl_launch_dependents();
   extern __shared__ int sh[];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int c = blockIdx.x * kWarps + warp;
   if (c >= n_chunks) return;
-  int* h = sh + warp * E;
-  for (int e = lane; e < E; e += 32) h[e] = 0;
+  int* h = sh + warp * EL;
+  for (int e = lane; e < EL; e += 32) h[e] = 0;
   __syncwarp();
   const int p0 = c * CH, p1 = min(P, p0 + CH);
   bool bad = false;
 #pragma unroll 8
   for (int p = p0 + lane; p < p1; p += 32) {
     const int e = __ldg(idx + p);
-    if ((unsigned)e < (unsigned)E)
-      atomicAdd(&h[e], 1);
-    else
+    if ((unsigned)e >= (unsigned)E)
       bad = true;
+    else if ((unsigned)(e - e0) < (unsigned)EL)
+      atomicAdd(&h[e - e0], 1);
   }
   if (bad) set_status(status, DEV_ERR_BOUNDS);
   __syncwarp();
-  for (int e = lane; e < E; e += 32) hist[(size_t)c * E + e] = h[e];
+  for (int e = lane; e < EL; e += 32) hist[(size_t)c * EL + e] = h[e];
 }
 
 // One CTA of 1024 threads: thread (seg, e) owns expert e over the seg-th slice of chunks.
@@ -120,10 +128,11 @@ __global__ void __launch_bounds__(1024) route_scan_kernel(const int32_t* __restr
 }
 
 __global__ void __launch_bounds__(kWarps * 32) route_scatter_kernel(const int32_t* __restrict__ idx, int P,
-                                                                    int E, int CH, int n_chunks,
+                                                                    int e0, int E, int CH, int n_chunks,
                                                                     const int32_t* __restrict__ base,
                                                                     int32_t* __restrict__ sorted_pair,
                                                                     int32_t* __restrict__ pair_pos) {
+  // E here is the number of local experts (the histogram width); e0 the first one.
   pdl_wait();
   pdl_launch_dependents();
   extern __shared__ int sh[];
@@ -141,7 +150,7 @@ __global__ void __launch_bounds__(kWarps * 32) route_scatter_kernel(const int32_
 #pragma unroll
     for (int b = 0; b < kBatch; ++b) {
       const int p = pg + b * 32 + lane;
-      ev[b] = (p < p1) ? __ldg(idx + p) : -1;
+      ev[b] = (p < p1) ? __ldg(idx + p) - e0 : -1;  // local expert index
     }
 #pragma unroll
     for (int b = 0; b < kBatch; ++b) {
@@ -161,6 +170,8 @@ __global__ void __launch_bounds__(kWarps * 32) route_scatter_kernel(const int32_
           pair_pos[p] = pos;
         }
         if ((peers >> lane) == 1u) cnt[e] = bs + __popc(peers);  // highest lane of the group
+      } else if (p < p1) {
+        pair_pos[p] = -1;  // not routed here (outside the local expert range, or an invalid index)
       }
       __syncwarp();
     }
@@ -175,9 +186,11 @@ constexpr int kExpandRows = 4;
 
 __global__ void __launch_bounds__(512) expand_rows_kernel(const uint4* __restrict__ x,
                                                           const int32_t* __restrict__ sorted_pair, int P, int k,
-                                                          int T, int H8, uint4* __restrict__ x_exp) {
+                                                          int T, int H8, uint4* __restrict__ x_exp,
+                                                          const int32_t* __restrict__ n_rows) {
   pdl_wait();
   pdl_launch_dependents();
+  if (n_rows) P = min(P, __ldg(n_rows));  // rows routed here (an expert range routes fewer than P)
   const int r0 = blockIdx.x * kExpandRows;
   const uint4* src[kExpandRows];
 #pragma unroll
@@ -216,25 +229,27 @@ size_t routing_scratch_bytes(int P, int E) {
 }
 
 cudaError_t launch_expand_rows(const uint16_t* x, const int32_t* sorted_pair, int P, int k, int H,
-                               uint16_t* x_exp, cudaStream_t stream, bool pdl) {
+                               uint16_t* x_exp, cudaStream_t stream, bool pdl, const int32_t* n_rows) {
   if (P == 0) return cudaSuccess;
   const int T = P / k;
   const int H8 = H / 8;
   const int threads = H8 >= 512 ? 512 : (H8 + 31) / 32 * 32;
   return launch_kernel(expand_rows_kernel, dim3((unsigned)((P + kExpandRows - 1) / kExpandRows)), dim3(threads), 0,
                        stream, pdl, reinterpret_cast<const uint4*>(x), sorted_pair, P, k, T, H8,
-                       reinterpret_cast<uint4*>(x_exp));
+                       reinterpret_cast<uint4*>(x_exp), n_rows);
 }
 
 cudaError_t launch_init_routing(const int32_t* topk_idx, int P, int E, int k, const uint16_t* x, int H,
                                 uint16_t* x_exp, int32_t* counts, int32_t* offsets, int32_t* sorted_pair,
                                 int32_t* pair_pos, int32_t* scratch, unsigned* status, cudaStream_t stream,
-                                bool pdl, unsigned* zero, int n_zero) {
+                                bool pdl, unsigned* zero, int n_zero, int e0, int e1) {
+  if (e1 < 0) e1 = E;
+  const int EL = e1 - e0;  // local experts: [e0, e1)
   const int CH = routing_chunk_pairs(P);
   const int n_chunks = (P + CH - 1) / CH;
   int32_t* hist = scratch;
-  int32_t* base = scratch + (size_t)n_chunks * E;
-  const size_t smem = (size_t)kWarps * E * sizeof(int);
+  int32_t* base = scratch + (size_t)n_chunks * EL;
+  const size_t smem = (size_t)kWarps * EL * sizeof(int);
   const int blocks = (n_chunks + kWarps - 1) / kWarps;
   cudaError_t err;
   if (smem > 48 * 1024) {
@@ -244,19 +259,20 @@ cudaError_t launch_init_routing(const int32_t* topk_idx, int P, int E, int k, co
     if (err != cudaSuccess) return err;
   }
   if (n_chunks > 0) {
-    err = launch_kernel(route_hist_kernel, dim3(blocks), dim3(kWarps * 32), smem, stream, pdl, topk_idx, P, E, CH,
-                        n_chunks, hist, status);
+    err = launch_kernel(route_hist_kernel, dim3(blocks), dim3(kWarps * 32), smem, stream, pdl, topk_idx, P, E, e0,
+                        EL, CH, n_chunks, hist, status);
     if (err != cudaSuccess) return err;
   }
-  err = launch_kernel(route_scan_kernel, dim3(1), dim3(1024), 0, stream, pdl, (const int32_t*)hist, base, n_chunks, E,
-                      counts, offsets, zero, n_zero);
+  err = launch_kernel(route_scan_kernel, dim3(1), dim3(1024), 0, stream, pdl, (const int32_t*)hist, base, n_chunks,
+                      EL, counts, offsets, zero, n_zero);
   if (err != cudaSuccess) return err;
   if (n_chunks > 0) {
-    err = launch_kernel(route_scatter_kernel, dim3(blocks), dim3(kWarps * 32), smem, stream, pdl, topk_idx, P, E, CH,
-                        n_chunks, (const int32_t*)base, sorted_pair, pair_pos);
+    err = launch_kernel(route_scatter_kernel, dim3(blocks), dim3(kWarps * 32), smem, stream, pdl, topk_idx, P, e0,
+                        EL, CH, n_chunks, (const int32_t*)base, sorted_pair, pair_pos);
     if (err != cudaSuccess) return err;
   }
-  if (x != nullptr && x_exp != nullptr) return launch_expand_rows(x, sorted_pair, P, k, H, x_exp, stream, pdl);
+  if (x != nullptr && x_exp != nullptr)
+    return launch_expand_rows(x, sorted_pair, P, k, H, x_exp, stream, pdl, EL < E ? offsets + EL : nullptr);
   return cudaSuccess;
 }
 

@@ -9,13 +9,15 @@ sides use is ``moe_inputs`` (seeded inputs, none of the method's arithmetic).
 What it computes, step by step, each function citing the passage it follows:
 
 * ``gating``   -- top-k expert choice and weights (softmax, or sigmoid with a
-  selection-only correction bias and a routed scaling factor).
+  selection-only correction bias and a routed scaling factor, or the fused op's
+  variant with the bias inside the sigmoid).
 * ``routing``  -- init-routing: stable sort of token-expert pairs by expert,
-  per-expert counts, offsets, the permutation and its inverse.
+  per-expert counts, offsets, the permutation and its inverse; and the same
+  restricted to a local expert range (the expert-parallel form).
 * ``ffn``      -- the expert FFN down(SiLU(gate(x)) * up(x)) over the
   concatenated [gate; up] weight, grouped per expert.
-* ``layer``    -- finalize-routing (unpermute, weighted sum, shared-expert add)
-  and the whole layer.
+* ``layer``    -- finalize-routing (unpermute, weighted sum, shared-expert add),
+  the whole layer, and the routed part of the layer over a local expert range.
 
 Precision: float64 everywhere, except the expert *selection*, which is an
 integer decided by floating point and is therefore taken in float32 with the
@@ -25,13 +27,14 @@ Every function is pinned by ``tests/test_oracle_*.py`` against closed forms,
 brute force and library routines (no function is "parity unpinned").
 """
 from .gating import exp_f32_pinned, sigmoid_f32_pinned, selection_keys, gating_topk
-from .routing import init_routing, expand_rows
+from .routing import init_routing, init_routing_range, expand_rows
 from .ffn import swiglu, expert_ffn, grouped_gemm_swiglu, grouped_gemm, bf16_to_f64
-from .layer import finalize_routing, moe_layer_forward, moe_layer_forward_tokens, shared_expert
+from .layer import (finalize_routing, moe_layer_forward, moe_layer_forward_range, moe_layer_forward_tokens,
+                    shared_expert)
 
 __all__ = [
     "exp_f32_pinned", "sigmoid_f32_pinned", "selection_keys", "gating_topk",
-    "init_routing", "expand_rows",
+    "init_routing", "init_routing_range", "expand_rows",
     "swiglu", "expert_ffn", "grouped_gemm_swiglu", "grouped_gemm", "bf16_to_f64",
-    "finalize_routing", "moe_layer_forward", "moe_layer_forward_tokens", "shared_expert",
+    "finalize_routing", "moe_layer_forward", "moe_layer_forward_range", "moe_layer_forward_tokens", "shared_expert",
 ]

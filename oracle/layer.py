@@ -17,13 +17,18 @@ import numpy as np
 
 from .ffn import _f64, expert_ffn, grouped_gemm, grouped_gemm_swiglu
 from .gating import gating_topk
-from .routing import expand_rows, init_routing
+from .routing import expand_rows, init_routing, init_routing_range
 
 
 def finalize_routing(y_perm, pair_pos, T: int, k: int, shared=None) -> np.ndarray:
-    """y[t] = sum_j y_perm[pair_pos[t*k+j]] (+ shared[t]); y_perm rows already carry the routing weights."""
+    """y[t] = sum_j y_perm[pair_pos[t*k+j]] (+ shared[t]); y_perm rows already carry the routing weights.
+
+    A pair with pair_pos = -1 was routed to experts outside the local range (expert-range routing)
+    and adds nothing here.
+    """
     y_perm = _f64(y_perm)
-    rows = y_perm[np.asarray(pair_pos, np.int64).reshape(T, k)]  # [T,k,H]
+    pp = np.asarray(pair_pos, np.int64).reshape(T, k)
+    rows = y_perm[np.maximum(pp, 0)] * (pp >= 0)[:, :, None]  # [T,k,H]
     y = rows.sum(axis=1)
     if shared is not None:
         y = y + _f64(shared)
@@ -78,3 +83,24 @@ def moe_layer_forward_tokens(tokens, x, logits, k, gate, w13, w2, bias=None, rou
         y += expert_ffn(x[tokens], w13_s, w2_s)
     return dict(topk_w=topk_w, topk_idx=topk_idx, counts=counts, offsets=offsets,
                 sorted_pair=sorted_pair, pair_pos=pair_pos, tokens=tokens, y=y)
+
+
+def moe_layer_forward_range(x, logits, k, gate, w13, w2, e0: int, e1: int, bias=None, routed_scaling_factor=1.0,
+                            eps=1e-20) -> dict:
+    """The routed part of the layer restricted to the local experts [e0, e1) (Qwen3-MoE practice, MoE
+    EP with AllGather + ReduceScatter: routing keeps the tokens of this rank's experts, the GMMs run
+    on them and finalize-routing gives this rank's partial output, which the reduce-scatter sums).
+
+    y_part[t] = sum over slots j with e0 <= idx[t,j] < e1 of w[t,j] * FFN_{idx[t,j]}(x[t]).
+    """
+    x = np.asarray(x)
+    T = x.shape[0]
+    E = np.asarray(w13).shape[0]
+    topk_w, topk_idx = gating_topk(logits, k, gate, bias, routed_scaling_factor, eps)
+    counts, offsets, sorted_pair, pair_pos = init_routing_range(topk_idx, E, e0, e1)
+    x_exp = expand_rows(x, sorted_pair, k)
+    act = grouped_gemm_swiglu(x_exp, w13[e0:e1], offsets)
+    y_perm = grouped_gemm(act, w2[e0:e1], offsets, topk_w.reshape(-1)[sorted_pair])
+    y = finalize_routing(y_perm, pair_pos, T, k)
+    return dict(topk_w=topk_w, topk_idx=topk_idx, counts=counts, offsets=offsets, sorted_pair=sorted_pair,
+                pair_pos=pair_pos, x_exp=x_exp, act=act, y_perm=y_perm, y=y)
