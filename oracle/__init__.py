@@ -18,6 +18,8 @@ What it computes, step by step, each function citing the passage it follows:
   concatenated [gate; up] weight, grouped per expert.
 * ``layer``    -- finalize-routing (unpermute, weighted sum, shared-expert add),
   the whole layer, and the routed part of the layer over a local expert range.
+* ``frontend`` -- the step before gating: fused residual add + RMSNorm + cast
+  (FP32 for the gate, BF16 for the experts) and the router gate GEMM.
 
 Precision: float64 everywhere, except the expert *selection*, which is an
 integer decided by floating point and is therefore taken in float32 with the
@@ -29,6 +31,7 @@ brute force and library routines (no function is "parity unpinned").
 from .gating import exp_f32_pinned, sigmoid_f32_pinned, selection_keys, gating_topk
 from .routing import init_routing, init_routing_range, expand_rows
 from .ffn import swiglu, expert_ffn, grouped_gemm_swiglu, grouped_gemm, bf16_to_f64
+from .frontend import add_rms_norm_cast, round_bf16, router_logits
 from .layer import (finalize_routing, moe_layer_forward, moe_layer_forward_range, moe_layer_forward_tokens,
                     shared_expert)
 
@@ -36,5 +39,6 @@ __all__ = [
     "exp_f32_pinned", "sigmoid_f32_pinned", "selection_keys", "gating_topk",
     "init_routing", "init_routing_range", "expand_rows",
     "swiglu", "expert_ffn", "grouped_gemm_swiglu", "grouped_gemm", "bf16_to_f64",
+    "add_rms_norm_cast", "round_bf16", "router_logits",
     "finalize_routing", "moe_layer_forward", "moe_layer_forward_range", "moe_layer_forward_tokens", "shared_expert",
 ]
