@@ -60,6 +60,7 @@ def _args(argv=None):
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-front-end", action="store_true", help="skip timing the front end (norm + router GEMM)")
     ap.add_argument("--cpu-baseline-child", action="store_true", help=argparse.SUPPRESS)
     ap.add_argument("--sample-tokens", type=int, default=8)
     ap.add_argument("--profile-steps", action="store_true",
@@ -291,6 +292,44 @@ def _config(cfg, world):
             "parallelism": f"replicas x{world}"}
 
 
+# ------------------------------------------------------------------ front end (the step before gating)
+def front_end(args, cfg, K, W, moe, mi, d16):
+    """Times the fused residual add + RMSNorm + cast and the router gate GEMM on the workload's
+    [T, H] hidden state and E experts (synthetic bf16 hidden state, residual, norm and gate weights).
+    Reported beside the layer, not part of its value."""
+    import torch
+    T, H, E = cfg.T, cfg.H, cfg.E
+    h = d16(mi.normal_bf16(cfg.seed, 101, (T, H)))
+    res = d16(mi.normal_bf16(cfg.seed, 102, (T, H)))
+    w = d16(mi.normal_bf16(cfg.seed, 103, (H,), 1.0, 0.1))
+    wg = d16(mi.normal_bf16(cfg.seed, 104, (E, H), 0.0, 0.02))
+    y32 = torch.empty((T, H), dtype=torch.float32, device="cuda")
+    y16 = torch.empty((T, H), dtype=torch.bfloat16, device="cuda")
+    r_out = torch.empty((T, H), dtype=torch.bfloat16, device="cuda")
+    logits = torch.empty((T, E), dtype=torch.float32, device="cuda")
+    ws = torch.empty(moe.lib().moe_router_logits_workspace_size(T, H, E), dtype=torch.uint8, device="cuda")
+    for _ in range(W):
+        moe.moe_add_rms_norm_cast(h, res, w, 1e-6, y32, y16, r_out)
+        moe.moe_router_logits(y32, wg, logits, ws)
+    torch.cuda.synchronize()
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
+    n_ms, r_ms = 0.0, 0.0
+    for _ in range(K):
+        ev[0].record()
+        moe.moe_add_rms_norm_cast(h, res, w, 1e-6, y32, y16, r_out)
+        ev[1].record()
+        moe.moe_router_logits(y32, wg, logits, ws)
+        ev[2].record()
+        torch.cuda.synchronize()
+        n_ms += ev[0].elapsed_time(ev[1])
+        r_ms += ev[1].elapsed_time(ev[2])
+    return {"what": "fused residual add + RMSNorm + cast (fp32 and bf16 out), then the fp32 router gate GEMM; "
+                    "synthetic bf16 inputs of the workload's T, H, E; CUDA events per kernel, mean of K",
+            "norm_ms": n_ms / K, "router_ms": r_ms / K,
+            "gpu_launches": (1 + (2 if ws.numel() > moe.lib().moe_status_bytes() else 1)) * K,
+            "norm_bytes": T * H * 2 * 2 + H * 2 + T * H * (4 + 2 + 2), "router_flops": 2 * T * H * E}
+
+
 # ------------------------------------------------------------------ GB300 arm
 def run_gb300(args, rank, world, local):
     import numpy as np
@@ -376,6 +415,8 @@ def run_gb300(args, rank, world, local):
     names = ["gating", "init_routing", "gemm_w13_swiglu", "gemm_down", "finalize"]
     kern_ms = {n: statistics.mean(evs[i][j].elapsed_time(evs[i][j + 1]) for i in range(K))
                for j, n in enumerate(names)}
+
+    front = None if args.no_front_end else front_end(args, cfg, K, W, moe, mi, d16)
 
     # end to end: pinned host inputs -> device, forward, result -> pinned host, every step
     e2e = None
@@ -465,6 +506,20 @@ def run_gb300(args, rank, world, local):
     }
     if e2e:
         line["e2e"] = e2e
+    if front:
+        sm_mhz = (clk or {}).get("sm_mhz") or peaks.get("sm_max_mhz", 2070.0)
+        fp32_tflops = torch.cuda.get_device_properties(local).multi_processor_count * 128 * 2 * sm_mhz * 1e6 / 1e12
+        nb = front.pop("norm_bytes")
+        rf = front.pop("router_flops")
+        front["norm_roofline"] = {"bound": "hbm", "achieved": nb / (front["norm_ms"] * 1e-3) / 1e9,
+                                  "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                                  "frac": nb / (front["norm_ms"] * 1e-3) / 1e9 / peaks["hbm_gbs"]}
+        front["router_roofline"] = {"bound": "alu", "achieved": rf / (front["router_ms"] * 1e-3) / 1e12,
+                                    "peak": fp32_tflops, "unit": "TFLOP/s",
+                                    "frac": rf / (front["router_ms"] * 1e-3) / 1e12 / fp32_tflops,
+                                    "peak_source": f"SMs x 128 FP32 lanes x 2 FLOP/FMA x {sm_mhz:.0f} MHz "
+                                                   "(median SM clock of the timed region)"}
+        line["front_end"] = front
     if world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(args)
     print(json.dumps(line), flush=True)

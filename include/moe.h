@@ -105,6 +105,46 @@ MOE_API int moe_workspace_init(void* ws, size_t ws_bytes, void* stream);
 MOE_API int moe_get_device_status(const void* ws, void* stream);
 
 /*
+ * Front end (the step before a1).  [Q3] "fused RMSNorm + Cast": the norm before the MoE gives
+ * the hidden state in FP32 for the gate and in BF16 for the experts, and one op does the
+ * residual add, the RMSNorm and the casts; without a residual (first layer) it is RMSNorm +
+ * cast.  The FP32 output feeds moe_router_logits, the BF16 one the experts (x of
+ * moe_layer_forward).
+ *
+ *  hidden        [T,H] bf16 in.
+ *  residual      [T,H] bf16 in, or NULL (no add: the residual stream is `hidden`).
+ *  norm_weight   [H] bf16.
+ *  eps           variance epsilon (>= 0).
+ *  y_fp32        [T,H] fp32 out: r * rsqrt(mean_h(r^2) + eps) * norm_weight, with
+ *                r = bf16(hidden + residual) (rounded once) or hidden; fp32 arithmetic.
+ *  y_bf16        [T,H] bf16 out (NULL: not written): y_fp32 rounded to nearest even.
+ *  residual_out  [T,H] bf16 out: r, the residual stream for the next layer; required when
+ *                residual is given, optional (NULL) otherwise.  May alias `residual`.
+ *  Constraints: H % 64 == 0, H <= 8192 (one token row is held in registers), 16-byte aligned
+ *  pointers.  Errors as everywhere: negative status, nothing launched.
+ */
+MOE_API int moe_add_rms_norm_cast(const uint16_t* hidden, const uint16_t* residual, const uint16_t* norm_weight,
+                                  int T, int H, float eps, float* y_fp32, uint16_t* y_bf16, uint16_t* residual_out,
+                                  void* stream);
+
+/*
+ * Router gate GEMM (the step before a1): router_logits = y_fp32 . w_gate^T in fp32 ([Q3] "fused
+ * RMSNorm + Cast": the gate is computed from the FP32 hidden state).  Runs on the FP32 pipes:
+ * the tensor-core bf16/tf32 paths would round the fp32 input.
+ *
+ *  y_fp32  [T,H] fp32 (moe_add_rms_norm_cast's FP32 output).
+ *  w_gate  [E,H] bf16 gate weight ([out_features, in_features]), widened exactly.
+ *  logits  [T,E] fp32 out.  H is cut into S slices (S chosen from T, H, E and the SM count);
+ *          each slice is summed in ascending h with fp32 FMA and the slices are added in order,
+ *          so the result is the same on every run.
+ *  ws      at least moe_router_logits_workspace_size(T, H, E) bytes (the slices' partial sums).
+ *  Constraints: H % 64 == 0, E <= 1024, 16-byte aligned pointers.
+ */
+MOE_API size_t moe_router_logits_workspace_size(int T, int H, int E);
+MOE_API int moe_router_logits(const float* y_fp32, const uint16_t* w_gate, int T, int H, int E, float* logits,
+                              void* ws, size_t ws_bytes, void* stream);
+
+/*
  * a1. Gating top-k.  [Q3] "GMM enablement and routing optimisation" (one fused
  * op replaces top-k followed by softmax); [HY3] 1.3 (sigmoid router with
  * correction bias, norm_type=1, routed_scaling_factor, eps) and 5.1 (the bias

@@ -8,7 +8,8 @@ built, every call raises.
 Functions carry the C names:
 
     moe_gating_topk, moe_init_routing, moe_grouped_gemm_swiglu, moe_grouped_gemm,
-    moe_finalize_routing, moe_layer_forward (+ MoELayer, which owns a workspace).
+    moe_finalize_routing, moe_layer_forward (+ MoELayer, which owns a workspace); the front end
+    moe_add_rms_norm_cast and moe_router_logits; moe_init_routing_range.
 """
 from __future__ import annotations
 
@@ -67,6 +68,12 @@ _SIGS = {
                                                        ctypes.c_void_p, ctypes.c_int, ctypes.c_void_p,
                                                        ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
                                                        ctypes.c_void_p, ctypes.c_void_p]),
+    "moe_add_rms_norm_cast": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int,
+                                             ctypes.c_int, ctypes.c_float, ctypes.c_void_p, ctypes.c_void_p,
+                                             ctypes.c_void_p, ctypes.c_void_p]),
+    "moe_router_logits_workspace_size": (ctypes.c_size_t, [ctypes.c_int, ctypes.c_int, ctypes.c_int]),
+    "moe_router_logits": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                                         ctypes.c_void_p, ctypes.c_void_p, ctypes.c_size_t, ctypes.c_void_p]),
     "moe_prepack_w13": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_void_p,
                                        ctypes.c_void_p]),
     "moe_grouped_gemm_workspace_size": (ctypes.c_size_t, []),
@@ -182,6 +189,36 @@ def moe_init_routing(topk_idx, E: int, x=None, ws=None, out: Optional[dict] = No
                                   ws.numel(), _stream(stream)), "moe_init_routing")
     o["ws"] = ws
     return o
+
+
+def moe_add_rms_norm_cast(hidden, residual, norm_weight, eps: float, y_fp32=None, y_bf16=None, residual_out=None,
+                          stream=None):
+    """Front end: returns (y_fp32 [T,H] fp32, y_bf16 [T,H] bf16, residual_out [T,H] bf16 or None)."""
+    torch = _torch()
+    T, H = hidden.shape
+    dev = hidden.device
+    if y_fp32 is None:
+        y_fp32 = torch.empty((T, H), dtype=torch.float32, device=dev)
+    if y_bf16 is None:
+        y_bf16 = torch.empty((T, H), dtype=torch.bfloat16, device=dev)
+    if residual is not None and residual_out is None:
+        residual_out = torch.empty((T, H), dtype=torch.bfloat16, device=dev)
+    _check(lib().moe_add_rms_norm_cast(_ptr(hidden), _ptr(residual), _ptr(norm_weight), T, H, eps, _ptr(y_fp32),
+                                       _ptr(y_bf16), _ptr(residual_out), _stream(stream)), "moe_add_rms_norm_cast")
+    return y_fp32, y_bf16, residual_out
+
+
+def moe_router_logits(y_fp32, w_gate, logits=None, ws=None, stream=None):
+    """Router gate GEMM: logits[T,E] = y_fp32 . w_gate^T in fp32 (w_gate [E,H] bf16)."""
+    torch = _torch()
+    T, H = y_fp32.shape
+    E = w_gate.shape[0]
+    if logits is None:
+        logits = torch.empty((T, E), dtype=torch.float32, device=y_fp32.device)
+    ws = _ws(lib().moe_router_logits_workspace_size(T, H, E), y_fp32.device, ws)
+    _check(lib().moe_router_logits(_ptr(y_fp32), _ptr(w_gate), T, H, E, _ptr(logits), _ptr(ws), ws.numel(),
+                                   _stream(stream)), "moe_router_logits")
+    return logits
 
 
 def moe_init_routing_range(topk_idx, E: int, e0: int, e1: int, x=None, ws=None, out: Optional[dict] = None,

@@ -18,6 +18,15 @@ inline size_t align_up(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
 
 inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
+// SMs of the current device (152 on a GB300; also the answer without a device, so that a
+// workspace size computed on the host matches the one the launch uses there).
+int sm_count() {
+  int dev = 0, n = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 152;
+  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) return 152;
+  return n;
+}
+
 inline cudaStream_t as_stream(void* s) { return reinterpret_cast<cudaStream_t>(s); }
 
 inline int cuda_status(cudaError_t e) { return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA; }
@@ -179,6 +188,40 @@ int moe_init_routing_range(const int32_t* topk_idx, int T, int E, int k, int e0,
                            int32_t* pair_pos, void* ws, size_t ws_bytes, void* stream) {
   return init_routing_impl(topk_idx, T, E, k, e0, e1, x, H, x_exp, counts, offsets, sorted_pair, pair_pos, ws,
                            ws_bytes, stream);
+}
+
+int moe_add_rms_norm_cast(const uint16_t* hidden, const uint16_t* residual, const uint16_t* norm_weight, int T,
+                          int H, float eps, float* y_fp32, uint16_t* y_bf16, uint16_t* residual_out, void* stream) {
+  if (T < 0 || H <= 0 || !(eps >= 0.0f)) return MOE_ERR_INVALID_ARG;
+  if (H % 64 != 0 || H > 8192) return MOE_ERR_UNSUPPORTED;
+  if (T == 0) return MOE_OK;
+  if (!hidden || !norm_weight || !y_fp32) return MOE_ERR_INVALID_ARG;
+  if (residual && !residual_out) return MOE_ERR_INVALID_ARG;  // the new residual stream must go somewhere
+  const void* ptrs[] = {hidden, residual, norm_weight, y_fp32, y_bf16, residual_out};
+  for (const void* p : ptrs)
+    if (p && !aligned16(p)) return MOE_ERR_INVALID_ARG;
+  return cuda_status(moe::launch_add_rms_norm_cast(hidden, residual, norm_weight, T, H, eps, y_fp32, y_bf16,
+                                                   residual_out, as_stream(stream)));
+}
+
+size_t moe_router_logits_workspace_size(int T, int H, int E) {
+  if (T <= 0 || H <= 0 || E <= 0) return kHeader;
+  const int S = moe::router_splits(T, H, E, sm_count());
+  return align_up(kHeader + (S > 1 ? (size_t)S * T * E * sizeof(float) : 0));
+}
+
+int moe_router_logits(const float* y_fp32, const uint16_t* w_gate, int T, int H, int E, float* logits, void* ws,
+                      size_t ws_bytes, void* stream) {
+  if (T < 0 || H <= 0 || E <= 0) return MOE_ERR_INVALID_ARG;
+  if (H % 64 != 0 || E > 1024) return MOE_ERR_UNSUPPORTED;
+  if (T == 0) return MOE_OK;
+  if (!y_fp32 || !w_gate || !logits || !ws || !aligned16(y_fp32) || !aligned16(w_gate) || !aligned16(logits) ||
+      !aligned16(ws))
+    return MOE_ERR_INVALID_ARG;
+  if (ws_bytes < moe_router_logits_workspace_size(T, H, E)) return MOE_ERR_WORKSPACE;
+  const int S = moe::router_splits(T, H, E, sm_count());
+  float* part = reinterpret_cast<float*>(static_cast<char*>(ws) + kHeader);
+  return cuda_status(moe::launch_router_logits(y_fp32, w_gate, T, H, E, logits, part, S, as_stream(stream)));
 }
 
 int moe_prepack_w13(const uint16_t* w13, int E, int I, int H, uint16_t* w13_packed, void* stream) {

@@ -68,6 +68,14 @@ cudaError_t launch_grouped_gemm(const GroupedGemmProblem& p, cudaStream_t stream
 // w13 [E,2I,H] -> packed gate/up layout read by the mode-0 grouped GEMM.
 cudaError_t launch_prepack_w13(const uint16_t* w13, int E, int I, int H, uint16_t* w13p, cudaStream_t stream);
 
+// Front end: fused residual add + RMSNorm + cast (H <= 8192), router gate GEMM in fp32.
+cudaError_t launch_add_rms_norm_cast(const uint16_t* h, const uint16_t* res, const uint16_t* w, int T, int H,
+                                     float eps, float* y32, uint16_t* y16, uint16_t* res_out, cudaStream_t stream);
+// S K-slices (router_splits); with S > 1, part holds S*T*E fp32 partial sums.
+int router_splits(int T, int H, int E, int n_sms);
+cudaError_t launch_router_logits(const float* y32, const uint16_t* w_gate, int T, int H, int E, float* logits,
+                                 float* part, int S, cudaStream_t stream);
+
 cudaError_t launch_finalize(const uint16_t* y_perm, const int32_t* pair_pos, const uint16_t* shared, int T, int k,
                             int H, uint16_t* y, cudaStream_t stream, bool pdl = false);
 

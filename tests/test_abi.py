@@ -133,3 +133,21 @@ def test_missing_library_fails_loudly(tmp_path, monkeypatch):
     monkeypatch.setattr(moe, "_lib", None)
     with pytest.raises(RuntimeError, match="no CPU fallback"):
         moe.lib()
+
+
+def test_front_end_validation_returns_before_launch(L):
+    P16 = 16  # an aligned non-null dummy address: never dereferenced since validation fails first
+    # moe_add_rms_norm_cast(hidden, residual, weight, T, H, eps, y32, y16, residual_out, stream)
+    assert L.moe_add_rms_norm_cast(P16, None, P16, 4, 100, 1e-6, P16, P16, None, None) == moe.MOE_ERR_UNSUPPORTED
+    assert L.moe_add_rms_norm_cast(P16, None, P16, 4, 16384, 1e-6, P16, P16, None, None) == moe.MOE_ERR_UNSUPPORTED
+    assert L.moe_add_rms_norm_cast(P16, P16, P16, 4, 256, 1e-6, P16, P16, None, None) == moe.MOE_ERR_INVALID_ARG
+    assert L.moe_add_rms_norm_cast(P16, None, P16, 4, 256, -1.0, P16, P16, None, None) == moe.MOE_ERR_INVALID_ARG
+    assert L.moe_add_rms_norm_cast(P16 + 4, None, P16, 4, 256, 1e-6, P16, P16, None, None) == moe.MOE_ERR_INVALID_ARG
+    assert L.moe_add_rms_norm_cast(None, None, None, 0, 256, 1e-6, None, None, None, None) == moe.MOE_OK
+    # moe_router_logits(y32, w_gate, T, H, E, logits, stream)
+    assert L.moe_router_logits(P16, P16, 4, 100, 8, P16, P16, 1 << 20, None) == moe.MOE_ERR_UNSUPPORTED
+    assert L.moe_router_logits(P16, P16, 4, 256, 2000, P16, P16, 1 << 20, None) == moe.MOE_ERR_UNSUPPORTED
+    assert L.moe_router_logits(P16, None, 4, 256, 8, P16, P16, 1 << 20, None) == moe.MOE_ERR_INVALID_ARG
+    assert L.moe_router_logits(P16, P16, 4, 256, 8, P16, P16, 0, None) == moe.MOE_ERR_WORKSPACE
+    assert L.moe_router_logits(None, None, 0, 256, 8, None, None, 0, None) == moe.MOE_OK
+    assert L.moe_router_logits_workspace_size(64, 4096, 128) >= L.moe_status_bytes()
