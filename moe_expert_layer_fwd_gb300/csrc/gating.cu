@@ -9,9 +9,10 @@
 // it inside the sigmoid instead, MOE_GATE_SIGMOID_INNER_BIAS here).
 //
 // Each lane holds experts e = lane + 32*i.  The selection key is turned into
-// an order-preserving 32-bit integer and packed with the complement of the
-// expert index, so one 64-bit max over the warp picks "largest key, then
-// lowest index"; k rounds pick the k experts in order.  The sigmoid key is
+// an order-preserving 32-bit integer (0 marks a removed or absent expert).
+// Each of k rounds takes the warp-wide maximum key (redux.sync), then the
+// lowest expert index holding it (each lane's lowest slot with that key, then
+// a warp-wide minimum): "largest key, then lowest index", k experts in order.  The sigmoid key is
 // computed with a fixed sequence of IEEE fp32 operations (Cody-Waite reduced
 // exp with a degree-7 Taylor polynomial, each multiply and add rounded
 // separately), so the choice is reproducible bit for bit on any IEEE machine.
@@ -53,15 +54,6 @@ __device__ __forceinline__ uint32_t ordered_key(float f) {
   return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
 }
 
-__device__ __forceinline__ unsigned long long warp_max_u64(unsigned long long v) {
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) {
-    unsigned long long w = __shfl_xor_sync(0xffffffffu, v, o);
-    v = w > v ? w : v;
-  }
-  return v;
-}
-
 __device__ __forceinline__ float warp_sum(float v) {
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
@@ -81,10 +73,10 @@ __global__ void __launch_bounds__(256) gating_topk_kernel(const float* __restric
   const int t = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
   if (t >= T) return;
   const float* row = logits + (size_t)t * E;
-  unsigned long long packed[VPL];
+  uint32_t keys[VPL];
 #pragma unroll
   for (int i = 0; i < VPL; ++i) {
-    packed[i] = 0ull;  // below every real key: never chosen
+    keys[i] = 0u;  // below every real key: never chosen
     const int e = lane + 32 * i;
     if (e < E) {
       const float l = __ldg(row + e);
@@ -95,21 +87,24 @@ __global__ void __launch_bounds__(256) gating_topk_kernel(const float* __restric
       } else if (gate == MOE_GATE_SIGMOID_INNER_BIAS) {
         key = sigmoid_fixed_f32(bias ? __fadd_rn(l, __ldg(bias + e)) : l);
       }
-      packed[i] = ((unsigned long long)ordered_key(key) << 32) | (unsigned long long)(0xFFFFFFFFu - (uint32_t)e);
+      keys[i] = ordered_key(key);
     }
   }
 
   int my_e = -1;  // lane j keeps the j-th chosen expert
   for (int j = 0; j < k; ++j) {
-    unsigned long long best = 0ull;
+    uint32_t lm = 0u;
 #pragma unroll
-    for (int i = 0; i < VPL; ++i) best = packed[i] > best ? packed[i] : best;
-    best = warp_max_u64(best);
-    const int e = (int)(0xFFFFFFFFu - (uint32_t)(best & 0xFFFFFFFFull));
+    for (int i = 0; i < VPL; ++i) lm = keys[i] > lm ? keys[i] : lm;
+    const uint32_t m = __reduce_max_sync(0xffffffffu, lm);
+    uint32_t cand = 0xFFFFFFFFu;  // this lane's lowest expert holding the maximum key
+#pragma unroll
+    for (int i = VPL - 1; i >= 0; --i) cand = keys[i] == m ? (uint32_t)(lane + 32 * i) : cand;
+    const int e = (int)__reduce_min_sync(0xffffffffu, cand);
     const bool mine = lane == (e & 31);
     const int slot = e >> 5;
 #pragma unroll
-    for (int i = 0; i < VPL; ++i) packed[i] = (mine && i == slot) ? 0ull : packed[i];
+    for (int i = 0; i < VPL; ++i) keys[i] = (mine && i == slot) ? 0u : keys[i];
     if (lane == j) my_e = e;
   }
 

@@ -136,7 +136,6 @@ struct Layout {
   static constexpr uint32_t kTmemCols = (2 * kAccCols <= 32) ? 32 : (2 * kAccCols <= 64 ? 64 : (2 * kAccCols <= 128 ? 128 : (2 * kAccCols <= 256 ? 256 : 512)));
   static constexpr int kFeatPerBox = MODE == 0 ? 64 : 128;       // output features of one weight box
   static constexpr int kFeatPerTile = kFeatPerBox * APARTS * PAIR;
-  static_assert(PAIR == 1 || APARTS == 1, "CTA pairs stage one weight box per CTA");
   static_assert(2 * kAccCols <= 512, "accumulators exceed TMEM");
   static_assert(kBRows % BBOX == 0 && KC * (kBRows / BBOX) <= 24 && KC * APARTS <= 8, "boxes per stage");
   static_assert(kAChunk % 1024 == 0 && kBChunk % 1024 == 0, "chunk alignment");
@@ -542,18 +541,21 @@ __global__ void __launch_bounds__(64 + 32 * (EPI + GW), 1)
           }
         }
       } else {
-        const int feat = t.f * L::kFeatPerTile + (int)rank * kBM + qw * 32 + lane;
-        const bool feat_ok = feat < n_feat;
-        uint16_t* orow = out + (size_t)t.row_base * ld + feat;
-        for (int c = half_c; c < nch; c += kPerQ) {
-          uint32_t v[32];
-          tmem_ld32_async(tb + (uint32_t)(c * 32), v);
-          tmem_wait_ld();
-          float o[32];
 #pragma unroll
-          for (int i = 0; i < 32; ++i) o[i] = __uint_as_float(v[i]) * (scale ? wsc[c * 32 + i] : 1.0f);
-          store_pairs16(o, lane, orow, ld, c * 32, t.rows, feat_ok);
-          store_pairs16(o + 16, lane, orow, ld, c * 32 + 16, t.rows, feat_ok);
+        for (int part = 0; part < APARTS; ++part) {
+          const int feat = t.f * L::kFeatPerTile + ((int)rank * APARTS + part) * kBM + qw * 32 + lane;
+          const bool feat_ok = feat < n_feat;
+          uint16_t* orow = out + (size_t)t.row_base * ld + feat;
+          for (int c = half_c; c < nch; c += kPerQ) {
+            uint32_t v[32];
+            tmem_ld32_async(tb + (uint32_t)(part * NTMAX + c * 32), v);
+            tmem_wait_ld();
+            float o[32];
+#pragma unroll
+            for (int i = 0; i < 32; ++i) o[i] = __uint_as_float(v[i]) * (scale ? wsc[c * 32 + i] : 1.0f);
+            store_pairs16(o, lane, orow, ld, c * 32, t.rows, feat_ok);
+            store_pairs16(o + 16, lane, orow, ld, c * 32 + 16, t.rows, feat_ok);
+          }
         }
         __syncwarp();  // the next tile rewrites this warp's scales
       }

@@ -80,9 +80,19 @@ __global__ void __launch_bounds__(1024) route_scan_kernel(const int32_t* __restr
   const bool active = seg < S;
   const int cps = (n_chunks + S - 1) / S;
   const int c0 = min(n_chunks, seg * cps), c1 = min(n_chunks, c0 + cps);
+  // chunk histograms are read 8 at a time so that their loads overlap
+  constexpr int kU = 8;
   if (active) {
     int s = 0;
-    for (int c = c0; c < c1; ++c) s += hist[(size_t)c * E + e];
+    int c = c0;
+    for (; c + kU <= c1; c += kU) {
+      int v[kU];
+#pragma unroll
+      for (int u = 0; u < kU; ++u) v[u] = __ldg(hist + (size_t)(c + u) * E + e);
+#pragma unroll
+      for (int u = 0; u < kU; ++u) s += v[u];
+    }
+    for (; c < c1; ++c) s += __ldg(hist + (size_t)c * E + e);
     part[seg * E + e] = s;
   }
   __syncthreads();
@@ -120,9 +130,20 @@ __global__ void __launch_bounds__(1024) route_scan_kernel(const int32_t* __restr
   if (active) {
     int run = excl_s[e];
     for (int g = 0; g < seg; ++g) run += part[g * E + e];
-    for (int c = c0; c < c1; ++c) {
+    int c = c0;
+    for (; c + kU <= c1; c += kU) {
+      int v[kU];
+#pragma unroll
+      for (int u = 0; u < kU; ++u) v[u] = __ldg(hist + (size_t)(c + u) * E + e);
+#pragma unroll
+      for (int u = 0; u < kU; ++u) {
+        base[(size_t)(c + u) * E + e] = run;
+        run += v[u];
+      }
+    }
+    for (; c < c1; ++c) {
       base[(size_t)c * E + e] = run;
-      run += hist[(size_t)c * E + e];
+      run += __ldg(hist + (size_t)c * E + e);
     }
   }
 }
