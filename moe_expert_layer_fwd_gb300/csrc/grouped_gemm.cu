@@ -477,6 +477,41 @@ __global__ void __launch_bounds__(64 + 32 * (EPI + GW), 1)
     constexpr int kPerQ = EPI / 4;           // epilogue warps sharing one TMEM lane quarter
     const int half_c = (warp - 2) >> 2;      // this warp takes 32-column chunks half_c, half_c + kPerQ, ...
     const uint32_t tempty_leader = PAIR == 2 ? mapa_shared(smem_u32(&tempty[0]), 0) : 0u;
+    if (GW > 0 && p.g_flags != nullptr) {
+      // Until the first accumulator is ready the epilogue warps are idle: they gather this CTA's
+      // first GW row chunks (one row per warp at a time), which the first tiles of the GPU wait for;
+      // the gather warps take the CTA's later chunks.
+      pdl_wait();  // sorted_pair comes from the previous kernel
+      const int ew = warp - 2;
+      const int n_chunks = (p.M + kGatherRows - 1) / kGatherRows;
+      for (int g = 0; g < GW; ++g) {
+        const int q = GW * (int)blockIdx.x + g;
+        if (q >= n_chunks) break;  // uniform over the epilogue warps
+        const int r0 = q * kGatherRows, nrow = min(kGatherRows, p.M - r0);
+        for (int i = ew; i < nrow; i += EPI) {
+          const int t = __ldg(p.g_sp + r0 + i) / p.g_k;
+          if ((unsigned)t >= (unsigned)p.g_T) continue;
+          const uint4* src = p.g_x + (size_t)t * p.g_H8;
+          uint4* dst = p.g_xexp + (size_t)(r0 + i) * p.g_H8;
+          for (int c = lane; c < p.g_H8; c += 4 * 32) {
+            uint4 v[4];
+#pragma unroll
+            for (int w = 0; w < 4; ++w)
+              if (c + 32 * w < p.g_H8) v[w] = __ldg(src + c + 32 * w);
+#pragma unroll
+            for (int w = 0; w < 4; ++w)
+              if (c + 32 * w < p.g_H8) dst[c + 32 * w] = v[w];
+          }
+        }
+        // every epilogue warp has written its rows of chunk q: publish it
+        asm volatile("bar.sync 1, %0;" ::"r"(32 * EPI) : "memory");
+        if (warp == 2 && lane == 0) {
+          fence_proxy_async_global();
+          __threadfence();
+          st_release_gpu(p.g_flags + q, 1u);
+        }
+      }
+    }
     int it = 0;
     for (int tile = group; tile < total; tile += ngroups, ++it) {
       const Tile t = decode_tile(tile, routed_total, s_off, s_tt, p);
@@ -575,7 +610,8 @@ __global__ void __launch_bounds__(64 + 32 * (EPI + GW), 1)
     const int gw = warp - 2 - EPI;
     const int n_chunks = (p.M + kGatherRows - 1) / kGatherRows;
     const int H8 = p.g_H8;
-    for (int q = GW * (int)blockIdx.x + gw; q < n_chunks; q += GW * (int)gridDim.x) {
+    // the CTA's first GW chunks are gathered by the epilogue warps
+    for (int q = GW * ((int)blockIdx.x + (int)gridDim.x) + gw; q < n_chunks; q += GW * (int)gridDim.x) {
       const int r0 = q * kGatherRows, nrow = min(kGatherRows, p.M - r0);
       int tl = -1;  // lane i < nrow: source token of row r0 + i
       if (lane < nrow) {
