@@ -20,6 +20,7 @@ What it computes, step by step, each function citing the passage it follows:
   the whole layer, and the routed part of the layer over a local expert range.
 * ``frontend`` -- the step before gating: fused residual add + RMSNorm + cast
   (FP32 for the gate, BF16 for the experts) and the router gate GEMM.
+* ``mx``       -- MXFP8 (E4M3 elements, E8M0 scale per 32) dynamic quantisation.
 
 Precision: float64 everywhere, except the expert *selection*, which is an
 integer decided by floating point and is therefore taken in float32 with the
@@ -32,6 +33,7 @@ from .gating import exp_f32_pinned, sigmoid_f32_pinned, selection_keys, gating_t
 from .routing import init_routing, init_routing_range, expand_rows
 from .ffn import swiglu, expert_ffn, grouped_gemm_swiglu, grouped_gemm, bf16_to_f64
 from .frontend import add_rms_norm_cast, round_bf16, router_logits
+from .mx import mx_dequantize_e4m3, mx_quantize_e4m3
 from .layer import (finalize_routing, moe_layer_forward, moe_layer_forward_range, moe_layer_forward_tokens,
                     shared_expert)
 
@@ -39,6 +41,6 @@ __all__ = [
     "exp_f32_pinned", "sigmoid_f32_pinned", "selection_keys", "gating_topk",
     "init_routing", "init_routing_range", "expand_rows",
     "swiglu", "expert_ffn", "grouped_gemm_swiglu", "grouped_gemm", "bf16_to_f64",
-    "add_rms_norm_cast", "round_bf16", "router_logits",
+    "add_rms_norm_cast", "round_bf16", "router_logits", "mx_quantize_e4m3", "mx_dequantize_e4m3",
     "finalize_routing", "moe_layer_forward", "moe_layer_forward_range", "moe_layer_forward_tokens", "shared_expert",
 ]

@@ -1,0 +1,66 @@
+"""Pins of the oracle's MXFP8 (E4M3) dynamic quantisation.
+
+Passage: Qwen3-MoE low-latency inference practice, W4A8 section (MXFP8 quantisation of the
+hidden state: npu_dynamic_mx_quant; fused add + RMSNorm + MXFP8 quant with round_mode 'rint',
+dst_type float8_e4m3fn).  Pinned by closed forms of the E4M3 grid, by torch's float8_e4m3fn
+conversion (inside the finite range), by exhaustive encode/decode of all 254 finite codes, and by
+the block-scale rule on hand-made blocks.
+"""
+import numpy as np
+import pytest
+import torch
+
+from oracle.mx import e4m3_decode, e4m3_encode, e4m3_round, mx_dequantize_e4m3, mx_quantize_e4m3
+
+
+def test_e4m3_grid_closed_forms():
+    cases = {0.0: 0.0, 1.0: 1.0, 1.0625: 1.0, 1.1875: 1.25, 1.125: 1.125, 448.0: 448.0, 460.0: 448.0,
+             1e6: 448.0, 2.0 ** -9: 2.0 ** -9, 2.0 ** -10: 0.0, 3 * 2.0 ** -11: 2.0 ** -9, -3.3: -3.25,
+             240.0: 240.0, 248.0: 256.0, 17.0: 16.0}
+    for v, ref in cases.items():
+        assert e4m3_round(np.float64(v)) == ref, v
+
+
+def test_all_codes_round_trip():
+    codes = np.array([c for c in range(256) if c & 0x7F != 0x7F], np.uint8)
+    vals = e4m3_decode(codes)
+    assert (e4m3_encode(vals)[vals != 0] == codes[vals != 0]).all()
+    assert (e4m3_round(vals) == vals).all()
+    assert np.abs(vals).max() == 448.0
+
+
+def test_e4m3_matches_torch_in_range():
+    rng = np.random.default_rng(0)
+    v = (rng.normal(size=50000) * np.exp(rng.uniform(-12, 6, size=50000))).astype(np.float32)
+    v = v[np.abs(v) <= 448]
+    ref = torch.from_numpy(v).to(torch.float8_e4m3fn).to(torch.float64).numpy()
+    assert (e4m3_round(v.astype(np.float64)) == ref).all()
+
+
+def test_block_scale_rule():
+    blk = np.zeros((2, 32))
+    blk[0, 5] = 1.0          # amax 1 -> floor(log2) 0 -> shared -8 -> scale byte 119
+    blk[0, 6] = -0.0078125   # 2^-7 -> 2^-7 / 2^-8 = 2 exactly
+    codes, scales = mx_quantize_e4m3(blk)
+    assert scales[:, 0].tolist() == [119, 0]            # second block all zero -> byte 0
+    assert e4m3_decode(codes[0, 5]) == 256.0 and e4m3_decode(codes[0, 6]) == -2.0
+    assert (codes[1] == 0).all()
+    back = mx_dequantize_e4m3(codes, scales)
+    np.testing.assert_array_equal(back[0], blk[0])
+    # amax just below a power of two: 1.99 -> shared -8, 1.99 * 256 = 509.4 saturates to 448
+    c2, s2 = mx_quantize_e4m3(np.full((1, 32), 1.99))
+    assert s2[0, 0] == 119 and e4m3_decode(c2[0, 0]) == 448.0
+
+
+@pytest.mark.parametrize("seed", range(3))
+def test_dequantisation_error_bound(seed):
+    rng = np.random.default_rng(seed)
+    v = rng.normal(size=(64, 256)) * np.exp(rng.uniform(-8, 8, size=(64, 1)))
+    codes, scales = mx_quantize_e4m3(v)
+    back = mx_dequantize_e4m3(codes, scales)
+    x = np.exp2(scales.astype(np.float64) - 127.0).repeat(32, axis=1)
+    # below saturation the error is at most half a quantum of v's binade in units of the scale
+    q = np.abs(v) / x
+    ok = q <= 448
+    bound = 0.5 * np.exp2(np.floor(np.log2(np.maximum(q, 2.0 ** -6))) - 3.0) * x
+    assert (np.abs(back - v)[ok] <= bound[ok] * (1 + 1e-12)).all()
