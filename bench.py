@@ -312,8 +312,23 @@ def front_end(args, cfg, K, W, moe, mi, d16):
         moe.moe_add_rms_norm_cast(h, res, w, 1e-6, y32, y16, r_out)
         moe.moe_router_logits(y32, wg, logits, ws)
     torch.cuda.synchronize()
+    codes = torch.empty((T, H), dtype=torch.uint8, device="cuda")
+    scales = torch.empty((T, H // 32), dtype=torch.uint8, device="cuda")
+
+    def mx():
+        moe.lib().moe_add_rms_norm_mxfp8(h.data_ptr(), res.data_ptr(), w.data_ptr(), T, H, 1e-6, codes.data_ptr(),
+                                         scales.data_ptr(), None, r_out.data_ptr(), None)
+
+    for _ in range(W):
+        mx()
     ev = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
-    n_ms, r_ms = 0.0, 0.0
+    n_ms, r_ms, m_ms = 0.0, 0.0, 0.0
+    for _ in range(K):
+        ev[0].record()
+        mx()
+        ev[1].record()
+        torch.cuda.synchronize()
+        m_ms += ev[0].elapsed_time(ev[1])
     for _ in range(K):
         ev[0].record()
         moe.moe_add_rms_norm_cast(h, res, w, 1e-6, y32, y16, r_out)
@@ -324,10 +339,12 @@ def front_end(args, cfg, K, W, moe, mi, d16):
         n_ms += ev[0].elapsed_time(ev[1])
         r_ms += ev[1].elapsed_time(ev[2])
     return {"what": "fused residual add + RMSNorm + cast (fp32 and bf16 out), then the fp32 router gate GEMM; "
+                    "separately the fused add + RMSNorm + MXFP8 quantisation (E4M3 codes, E8M0 scales); "
                     "synthetic bf16 inputs of the workload's T, H, E; CUDA events per kernel, mean of K",
-            "norm_ms": n_ms / K, "router_ms": r_ms / K,
-            "gpu_launches": (1 + (2 if ws.numel() > moe.lib().moe_status_bytes() else 1)) * K,
-            "norm_bytes": T * H * 2 * 2 + H * 2 + T * H * (4 + 2 + 2), "router_flops": 2 * T * H * E}
+            "norm_ms": n_ms / K, "router_ms": r_ms / K, "norm_mxfp8_ms": m_ms / K,
+            "gpu_launches": (2 + (2 if ws.numel() > moe.lib().moe_status_bytes() else 1)) * K,
+            "norm_bytes": T * H * 2 * 2 + H * 2 + T * H * (4 + 2 + 2), "router_flops": 2 * T * H * E,
+            "mx_bytes": T * H * 2 * 2 + H * 2 + T * H * (1 + 2) + T * H // 32}
 
 
 # ------------------------------------------------------------------ GB300 arm
@@ -510,6 +527,10 @@ def run_gb300(args, rank, world, local):
         sm_mhz = (clk or {}).get("sm_mhz") or peaks.get("sm_max_mhz", 2070.0)
         fp32_tflops = torch.cuda.get_device_properties(local).multi_processor_count * 128 * 2 * sm_mhz * 1e6 / 1e12
         nb = front.pop("norm_bytes")
+        mb = front.pop("mx_bytes")
+        front["norm_mxfp8_roofline"] = {"bound": "hbm", "achieved": mb / (front["norm_mxfp8_ms"] * 1e-3) / 1e9,
+                                        "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                                        "frac": mb / (front["norm_mxfp8_ms"] * 1e-3) / 1e9 / peaks["hbm_gbs"]}
         rf = front.pop("router_flops")
         front["norm_roofline"] = {"bound": "hbm", "achieved": nb / (front["norm_ms"] * 1e-3) / 1e9,
                                   "peak": peaks["hbm_gbs"], "unit": "GB/s",

@@ -128,6 +128,24 @@ MOE_API int moe_add_rms_norm_cast(const uint16_t* hidden, const uint16_t* residu
                                   void* stream);
 
 /*
+ * Front end of the W4A8 path: fused residual add + RMSNorm + MXFP8 dynamic quantisation ([Q3]
+ * W4A8 section: add_rms_norm_dynamic_mx_quant, round_mode 'rint', dst_type float8_e4m3fn; without
+ * a residual, rms_norm_dynamic_mx_quant).  The normalised row y (fp32, as moe_add_rms_norm_cast
+ * computes it) is cut into blocks of 32 consecutive elements; a block's scale is
+ * X = 2^(floor(log2 max|y|) - 8) (8: the largest E4M3 exponent), stored as an E8M0 byte
+ * (exponent + 127, clamped to [-127, 127]; an all-zero block gets 0); each element y / X is
+ * rounded to E4M3 (the "fn" variant: no infinities), nearest even, saturating at +-448.
+ *
+ *  y_fp8         [T,H] uint8 out: E4M3 codes.
+ *  y_scale       [T,H/32] uint8 out: E8M0 scale bytes (no alignment requirement).
+ *  y_fp32        [T,H] fp32 out, or NULL: the unquantised y (e.g. for the gate GEMM).
+ *  others        as moe_add_rms_norm_cast; same constraints (H % 64 == 0, H <= 8192).
+ */
+MOE_API int moe_add_rms_norm_mxfp8(const uint16_t* hidden, const uint16_t* residual, const uint16_t* norm_weight,
+                                   int T, int H, float eps, uint8_t* y_fp8, uint8_t* y_scale, float* y_fp32,
+                                   uint16_t* residual_out, void* stream);
+
+/*
  * Router gate GEMM (the step before a1): router_logits = y_fp32 . w_gate^T in fp32 ([Q3] "fused
  * RMSNorm + Cast": the gate is computed from the FP32 hidden state).  Runs on the FP32 pipes:
  * the tensor-core bf16/tf32 paths would round the fp32 input.

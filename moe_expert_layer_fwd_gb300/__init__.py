@@ -71,6 +71,9 @@ _SIGS = {
     "moe_add_rms_norm_cast": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int,
                                              ctypes.c_int, ctypes.c_float, ctypes.c_void_p, ctypes.c_void_p,
                                              ctypes.c_void_p, ctypes.c_void_p]),
+    "moe_add_rms_norm_mxfp8": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int,
+                                              ctypes.c_int, ctypes.c_float, ctypes.c_void_p, ctypes.c_void_p,
+                                              ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p]),
     "moe_router_logits_workspace_size": (ctypes.c_size_t, [ctypes.c_int, ctypes.c_int, ctypes.c_int]),
     "moe_router_logits": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int, ctypes.c_int, ctypes.c_int,
                                          ctypes.c_void_p, ctypes.c_void_p, ctypes.c_size_t, ctypes.c_void_p]),
@@ -206,6 +209,22 @@ def moe_add_rms_norm_cast(hidden, residual, norm_weight, eps: float, y_fp32=None
     _check(lib().moe_add_rms_norm_cast(_ptr(hidden), _ptr(residual), _ptr(norm_weight), T, H, eps, _ptr(y_fp32),
                                        _ptr(y_bf16), _ptr(residual_out), _stream(stream)), "moe_add_rms_norm_cast")
     return y_fp32, y_bf16, residual_out
+
+
+def moe_add_rms_norm_mxfp8(hidden, residual, norm_weight, eps: float, with_fp32: bool = True, stream=None):
+    """W4A8 front end: returns (codes [T,H] uint8 E4M3, scales [T,H/32] uint8 E8M0, y_fp32 or None,
+    residual_out or None)."""
+    torch = _torch()
+    T, H = hidden.shape
+    dev = hidden.device
+    codes = torch.empty((T, H), dtype=torch.uint8, device=dev)
+    scales = torch.empty((T, H // 32), dtype=torch.uint8, device=dev)
+    y32 = torch.empty((T, H), dtype=torch.float32, device=dev) if with_fp32 else None
+    r_out = torch.empty((T, H), dtype=torch.bfloat16, device=dev) if residual is not None else None
+    _check(lib().moe_add_rms_norm_mxfp8(_ptr(hidden), _ptr(residual), _ptr(norm_weight), T, H, eps, _ptr(codes),
+                                        _ptr(scales), _ptr(y32), _ptr(r_out), _stream(stream)),
+           "moe_add_rms_norm_mxfp8")
+    return codes, scales, y32, r_out
 
 
 def moe_router_logits(y_fp32, w_gate, logits=None, ws=None, stream=None):

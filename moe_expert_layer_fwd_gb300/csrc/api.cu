@@ -204,6 +204,21 @@ int moe_add_rms_norm_cast(const uint16_t* hidden, const uint16_t* residual, cons
                                                    residual_out, as_stream(stream)));
 }
 
+int moe_add_rms_norm_mxfp8(const uint16_t* hidden, const uint16_t* residual, const uint16_t* norm_weight, int T,
+                           int H, float eps, uint8_t* y_fp8, uint8_t* y_scale, float* y_fp32, uint16_t* residual_out,
+                           void* stream) {
+  if (T < 0 || H <= 0 || !(eps >= 0.0f)) return MOE_ERR_INVALID_ARG;
+  if (H % 64 != 0 || H > 8192) return MOE_ERR_UNSUPPORTED;
+  if (T == 0) return MOE_OK;
+  if (!hidden || !norm_weight || !y_fp8 || !y_scale) return MOE_ERR_INVALID_ARG;
+  if (residual && !residual_out) return MOE_ERR_INVALID_ARG;
+  const void* ptrs[] = {hidden, residual, norm_weight, y_fp8, y_fp32, residual_out};
+  for (const void* p : ptrs)
+    if (p && !aligned16(p)) return MOE_ERR_INVALID_ARG;
+  return cuda_status(moe::launch_add_rms_norm_cast(hidden, residual, norm_weight, T, H, eps, y_fp32, nullptr,
+                                                   residual_out, as_stream(stream), y_fp8, y_scale));
+}
+
 size_t moe_router_logits_workspace_size(int T, int H, int E) {
   if (T <= 0 || H <= 0 || E <= 0) return kHeader;
   const int S = moe::router_splits(T, H, E, sm_count());

@@ -7,14 +7,19 @@
 //
 // add_rms_norm_cast_kernel: one block per token, the row held in registers (VPT 16-byte words of 8
 // bf16 per thread): r = bf16(h + res) rounded once (the residual stream, stored), sum of r^2 in
-// fp32, one block reduction, y = r * rsqrt(mean + eps) * w, stored as fp32 and as bf16.
-// HBM-bound: reads 2*T*H*2 B (+ H*2 weight), writes T*H*(4 + 2 + 2) B.
+// fp32, one block reduction, y = r * rsqrt(mean + eps) * w, stored as fp32 and/or bf16 and/or
+// MXFP8 (the same section's fused add + RMSNorm + dynamic MX quantisation, W4A8 path): blocks of
+// 32 elements (4 words, held by 4 adjacent lanes) share the scale 2^(floor(log2 amax) - 8) as an
+// E8M0 byte; each element y / scale is rounded to E4M3, nearest even, saturating at 448.
+// HBM-bound: reads 2*T*H*2 B (+ H*2 weight), writes T*H*(4 + 2 + 2) B (cast outputs).
 //
 // router_logits_kernel: logits[T,E] = y32[T,H] . w_gate[E,H]^T in fp32 on the FP32 pipes (the
 // fp32 input would be rounded by the bf16/tf32 tensor-core paths).  128 x 128 output tiles, 256
 // threads with 8 x 8 outputs each, K in steps of 32 staged in shared memory (the bf16 weight
 // widened there), split over K into slices added in order by a second kernel when there are
 // too few tiles for the GPU; each slice accumulates in ascending k.  ALU-bound: 2*T*H*E FLOPs.
+#include <cuda_fp8.h>
+
 #include "moe_common.cuh"
 #include "moe_internal.h"
 
@@ -49,7 +54,8 @@ __device__ __forceinline__ void unpack8(const uint4& u, float (&f)[8]) {
 template <int VPT>
 __global__ void __launch_bounds__(kNormThreads) add_rms_norm_cast_kernel(
     const uint4* __restrict__ h, const uint4* res, const uint4* __restrict__ w, int H8, float eps,
-    float4* __restrict__ y32, uint4* __restrict__ y16, uint4* res_out) {
+    float4* __restrict__ y32, uint4* __restrict__ y16, uint4* res_out, uint2* __restrict__ mx_codes,
+    uint8_t* __restrict__ mx_scales) {
   // res_out may alias res: each word is read and then written by the same thread
   __shared__ float red[32];
   const size_t row = (size_t)blockIdx.x * H8;
@@ -88,13 +94,44 @@ __global__ void __launch_bounds__(kNormThreads) add_rms_norm_cast_kernel(
 #pragma unroll
   for (int v = 0; v < VPT; ++v) {
     const int c = threadIdx.x + v * kNormThreads;
+    float y[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
     if (c < H8) {
-      float g[8], y[8];
+      float g[8];
       unpack8(__ldg(w + c), g);
 #pragma unroll
       for (int i = 0; i < 8; ++i) y[i] = r[v][i] * rstd * g[i];
-      y32[2 * (row + c)] = make_float4(y[0], y[1], y[2], y[3]);
-      y32[2 * (row + c) + 1] = make_float4(y[4], y[5], y[6], y[7]);
+    }
+    if (mx_codes) {  // uniform: every lane takes part in the block maximum
+      float m = 0.0f;
+#pragma unroll
+      for (int i = 0; i < 8; ++i) m = fmaxf(m, fabsf(y[i]));
+      m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 1));
+      m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 2));
+      // shared exponent floor(log2 m) - 8, clamped to the E8M0 range; m == 0 or subnormal -> -127
+      const int eb = (int)((__float_as_uint(m) >> 23) & 0xFF);
+      const int shared = eb == 0 ? -127 : max(-127, min(127, eb - 127 - 8));
+      const int k = -shared;  // y * 2^k: exact power-of-two scaling
+      const float inv = k >= -126 ? __uint_as_float((uint32_t)(k + 127) << 23) : __uint_as_float(0x00400000u);
+      if (c < H8) {
+        uint32_t lo = 0, hi = 0;
+#pragma unroll
+        for (int i = 0; i < 4; i += 2) {
+          const __nv_fp8x2_storage_t a = __nv_cvt_float2_to_fp8x2(make_float2(y[i] * inv, y[i + 1] * inv),
+                                                                  __NV_SATFINITE, __NV_E4M3);
+          const __nv_fp8x2_storage_t b = __nv_cvt_float2_to_fp8x2(make_float2(y[i + 4] * inv, y[i + 5] * inv),
+                                                                  __NV_SATFINITE, __NV_E4M3);
+          lo |= (uint32_t)a << (8 * i);
+          hi |= (uint32_t)b << (8 * i);
+        }
+        mx_codes[row + c] = make_uint2(lo, hi);
+        if ((c & 3) == 0) mx_scales[(row + c) / 4] = (uint8_t)(shared + 127);
+      }
+    }
+    if (c < H8) {
+      if (y32) {
+        y32[2 * (row + c)] = make_float4(y[0], y[1], y[2], y[3]);
+        y32[2 * (row + c) + 1] = make_float4(y[4], y[5], y[6], y[7]);
+      }
       if (y16) {
         uint4 o;
         o.x = pack_bf16x2(y[0], y[1]);
@@ -211,14 +248,16 @@ int router_splits(int T, int H, int E, int n_sms) {
 }
 
 cudaError_t launch_add_rms_norm_cast(const uint16_t* h, const uint16_t* res, const uint16_t* w, int T, int H,
-                                     float eps, float* y32, uint16_t* y16, uint16_t* res_out, cudaStream_t stream) {
+                                     float eps, float* y32, uint16_t* y16, uint16_t* res_out, cudaStream_t stream,
+                                     uint8_t* mx_codes, uint8_t* mx_scales) {
   if (T == 0) return cudaSuccess;
   const int H8 = H / 8;
   const int vpt = (H8 + kNormThreads - 1) / kNormThreads;
   auto args = [&](auto kern) {
     kern<<<T, kNormThreads, 0, stream>>>(reinterpret_cast<const uint4*>(h), reinterpret_cast<const uint4*>(res),
                                           reinterpret_cast<const uint4*>(w), H8, eps, reinterpret_cast<float4*>(y32),
-                                          reinterpret_cast<uint4*>(y16), reinterpret_cast<uint4*>(res_out));
+                                          reinterpret_cast<uint4*>(y16), reinterpret_cast<uint4*>(res_out),
+                                          reinterpret_cast<uint2*>(mx_codes), mx_scales);
     return cudaGetLastError();
   };
   if (vpt <= 1) return args(add_rms_norm_cast_kernel<1>);

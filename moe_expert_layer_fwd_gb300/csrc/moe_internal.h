@@ -69,8 +69,10 @@ cudaError_t launch_grouped_gemm(const GroupedGemmProblem& p, cudaStream_t stream
 cudaError_t launch_prepack_w13(const uint16_t* w13, int E, int I, int H, uint16_t* w13p, cudaStream_t stream);
 
 // Front end: fused residual add + RMSNorm + cast (H <= 8192), router gate GEMM in fp32.
+// mx_codes / mx_scales (optional): the MXFP8 output, E4M3 codes [T,H] and E8M0 scales [T,H/32].
 cudaError_t launch_add_rms_norm_cast(const uint16_t* h, const uint16_t* res, const uint16_t* w, int T, int H,
-                                     float eps, float* y32, uint16_t* y16, uint16_t* res_out, cudaStream_t stream);
+                                     float eps, float* y32, uint16_t* y16, uint16_t* res_out, cudaStream_t stream,
+                                     uint8_t* mx_codes = nullptr, uint8_t* mx_scales = nullptr);
 // S K-slices (router_splits); with S > 1, part holds S*T*E fp32 partial sums.
 int router_splits(int T, int H, int E, int n_sms);
 cudaError_t launch_router_logits(const float* y32, const uint16_t* w_gate, int T, int H, int E, float* logits,

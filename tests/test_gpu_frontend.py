@@ -95,3 +95,48 @@ def test_front_end_feeds_the_layer(moe):
     ref = oracle.moe_layer_forward(x16, host(logits), cfg.k, cfg.gate, inp.w13, inp.w2)
     assert (host(layer.topk_idx) == ref["topk_idx"]).all()
     assert_close(host_bf16_f64(layer.y), ref["y"], "layer y")
+
+
+# ---------------------------------------------------------------- MXFP8 (W4A8 front end)
+@pytest.mark.parametrize("T,H,with_res", [(1, 256, True), (37, 2048, True), (64, 4096, False), (300, 8192, True)])
+def test_add_rms_norm_mxfp8_parity(moe, T, H, with_res):
+    """Codes and scales are integers decided by fp32 arithmetic: the oracle quantises the GPU's own
+    fp32 normalised row (same precision); that row is itself checked against float64."""
+    import torch
+    from oracle.mx import mx_dequantize_e4m3, mx_quantize_e4m3
+    h = _bf16(T + H, 11, (T, H))
+    res = _bf16(T + H, 12, (T, H), 0.0, 3.0) if with_res else None
+    w = _bf16(T + H, 13, (H,), 1.0, 0.3)
+    eps = 1e-6
+    codes, scales, y32, r = moe.moe_add_rms_norm_mxfp8(dev_bf16(h), dev_bf16(res) if with_res else None,
+                                                       dev_bf16(w), eps)
+    torch.cuda.synchronize()
+    y_ref, _, r_ref = oracle.add_rms_norm_cast(h, res, w, eps)
+    y_gpu = host(y32).astype(np.float64)
+    assert np.abs(y_gpu - y_ref).max() <= 1e-5 * np.abs(y_ref).max()
+    if with_res:
+        assert (host_bf16_f64(r) == r_ref).all()
+    c_ref, s_ref = mx_quantize_e4m3(y_gpu)
+    assert (host(scales) == s_ref).all()
+    assert (host(codes) == c_ref).all()
+    # the dequantised row: half an E4M3 step of each element, or +-448 X where y / X > 448 (clipped)
+    back = mx_dequantize_e4m3(host(codes), host(scales))
+    x = np.exp2(host(scales).astype(np.float64) - 127.0).repeat(32, axis=1)
+    sat = np.abs(y_gpu) / x > 448
+    assert (np.abs(back - y_gpu)[~sat] <= 2.0 ** -4 * np.abs(y_gpu)[~sat] + 2.0 ** -10 * x[~sat]).all()
+    assert (np.abs(back[sat]) == 448 * x[sat]).all()
+
+
+def test_mxfp8_zero_rows_and_saturation(moe):
+    import torch
+    from oracle.mx import mx_quantize_e4m3
+    T, H = 4, 256
+    h = np.zeros((T, H), np.uint16)          # bf16 zeros: y = 0 everywhere -> scale byte 0, codes 0
+    h[1] = mi.normal_bf16(3, 1, (H,))
+    h[2, :32] = 0x3F80                       # a block of equal values 1.0 (each 448 after scaling? no:
+    w = np.full(H, 0x3F80, np.uint16)        #  amax/X in [256, 512): 1.0 -> 256 exactly)
+    codes, scales, y32, _ = moe.moe_add_rms_norm_mxfp8(dev_bf16(h), None, dev_bf16(w), 1e-6)
+    torch.cuda.synchronize()
+    assert (host(scales)[0] == 0).all() and (host(codes)[0] == 0).all()
+    c_ref, s_ref = mx_quantize_e4m3(host(y32).astype(np.float64))
+    assert (host(codes) == c_ref).all() and (host(scales) == s_ref).all()
