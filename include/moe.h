@@ -100,6 +100,18 @@ MOE_API size_t moe_status_bytes(void);
  * Call once after allocating a workspace, and after handling an error. */
 MOE_API int moe_workspace_init(void* ws, size_t ws_bytes, void* stream);
 
+/*
+ * Failure injection, for testing the bounded waits (process-wide, not thread-safe; set it back to
+ * 0 afterwards).  what = 1: the limit, in ns, of every wait inside the grouped GEMMs (0: the
+ * default, 2 s).  what = 2: value != 0 makes the gate/up GEMM's in-kernel row gather (taken by
+ * compute-bound problems inside moe_layer_forward) write nothing and set none of its flags, so its
+ * producers wait for flags that nothing sets: after the limit the kernel records MOE_ERR_TIMEOUT in
+ * the workspace status, every CTA leaves its loops, waits for nothing in flight, frees its tensor
+ * memory and returns; the rest of the layer runs on whatever act then holds.  Unknown `what` ->
+ * MOE_ERR_INVALID_ARG.  The pages have no counterpart.
+ */
+MOE_API int moe_debug_set(int what, unsigned long long value);
+
 /* Synchronises `stream`, then reads the sticky status word of `ws`.
  * Returns MOE_OK, MOE_ERR_TIMEOUT or MOE_ERR_DEVICE_CHECK (or MOE_ERR_CUDA). */
 MOE_API int moe_get_device_status(const void* ws, void* stream);

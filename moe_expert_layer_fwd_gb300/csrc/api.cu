@@ -190,6 +190,10 @@ int moe_init_routing_range(const int32_t* topk_idx, int T, int E, int k, int e0,
                            ws_bytes, stream);
 }
 
+int moe_debug_set(int what, unsigned long long value) {
+  return moe::grouped_gemm_debug_set(what, value) == 0 ? MOE_OK : MOE_ERR_INVALID_ARG;
+}
+
 int moe_add_rms_norm_cast(const uint16_t* hidden, const uint16_t* residual, const uint16_t* norm_weight, int T,
                           int H, float eps, float* y_fp32, uint16_t* y_bf16, uint16_t* residual_out, void* stream) {
   if (T < 0 || H <= 0 || !(eps >= 0.0f)) return MOE_ERR_INVALID_ARG;

@@ -96,6 +96,7 @@ struct GemmParams {
   uint4* g_xexp;
   int g_k, g_T, g_H8;
   unsigned* g_flags;
+  int g_skip;  // failure injection (tests only): nobody gathers, so no flag is ever set
 };
 
 constexpr int kGatherRows = 16;  // rows per gather chunk (one flag each)
@@ -477,7 +478,7 @@ __global__ void __launch_bounds__(64 + 32 * (EPI + GW), 1)
     constexpr int kPerQ = EPI / 4;           // epilogue warps sharing one TMEM lane quarter
     const int half_c = (warp - 2) >> 2;      // this warp takes 32-column chunks half_c, half_c + kPerQ, ...
     const uint32_t tempty_leader = PAIR == 2 ? mapa_shared(smem_u32(&tempty[0]), 0) : 0u;
-    if (GW > 0 && p.g_flags != nullptr) {
+    if (GW > 0 && p.g_flags != nullptr && !p.g_skip) {
       // Until the first accumulator is ready the epilogue warps are idle: they gather this CTA's
       // first GW row chunks (one row per warp at a time), which the first tiles of the GPU wait for;
       // the gather warps take the CTA's later chunks.
@@ -601,7 +602,7 @@ __global__ void __launch_bounds__(64 + 32 * (EPI + GW), 1)
         else mbar_arrive(&tempty[buf]);
       }
     }
-  } else if (GW > 0 && p.g_flags != nullptr) {
+  } else if (GW > 0 && p.g_flags != nullptr && !p.g_skip) {
     // ------------------------------------------------------------ row gather
     // Chunk q (rows [16q, 16q+16)) belongs to CTA (q / GW) % gridDim.x, warp q % GW; every warp
     // walks its chunks in ascending order, so rows are gathered in the order the tiles need them
@@ -779,6 +780,18 @@ cudaError_t launch_instance(const GroupedGemmProblem& pr, GemmParams gp, cudaStr
 
 }  // namespace
 
+// Failure injection for the tests of the bounded waits (moe_debug_set): a shorter wait limit, and
+// a gate/up GEMM whose gather sets no flag, so that its producers' waits run out.
+static unsigned long long g_debug_timeout_ns = 0;
+static int g_debug_no_gather = 0;
+
+int grouped_gemm_debug_set(int what, unsigned long long value) {
+  if (what == 1) g_debug_timeout_ns = value;
+  else if (what == 2) g_debug_no_gather = value != 0;
+  else return -1;
+  return 0;
+}
+
 bool grouped_gemm_narrow(int M, int E, bool has_shared, int T_s) {
   // Decode-like problems (a few rows per expert) take the 32-column single-CTA instances with
   // a deep pipeline; prefill-like ones the 256-column CTA-pair instances.
@@ -820,7 +833,8 @@ cudaError_t launch_grouped_gemm(const GroupedGemmProblem& pr, cudaStream_t strea
   gp.topk_w = pr.topk_w;
   gp.sorted_pair = pr.sorted_pair;
   gp.status = pr.status;
-  gp.timeout_ns = kTimeoutNs;
+  gp.timeout_ns = g_debug_timeout_ns ? g_debug_timeout_ns : kTimeoutNs;
+  gp.g_skip = g_debug_no_gather;
   const bool gather = pr.mode == 0 && pr.g_x != nullptr && pr.M > 0;
   // Among the CTA-pair instances, segments averaging fewer than 256 rows do fewer than
   // 256 FLOPs per weight byte, below the GPU's ratio of tensor rate to HBM bandwidth:

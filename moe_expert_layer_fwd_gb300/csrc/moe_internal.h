@@ -56,6 +56,11 @@ struct GroupedGemmProblem {
   unsigned* g_flags;
 };
 
+// Failure injection (tests only): what 1 = wait limit of the grouped GEMMs' waits in ns (0: the
+// default 2 s), what 2 = nonzero: the gate/up GEMM's in-kernel gather writes nothing and sets no
+// flag.  Returns 0, or -1 for an unknown `what`.
+int grouped_gemm_debug_set(int what, unsigned long long value);
+
 // Whether the problem takes the 32-column (decode) instances; whether its CTA-pair instance
 // streams weights (under 256 rows per expert); whether a gate/up GEMM asked to gather its rows
 // does so inside the GEMM (else a separate gather kernel runs first).

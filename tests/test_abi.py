@@ -151,3 +151,8 @@ def test_front_end_validation_returns_before_launch(L):
     assert L.moe_router_logits(P16, P16, 4, 256, 8, P16, P16, 0, None) == moe.MOE_ERR_WORKSPACE
     assert L.moe_router_logits(None, None, 0, 256, 8, None, None, 0, None) == moe.MOE_OK
     assert L.moe_router_logits_workspace_size(64, 4096, 128) >= L.moe_status_bytes()
+
+
+def test_debug_set_validation(L):
+    assert L.moe_debug_set(3, 0) == moe.MOE_ERR_INVALID_ARG
+    assert L.moe_debug_set(1, 0) == moe.MOE_OK and L.moe_debug_set(2, 0) == moe.MOE_OK
