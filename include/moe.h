@@ -14,10 +14,16 @@
  *   moe_finalize_routing     unpermute + weighted sum (+ shared expert)
  *   moe_layer_forward        the whole path on one stream
  *
+ * and around it: moe_add_rms_norm_cast / moe_add_rms_norm_mxfp8 and
+ * moe_router_logits (the step before gating), moe_init_routing_range (routing
+ * restricted to a local expert range), moe_prepack_w13 (one-time weight layout).
+ *
  * Sources (page titles and sections):
  *  [Q3]  "Qwen3-MoE low-latency inference practice on Atlas A3/950 clusters"
  *        (cann-recipes-infer), sections "MoE TP optimisation: computation
  *        decomposition" and "GMM enablement and routing optimisation".
+ *        Also its W4A8 / EP sections (MXFP8 quantisation, expert-range routing)
+ *        and "fused RMSNorm + Cast".
  *  [HY3] "Hy3 295B MoE end-to-end inference optimisation practice on Atlas A3"
  *        (cann-recipes-infer), sections 1.1-1.3, 5.1, 6.2, 8.1.
  *
