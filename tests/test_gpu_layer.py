@@ -61,6 +61,8 @@ SMALL = [
     mi.CONFIGS["hy3_prefill"].with_(T=1000, H=384, E=8, k=4, I=192, I_s=320, zipf_beta=0.3, n_dead=1),
     # the fused op's bias placement (inside the sigmoid), shared expert
     mi.CONFIGS["hy3_decode"].with_(T=24, H=256, E=32, k=8, I=128, I_s=128, gate="sigmoid_inner_bias", bias_std=0.5),
+    # the documented limits: E = 1024 experts, k = 32
+    mi.CONFIGS["tiny"].with_(T=64, H=256, E=1024, k=32, I=128),
 ]
 
 
