@@ -76,3 +76,50 @@ def mx_dequantize_e4m3(codes, scales, block: int = 32) -> np.ndarray:
     vals = e4m3_decode(codes).reshape(*shp[:-1], shp[-1] // block, block)
     x = np.exp2(np.asarray(scales, np.float64) - 127.0)
     return (vals * x[..., None]).reshape(shp)
+
+
+# ---------------------------------------------------------------- MXFP4 (E2M1) weights
+# The W4A8 path's expert weights (Qwen3-MoE practice, W4A8 section: MXFP4 weights).  Same block
+# rule with the E2M1 element: blocks of 32 along the reduction dimension K, scale
+# X = 2^(floor(log2 amax) - 2) (2 = the largest E2M1 exponent), elements v / X rounded to the E2M1
+# grid {0, 0.5, 1, 1.5, 2, 3, 4, 6} (with sign) nearest-even, saturating at +-6.  Code: sign bit 3,
+# magnitude index 0..7 in bits 0-2 (E2M1: 2 exponent bits, 1 mantissa bit).  Two codes per byte,
+# element 2j in the low nibble, 2j+1 in the high nibble.
+E2M1_GRID = np.array([0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0])
+
+
+def e2m1_round_index(q) -> np.ndarray:
+    """Magnitude index (0..7) of the E2M1 value nearest |q|, ties to the even mantissa, saturating."""
+    a = np.minimum(np.abs(np.asarray(q, np.float64)), 6.0)
+    # the grid's quantum: 0.5 below 2, 1 in [2, 4), 2 in [4, 6]
+    quantum = np.where(a < 2.0, 0.5, np.where(a < 4.0, 1.0, 2.0))
+    r = np.rint(a / quantum) * quantum                       # halves to even multiples of the quantum
+    r = np.minimum(r, 6.0)
+    return np.searchsorted(E2M1_GRID, r).astype(np.int64)
+
+
+def mx_quantize_e2m1(w, block: int = 32):
+    """w [R, K] (K a multiple of 32) -> (codes uint8 [R, K/2], scales uint8 [R, K/32])."""
+    w = np.asarray(w, np.float64)
+    R, K = w.shape
+    b = w.reshape(R, K // block, block)
+    amax = np.abs(b).max(axis=-1)
+    fl = np.floor(np.log2(np.where(amax > 0, amax, 1.0)))
+    shared = np.where(amax > 0, np.clip(fl - 2.0, -127.0, 127.0), -127.0)
+    q = b / np.exp2(shared)[..., None]
+    idx = e2m1_round_index(q)
+    sign = (np.signbit(q) & (idx > 0)).astype(np.int64)
+    code = (sign << 3 | idx).reshape(R, K)
+    packed = (code[:, 0::2] | (code[:, 1::2] << 4)).astype(np.uint8)
+    return packed, (shared + 127.0).astype(np.uint8)
+
+
+def mx_dequantize_e2m1(codes, scales, block: int = 32) -> np.ndarray:
+    codes = np.asarray(codes, np.uint8).astype(np.int64)
+    R, K2 = codes.shape
+    c = np.empty((R, 2 * K2), np.int64)
+    c[:, 0::2] = codes & 0xF
+    c[:, 1::2] = codes >> 4
+    v = np.where(c & 8, -1.0, 1.0) * E2M1_GRID[c & 7]
+    x = np.exp2(np.asarray(scales, np.float64) - 127.0).repeat(block, axis=1)
+    return v * x

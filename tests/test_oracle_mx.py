@@ -64,3 +64,43 @@ def test_dequantisation_error_bound(seed):
     ok = q <= 448
     bound = 0.5 * np.exp2(np.floor(np.log2(np.maximum(q, 2.0 ** -6))) - 3.0) * x
     assert (np.abs(back - v)[ok] <= bound[ok] * (1 + 1e-12)).all()
+
+
+# ---------------------------------------------------------------- MXFP4 (E2M1) weights
+from oracle.mx import E2M1_GRID, e2m1_round_index, mx_dequantize_e2m1, mx_quantize_e2m1  # noqa: E402
+
+
+def test_e2m1_grid_closed_forms():
+    cases = {0.0: 0.0, 0.2: 0.0, 0.25: 0.0, 0.26: 0.5, 0.75: 1.0, 1.25: 1.0, 1.75: 2.0, 2.5: 2.0, 3.5: 4.0,
+             5.0: 4.0, 5.1: 6.0, 7.0: 6.0, 100.0: 6.0, -1.3: -1.5, -0.74: -0.5}
+    for v, ref in cases.items():
+        got = np.sign(v) * E2M1_GRID[e2m1_round_index(np.float64(v))]
+        assert got == ref, v
+
+
+def test_e2m1_blocks_and_packing():
+    w = np.zeros((2, 64))
+    w[0, 0], w[0, 1], w[0, 2] = 6.0, -0.5, 1.0    # amax 6 -> floor(log2 6) = 2 -> shared 0 -> scale byte 127
+    w[0, 33] = 0.75                               # second block: amax 0.75 -> floor -1 -> shared -3
+    w[1, 5] = 3.0 * 2.0 ** -10                    # amax 3*2^-10 -> floor -9 -> shared -11: 3.0 exactly
+    codes, scales = mx_quantize_e2m1(w)
+    assert scales.tolist() == [[127, 124], [116, 0]]
+    assert codes[0, 0] == (7 | (8 | 1) << 4)      # 6.0 (idx 7) low nibble, -0.5 (sign, idx 1) high nibble
+    assert codes[0, 1] & 0xF == 2                 # 1.0 -> idx 2
+    assert (codes[0, 16] >> 4) == 7               # element 33: 0.75 / 2^-3 = 6.0 -> idx 7, high nibble
+    back = mx_dequantize_e2m1(codes, scales)
+    np.testing.assert_array_equal(back, w)
+
+
+@pytest.mark.parametrize("seed", range(3))
+def test_e2m1_error_bound(seed):
+    rng = np.random.default_rng(seed)
+    w = rng.normal(0, 0.02, size=(32, 256))
+    codes, scales = mx_quantize_e2m1(w)
+    back = mx_dequantize_e2m1(codes, scales)
+    x = np.exp2(scales.astype(np.float64) - 127.0).repeat(32, axis=1)
+    q = np.abs(w) / x
+    half = np.where(q < 2, 0.25, np.where(q < 4, 0.5, 1.0)) * x
+    ok = q <= 6
+    assert (np.abs(back - w)[ok] <= half[ok] * (1 + 1e-12)).all()
+    assert (np.abs(back[~ok]) == 6 * x[~ok]).all()
