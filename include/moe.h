@@ -16,7 +16,9 @@
  *
  * and around it: moe_add_rms_norm_cast / moe_add_rms_norm_mxfp8 and
  * moe_router_logits (the step before gating), moe_init_routing_range (routing
- * restricted to a local expert range), moe_prepack_w13 (one-time weight layout).
+ * restricted to a local expert range), moe_prepack_w13 (one-time weight layout),
+ * and the 4-bit-weight decode GEMMs (moe_mxfp4_quantize, moe_mxfp4_prepack,
+ * moe_gather_rows_f16, moe_grouped_gemm_swiglu_mxfp4, moe_grouped_gemm_mxfp4).
  *
  * Sources (page titles and sections):
  *  [Q3]  "Qwen3-MoE low-latency inference practice on Atlas A3/950 clusters"
@@ -325,6 +327,59 @@ MOE_API int moe_grouped_gemm_swiglu(const uint16_t* x_rows, const uint16_t* w13,
 MOE_API int moe_grouped_gemm(const uint16_t* a, const uint16_t* w, const int32_t* offsets, const float* topk_w,
                      const int32_t* sorted_pair, int E, int M, int N, int K, uint16_t* out, void* ws,
                      size_t ws_bytes, void* stream);
+
+/*
+ * MXFP4 expert weights (decode): a3/a4 on 4-bit weights.  [Q3] MoE EP / W4A8
+ * section (MXFP4 expert weights read by the grouped matmuls).  Format (OCP
+ * microscaling): blocks of 32 consecutive elements along K share an E8M0 scale
+ * byte s (2^(s - 127)); each element is an E2M1 code (sign bit 3, magnitude
+ * index 0-7 of {0, 0.5, 1, 1.5, 2, 3, 4, 6} in bits 0-2), two per byte, element
+ * 2j in the low nibble of byte j.  The 4-bit GEMMs compute on f16 operands:
+ * token rows and act are f16 (saturated to +-65504), products accumulate in fp32.
+ *
+ * moe_mxfp4_quantize: w [rows,K] bf16 (K % 32 == 0) -> codes [rows,K/2] and
+ *   scales [rows,K/32]: scale 2^(floor(log2 amax) - 2) (exponent clamped to
+ *   [-127,127]; an all-zero block gets byte 0), element v / scale rounded to the
+ *   E2M1 grid nearest-even, saturating at +-6.  w finite.
+ *
+ * moe_mxfp4_prepack: one-time layout for the GEMMs.  codes/scales of [E,n_out,K]
+ *   weights (n_out % 128 == 0, K % 64 == 0) -> codes_p [E*n_out,K/2] (rows in the
+ *   packed gate/up order of moe_prepack_w13 when gate_up, else unchanged),
+ *   scales_p (E*n_out*K/32 bytes: per 128-row tile, K/32 lines of the tile's 128
+ *   rows) holding each block's exponent relative to its row, and omega
+ *   [E*n_out] fp32, the power of two the epilogue applies to the row: with
+ *   W = (largest scale exponent of the row) - 13, omega = 2^W and a block of
+ *   exponent X enters the f16 operand scaled by 2^(X - W) (exact for
+ *   X - W >= -23, i.e. blocks within 36 binades of the row's largest; blocks
+ *   below 2^-24 relative are dropped).  Scale byte 255 (NaN) unsupported.
+ *   Not in place.
+ *
+ * moe_gather_rows_f16: x_rows16[pos] = f16(x[sorted_pair[pos] / k]) for pos < M
+ *   (x [T,H] bf16, H % 64 == 0); an index outside [0,T*k) skips the row and
+ *   raises MOE_ERR_DEVICE_CHECK in ws's status word.
+ *
+ * moe_grouped_gemm_swiglu_mxfp4: as moe_grouped_gemm_swiglu with x_rows16 [M,H]
+ *   f16, the w13 weights prepacked with gate_up = 1 (n_out = 2I), and act16 [M,I]
+ *   f16 out: act = SiLU(g) * u of (g, u) = x_rows16[pos] . dequant(w13[e])^T.
+ * moe_grouped_gemm_mxfp4: as moe_grouped_gemm with a16 [M,K] f16 and the down
+ *   weights [E,N,K] prepacked with gate_up = 0 (N % 128 == 0); out [M,N] bf16.
+ * Both walk 32 token columns per tile: meant for decode (a few rows per expert);
+ * correct for any M.  ws: at least moe_grouped_gemm_workspace_size() bytes.
+ */
+MOE_API int moe_mxfp4_quantize(const uint16_t* w, long long rows, int K, uint8_t* codes, uint8_t* scales,
+                               void* stream);
+MOE_API int moe_mxfp4_prepack(const uint8_t* codes, const uint8_t* scales, int E, int n_out, int K, int gate_up,
+                              uint8_t* codes_p, uint8_t* scales_p, float* omega, void* stream);
+MOE_API int moe_gather_rows_f16(const uint16_t* x, const int32_t* sorted_pair, int T, int k, int H, int M,
+                                uint16_t* x_rows16, void* ws, size_t ws_bytes, void* stream);
+MOE_API int moe_grouped_gemm_swiglu_mxfp4(const uint16_t* x_rows16, const uint8_t* w13_codes,
+                                          const uint8_t* w13_scales, const float* w13_omega, const int32_t* offsets,
+                                          int E, int M, int H, int I, uint16_t* act16, void* ws, size_t ws_bytes,
+                                          void* stream);
+MOE_API int moe_grouped_gemm_mxfp4(const uint16_t* a16, const uint8_t* w_codes, const uint8_t* w_scales,
+                                   const float* w_omega, const int32_t* offsets, const float* topk_w,
+                                   const int32_t* sorted_pair, int E, int M, int N, int K, uint16_t* out, void* ws,
+                                   size_t ws_bytes, void* stream);
 
 /*
  * a6. Finalize-routing.  [Q3] "GMM enablement and routing optimisation"

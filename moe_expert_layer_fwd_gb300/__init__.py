@@ -16,7 +16,7 @@ from __future__ import annotations
 import ctypes
 import os
 import threading
-from typing import Optional
+from typing import NamedTuple, Optional
 
 HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(HERE, "libmoe_gb300.so")
@@ -68,6 +68,22 @@ _SIGS = {
                                                        ctypes.c_void_p, ctypes.c_int, ctypes.c_void_p,
                                                        ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
                                                        ctypes.c_void_p, ctypes.c_void_p]),
+    "moe_mxfp4_quantize": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_longlong, ctypes.c_int, ctypes.c_void_p,
+                                          ctypes.c_void_p, ctypes.c_void_p]),
+    "moe_mxfp4_prepack": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                                         ctypes.c_int, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
+                                         ctypes.c_void_p]),
+    "moe_gather_rows_f16": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                                           ctypes.c_int, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_size_t,
+                                           ctypes.c_void_p]),
+    "moe_grouped_gemm_swiglu_mxfp4": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
+                                                     ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int, ctypes.c_int,
+                                                     ctypes.c_int, ctypes.c_int, ctypes.c_void_p, ctypes.c_void_p,
+                                                     ctypes.c_size_t, ctypes.c_void_p]),
+    "moe_grouped_gemm_mxfp4": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
+                                              ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int,
+                                              ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_void_p,
+                                              ctypes.c_void_p, ctypes.c_size_t, ctypes.c_void_p]),
     "moe_debug_set": (ctypes.c_int, [ctypes.c_int, ctypes.c_ulonglong]),
     "moe_add_rms_norm_cast": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int,
                                              ctypes.c_int, ctypes.c_float, ctypes.c_void_p, ctypes.c_void_p,
@@ -327,6 +343,86 @@ def moe_grouped_gemm(a, w, offsets, topk_w=None, sorted_pair=None, out=None, ws=
     ws = _ws(lib().moe_grouped_gemm_workspace_size(), a.device, ws)
     _check(lib().moe_grouped_gemm(_ptr(a), _ptr(w), _ptr(offsets), _ptr(topk_w), _ptr(sorted_pair), E, M, N, K,
                                   _ptr(out), _ptr(ws), ws.numel(), _stream(stream)), "moe_grouped_gemm")
+    return out
+
+
+# ------------------------------------------------------------------ MXFP4 expert weights (decode)
+class Mxfp4Weights(NamedTuple):
+    """Expert weights [E, n_out, K] in the kernel layout of moe_mxfp4_prepack."""
+    codes: object    # [E*n_out, K/2] uint8
+    scales: object   # [E*n_out/128, K/32, 128] uint8
+    omega: object    # [E*n_out] float32
+    E: int
+    n_out: int
+    K: int
+
+
+def moe_mxfp4_quantize(w, stream=None):
+    """w [..., K] bf16 -> (codes uint8 [..., K/2], scales uint8 [..., K/32]), the OCP MXFP4 encoding."""
+    torch = _torch()
+    K = w.shape[-1]
+    rows = w.numel() // K if K else 0
+    codes = torch.empty((*w.shape[:-1], K // 2), dtype=torch.uint8, device=w.device)
+    scales = torch.empty((*w.shape[:-1], K // 32), dtype=torch.uint8, device=w.device)
+    _check(lib().moe_mxfp4_quantize(_ptr(w), rows, K, _ptr(codes), _ptr(scales), _stream(stream)),
+           "moe_mxfp4_quantize")
+    return codes, scales
+
+
+def moe_mxfp4_prepack(codes, scales, gate_up: bool, stream=None) -> Mxfp4Weights:
+    """codes [E,n_out,K/2], scales [E,n_out,K/32] -> the layout the 4-bit GEMMs read (gate_up: w13)."""
+    torch = _torch()
+    if codes.dim() == 2:
+        codes, scales = codes.unsqueeze(0), scales.unsqueeze(0)
+    E, n_out, K2 = codes.shape
+    K = 2 * K2
+    dev = codes.device
+    cp = torch.empty((E * n_out, K2), dtype=torch.uint8, device=dev)
+    sp = torch.empty((E * n_out // 128, K // 32, 128), dtype=torch.uint8, device=dev)
+    om = torch.empty((E * n_out,), dtype=torch.float32, device=dev)
+    _check(lib().moe_mxfp4_prepack(_ptr(codes), _ptr(scales), E, n_out, K, int(bool(gate_up)), _ptr(cp), _ptr(sp),
+                                   _ptr(om), _stream(stream)), "moe_mxfp4_prepack")
+    return Mxfp4Weights(cp, sp, om, E, n_out, K)
+
+
+def moe_gather_rows_f16(x, sorted_pair, k: int, M: Optional[int] = None, out=None, ws=None, stream=None):
+    """x_rows16[pos] = f16(x[sorted_pair[pos] // k]) for pos < M (default: all of sorted_pair)."""
+    torch = _torch()
+    T, H = x.shape
+    M = sorted_pair.numel() if M is None else M
+    if out is None:
+        out = torch.empty((M, H), dtype=torch.float16, device=x.device)
+    ws = _ws(lib().moe_grouped_gemm_workspace_size(), x.device, ws)
+    _check(lib().moe_gather_rows_f16(_ptr(x), _ptr(sorted_pair), T, k, H, M, _ptr(out), _ptr(ws), ws.numel(),
+                                     _stream(stream)), "moe_gather_rows_f16")
+    return out
+
+
+def moe_grouped_gemm_swiglu_mxfp4(x_rows16, w13: Mxfp4Weights, offsets, act=None, ws=None, stream=None):
+    """a3 on MXFP4 weights: act16[M,I] = SwiGLU(x_rows16 . dequant(w13[e])^T)."""
+    torch = _torch()
+    M, H = x_rows16.shape
+    I = w13.n_out // 2
+    if act is None:
+        act = torch.empty((M, I), dtype=torch.float16, device=x_rows16.device)
+    ws = _ws(lib().moe_grouped_gemm_workspace_size(), x_rows16.device, ws)
+    _check(lib().moe_grouped_gemm_swiglu_mxfp4(_ptr(x_rows16), _ptr(w13.codes), _ptr(w13.scales), _ptr(w13.omega),
+                                               _ptr(offsets), w13.E, M, H, I, _ptr(act), _ptr(ws), ws.numel(),
+                                               _stream(stream)), "moe_grouped_gemm_swiglu_mxfp4")
+    return act
+
+
+def moe_grouped_gemm_mxfp4(a16, w: Mxfp4Weights, offsets, topk_w=None, sorted_pair=None, out=None, ws=None,
+                           stream=None):
+    """a4 on MXFP4 weights: out[M,N] (bf16) = scale * (a16 . dequant(w[e])^T)."""
+    torch = _torch()
+    M, K = a16.shape
+    if out is None:
+        out = torch.empty((M, w.n_out), dtype=torch.bfloat16, device=a16.device)
+    ws = _ws(lib().moe_grouped_gemm_workspace_size(), a16.device, ws)
+    _check(lib().moe_grouped_gemm_mxfp4(_ptr(a16), _ptr(w.codes), _ptr(w.scales), _ptr(w.omega), _ptr(offsets),
+                                        _ptr(topk_w), _ptr(sorted_pair), w.E, M, w.n_out, K, _ptr(out), _ptr(ws),
+                                        ws.numel(), _stream(stream)), "moe_grouped_gemm_mxfp4")
     return out
 
 

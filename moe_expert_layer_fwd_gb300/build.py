@@ -20,8 +20,8 @@ ROOT = os.path.dirname(HERE)
 CSRC = os.path.join(HERE, "csrc")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libmoe_gb300.so")
-SOURCES = ["gating.cu", "routing.cu", "routing_static.cu", "grouped_gemm.cu", "finalize.cu", "frontend.cu",
-           "api.cu"]
+SOURCES = ["gating.cu", "routing.cu", "routing_static.cu", "grouped_gemm.cu", "grouped_gemm_mxfp4.cu",
+           "finalize.cu", "frontend.cu", "api.cu"]
 HEADERS = ["moe_common.cuh", "moe_internal.h"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-fvisibility=hidden",

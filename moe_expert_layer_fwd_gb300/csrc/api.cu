@@ -313,6 +313,88 @@ int moe_grouped_gemm(const uint16_t* a, const uint16_t* w, const int32_t* offset
   return cuda_status(moe::launch_grouped_gemm(p, as_stream(stream)));
 }
 
+int moe_mxfp4_quantize(const uint16_t* w, long long rows, int K, uint8_t* codes, uint8_t* scales, void* stream) {
+  if (rows < 0 || K <= 0) return MOE_ERR_INVALID_ARG;
+  if (K % 32 != 0 || rows * (long long)K >= (1LL << 40)) return MOE_ERR_UNSUPPORTED;
+  if (rows == 0) return MOE_OK;
+  if (!w || !codes || !scales || !aligned16(w) || !aligned16(codes)) return MOE_ERR_INVALID_ARG;
+  return cuda_status(moe::launch_mxfp4_quantize(w, rows, K, codes, scales, as_stream(stream)));
+}
+
+int moe_mxfp4_prepack(const uint8_t* codes, const uint8_t* scales, int E, int n_out, int K, int gate_up,
+                      uint8_t* codes_p, uint8_t* scales_p, float* omega, void* stream) {
+  if (E < 1 || n_out <= 0 || K <= 0) return MOE_ERR_INVALID_ARG;
+  if (n_out % 128 != 0 || K % 64 != 0 || (long long)E * n_out * K >= (1LL << 40)) return MOE_ERR_UNSUPPORTED;
+  if (!codes || !scales || !codes_p || !scales_p || !omega) return MOE_ERR_INVALID_ARG;
+  if (codes == codes_p || scales == scales_p) return MOE_ERR_INVALID_ARG;
+  if (!aligned16(codes) || !aligned16(codes_p) || !aligned16(scales_p) || !aligned16(omega)) return MOE_ERR_INVALID_ARG;
+  return cuda_status(
+      moe::launch_mxfp4_prepack(codes, scales, E, n_out, K, gate_up ? 1 : 0, codes_p, scales_p, omega, as_stream(stream)));
+}
+
+int moe_gather_rows_f16(const uint16_t* x, const int32_t* sorted_pair, int T, int k, int H, int M, uint16_t* x_rows16,
+                        void* ws, size_t ws_bytes, void* stream) {
+  if (T < 0 || k < 1 || M < 0 || H <= 0) return MOE_ERR_INVALID_ARG;
+  if (H % 64 != 0 || (long long)T * k >= (1LL << 31) || (long long)M * H >= (1LL << 40)) return MOE_ERR_UNSUPPORTED;
+  if (!ws || ws_bytes < kHeader || !aligned16(ws)) return MOE_ERR_WORKSPACE;
+  if (M == 0) return MOE_OK;
+  if (!x || !sorted_pair || !x_rows16 || !aligned16(x) || !aligned16(x_rows16)) return MOE_ERR_INVALID_ARG;
+  return cuda_status(
+      moe::launch_gather_rows_f16(x, sorted_pair, M, k, T, H, x_rows16, status_word(ws), as_stream(stream)));
+}
+
+namespace {
+int mxfp4_gemm(int mode, const uint16_t* a, const uint8_t* codes, const uint8_t* scales, const float* omega,
+               const int32_t* offsets, const float* topk_w, const int32_t* sorted_pair, int E, int M, int n_out,
+               int K, uint16_t* out, int ld_out, void* ws, size_t ws_bytes, void* stream) {
+  if (E < 1 || M < 0) return MOE_ERR_INVALID_ARG;
+  if (E > 1024) return MOE_ERR_UNSUPPORTED;
+  int s = check_dims(M, n_out, K);
+  if (s) return s;
+  if (n_out % 128 != 0) return MOE_ERR_UNSUPPORTED;
+  if ((topk_w == nullptr) != (sorted_pair == nullptr)) return MOE_ERR_INVALID_ARG;
+  if (!codes || !scales || !omega || !offsets || !ws) return MOE_ERR_INVALID_ARG;
+  if (ws_bytes < kHeader) return MOE_ERR_WORKSPACE;
+  if (M == 0) return MOE_OK;
+  if (!a || !out) return MOE_ERR_INVALID_ARG;
+  if (!aligned16(a) || !aligned16(codes) || !aligned16(scales) || !aligned16(omega) || !aligned16(offsets) ||
+      !aligned16(out) || !aligned16(ws) || (topk_w && (!aligned16(topk_w) || !aligned16(sorted_pair))))
+    return MOE_ERR_INVALID_ARG;
+  moe::Mxfp4GemmProblem p{};
+  p.mode = mode;
+  p.a_rows = a;
+  p.codes = codes;
+  p.scales = scales;
+  p.omega = omega;
+  p.offsets = offsets;
+  p.E = E;
+  p.M = M;
+  p.K = K;
+  p.n_out = n_out;
+  p.out = out;
+  p.ld_out = ld_out;
+  p.topk_w = topk_w;
+  p.sorted_pair = sorted_pair;
+  p.status = status_word(ws);
+  return cuda_status(moe::launch_grouped_gemm_mxfp4(p, as_stream(stream)));
+}
+}  // namespace
+
+int moe_grouped_gemm_swiglu_mxfp4(const uint16_t* x_rows16, const uint8_t* w13_codes, const uint8_t* w13_scales,
+                                  const float* w13_omega, const int32_t* offsets, int E, int M, int H, int I,
+                                  uint16_t* act16, void* ws, size_t ws_bytes, void* stream) {
+  if (I <= 0) return MOE_ERR_INVALID_ARG;
+  return mxfp4_gemm(0, x_rows16, w13_codes, w13_scales, w13_omega, offsets, nullptr, nullptr, E, M, 2 * I, H, act16,
+                    I, ws, ws_bytes, stream);
+}
+
+int moe_grouped_gemm_mxfp4(const uint16_t* a16, const uint8_t* w_codes, const uint8_t* w_scales, const float* w_omega,
+                           const int32_t* offsets, const float* topk_w, const int32_t* sorted_pair, int E, int M,
+                           int N, int K, uint16_t* out, void* ws, size_t ws_bytes, void* stream) {
+  return mxfp4_gemm(1, a16, w_codes, w_scales, w_omega, offsets, topk_w, sorted_pair, E, M, N, K, out, N, ws, ws_bytes,
+                    stream);
+}
+
 int moe_finalize_routing(const uint16_t* y_perm, const int32_t* pair_pos, const uint16_t* shared, int T, int k,
                          int H, uint16_t* y, void* stream) {
   if (T < 0 || k < 1 || H <= 0) return MOE_ERR_INVALID_ARG;

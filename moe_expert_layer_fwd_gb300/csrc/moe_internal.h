@@ -86,4 +86,29 @@ cudaError_t launch_router_logits(const float* y32, const uint16_t* w_gate, int T
 cudaError_t launch_finalize(const uint16_t* y_perm, const int32_t* pair_pos, const uint16_t* shared, int T, int k,
                             int H, uint16_t* y, cudaStream_t stream, bool pdl = false);
 
+// MXFP4 expert weights (decode).  Grouped GEMMs on f16 token rows and prepacked MXFP4 weights:
+// mode 0 writes act [M, ld_out] in f16 (SwiGLU), mode 1 writes bf16 [M, ld_out] times the routing
+// weight.  n_out a multiple of 128, K of 64.
+struct Mxfp4GemmProblem {
+  int mode;
+  const uint16_t* a_rows;    // [M,K] f16 token rows in expert-sorted order
+  const uint8_t* codes;      // [E*n_out, K/2] prepacked E2M1 codes
+  const uint8_t* scales;     // prepacked scale lines (E*n_out/128 tiles x K/32 lines x 128 bytes)
+  const float* omega;        // [E*n_out] per-row 2^W_r
+  const int32_t* offsets;    // [E+1] device
+  int E, M, K, n_out;
+  uint16_t* out;
+  int ld_out;
+  const float* topk_w;       // mode 1, optional (with sorted_pair)
+  const int32_t* sorted_pair;
+  unsigned* status;
+};
+cudaError_t launch_grouped_gemm_mxfp4(const Mxfp4GemmProblem& p, cudaStream_t stream, bool pdl = false);
+cudaError_t launch_mxfp4_quantize(const uint16_t* w, long long rows, int K, uint8_t* codes, uint8_t* scales,
+                                  cudaStream_t stream);
+cudaError_t launch_mxfp4_prepack(const uint8_t* codes, const uint8_t* scales, int E, int n_out, int K, int gate_up,
+                                 uint8_t* codes_p, uint8_t* scales_p, float* omega, cudaStream_t stream);
+cudaError_t launch_gather_rows_f16(const uint16_t* x, const int32_t* sorted_pair, int M, int k, int T, int H,
+                                   uint16_t* out, unsigned* status, cudaStream_t stream, bool pdl = false);
+
 }  // namespace moe

@@ -20,7 +20,8 @@ What it computes, step by step, each function citing the passage it follows:
   the whole layer, and the routed part of the layer over a local expert range.
 * ``frontend`` -- the step before gating: fused residual add + RMSNorm + cast
   (FP32 for the gate, BF16 for the experts) and the router gate GEMM.
-* ``mx``       -- MXFP8 (E4M3 elements, E8M0 scale per 32) dynamic quantisation.
+* ``mx``       -- MXFP8 (E4M3 elements, E8M0 scale per 32) dynamic quantisation, and
+  MXFP4 (E2M1 elements) expert weights.
 
 Precision: float64 everywhere, except the expert *selection*, which is an
 integer decided by floating point and is therefore taken in float32 with the
@@ -33,14 +34,17 @@ from .gating import exp_f32_pinned, sigmoid_f32_pinned, selection_keys, gating_t
 from .routing import init_routing, init_routing_range, expand_rows
 from .ffn import swiglu, expert_ffn, grouped_gemm_swiglu, grouped_gemm, bf16_to_f64
 from .frontend import add_rms_norm_cast, round_bf16, router_logits
-from .mx import mx_dequantize_e4m3, mx_quantize_e4m3
+from .mx import (mx_dequantize_e2m1, mx_dequantize_e4m3, mx_quantize_e2m1, mx_quantize_e4m3,
+                 mxfp4_weights)
 from .layer import (finalize_routing, moe_layer_forward, moe_layer_forward_range, moe_layer_forward_tokens,
-                    shared_expert)
+                    moe_layer_forward_tokens_mxfp4, shared_expert)
 
 __all__ = [
     "exp_f32_pinned", "sigmoid_f32_pinned", "selection_keys", "gating_topk",
     "init_routing", "init_routing_range", "expand_rows",
     "swiglu", "expert_ffn", "grouped_gemm_swiglu", "grouped_gemm", "bf16_to_f64",
     "add_rms_norm_cast", "round_bf16", "router_logits", "mx_quantize_e4m3", "mx_dequantize_e4m3",
-    "finalize_routing", "moe_layer_forward", "moe_layer_forward_range", "moe_layer_forward_tokens", "shared_expert",
+    "mx_quantize_e2m1", "mx_dequantize_e2m1", "mxfp4_weights",
+    "finalize_routing", "moe_layer_forward", "moe_layer_forward_range", "moe_layer_forward_tokens",
+    "moe_layer_forward_tokens_mxfp4", "shared_expert",
 ]

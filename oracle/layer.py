@@ -17,6 +17,7 @@ import numpy as np
 
 from .ffn import _f64, expert_ffn, grouped_gemm, grouped_gemm_swiglu
 from .gating import gating_topk
+from .mx import mxfp4_weights
 from .routing import expand_rows, init_routing, init_routing_range
 
 
@@ -104,3 +105,26 @@ def moe_layer_forward_range(x, logits, k, gate, w13, w2, e0: int, e1: int, bias=
     y = finalize_routing(y_perm, pair_pos, T, k)
     return dict(topk_w=topk_w, topk_idx=topk_idx, counts=counts, offsets=offsets, sorted_pair=sorted_pair,
                 pair_pos=pair_pos, x_exp=x_exp, act=act, y_perm=y_perm, y=y)
+
+
+def moe_layer_forward_tokens_mxfp4(tokens, x, logits, k, gate, w13, w2, bias=None, routed_scaling_factor=1.0,
+                                   eps=1e-20) -> dict:
+    """The layer with MXFP4 expert weights (Qwen3-MoE practice, W4A8 section: the experts' weights
+    are MXFP4), for the listed tokens: every needed expert's w13 and w2 are quantised to MXFP4 along
+    their input dimension and decoded (``mx.mxfp4_weights``), then the layer is the bf16 layer's
+    definition on those weights.  Routing for all tokens, y for ``tokens``.
+    """
+    x = np.asarray(x)
+    tokens = np.asarray(tokens, np.int64)
+    E = np.asarray(w13).shape[0]
+    topk_w, topk_idx = gating_topk(logits, k, gate, bias, routed_scaling_factor, eps)
+    counts, offsets, sorted_pair, pair_pos = init_routing(topk_idx, E)
+    y = np.zeros((tokens.size, x.shape[1]))
+    sel_idx = topk_idx[tokens]
+    sel_w = topk_w[tokens]
+    for e in np.unique(sel_idx):
+        rr, jj = np.nonzero(sel_idx == e)
+        out = expert_ffn(x[tokens[rr]], mxfp4_weights(w13[e]), mxfp4_weights(w2[e]))
+        y[rr] += sel_w[rr, jj][:, None] * out
+    return dict(topk_w=topk_w, topk_idx=topk_idx, counts=counts, offsets=offsets,
+                sorted_pair=sorted_pair, pair_pos=pair_pos, tokens=tokens, y=y)

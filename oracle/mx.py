@@ -1,4 +1,4 @@
-"""MXFP8 (E4M3) dynamic quantisation (oracle).  Test infrastructure only.
+"""MXFP8 (E4M3) dynamic quantisation and MXFP4 (E2M1) weights (oracle).  Test infrastructure only.
 
 Source: Qwen3-MoE low-latency inference practice (Atlas A3/950), MoE EP / W4A8 section: the
 MXFP8 quantisation of the hidden state (npu_dynamic_mx_quant, giving the MXFP8 data and its
@@ -115,6 +115,7 @@ def mx_quantize_e2m1(w, block: int = 32):
 
 
 def mx_dequantize_e2m1(codes, scales, block: int = 32) -> np.ndarray:
+    """codes [R, K/2], scales [R, K/32] -> the float64 weights they encode."""
     codes = np.asarray(codes, np.uint8).astype(np.int64)
     R, K2 = codes.shape
     c = np.empty((R, 2 * K2), np.int64)
@@ -123,3 +124,14 @@ def mx_dequantize_e2m1(codes, scales, block: int = 32) -> np.ndarray:
     v = np.where(c & 8, -1.0, 1.0) * E2M1_GRID[c & 7]
     x = np.exp2(np.asarray(scales, np.float64) - 127.0).repeat(block, axis=1)
     return v * x
+
+
+def mxfp4_weights(w) -> np.ndarray:
+    """The float64 weights an MXFP4 checkpoint holds for w [..., K] (bf16 bits or floats): w quantised
+    block by block along its last axis and decoded again."""
+    w = np.asarray(w)
+    if w.dtype == np.uint16:
+        w = (w.astype(np.uint32) << 16).view(np.float32)
+    K = w.shape[-1]
+    codes, scales = mx_quantize_e2m1(np.asarray(w, np.float64).reshape(-1, K))
+    return mx_dequantize_e2m1(codes, scales).reshape(w.shape)

@@ -156,3 +156,23 @@ def test_front_end_validation_returns_before_launch(L):
 def test_debug_set_validation(L):
     assert L.moe_debug_set(3, 0) == moe.MOE_ERR_INVALID_ARG
     assert L.moe_debug_set(1, 0) == moe.MOE_OK and L.moe_debug_set(2, 0) == moe.MOE_OK
+
+
+def test_mxfp4_validation_returns_before_launch(L):
+    P16 = 1 << 20
+    E = moe.MOE_ERR_INVALID_ARG
+    U = moe.MOE_ERR_UNSUPPORTED
+    assert L.moe_mxfp4_quantize(P16, 4, 48, P16, P16, None) == U            # K % 32
+    assert L.moe_mxfp4_quantize(P16, -1, 64, P16, P16, None) == E
+    assert L.moe_mxfp4_quantize(P16 + 4, 4, 64, P16, P16, None) == E        # misaligned weights
+    assert L.moe_mxfp4_quantize(P16, 0, 64, None, None, None) == moe.MOE_OK  # nothing to do
+    assert L.moe_mxfp4_prepack(P16, P16, 2, 192, 256, 1, P16 * 2, P16 * 3, P16 * 4, None) == U  # n_out % 128
+    assert L.moe_mxfp4_prepack(P16, P16, 2, 256, 96, 1, P16 * 2, P16 * 3, P16 * 4, None) == U   # K % 64
+    assert L.moe_mxfp4_prepack(P16, P16, 2, 256, 256, 1, P16, P16 * 3, P16 * 4, None) == E      # in place
+    assert L.moe_gather_rows_f16(P16, P16, 4, 2, 100, 8, P16, P16, 256, None) == U             # H % 64
+    assert L.moe_gather_rows_f16(P16, P16, 4, 2, 128, 8, P16, P16, 16, None) == moe.MOE_ERR_WORKSPACE
+    assert L.moe_grouped_gemm_swiglu_mxfp4(P16, P16, P16, P16, P16, 8, 32, 100, 128, P16, P16, 256, None) == U
+    assert L.moe_grouped_gemm_swiglu_mxfp4(P16, P16, P16, P16, P16, 2000, 32, 256, 128, P16, P16, 256, None) == U
+    assert L.moe_grouped_gemm_mxfp4(P16, P16, P16, P16, P16, P16, None, 8, 32, 256, 128, P16, P16, 256, None) == E
+    assert L.moe_grouped_gemm_mxfp4(P16, P16, P16, P16, P16, None, None, 8, 32, 192, 128, P16, P16, 256, None) == U
+    assert L.moe_grouped_gemm_mxfp4(P16, P16, P16, None, P16, None, None, 8, 32, 256, 128, P16, P16, 256, None) == E

@@ -67,6 +67,7 @@ def test_dequantisation_error_bound(seed):
 
 
 # ---------------------------------------------------------------- MXFP4 (E2M1) weights
+import oracle  # noqa: E402
 from oracle.mx import E2M1_GRID, e2m1_round_index, mx_dequantize_e2m1, mx_quantize_e2m1  # noqa: E402
 
 
@@ -104,3 +105,54 @@ def test_e2m1_error_bound(seed):
     ok = q <= 6
     assert (np.abs(back - w)[ok] <= half[ok] * (1 + 1e-12)).all()
     assert (np.abs(back[~ok]) == 6 * x[~ok]).all()
+
+
+def _representable_mxfp4(rng, shape):
+    """Weights that MXFP4 holds exactly: E2M1 grid values times a power of two per block of 32,
+    each block's largest magnitude being 4 or 6 times its scale (so the scale rule picks it)."""
+    R, K = shape
+    v = rng.choice(E2M1_GRID, size=(R, K)) * rng.choice([-1.0, 1.0], size=(R, K))
+    v = v.reshape(R, K // 32, 32)
+    v[:, :, 0] = rng.choice([4.0, 6.0, -4.0, -6.0], size=(R, K // 32))
+    X = rng.integers(-12, -3, size=(R, K // 32, 1)).astype(np.float64)
+    return (v * np.exp2(X)).reshape(R, K)
+
+
+def test_mxfp4_weights_identity_on_representable():
+    rng = np.random.default_rng(5)
+    w = _representable_mxfp4(rng, (24, 128))
+    np.testing.assert_array_equal(oracle.mxfp4_weights(w), w)
+    np.testing.assert_array_equal(oracle.mxfp4_weights(w.reshape(2, 12, 128)), w.reshape(2, 12, 128))
+
+
+def _layer_inputs(seed, T=6, H=64, E=4, k=2, I=32):
+    rng = np.random.default_rng(seed)
+    x = rng.normal(size=(T, H))
+    logits = rng.normal(size=(T, E)).astype(np.float32)
+    w13 = rng.normal(0, 0.05, size=(E, 2 * I, H))
+    w2 = rng.normal(0, 0.05, size=(E, H, I))
+    return rng, x, logits, w13, w2, k
+
+
+def test_mxfp4_layer_is_the_layer_on_decoded_weights():
+    rng, x, logits, w13, w2, k = _layer_inputs(1)
+    E, twoI, H = w13.shape
+    toks = np.arange(x.shape[0])
+    # representable weights: the 4-bit layer is the bf16 layer's definition exactly
+    w13r = _representable_mxfp4(rng, (E * twoI, H)).reshape(w13.shape)
+    w2r = _representable_mxfp4(rng, (E * H, w2.shape[2])).reshape(w2.shape)
+    a = oracle.moe_layer_forward_tokens_mxfp4(toks, x, logits, k, "softmax", w13r, w2r)
+    b = oracle.moe_layer_forward_tokens(toks, x, logits, k, "softmax", w13r, w2r)
+    np.testing.assert_allclose(a["y"], b["y"], rtol=1e-13, atol=1e-15)
+    # each of the two weights goes through the quantiser: w2 alone, then w13 alone
+    a = oracle.moe_layer_forward_tokens_mxfp4(toks, x, logits, k, "softmax", w13r, w2)
+    b = oracle.moe_layer_forward_tokens(toks, x, logits, k, "softmax", w13r, oracle.mxfp4_weights(w2))
+    np.testing.assert_allclose(a["y"], b["y"], rtol=1e-12, atol=1e-14)
+    a = oracle.moe_layer_forward_tokens_mxfp4(toks, x, logits, k, "softmax", w13, w2r)
+    b = oracle.moe_layer_forward_tokens(toks, x, logits, k, "softmax", oracle.mxfp4_weights(w13), w2r)
+    np.testing.assert_allclose(a["y"], b["y"], rtol=1e-12, atol=1e-14)
+    # and on general weights it is not the bf16 layer (4-bit weights round visibly)
+    a = oracle.moe_layer_forward_tokens_mxfp4(toks, x, logits, k, "softmax", w13, w2)
+    b = oracle.moe_layer_forward_tokens(toks, x, logits, k, "softmax", w13, w2)
+    rel = np.abs(a["y"] - b["y"]).max() / np.abs(b["y"]).max()
+    assert 1e-3 < rel < 0.5
