@@ -8,9 +8,12 @@
 //
 // Decode streams every active expert's weights once per step (HBM-bound), so 4-bit weights move
 // about a quarter of the bf16 bytes.  The product stays on the f16 tensor-core path
-// (tcgen05.mma kind::f16, fp32 accumulators in TMEM): dequantising warps turn each 128-row x 64-K
-// block of codes into f16 in shared memory, in the 128-byte swizzled K-major layout the MMA
-// reads, while TMA streams the next codes.  The dequantisation is exact: an E2M1 value times a
+// (tcgen05.mma kind::f16, fp32 accumulators in TMEM) with the weight operand A in TMEM:
+// dequantising warps turn each 128-row x 64-K block of codes into f16 and store it straight into
+// tensor memory (tcgen05.st, thread = weight row = TMEM lane), while TMA streams the next codes.
+// Staging the f16 weights in shared memory instead would move 8 bytes through it (a write and the
+// MMA's read) per code byte, more than shared memory delivers at HBM rate; with A in TMEM shared
+// memory only carries the codes and the token rows.  The dequantisation is exact: an E2M1 value times a
 // power of two is an f16 value while the power stays in f16's range, so every weight row r carries
 // an exponent offset W_r = (largest scale exponent of the row) - 13, applied in fp32 by the
 // epilogue, and a block with scale 2^X enters the f16 operand as e2m1 * 2^(X - W_r), at most
@@ -22,12 +25,14 @@
 // columns; f-major inside an expert, like the bf16 decode instances):
 //   warp 0      TMA: codes (128 rows x 256 K = 16 KB, 128-byte swizzle) and their scales (1 KB)
 //               into a RAW-deep ring;
-//   warp 1      TMEM allocation + the single MMA-issuing thread (M = 128, N = 16 or 32);
-//   warp 2      TMA: each operand stage's token rows (32 rows x 64 K f16, 128-byte swizzle);
-//   warps 3-10  dequantisation: thread (row r, half b) converts 32 codes of row r per operand
-//               stage (cvt e2m1x2 -> f16x2, times the block's f16 multiplier), stores four 16-byte
-//               chunks at their swizzled places, fences them for the async proxy; one arrival per
-//               warp on the stage's barrier;
+//   warp 1      TMEM allocation + the single MMA-issuing thread (M = 128, N = 16 or 32, A from
+//               TMEM, B from shared memory);
+//   warp 2      TMA: the token rows of each raw stage (32 rows x 256 K f16 as four 64-K boxes,
+//               128-byte swizzle) into an RB-deep ring, released when the stage's MMAs are done;
+//   warps 3-10  dequantisation, two groups of four warps taking alternate operand stages (two
+//               stages in flight); in a group, warp w covers TMEM lane quarter w % 4 and thread =
+//               weight row: 64 codes (cvt e2m1x2 -> f16x2, times the block's f16 multiplier) ->
+//               32 TMEM columns (tcgen05.st), then wait::st, fence, one arrival per warp;
 //   warps 11-14 epilogue: tcgen05.ld 32 lanes x 32 columns, times 2^W_r, then SwiGLU (mode 0,
 //               act in f16) or times the routing weight (mode 1, bf16 out).
 // Every wait is bounded (2 s): on expiry the CTA raises its abort flag, records DEV_ERR_TIMEOUT,
@@ -44,33 +49,38 @@ namespace {
 
 constexpr int kBM = 128;                       // weight rows per tile (UMMA M)
 constexpr int kNT = 32;                        // token columns per tile (UMMA N <= 32)
-constexpr int kAK = 64;                        // K per operand stage: one 128-byte row of f16
+constexpr int kAK = 128;                       // K per operand stage (8 MMAs of K = 16 between two waits)
+constexpr int kBK = 64;                        // K per token-row TMA box: one 128-byte row of f16
 constexpr int kRawK = 256;                     // K per raw stage: one 128-byte row of codes
 constexpr int kPerRaw = kRawK / kAK;           // operand stages per raw stage
 constexpr int kCodeBytes = kBM * kRawK / 2;    // 16 KB
 constexpr int kScaleBytes = (kRawK / 32) * kBM;  // 1 KB: 8 scale lines of 128 rows
-constexpr int kABytes = kBM * kAK * 2;         // 16 KB f16 weight operand
-constexpr int kBBytes = kNT * kAK * 2;         // 4 KB f16 token operand
-constexpr int kDQ = 8;                         // dequantising warps
+constexpr int kBBox = kNT * kBK * 2;           // 4 KB: 32 token rows x 64 K f16 (one swizzled TMA box)
+constexpr int kBBytes = (kRawK / kBK) * kBBox; // 16 KB: token rows of one raw stage (256 K)
+constexpr int kACols = kAK / 2;                // TMEM columns of one f16 weight operand stage
+constexpr int kDQ = 8;                         // dequantising warps: two groups of four
+constexpr int kDQG = 4;                        // warps per group (one per TMEM lane quarter)
 constexpr int kEPI = 4;                        // epilogue warps
 constexpr int kThreads = 32 * (3 + kDQ + kEPI);
 constexpr int kMaxDynSmem = 232448;
 constexpr unsigned long long kTimeoutNs = 2000000000ull;
-static_assert(kDQ * 32 == 2 * kBM, "one dequantising thread per (row, 32-K half) of an operand stage");
+static_assert(kDQG * 32 == kBM, "one dequantising thread per weight row in a group");
 
-template <int RAW, int OPS>
+template <int RAW, int RB, int OPS>
 struct W4Layout {
   static constexpr int kCodeOff = 0;
-  static constexpr int kAOff = RAW * kCodeBytes;
-  static constexpr int kBOff = kAOff + OPS * kABytes;
-  static constexpr int kScaleOff = kBOff + OPS * kBBytes;
+  static constexpr int kBOff = RAW * kCodeBytes;
+  static constexpr int kScaleOff = kBOff + RB * kBBytes;
   static constexpr int kBarOff = kScaleOff + RAW * kScaleBytes;
-  // full_r, empty_r (RAW each), full_a, full_b, empty_o (OPS each), tfull[2], tempty[2], done
-  static constexpr int kNumBars = 2 * RAW + 3 * OPS + 5;
+  // full_r, empty_r (RAW each), full_b, empty_b (RB each), full_a, empty_o (OPS each), tfull[2], tempty[2], done
+  static constexpr int kNumBars = 2 * RAW + 2 * RB + 2 * OPS + 5;
   static constexpr int kMiscOff = kBarOff + kNumBars * 8;
   static constexpr int kRowScaleOff = kMiscOff + 16;  // mode 1: routing weight per token column, per epilogue warp
   static constexpr int kTabOff = kRowScaleOff + kEPI * kNT * 4;
-  static constexpr uint32_t kTmemCols = 64;          // two 32-column accumulators
+  static constexpr int kACol0 = 2 * kNT;             // TMEM: two 32-column accumulators, then OPS A stages
+  static constexpr int kColsNeeded = kACol0 + OPS * kACols;
+  static constexpr uint32_t kTmemCols = kColsNeeded <= 128 ? 128 : (kColsNeeded <= 256 ? 256 : 512);
+  static_assert(kColsNeeded <= 512, "TMEM");
   static_assert(1024 + kTabOff + 2 * 1025 * 4 <= kMaxDynSmem, "shared memory");
   static size_t bytes(int E) { return 1024 + kTabOff + 2 * (size_t)(E + 1) * 4; }
 };
@@ -122,6 +132,33 @@ __device__ __forceinline__ uint32_t umma_idesc_f16(int M, int N) {
   return d;
 }
 
+// 32 lanes x 32 bits, 32 consecutive columns (thread = lane).
+__device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], "
+      "{%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,"
+      "%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};" ::"r"(taddr),
+      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]),
+      "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15]), "r"(r[16]),
+      "r"(r[17]), "r"(r[18]), "r"(r[19]), "r"(r[20]), "r"(r[21]), "r"(r[22]), "r"(r[23]), "r"(r[24]),
+      "r"(r[25]), "r"(r[26]), "r"(r[27]), "r"(r[28]), "r"(r[29]), "r"(r[30]), "r"(r[31])
+      : "memory");
+}
+
+__device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
+
+// D[tmem] (+)= A[tmem] . B[smem]^T, kind::f16: A is M x 16 in tensor memory (lane = row, column c
+// holding the f16 pair of K elements 2c, 2c + 1), B a shared-memory descriptor.
+__device__ __forceinline__ void umma_f16_tmem_a(uint32_t tmem_d, uint32_t tmem_a, uint64_t bdesc, uint32_t idesc,
+                                                uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(tmem_d),
+      "r"(tmem_a), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
 // Two E2M1 codes (bits 0-3 and 4-7 of v) -> f16x2 (the low nibble in the low half).
 __device__ __forceinline__ uint32_t e2m1x2_to_f16x2(uint32_t v) {
   uint32_t d;
@@ -150,10 +187,6 @@ __device__ __forceinline__ uint32_t pack_f16x2_sat(float lo, float hi) {
   return d;
 }
 
-__device__ __forceinline__ void fence_proxy_async_shared() {
-  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-}
-
 // All lanes wait (each lane's wait acquires the phase); false on any lane's timeout or abort.
 __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
                                           const W4Params& p) {
@@ -180,18 +213,19 @@ __device__ __forceinline__ void store_pairs16_w4(const float* v, int lane, uint1
   }
 }
 
-template <int RAW, int OPS, int MODE>
+template <int RAW, int RB, int OPS, int MODE>
 __global__ void __launch_bounds__(kThreads, 1)
     grouped_gemm_mxfp4_kernel(const __grid_constant__ CUtensorMap tmCodes, const __grid_constant__ CUtensorMap tmScales,
                               const __grid_constant__ CUtensorMap tmB, const W4Params p) {
-  using L = W4Layout<RAW, OPS>;
+  using L = W4Layout<RAW, RB, OPS>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint64_t* full_r = reinterpret_cast<uint64_t*>(smem + L::kBarOff);
   uint64_t* empty_r = full_r + RAW;
-  uint64_t* full_a = empty_r + RAW;
-  uint64_t* full_b = full_a + OPS;
-  uint64_t* empty_o = full_b + OPS;
+  uint64_t* full_b = empty_r + RAW;
+  uint64_t* empty_b = full_b + RB;
+  uint64_t* full_a = empty_b + RB;
+  uint64_t* empty_o = full_a + OPS;
   uint64_t* tfull = empty_o + OPS;
   uint64_t* tempty = tfull + 2;
   uint64_t* done = tempty + 2;
@@ -210,9 +244,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&full_r[s], 1);
       mbar_init(&empty_r[s], kDQ);
     }
-    for (int s = 0; s < OPS; ++s) {
-      mbar_init(&full_a[s], kDQ);
+    for (int s = 0; s < RB; ++s) {
       mbar_init(&full_b[s], 1);
+      mbar_init(&empty_b[s], 1);
+    }
+    for (int s = 0; s < OPS; ++s) {
+      mbar_init(&full_a[s], kDQG);
       mbar_init(&empty_o[s], 1);
     }
     for (int b = 0; b < 2; ++b) {
@@ -269,7 +306,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t tmem_base = *tmem_slot;
 
   const int total = *cfg_bad ? 0 : s_tt[E] * p.n_ftiles;
-  const int KA = p.K / kAK;                      // operand stages per tile
+  const int KA = (p.K + kAK - 1) / kAK;          // operand stages per tile (K is a multiple of 64: the
+                                                 // last one may hold 64)
   const int KR = (KA + kPerRaw - 1) / kPerRaw;   // raw stages per tile
   const int lines_per_tile = p.K / 32;           // scale lines of one 128-row weight tile
 
@@ -313,11 +351,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
-      int stage = 0;
-      uint32_t phase = 0;
+      int stage = 0, bst = 0;
+      uint32_t phase = 0, bph = 0;
       bool ok = true;
       int it = 0;
-      const uint64_t adesc0 = umma_desc_sw128(smem_u32(smem + L::kAOff));
       const uint64_t bdesc0 = umma_desc_sw128(smem_u32(smem + L::kBOff));
       for (int tile = blockIdx.x; ok && tile < total; tile += gridDim.x, ++it) {
         const W4Tile t = w4_tile(tile, s_off, s_tt, p);
@@ -328,22 +365,34 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t d = tmem_base + (uint32_t)(buf * kNT);
         const uint32_t idesc = umma_idesc_f16(kBM, (t.rows + 15) & ~15);
         for (int ka = 0; ka < KA; ++ka) {
-          if (!mbar_wait_bounded(&full_b[stage], phase, abort_flag, p.timeout_ns, p.status) ||
+          const int j = ka % kPerRaw;
+          if ((j == 0 && !mbar_wait_bounded(&full_b[bst], bph, abort_flag, p.timeout_ns, p.status)) ||
               !mbar_wait_bounded(&full_a[stage], phase, abort_flag, p.timeout_ns, p.status)) {
             ok = false;
             break;
           }
           tc_fence_after();
-          const uint64_t ad = adesc0 + (uint64_t)((stage * kABytes) >> 4);
-          const uint64_t bd = bdesc0 + (uint64_t)((stage * kBBytes) >> 4);
-          // kind::f16 MMA; the f16 operand types are in the instruction descriptor
+          const uint32_t a_tm = tmem_base + (uint32_t)(L::kACol0 + stage * kACols);
+          const uint64_t bd = bdesc0 + (uint64_t)((bst * kBBytes + j * (kAK / kBK) * kBBox) >> 4);
+          const bool full_k = p.K - ka * kAK >= kAK;  // false: the tile's last stage holds 64 of K
 #pragma unroll
-          for (int kk = 0; kk < kAK / 16; ++kk)
-            umma_bf16(d, ad + (uint64_t)((kk * 32) >> 4), bd + (uint64_t)((kk * 32) >> 4), idesc, (ka | kk) != 0);
+          for (int kk = 0; kk < kAK / 16; ++kk) {
+            if (kk >= kBK / 16 && !full_k) break;
+            // K step kk: TMEM columns 8kk.., token box kk / 4, 32-byte step kk % 4 inside it
+            const uint64_t bk = bd + (uint64_t)(((kk / (kBK / 16)) * kBBox + (kk % (kBK / 16)) * 32) >> 4);
+            umma_f16_tmem_a(d, a_tm + (uint32_t)(kk * 8), bk, idesc, (ka | kk) != 0);
+          }
           umma_commit(&empty_o[stage]);
           if (++stage == OPS) {
             stage = 0;
             phase ^= 1u;
+          }
+          if (j == kPerRaw - 1 || ka == KA - 1) {
+            umma_commit(&empty_b[bst]);  // the token rows of this raw stage are no longer read
+            if (++bst == RB) {
+              bst = 0;
+              bph ^= 1u;
+            }
           }
         }
         if (!ok) break;
@@ -365,31 +414,36 @@ __global__ void __launch_bounds__(kThreads, 1)
       bool ok = true;
       for (int tile = blockIdx.x; ok && tile < total; tile += gridDim.x) {
         const W4Tile t = w4_tile(tile, s_off, s_tt, p);
-        for (int ka = 0; ka < KA; ++ka) {
-          if (!mbar_wait_bounded(&empty_o[stage], phase ^ 1u, abort_flag, p.timeout_ns, p.status)) {
+        for (int kr = 0; kr < KR; ++kr) {
+          const int nbox = min(kRawK / kBK, (p.K - kr * kRawK) / kBK);
+          if (!mbar_wait_bounded(&empty_b[stage], phase ^ 1u, abort_flag, p.timeout_ns, p.status)) {
             ok = false;
             break;
           }
-          mbar_arrive_expect_tx(&full_b[stage], kBBytes);
-          tma_load_2d(smem + L::kBOff + stage * kBBytes, &tmB, ka * kAK, t.row_base, &full_b[stage], pol);
+          mbar_arrive_expect_tx(&full_b[stage], (uint32_t)(nbox * kBBox));
+          for (int j = 0; j < nbox; ++j)
+            tma_load_2d(smem + L::kBOff + stage * kBBytes + j * kBBox, &tmB, kr * kRawK + j * kBK, t.row_base,
+                        &full_b[stage], pol);
           ++issued;
-          if (++stage == OPS) {
+          if (++stage == RB) {
             stage = 0;
             phase ^= 1u;
           }
         }
       }
-      for (int s = 0; s < OPS; ++s) {
-        const uint32_t n = issued / OPS + ((uint32_t)s < issued % OPS ? 1u : 0u);
+      for (int s = 0; s < RB; ++s) {
+        const uint32_t n = issued / RB + ((uint32_t)s < issued % RB ? 1u : 0u);
         if (n) mbar_wait_bounded(&full_b[s], (n - 1u) & 1u, abort_flag, p.timeout_ns, p.status, false);
       }
     }
     __syncwarp();
   } else if (warp < 3 + kDQ) {
     // ------------------------------------------------------------ dequantisation
-    const int tq = (warp - 3) * 32 + lane;
-    const int r = tq >> 1, b = tq & 1;  // weight row of the tile, 32-K half of the operand stage
+    const int g = (warp - 3) / kDQG;    // group: operand stages ka with ka % 2 == g
+    const int q = warp & 3;             // TMEM lane quarter
+    const int r = q * 32 + lane;        // weight row of the tile = TMEM lane
     const uint32_t sw = (uint32_t)(r & 7);
+    const uint32_t a_lane = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)L::kACol0;
     int rs = 0, os = 0;
     uint32_t rph = 0, oph = 0;
     bool ok = true;
@@ -400,31 +454,40 @@ __global__ void __launch_bounds__(kThreads, 1)
           ok = false;
           break;
         }
-        if (!warp_wait(&empty_o[os], oph ^ 1u, abort_flag, p)) {
-          ok = false;
-          break;
-        }
-        const uint8_t* codes = smem + L::kCodeOff + rs * kCodeBytes + r * 128;
-        const uint32_t chunk = (uint32_t)(2 * j + b);  // 16-byte chunk of the row's 128 code bytes
-        const uint4 cw = *reinterpret_cast<const uint4*>(codes + ((chunk ^ sw) << 4));
-        const uint32_t u = smem[L::kScaleOff + rs * kScaleBytes + chunk * kBM + r];
-        const uint32_t mult = block_multiplier_f16x2(u);
-        uint8_t* arow = smem + L::kAOff + os * kABytes + r * 128;
-        const uint32_t words[4] = {cw.x, cw.y, cw.z, cw.w};
+        if ((ka & 1) == g) {
+          if (!warp_wait(&empty_o[os], oph ^ 1u, abort_flag, p)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint8_t* codes = smem + L::kCodeOff + rs * kCodeBytes + r * 128;
+          const uint8_t* scl = smem + L::kScaleOff + rs * kScaleBytes + r;
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          const uint32_t w = words[i];
-          uint4 h;
-          h.x = mul_f16x2(e2m1x2_to_f16x2(w), mult);
-          h.y = mul_f16x2(e2m1x2_to_f16x2(w >> 8), mult);
-          h.z = mul_f16x2(e2m1x2_to_f16x2(w >> 16), mult);
-          h.w = mul_f16x2(e2m1x2_to_f16x2(w >> 24), mult);
-          *reinterpret_cast<uint4*>(arow + ((((uint32_t)(4 * b + i)) ^ sw) << 4)) = h;
+          for (int hh = 0; hh < kAK / 64; ++hh) {
+            uint32_t v[32];
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+              // 16-byte chunk of the row's 128 code bytes (32 codes, one scale block)
+              const uint32_t chunk = (uint32_t)((kAK / 32) * j + 2 * hh + h);
+              const uint4 cw = *reinterpret_cast<const uint4*>(codes + ((chunk ^ sw) << 4));
+              const uint32_t mult = block_multiplier_f16x2(scl[chunk * kBM]);
+              const uint32_t words[4] = {cw.x, cw.y, cw.z, cw.w};
+#pragma unroll
+              for (int i = 0; i < 4; ++i) {
+#pragma unroll
+                for (int by = 0; by < 4; ++by)
+                  v[16 * h + 4 * i + by] = mul_f16x2(e2m1x2_to_f16x2(words[i] >> (8 * by)), mult);
+              }
+            }
+            tmem_st32(a_lane + (uint32_t)(os * kACols + 32 * hh), v);
+          }
+          tmem_wait_st();
+          tc_fence_before();  // the MMA thread reads these columns after the barrier
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&full_a[os]);
         }
-        fence_proxy_async_shared();  // the MMA (async proxy) reads what these threads wrote
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&full_a[os]);
         if (j == kPerRaw - 1 || ka == KA - 1) {
+          __syncwarp();
           if (lane == 0) mbar_arrive(&empty_r[rs]);
           if (++rs == RAW) {
             rs = 0;
@@ -650,23 +713,23 @@ bool make_map_f16(CUtensorMap* m, const void* base, int K, long long rows) {
   if (!fn) return false;
   cuuint64_t dims[2] = {(cuuint64_t)K, (cuuint64_t)rows};
   cuuint64_t strides[1] = {(cuuint64_t)K * 2};
-  cuuint32_t box[2] = {(cuuint32_t)kAK, (cuuint32_t)kNT};
+  cuuint32_t box[2] = {(cuuint32_t)kBK, (cuuint32_t)kNT};
   cuuint32_t estr[2] = {1, 1};
   return fn(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <int RAW, int OPS, int MODE>
+template <int RAW, int RB, int OPS, int MODE>
 cudaError_t launch_w4(const Mxfp4GemmProblem& pr, const W4Params& gp, cudaStream_t stream, bool pdl) {
-  using L = W4Layout<RAW, OPS>;
+  using L = W4Layout<RAW, RB, OPS>;
   const long long wrows = (long long)pr.E * pr.n_out;
   CUtensorMap tc, ts, tb;
   if (!make_map_u8(&tc, pr.codes, pr.K / 2, wrows, kRawK / 2, kBM, true)) return cudaErrorInvalidValue;
   if (!make_map_u8(&ts, pr.scales, kBM, wrows / kBM * (pr.K / 32), kBM, kRawK / 32, false))
     return cudaErrorInvalidValue;
   if (!make_map_f16(&tb, pr.a_rows, pr.K, pr.M)) return cudaErrorInvalidValue;
-  auto kern = grouped_gemm_mxfp4_kernel<RAW, OPS, MODE>;
+  auto kern = grouped_gemm_mxfp4_kernel<RAW, RB, OPS, MODE>;
   const size_t smem = L::bytes(pr.E);
   cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (err != cudaSuccess) return err;
@@ -695,7 +758,7 @@ cudaError_t launch_grouped_gemm_mxfp4(const Mxfp4GemmProblem& pr, cudaStream_t s
   gp.sorted_pair = pr.sorted_pair;
   gp.status = pr.status;
   gp.timeout_ns = kTimeoutNs;
-  return pr.mode == 0 ? launch_w4<6, 4, 0>(pr, gp, stream, pdl) : launch_w4<6, 4, 1>(pr, gp, stream, pdl);
+  return pr.mode == 0 ? launch_w4<7, 4, 7, 0>(pr, gp, stream, pdl) : launch_w4<7, 4, 7, 1>(pr, gp, stream, pdl);
 }
 
 cudaError_t launch_mxfp4_quantize(const uint16_t* w, long long rows, int K, uint8_t* codes, uint8_t* scales,
