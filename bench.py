@@ -61,6 +61,9 @@ def _args(argv=None):
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-front-end", action="store_true", help="skip timing the front end (norm + router GEMM)")
+    ap.add_argument("--no-mxfp4", action="store_true", help="skip timing the layer on MXFP4 expert weights")
+    ap.add_argument("--profile-mxfp4", action="store_true",
+                    help="with --profile-steps: the MXFP4-weight layer loop instead (for ncu launch lists)")
     ap.add_argument("--cpu-baseline-child", action="store_true", help=argparse.SUPPRESS)
     ap.add_argument("--sample-tokens", type=int, default=8)
     ap.add_argument("--profile-steps", action="store_true",
@@ -347,6 +350,58 @@ def front_end(args, cfg, K, W, moe, mi, d16):
             "mx_bytes": T * H * 2 * 2 + H * 2 + T * H * (1 + 2) + T * H // 32}
 
 
+# ------------------------------------------------------------------ the layer on MXFP4 expert weights
+def mxfp4_leg(args, cfg, K, W, moe, inp, t, d16, peaks, peak_src, y_bf16):
+    """Times moe.Mxfp4Layer (gating, routing, f16 row gather, the two 4-bit grouped GEMMs, finalize)
+    on the workload with its expert weights quantised to MXFP4 on the GPU (one-time, not timed).
+    Reported beside the bf16 layer, not part of its value (a lower weight precision)."""
+    import torch
+    w13q = moe.moe_mxfp4_prepack(*moe.moe_mxfp4_quantize(d16(inp.w13)), gate_up=True)
+    w2q = moe.moe_mxfp4_prepack(*moe.moe_mxfp4_quantize(t["w2"]), gate_up=False)
+    torch.cuda.empty_cache()
+    layer = moe.Mxfp4Layer(cfg.T, cfg.H, cfg.E, cfg.k, cfg.I, cfg.gate, cfg.routed_scaling_factor, cfg.eps)
+    args_fw = dict(x=t["x"], logits=t["logits"], w13=w13q, w2=w2q, bias=t["bias"])
+    for _ in range(W):
+        layer.forward(**args_fw)
+    torch.cuda.synchronize()
+    s0, s1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    s0.record()
+    for _ in range(K):
+        layer.forward(**args_fw)
+    s1.record()
+    torch.cuda.synchronize()
+    ms = s0.elapsed_time(s1) / K
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(K)]
+    for i in range(K):
+        layer.forward(events=evs[i], **args_fw)
+    torch.cuda.synchronize()
+    names = ["gating_routing_gather", "gemm_w13_swiglu_mxfp4", "gemm_down_mxfp4", "finalize"]
+    kern = {n: statistics.mean(evs[i][j].elapsed_time(evs[i][j + 1]) for i in range(K)) for j, n in enumerate(names)}
+    for w_ in (layer.ws, layer.routing_ws):
+        st = moe.moe_get_device_status(w_)
+        if st != moe.MOE_OK:
+            raise SystemExit(f"MXFP4 layer device status: {moe.status_string(st)}")
+    A = int((layer.routing["counts"].cpu() > 0).sum())
+    per_w = 0.5 + 1.0 / 32  # code + scale bytes per weight
+    b1 = A * 2 * cfg.I * cfg.H * per_w + A * 2 * cfg.I * 4   # + the per-row fp32 exponent offsets
+    b2 = A * cfg.H * cfg.I * per_w + A * cfg.H * 4
+    t1 = kern["gemm_w13_swiglu_mxfp4"] * 1e-3
+    y = layer.y.float()
+    return {
+        "value": cfg.T / (ms * 1e-3), "unit": "tokens/s", "ms_per_step": ms, "kernels_ms": kern,
+        "gpu_launches": moe.Mxfp4Layer.KERNELS_PER_FORWARD * K,
+        "weights": "MXFP4 (E2M1 codes, E8M0 scale per 32 along K), quantised on the GPU from the bf16 weights; "
+                   "token rows and act in f16",
+        "roofline": {"bound": "hbm", "kernel": "gemm_w13_swiglu_mxfp4", "achieved": b1 / t1 / 1e9,
+                     "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": b1 / t1 / 1e9 / peaks["hbm_gbs"],
+                     "peak_source": f"{peak_src} (hbm_gbs)", "algorithmic_bytes_per_launch": b1,
+                     "per_unit": f"{2 * cfg.I * cfg.H} weights x {per_w} B + {2 * cfg.I} x 4 B row offsets per "
+                                 f"active expert (x {A})", "traffic": None},
+        "gemm_down_mxfp4_gbs": b2 / (kern["gemm_down_mxfp4"] * 1e-3) / 1e9,
+        "max_rel_diff_vs_bf16_layer": float((y - y_bf16).abs().max() / y_bf16.abs().max()),
+    }
+
+
 # ------------------------------------------------------------------ GB300 arm
 def run_gb300(args, rank, world, local):
     import numpy as np
@@ -380,8 +435,15 @@ def run_gb300(args, rank, world, local):
     K, W = args.steps, args.warmup
 
     if args.profile_steps:
-        for _ in range(W + K):
-            layer.forward(**t)
+        if args.profile_mxfp4:
+            w13q = moe.moe_mxfp4_prepack(*moe.moe_mxfp4_quantize(d16(inp.w13)), gate_up=True)
+            w2q = moe.moe_mxfp4_prepack(*moe.moe_mxfp4_quantize(t["w2"]), gate_up=False)
+            l4 = moe.Mxfp4Layer(cfg.T, cfg.H, cfg.E, cfg.k, cfg.I, cfg.gate, cfg.routed_scaling_factor, cfg.eps)
+            for _ in range(W + K):
+                l4.forward(t["x"], t["logits"], w13q, w2q, t["bias"])
+        else:
+            for _ in range(W + K):
+                layer.forward(**t)
         torch.cuda.synchronize()
         return
 
@@ -434,6 +496,11 @@ def run_gb300(args, rank, world, local):
                for j, n in enumerate(names)}
 
     front = None if args.no_front_end else front_end(args, cfg, K, W, moe, mi, d16)
+    peaks, src = _peaks()
+    # the 4-bit-weight layer: decode-sized routed-only workloads (the 4-bit GEMMs walk 32 token columns)
+    w4 = None
+    if not args.no_mxfp4 and cfg.n_shared == 0 and cfg.T * cfg.k <= 32 * cfg.E:
+        w4 = mxfp4_leg(args, cfg, K, W, moe, inp, t, d16, peaks, src, layer.y.float())
 
     # end to end: pinned host inputs -> device, forward, result -> pinned host, every step.  Served
     # as a pipeline: two buffer sets (inputs, layer outputs, pinned results) and three streams, so
@@ -515,7 +582,6 @@ def run_gb300(args, rank, world, local):
     if rank != 0:
         return
 
-    peaks, src = _peaks()
     work = layer_work(cfg, counts)
     ms = ms_total / K
     # dominant kernel: the gate/up grouped GEMM (2/3 of the weight bytes and FLOPs)
@@ -564,6 +630,8 @@ def run_gb300(args, rank, world, local):
     }
     if e2e:
         line["e2e"] = e2e
+    if w4:
+        line["mxfp4_weights"] = w4
     if front:
         sm_mhz = (clk or {}).get("sm_mhz") or peaks.get("sm_max_mhz", 2070.0)
         fp32_tflops = torch.cuda.get_device_properties(local).multi_processor_count * 128 * 2 * sm_mhz * 1e6 / 1e12

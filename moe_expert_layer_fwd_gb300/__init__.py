@@ -426,6 +426,58 @@ def moe_grouped_gemm_mxfp4(a16, w: Mxfp4Weights, offsets, topk_w=None, sorted_pa
     return out
 
 
+class Mxfp4Layer:
+    """The decode layer on MXFP4 expert weights, composed from the C entry points on one stream:
+    moe_gating_topk, moe_init_routing, moe_gather_rows_f16, moe_grouped_gemm_swiglu_mxfp4,
+    moe_grouped_gemm_mxfp4, moe_finalize_routing (8 kernels), into buffers allocated once here.
+    No shared expert (the 4-bit GEMMs cover the routed experts)."""
+
+    KERNELS_PER_FORWARD = 8
+
+    def __init__(self, T: int, H: int, E: int, k: int, I: int, gate: str = "softmax",
+                 routed_scaling_factor: float = 1.0, eps: float = 1e-20, device="cuda"):
+        torch = _torch()
+        self.T, self.H, self.E, self.k, self.I = T, H, E, k, I
+        self.gate, self.rsf, self.eps = gate, routed_scaling_factor, eps
+        P = T * k
+        self.topk_w = torch.empty((T, k), dtype=torch.float32, device=device)
+        self.topk_idx = torch.empty((T, k), dtype=torch.int32, device=device)
+        self.routing = dict(counts=torch.empty(E, dtype=torch.int32, device=device),
+                            offsets=torch.empty(E + 1, dtype=torch.int32, device=device),
+                            sorted_pair=torch.empty(P, dtype=torch.int32, device=device),
+                            pair_pos=torch.empty(P, dtype=torch.int32, device=device))
+        self.routing_ws = _ws(lib().moe_init_routing_workspace_size(T, E, k), device)
+        self.ws = _ws(lib().moe_grouped_gemm_workspace_size(), device)
+        self.x16 = torch.empty((P, H), dtype=torch.float16, device=device)
+        self.act16 = torch.empty((P, I), dtype=torch.float16, device=device)
+        self.y_perm = torch.empty((P, H), dtype=torch.bfloat16, device=device)
+        self.y = torch.empty((T, H), dtype=torch.bfloat16, device=device)
+
+    def forward(self, x, logits, w13: Mxfp4Weights, w2: Mxfp4Weights, bias=None, stream=None, events=None):
+        """y [T,H] bf16.  events: optional list of 5 CUDA events recorded around the steps
+        (gating + routing + gather | gate/up GEMM | down GEMM | finalize)."""
+        s = stream
+        r = self.routing
+
+        def ev(i):
+            if events is not None:
+                events[i].record(s if s is not None else _torch().cuda.current_stream())
+
+        ev(0)
+        moe_gating_topk(logits, self.k, self.gate, bias, self.rsf, self.eps, self.topk_w, self.topk_idx, stream=s)
+        moe_init_routing(self.topk_idx, self.E, ws=self.routing_ws, out=r, stream=s)
+        moe_gather_rows_f16(x, r["sorted_pair"], self.k, out=self.x16, ws=self.ws, stream=s)
+        ev(1)
+        moe_grouped_gemm_swiglu_mxfp4(self.x16, w13, r["offsets"], act=self.act16, ws=self.ws, stream=s)
+        ev(2)
+        moe_grouped_gemm_mxfp4(self.act16, w2, r["offsets"], self.topk_w, r["sorted_pair"], out=self.y_perm,
+                               ws=self.ws, stream=s)
+        ev(3)
+        moe_finalize_routing(self.y_perm, r["pair_pos"], self.T, self.k, y=self.y, stream=s)
+        ev(4)
+        return self.y
+
+
 def moe_finalize_routing(y_perm, pair_pos, T: int, k: int, shared=None, y=None, stream=None):
     """a6: y[t] = sum_j y_perm[pair_pos[t*k+j]] (+ shared[t])."""
     torch = _torch()

@@ -177,34 +177,27 @@ def test_gather_rows_f16(moe):
     np.testing.assert_array_equal(got, ref)
 
 
-# ---------------------------------------------------------------- the layer on 4-bit weights
-def mxfp4_layer(moe, cfg, x, logits, bias, w13q, w2q, stream=None):
-    """The decode layer on MXFP4 expert weights from the C entry points (bench.py's 4-bit leg)."""
-    w, idx = moe.moe_gating_topk(logits, cfg.k, cfg.gate, bias, cfg.routed_scaling_factor, cfg.eps)
-    r = moe.moe_init_routing(idx, cfg.E)
-    x16 = moe.moe_gather_rows_f16(x, r["sorted_pair"], cfg.k)
-    act = moe.moe_grouped_gemm_swiglu_mxfp4(x16, w13q, r["offsets"])
-    yp = moe.moe_grouped_gemm_mxfp4(act, w2q, r["offsets"], w, r["sorted_pair"])
-    y = moe.moe_finalize_routing(yp, r["pair_pos"], cfg.T, cfg.k)
-    return dict(topk_w=w, topk_idx=idx, y=y, **r)
-
-
+# ---------------------------------------------------------------- the layer on 4-bit weights (moe.Mxfp4Layer, as bench.py runs it)
 @pytest.mark.parametrize("name,over", [("qwen3_decode", dict(T=24, H=512, E=16, I=256)),
                                        ("tiny", dict(I=128)),
-                                       ("qwen3_decode", {})])
+                                       pytest.param("qwen3_decode", {}, marks=pytest.mark.slow)])
 def test_mxfp4_layer_parity(moe, name, over):
     cfg = mi.CONFIGS[name].with_(**over)
     inp = mi.generate(cfg)
     w13q = moe.moe_mxfp4_prepack(*moe.moe_mxfp4_quantize(dev_bf16(inp.w13)), gate_up=True)
     w2q = moe.moe_mxfp4_prepack(*moe.moe_mxfp4_quantize(dev_bf16(inp.w2)), gate_up=False)
-    got = mxfp4_layer(moe, cfg, dev_bf16(inp.x), dev(inp.logits), dev(inp.bias) if inp.bias is not None else None,
-                      w13q, w2q)
+    layer = moe.Mxfp4Layer(cfg.T, cfg.H, cfg.E, cfg.k, cfg.I, cfg.gate, cfg.routed_scaling_factor, cfg.eps)
+    y_dev = layer.forward(dev_bf16(inp.x), dev(inp.logits), w13q, w2q,
+                          dev(inp.bias) if inp.bias is not None else None)
     toks = np.arange(cfg.T) if cfg.T * cfg.E * cfg.I * cfg.H < 2 ** 31 else np.array([0, cfg.T - 1])
     ref = oracle.moe_layer_forward_tokens_mxfp4(toks, inp.x, inp.logits, cfg.k, cfg.gate, inp.w13, inp.w2, inp.bias,
                                                 cfg.routed_scaling_factor, cfg.eps)
-    assert (host(got["topk_idx"]) == ref["topk_idx"]).all()
-    assert (host(got["offsets"]) == ref["offsets"]).all()
-    assert (host(got["sorted_pair"]) == ref["sorted_pair"]).all()
-    y = host_bf16_f64(got["y"])
+    assert (host(layer.topk_idx) == ref["topk_idx"]).all()
+    assert (host(layer.routing["offsets"]) == ref["offsets"]).all()
+    assert (host(layer.routing["sorted_pair"]) == ref["sorted_pair"]).all()
+    assert (host(layer.routing["pair_pos"]) == ref["pair_pos"]).all()
+    y = host_bf16_f64(y_dev)
     assert_close(y[toks], ref["y"], f"{name} y")
-    assert _torch().isfinite(got["y"].float()).all()
+    assert _torch().isfinite(y_dev.float()).all()
+    assert moe.moe_get_device_status(layer.ws) == moe.MOE_OK
+    assert moe.moe_get_device_status(layer.routing_ws) == moe.MOE_OK
