@@ -187,7 +187,7 @@ def layer_work(cfg, counts):
     return dict(active_experts=A, gemm_w13=dict(bytes=w13_b, flops=f1), gemm_down=dict(bytes=w2_b, flops=f2))
 
 
-def _traffic(workload, kernel):
+def _traffic(workload, kernel, src_file="grouped_gemm.cu"):
     """DRAM bytes per launch from the committed ncu summary, if it matches the current kernel source."""
     p = os.path.join(ROOT, "profiles", "dram_traffic.json")
     if not os.path.exists(p):
@@ -197,7 +197,7 @@ def _traffic(workload, kernel):
     e = d.get(workload, {}).get(kernel)
     if not e:
         return None
-    src = os.path.join(ROOT, "moe_expert_layer_fwd_gb300", "csrc", "grouped_gemm.cu")
+    src = os.path.join(ROOT, "moe_expert_layer_fwd_gb300", "csrc", src_file)
     with open(src, "rb") as f:
         sha = hashlib.sha256(f.read()).hexdigest()[:16]
     return e.get("bytes_per_launch") if e.get("src_sha") == sha else None
@@ -396,7 +396,8 @@ def mxfp4_leg(args, cfg, K, W, moe, inp, t, d16, peaks, peak_src, y_bf16):
                      "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": b1 / t1 / 1e9 / peaks["hbm_gbs"],
                      "peak_source": f"{peak_src} (hbm_gbs)", "algorithmic_bytes_per_launch": b1,
                      "per_unit": f"{2 * cfg.I * cfg.H} weights x {per_w} B + {2 * cfg.I} x 4 B row offsets per "
-                                 f"active expert (x {A})", "traffic": None},
+                                 f"active expert (x {A})",
+                     "traffic": _traffic(cfg.name, "gemm_w13_swiglu_mxfp4", "grouped_gemm_mxfp4.cu")},
         "gemm_down_mxfp4_gbs": b2 / (kern["gemm_down_mxfp4"] * 1e-3) / 1e9,
         "max_rel_diff_vs_bf16_layer": float((y - y_bf16).abs().max() / y_bf16.abs().max()),
     }
