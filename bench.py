@@ -232,8 +232,8 @@ def cpu_baseline_child(args):
     print(json.dumps({"tokens": n, "seconds": dt}))
 
 
-def cpu_baseline(args):
-    cores = len(os.sched_getaffinity(0))
+def cpu_baseline(args, cores=None):
+    cores = cores or len(os.sched_getaffinity(0))
     env = dict(os.environ, OMP_NUM_THREADS=str(cores), OPENBLAS_NUM_THREADS=str(cores), MKL_NUM_THREADS=str(cores))
     for k in ("RANK", "WORLD_SIZE", "LOCAL_RANK", "MASTER_ADDR", "MASTER_PORT"):
         env.pop(k, None)
@@ -246,7 +246,8 @@ def cpu_baseline(args):
     d = json.loads(r.stdout.strip().splitlines()[-1])
     return {"value": d["tokens"] / d["seconds"], "unit": "tokens/s", "cores": cores, "kind": "oracle",
             "sample": f"{d['tokens']} tokens of the {args.workload} workload (routing of all tokens, expert FFNs of the "
-                      f"sampled tokens, float64 numpy with BLAS on {cores} threads): {d['seconds']:.2f} s"}
+                      f"sampled tokens, float64 numpy with BLAS on {cores} thread{'s' if cores > 1 else ''}): "
+                      f"{d['seconds']:.2f} s"}
 
 
 # ------------------------------------------------------------------ reference arm (the oracle)
@@ -456,6 +457,14 @@ def run_gb300(args, rank, world, local):
     clocks = Clocks(dev_id) if rank == 0 else None
     if clocks:
         clocks.start()
+    # the first (cold) call, timed on its own: tensor-map encoding, first launches, cold L2 and TLBs
+    c0, c1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    c0.record()
+    layer.forward(**t)
+    c1.record()
+    torch.cuda.synchronize()
+    cold_ms = c0.elapsed_time(c1)
     for _ in range(W):
         layer.forward(**t)
     torch.cuda.synchronize()
@@ -495,6 +504,7 @@ def run_gb300(args, rank, world, local):
     names = ["gating", "init_routing", "gemm_w13_swiglu", "gemm_down", "finalize"]
     kern_ms = {n: statistics.mean(evs[i][j].elapsed_time(evs[i][j + 1]) for i in range(K))
                for j, n in enumerate(names)}
+    step_ms = sorted(evs[i][0].elapsed_time(evs[i][5]) for i in range(K))
 
     front = None if args.no_front_end else front_end(args, cfg, K, W, moe, mi, d16)
     peaks, src = _peaks()
@@ -616,6 +626,9 @@ def run_gb300(args, rank, world, local):
         "value": world * cfg.T * K / (ms_total * 1e-3),
         "unit": "tokens/s",
         "n_gpus": world, "steps": K, "warmup": W, "ms_per_step": ms,
+        "step_ms": {"median": statistics.median(step_ms), "min": step_ms[0], "cold_first_call": cold_ms,
+                    "how": "median and minimum of the K per-call durations of the events loop; the first call "
+                           "of the process timed alone"},
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "bf16", "data": "synthetic (seeded Philox inputs, random-init weights)",
         "config": _config(cfg, world),
@@ -653,6 +666,8 @@ def run_gb300(args, rank, world, local):
         line["front_end"] = front
     if world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(args)
+        if cfg.T * cfg.k <= 32 * cfg.E:  # the small and decode configs: the oracle on one core as well
+            line["cpu_baseline_1core"] = cpu_baseline(args, cores=1)
     print(json.dumps(line), flush=True)
 
 
