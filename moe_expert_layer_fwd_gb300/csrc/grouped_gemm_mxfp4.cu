@@ -9,8 +9,9 @@
 // Decode streams every active expert's weights once per step (HBM-bound), so 4-bit weights move
 // about a quarter of the bf16 bytes.  The product stays on the f16 tensor-core path
 // (tcgen05.mma kind::f16, fp32 accumulators in TMEM) with the weight operand A in TMEM:
-// dequantising warps turn each 128-row x 64-K block of codes into f16 and store it straight into
-// tensor memory (tcgen05.st, thread = weight row = TMEM lane), while TMA streams the next codes.
+// dequantising warps turn each 128-row x 128-K operand stage of codes into f16 and store it straight
+// into tensor memory (tcgen05.st, thread = weight row = TMEM lane), while TMA streams the next codes;
+// one MMA thread issues 8 MMAs of K = 16 per stage.
 // Staging the f16 weights in shared memory instead would move 8 bytes through it (a write and the
 // MMA's read) per code byte, more than shared memory delivers at HBM rate; with A in TMEM shared
 // memory only carries the codes and the token rows.  The dequantisation is exact: an E2M1 value times a
@@ -31,8 +32,8 @@
 //               128-byte swizzle) into an RB-deep ring, released when the stage's MMAs are done;
 //   warps 3-10  dequantisation, two groups of four warps taking alternate operand stages (two
 //               stages in flight); in a group, warp w covers TMEM lane quarter w % 4 and thread =
-//               weight row: 64 codes (cvt e2m1x2 -> f16x2, times the block's f16 multiplier) ->
-//               32 TMEM columns (tcgen05.st), then wait::st, fence, one arrival per warp;
+//               weight row: 128 codes (cvt e2m1x2 -> f16x2, times the block's f16 multiplier)
+//               -> 64 TMEM columns (two tcgen05.st), then wait::st, fence, one arrival per warp;
 //   warps 11-14 epilogue: tcgen05.ld 32 lanes x 32 columns, times 2^W_r, then SwiGLU (mode 0,
 //               act in f16) or times the routing weight (mode 1, bf16 out).
 // Every wait is bounded (2 s): on expiry the CTA raises its abort flag, records DEV_ERR_TIMEOUT,
