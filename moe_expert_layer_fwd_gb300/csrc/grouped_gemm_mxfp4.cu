@@ -665,11 +665,12 @@ __global__ void __launch_bounds__(128) gather_rows_f16_kernel(const uint4* __res
   pdl_launch_dependents();
   const int pos = blockIdx.x;
   if (pos >= M) return;
-  const int t = __ldg(sorted_pair + pos) / k;
-  if ((unsigned)t >= (unsigned)T) {
+  const int sp = __ldg(sorted_pair + pos);
+  if (sp < 0 || (long long)sp >= (long long)T * k) {  // the pair index itself, before the division
     if (threadIdx.x == 0) set_status(status, DEV_ERR_BOUNDS);
     return;
   }
+  const int t = sp / k;
   for (int c = threadIdx.x; c < H8; c += blockDim.x) {
     const uint4 v = __ldg(x + (size_t)t * H8 + c);
     uint4 h;

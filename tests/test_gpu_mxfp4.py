@@ -175,6 +175,19 @@ def test_gather_rows_f16(moe):
     got = host(moe.moe_gather_rows_f16(dev_bf16(x), dev(sp), k)).astype(np.float64)
     ref = np.clip(oracle.bf16_to_f64(x)[sp // k], -65504.0, 65504.0).astype(np.float16).astype(np.float64)
     np.testing.assert_array_equal(got, ref)
+    # pair indices outside [0, T*k) (also small negative ones, which divide to token 0): row skipped, flagged
+    torch = _torch()
+    bad = sp.copy()
+    bad[3], bad[5] = -1, T * k
+    ws = torch.zeros(256, dtype=torch.uint8, device="cuda")
+    out = torch.full((T * k, H), 7.0, dtype=torch.float16, device="cuda")
+    moe.moe_gather_rows_f16(dev_bf16(x), dev(bad), k, out=out, ws=ws)
+    assert moe.moe_get_device_status(ws) == moe.MOE_ERR_DEVICE_CHECK
+    o = host(out).astype(np.float64)
+    assert (o[3] == 7.0).all() and (o[5] == 7.0).all()
+    keep = np.ones(T * k, bool)
+    keep[[3, 5]] = False
+    np.testing.assert_array_equal(o[keep], ref[keep])
 
 
 # ---------------------------------------------------------------- the layer on 4-bit weights (moe.Mxfp4Layer, as bench.py runs it)
