@@ -24,8 +24,8 @@
  *  [Q3]  "Qwen3-MoE low-latency inference practice on Atlas A3/950 clusters"
  *        (cann-recipes-infer), sections "MoE TP optimisation: computation
  *        decomposition" and "GMM enablement and routing optimisation".
- *        Also its W4A8 / EP sections (MXFP8 quantisation, expert-range routing)
- *        and "fused RMSNorm + Cast".
+ *        Also its W4A8 / EP sections (MXFP8 activation quantisation, MXFP4
+ *        expert weights, expert-range routing) and "fused RMSNorm + Cast".
  *  [HY3] "Hy3 295B MoE end-to-end inference optimisation practice on Atlas A3"
  *        (cann-recipes-infer), sections 1.1-1.3, 5.1, 6.2, 8.1.
  *

@@ -17,7 +17,8 @@ What it computes, step by step, each function citing the passage it follows:
 * ``ffn``      -- the expert FFN down(SiLU(gate(x)) * up(x)) over the
   concatenated [gate; up] weight, grouped per expert.
 * ``layer``    -- finalize-routing (unpermute, weighted sum, shared-expert add),
-  the whole layer, and the routed part of the layer over a local expert range.
+  the whole layer, the routed part of the layer over a local expert range, and the
+  layer on MXFP4 expert weights (for sampled tokens).
 * ``frontend`` -- the step before gating: fused residual add + RMSNorm + cast
   (FP32 for the gate, BF16 for the experts) and the router gate GEMM.
 * ``mx``       -- MXFP8 (E4M3 elements, E8M0 scale per 32) dynamic quantisation, and

@@ -13,6 +13,13 @@ X = 2^(floor(log2(amax)) - 8) stored as an E8M0 byte (exponent + 127, clamped to
 round-half-to-even ('rint') and saturated to +-448; an all-zero block gets scale byte 0 and zero
 codes.  E4M3 (the "fn" variant): sign, 4 exponent bits (bias 7), 3 mantissa bits, subnormals
 with exponent 0 (2^-6 * m/8), no infinities, 0x7F/0xFF not produced.
+
+MXFP4 expert weights (same section: the W4A8 path's weights are MXFP4).  Reading: the same block
+rule with the E2M1 element -- blocks of 32 along the weight's input dimension, scale
+X = 2^(floor(log2 amax) - 2) (2 being the largest E2M1 exponent), elements v / X rounded to the E2M1
+grid {0, 0.5, 1, 1.5, 2, 3, 4, 6} nearest-even and saturated at 6; a code is sign << 3 | magnitude
+index, two codes per byte with element 2j in the low nibble.  ``mxfp4_weights`` gives the float64
+weights such a checkpoint holds.
 """
 from __future__ import annotations
 
