@@ -156,3 +156,47 @@ def test_mxfp4_layer_is_the_layer_on_decoded_weights():
     b = oracle.moe_layer_forward_tokens(toks, x, logits, k, "softmax", w13, w2)
     rel = np.abs(a["y"] - b["y"]).max() / np.abs(b["y"]).max()
     assert 1e-3 < rel < 0.5
+
+
+def _nearest_e2m1_index_brute(q: float) -> int:
+    """Nearest E2M1 magnitude by searching all eight, ties to the even index (even mantissa bit),
+    anything beyond 6 -> 6."""
+    a = min(abs(q), 6.0)
+    d = [abs(a - g) for g in E2M1_GRID]
+    best = min(d)
+    cands = [i for i, x in enumerate(d) if x == best]
+    even = [i for i in cands if i % 2 == 0]
+    return even[0] if even else cands[0]
+
+
+@pytest.mark.parametrize("seed", range(4))
+def test_e2m1_rounding_brute_force(seed):
+    rng = np.random.default_rng(100 + seed)
+    # values on a fine dyadic grid (many exact ties) and plain random values, up to beyond 6
+    q = np.concatenate([np.round(rng.uniform(-7, 7, 4000) * 8) / 8, rng.uniform(-7, 7, 4000)])
+    got = e2m1_round_index(q)
+    ref = np.array([_nearest_e2m1_index_brute(float(v)) for v in q])
+    np.testing.assert_array_equal(got, ref)
+
+
+@pytest.mark.parametrize("seed", range(3))
+def test_mxfp4_scale_rule_via_frexp(seed):
+    import math
+    rng = np.random.default_rng(200 + seed)
+    w = rng.normal(0, 1, size=(16, 128)) * np.exp2(rng.integers(-30, 30, size=(16, 1)))
+    w[0, :32] = 0.0
+    codes, scales = mx_quantize_e2m1(w)
+    for r in range(16):
+        for b in range(4):
+            amax = float(np.abs(w[r, 32 * b:32 * b + 32]).max())
+            if amax == 0.0:
+                assert scales[r, b] == 0
+                continue
+            m, e = math.frexp(amax)          # amax = m * 2^e, 0.5 <= m < 1: floor(log2 amax) = e - 1
+            assert int(scales[r, b]) - 127 == max(-127, min(127, (e - 1) - 2))
+    # and every decoded element is the brute-force nearest grid point of v / scale, with v's sign
+    back = mx_dequantize_e2m1(codes, scales)
+    x = np.exp2(scales.astype(np.float64) - 127.0).repeat(32, axis=1)
+    for v, bk, s in zip(w.ravel()[:2000], back.ravel()[:2000], x.ravel()[:2000]):
+        i = _nearest_e2m1_index_brute(v / s)
+        assert bk == (np.sign(v) if i else 1.0) * E2M1_GRID[i] * s
