@@ -365,6 +365,9 @@ MOE_API int moe_grouped_gemm(const uint16_t* a, const uint16_t* w, const int32_t
  *   weights [E,N,K] prepacked with gate_up = 0 (N % 128 == 0); out [M,N] bf16.
  * Both walk 32 token columns per tile: meant for decode (a few rows per expert);
  * correct for any M.  ws: at least moe_grouped_gemm_workspace_size() bytes.
+ * Local expert range [e0, e1) (with moe_init_routing_range's offsets): pass
+ * codes_p + e0*n_out*K/2, scales_p + e0*n_out*K/32, omega + e0*n_out and E = e1 - e0
+ * (every expert owns whole 128-row tiles of the prepacked layout).
  */
 MOE_API int moe_mxfp4_quantize(const uint16_t* w, long long rows, int K, uint8_t* codes, uint8_t* scales,
                                void* stream);

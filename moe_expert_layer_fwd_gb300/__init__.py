@@ -356,6 +356,15 @@ class Mxfp4Weights(NamedTuple):
     n_out: int
     K: int
 
+    def experts(self, e0: int, e1: int) -> "Mxfp4Weights":
+        """The local experts [e0, e1) as views (no copy): the weights the 4-bit GEMMs take together
+        with the offsets of moe_init_routing_range (every expert owns whole 128-row tiles)."""
+        if not 0 <= e0 < e1 <= self.E:
+            raise ValueError(f"expert range [{e0}, {e1}) outside [0, {self.E})")
+        r0, r1 = e0 * self.n_out, e1 * self.n_out
+        return Mxfp4Weights(self.codes[r0:r1], self.scales[r0 // 128:r1 // 128], self.omega[r0:r1], e1 - e0,
+                            self.n_out, self.K)
+
 
 def moe_mxfp4_quantize(w, stream=None):
     """w [..., K] bf16 -> (codes uint8 [..., K/2], scales uint8 [..., K/32]), the OCP MXFP4 encoding."""

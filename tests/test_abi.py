@@ -176,3 +176,23 @@ def test_mxfp4_validation_returns_before_launch(L):
     assert L.moe_grouped_gemm_mxfp4(P16, P16, P16, P16, P16, P16, None, 8, 32, 256, 128, P16, P16, 256, None) == E
     assert L.moe_grouped_gemm_mxfp4(P16, P16, P16, P16, P16, None, None, 8, 32, 192, 128, P16, P16, 256, None) == U
     assert L.moe_grouped_gemm_mxfp4(P16, P16, P16, None, P16, None, None, 8, 32, 256, 128, P16, P16, 256, None) == E
+
+
+def test_mxfp4_weights_expert_slice_is_a_view_of_the_local_rows():
+    import torch
+    E, n_out, K = 5, 256, 128
+    codes = torch.arange(E * n_out * K // 2, dtype=torch.int64).to(torch.uint8).view(E * n_out, K // 2)
+    scales = torch.arange(E * n_out * K // 32, dtype=torch.int64).to(torch.uint8).view(E * n_out // 128, K // 32, 128)
+    omega = torch.arange(E * n_out, dtype=torch.float32)
+    w = moe.Mxfp4Weights(codes, scales, omega, E, n_out, K)
+    loc = w.experts(1, 3)
+    assert (loc.E, loc.n_out, loc.K) == (2, n_out, K)
+    assert loc.codes.data_ptr() == codes.data_ptr() + 1 * n_out * (K // 2)
+    assert loc.scales.data_ptr() == scales.data_ptr() + 1 * n_out * (K // 32)
+    assert loc.omega.data_ptr() == omega.data_ptr() + 1 * n_out * 4
+    assert loc.codes.is_contiguous() and loc.scales.is_contiguous() and loc.omega.is_contiguous()
+    assert torch.equal(loc.omega, omega[n_out:3 * n_out])
+    with pytest.raises(ValueError):
+        w.experts(3, 3)
+    with pytest.raises(ValueError):
+        w.experts(0, 6)
