@@ -23,6 +23,8 @@ What it computes, step by step, each function citing the passage it follows:
   (FP32 for the gate, BF16 for the experts) and the router gate GEMM.
 * ``mx``       -- MXFP8 (E4M3 elements, E8M0 scale per 32) dynamic quantisation, and
   MXFP4 (E2M1 elements) expert weights.
+* ``w4a8``     -- the W4A8 layer: MXFP8 hidden state times MXFP4 expert weights, the SwiGLU
+  output quantised to MXFP8 before the down projection.
 
 Precision: float64 everywhere, except the expert *selection*, which is an
 integer decided by floating point and is therefore taken in float32 with the
@@ -37,6 +39,7 @@ from .ffn import swiglu, expert_ffn, grouped_gemm_swiglu, grouped_gemm, bf16_to_
 from .frontend import add_rms_norm_cast, round_bf16, router_logits
 from .mx import (mx_dequantize_e2m1, mx_dequantize_e4m3, mx_quantize_e2m1, mx_quantize_e4m3,
                  mxfp4_weights)
+from .w4a8 import ffn_w4a8, moe_layer_forward_w4a8
 from .layer import (finalize_routing, moe_layer_forward, moe_layer_forward_range, moe_layer_forward_tokens,
                     moe_layer_forward_tokens_mxfp4, shared_expert)
 
@@ -47,5 +50,5 @@ __all__ = [
     "add_rms_norm_cast", "round_bf16", "router_logits", "mx_quantize_e4m3", "mx_dequantize_e4m3",
     "mx_quantize_e2m1", "mx_dequantize_e2m1", "mxfp4_weights",
     "finalize_routing", "moe_layer_forward", "moe_layer_forward_range", "moe_layer_forward_tokens",
-    "moe_layer_forward_tokens_mxfp4", "shared_expert",
+    "moe_layer_forward_tokens_mxfp4", "shared_expert", "ffn_w4a8", "moe_layer_forward_w4a8",
 ]
