@@ -297,20 +297,34 @@ MOE_API int moe_prepack_w13(const uint16_t* w13, int E, int I, int H, uint16_t* 
  * a3. Grouped gate/up GEMM with fused SwiGLU.  [Q3] "MoE TP optimisation:
  * computation decomposition" (w13 = [gate_proj; up_proj]; SwiGLU splits the
  * last axis in two halves and returns SiLU(x[0]) * x[1]) and "GMM enablement"
- * (all experts in one grouped matmul).
+ * (all experts in one grouped matmul, in the order init-routing gives).
  *
- *  x_rows  [M,H] bf16: rows in expert-sorted order (x_exp of moe_init_routing).
- *  w13     [E,2I,H] bf16 in the packed layout of moe_prepack_w13 (made from the
- *          checkpoint [out_features, in_features] rows [gate; up], [HY3] 6.2).
- *  offsets [E+1] int32 device: expert e owns rows [offsets[e], offsets[e+1]);
- *          offsets[E] <= M.
- *  act     [M,I] bf16 out: act[pos] = SiLU(g) * u, (g, u) = x_rows[pos] . w13[e]^T,
- *          accumulated in fp32, rounded once to bf16.  Rows >= offsets[E] untouched.
- *  ws      at least moe_grouped_gemm_workspace_size() bytes.
+ *  x        row_src == NULL: [M,H] bf16 rows already in expert-sorted order (x_exp of
+ *           moe_init_routing).  row_src != NULL: [T,H] bf16 token rows; row pos of the
+ *           GEMM is x[row_src[pos] / k], gathered by the call itself (pass sorted_pair of
+ *           moe_init_routing / moe_init_routing_range as row_src).
+ *  row_src  [M] int32 device or NULL; only entries pos < offsets[E] are read, each must
+ *           lie in [0, T*k): one outside is skipped (its row of act is unspecified) and
+ *           raises MOE_ERR_DEVICE_CHECK in the workspace status word.
+ *  k, T     experts per token and token rows of x; used only with row_src.
+ *  w13      [E,2I,H] bf16 in the packed layout of moe_prepack_w13 (made from the
+ *           checkpoint [out_features, in_features] rows [gate; up], [HY3] 6.2).
+ *  offsets  [E+1] int32 device: expert e owns rows [offsets[e], offsets[e+1]);
+ *           offsets[E] <= M.
+ *  act      [M,I] bf16 out: act[pos] = SiLU(g) * u, (g, u) = row(pos) . w13[e]^T,
+ *           accumulated in fp32, rounded once to bf16.  Rows >= offsets[E] untouched.
+ *  ws       at least moe_grouped_gemm_swiglu_workspace_size(M, H, row_src != NULL)
+ *           bytes: the status header, and with row_src the gathered rows (M*H*2 bytes)
+ *           and one flag per 16 of them.
+ *  The gather runs as moe_layer_forward runs it: inside the GEMM (two extra warps per
+ *  CTA, overlapping the matmuls) when the problem is compute-bound (>= 256 rows per
+ *  expert on average), else as a separate kernel before it.
  */
 MOE_API size_t moe_grouped_gemm_workspace_size(void);
-MOE_API int moe_grouped_gemm_swiglu(const uint16_t* x_rows, const uint16_t* w13, const int32_t* offsets, int E, int M,
-                            int H, int I, uint16_t* act, void* ws, size_t ws_bytes, void* stream);
+MOE_API size_t moe_grouped_gemm_swiglu_workspace_size(int M, int H, int gather);
+MOE_API int moe_grouped_gemm_swiglu(const uint16_t* x, const int32_t* row_src, int k, int T, const uint16_t* w13,
+                                    const int32_t* offsets, int E, int M, int H, int I, uint16_t* act, void* ws,
+                                    size_t ws_bytes, void* stream);
 
 /*
  * a4. Grouped GEMM (down projection) with the routing weight fused.  [Q3]

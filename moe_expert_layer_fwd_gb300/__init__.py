@@ -97,9 +97,11 @@ _SIGS = {
     "moe_prepack_w13": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_void_p,
                                        ctypes.c_void_p]),
     "moe_grouped_gemm_workspace_size": (ctypes.c_size_t, []),
-    "moe_grouped_gemm_swiglu": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int,
-                                               ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_void_p,
-                                               ctypes.c_void_p, ctypes.c_size_t, ctypes.c_void_p]),
+    "moe_grouped_gemm_swiglu_workspace_size": (ctypes.c_size_t, [ctypes.c_int, ctypes.c_int, ctypes.c_int]),
+    "moe_grouped_gemm_swiglu": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int, ctypes.c_int,
+                                               ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int, ctypes.c_int,
+                                               ctypes.c_int, ctypes.c_int, ctypes.c_void_p, ctypes.c_void_p,
+                                               ctypes.c_size_t, ctypes.c_void_p]),
     "moe_grouped_gemm": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
                                         ctypes.c_void_p, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
                                         ctypes.c_void_p, ctypes.c_void_p, ctypes.c_size_t, ctypes.c_void_p]),
@@ -319,17 +321,28 @@ def moe_prepack_w13(w13, out=None, stream=None):
     return out
 
 
-def moe_grouped_gemm_swiglu(x_rows, w13, offsets, act=None, ws=None, stream=None):
-    """a3: act[M,I] = SwiGLU(x_rows . w13[e]^T) per expert segment; w13 packed by moe_prepack_w13."""
+def moe_grouped_gemm_swiglu(x, w13, offsets, act=None, ws=None, row_src=None, k: int = 1, M: Optional[int] = None,
+                            stream=None):
+    """a3: act[M,I] = SwiGLU(row(pos) . w13[e]^T) per expert segment; w13 packed by moe_prepack_w13.
+
+    row_src None: x [M,H] holds the rows in expert-sorted order.  row_src given (sorted_pair of
+    init-routing): x [T,H] holds the token rows and row pos is x[row_src[pos] // k], gathered by the
+    call (M defaults to row_src's length)."""
     torch = _torch()
-    M, H = x_rows.shape
-    E, twoI, _ = w13.shape
+    E, twoI, H = w13.shape
     I = twoI // 2
+    if row_src is None:
+        M, T = x.shape[0], 0
+    else:
+        T = x.shape[0]
+        M = row_src.numel() if M is None else M
     if act is None:
-        act = torch.empty((M, I), dtype=torch.bfloat16, device=x_rows.device)
-    ws = _ws(lib().moe_grouped_gemm_workspace_size(), x_rows.device, ws)
-    _check(lib().moe_grouped_gemm_swiglu(_ptr(x_rows), _ptr(w13), _ptr(offsets), E, M, H, I, _ptr(act), _ptr(ws),
-                                         ws.numel(), _stream(stream)), "moe_grouped_gemm_swiglu")
+        act = torch.empty((M, I), dtype=torch.bfloat16, device=x.device)
+    gather = row_src is not None
+    ws = _ws(lib().moe_grouped_gemm_swiglu_workspace_size(M, H, int(gather)), x.device, ws)
+    _check(lib().moe_grouped_gemm_swiglu(_ptr(x), _ptr(row_src), k, T, _ptr(w13), _ptr(offsets), E, M, H, I,
+                                         _ptr(act), _ptr(ws), ws.numel(), _stream(stream)),
+           "moe_grouped_gemm_swiglu")
     return act
 
 

@@ -12,7 +12,7 @@ namespace {
 
 constexpr size_t kHeader = 256;  // status word + padding
 constexpr size_t kAlign = 256;
-constexpr int kAbiVersion = 100;
+constexpr int kAbiVersion = 200;
 
 inline size_t align_up(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
 
@@ -254,21 +254,35 @@ int moe_prepack_w13(const uint16_t* w13, int E, int I, int H, uint16_t* w13_pack
 
 size_t moe_grouped_gemm_workspace_size(void) { return kHeader; }
 
-int moe_grouped_gemm_swiglu(const uint16_t* x_rows, const uint16_t* w13, const int32_t* offsets, int E, int M,
-                            int H, int I, uint16_t* act, void* ws, size_t ws_bytes, void* stream) {
+size_t moe_grouped_gemm_swiglu_workspace_size(int M, int H, int gather) {
+  if (M < 0 || H <= 0) return 0;
+  if (!gather) return kHeader;
+  return kHeader + align_up((size_t)(M + 15) / 16 * 4) + align_up((size_t)M * H * 2);
+}
+
+int moe_grouped_gemm_swiglu(const uint16_t* x, const int32_t* row_src, int k, int T, const uint16_t* w13,
+                            const int32_t* offsets, int E, int M, int H, int I, uint16_t* act, void* ws,
+                            size_t ws_bytes, void* stream) {
   if (E < 1 || M < 0) return MOE_ERR_INVALID_ARG;
   if (E > 1024) return MOE_ERR_UNSUPPORTED;
   int s = check_dims(M, H, I);
   if (s) return s;
+  const bool gather = row_src != nullptr;
+  if (gather) {
+    if (k < 1 || T < 0) return MOE_ERR_INVALID_ARG;
+    if (k > 32 || (long long)T * k >= (1LL << 31)) return MOE_ERR_UNSUPPORTED;
+  }
   if (!w13 || !offsets || !ws) return MOE_ERR_INVALID_ARG;
-  if (ws_bytes < kHeader) return MOE_ERR_WORKSPACE;
+  if (ws_bytes < moe_grouped_gemm_swiglu_workspace_size(M, H, gather ? 1 : 0)) return MOE_ERR_WORKSPACE;
   if (M == 0) return MOE_OK;
-  if (!x_rows || !act) return MOE_ERR_INVALID_ARG;
-  if (!aligned16(x_rows) || !aligned16(w13) || !aligned16(offsets) || !aligned16(act) || !aligned16(ws))
+  if (!x || !act) return MOE_ERR_INVALID_ARG;
+  if (!aligned16(x) || !aligned16(w13) || !aligned16(offsets) || !aligned16(act) || !aligned16(ws) ||
+      (gather && !aligned16(row_src)))
     return MOE_ERR_INVALID_ARG;
+  cudaStream_t st = as_stream(stream);
   moe::GroupedGemmProblem p{};
   p.mode = 0;
-  p.a_rows = x_rows;
+  p.a_rows = x;
   p.w = w13;
   p.offsets = offsets;
   p.E = E;
@@ -278,7 +292,24 @@ int moe_grouped_gemm_swiglu(const uint16_t* x_rows, const uint16_t* w13, const i
   p.out = act;
   p.ld_out = I;
   p.status = status_word(ws);
-  return cuda_status(moe::launch_grouped_gemm(p, as_stream(stream)));
+  if (gather) {
+    // The gathered rows live in the workspace after the status header and the gather flags.
+    char* base = static_cast<char*>(ws);
+    const size_t flags_off = kHeader;
+    const size_t rows_off = kHeader + align_up((size_t)(M + 15) / 16 * 4);
+    unsigned* flags = reinterpret_cast<unsigned*>(base + flags_off);
+    p.a_rows = reinterpret_cast<const uint16_t*>(base + rows_off);
+    p.g_x = x;
+    p.g_sorted_pair = row_src;
+    p.g_k = k;
+    p.g_T = T;
+    p.g_flags = flags;
+    // the in-kernel gather publishes one flag per 16 rows: they start at zero
+    if (moe::grouped_gemm_gathers_inline(M, E, false, 0) &&
+        cudaMemsetAsync(flags, 0, (size_t)(M + 15) / 16 * 4, st) != cudaSuccess)
+      return MOE_ERR_CUDA;
+  }
+  return cuda_status(moe::launch_grouped_gemm(p, st));
 }
 
 int moe_grouped_gemm(const uint16_t* a, const uint16_t* w, const int32_t* offsets, const float* topk_w,

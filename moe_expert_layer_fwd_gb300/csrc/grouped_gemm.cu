@@ -400,16 +400,22 @@ __global__ void __launch_bounds__(64 + 32 * (EPI + GW), 1)
       }
     }
     if (PAIR == 1) {
-      // Drain: the last fill of every stage must have landed before the CTA exits.
+      // Drain: the last fill of every stage must have landed before the CTA exits.  One deadline
+      // covers all stages, so a stalled pipeline costs one wait limit, not one per stage.
       if (lane == 0) {
+        const uint64_t deadline = globaltimer_ns() + p.timeout_ns;
         for (int s = 0; s < STAGES; ++s) {
           const uint32_t n = issued / STAGES + ((uint32_t)s < issued % STAGES ? 1u : 0u);
-          if (n) mbar_wait_bounded(&full[s], (n - 1u) & 1u, abort_flag, p.timeout_ns, p.status, false);
+          const uint64_t now = globaltimer_ns();
+          if (n) mbar_wait_bounded(&full[s], (n - 1u) & 1u, abort_flag, deadline > now ? deadline - now : 0,
+                                   p.status, false);
         }
       }
-    } else if (rank == 1 && lane == 0) {
+    } else if (lane == 0) {
+      // A CTA that gave up tells its peer, whose waits would otherwise run to their own limit.
+      if (*abort_flag) st_shared_cluster_u32(mapa_shared(smem_u32((const void*)abort_flag), rank ^ 1u), 1u);
       // the follower's loads complete on the leader's barriers: tell the leader how many it issued
-      st_shared_cluster_u32(mapa_shared(smem_u32((const void*)peer_issued), 0), issued);
+      if (rank == 1) st_shared_cluster_u32(mapa_shared(smem_u32((const void*)peer_issued), 0), issued);
     }
     __syncwarp();
   } else if (warp == 1) {
@@ -484,14 +490,19 @@ __global__ void __launch_bounds__(64 + 32 * (EPI + GW), 1)
       // the gather warps take the CTA's later chunks.
       pdl_wait();  // sorted_pair comes from the previous kernel
       const int ew = warp - 2;
-      const int n_chunks = (p.M + kGatherRows - 1) / kGatherRows;
+      const int g_rows = min(p.M, s_off[E]);  // rows past offsets[E] are never read
+      const int n_chunks = (g_rows + kGatherRows - 1) / kGatherRows;
       for (int g = 0; g < GW; ++g) {
         const int q = GW * (int)blockIdx.x + g;
         if (q >= n_chunks) break;  // uniform over the epilogue warps
-        const int r0 = q * kGatherRows, nrow = min(kGatherRows, p.M - r0);
+        const int r0 = q * kGatherRows, nrow = min(kGatherRows, g_rows - r0);
         for (int i = ew; i < nrow; i += EPI) {
-          const int t = __ldg(p.g_sp + r0 + i) / p.g_k;
-          if ((unsigned)t >= (unsigned)p.g_T) continue;
+          const int sp = __ldg(p.g_sp + r0 + i);
+          const int t = sp / p.g_k;
+          if (sp < 0 || (unsigned)t >= (unsigned)p.g_T) {
+            if (lane == 0) set_status(p.status, DEV_ERR_BOUNDS);
+            continue;
+          }
           const uint4* src = p.g_x + (size_t)t * p.g_H8;
           uint4* dst = p.g_xexp + (size_t)(r0 + i) * p.g_H8;
           for (int c = lane; c < p.g_H8; c += 4 * 32) {
@@ -609,15 +620,20 @@ __global__ void __launch_bounds__(64 + 32 * (EPI + GW), 1)
     // (tiles are dealt out in expert order).  Nothing here waits on another CTA.
     pdl_wait();  // sorted_pair comes from the previous kernel
     const int gw = warp - 2 - EPI;
-    const int n_chunks = (p.M + kGatherRows - 1) / kGatherRows;
+    const int g_rows = min(p.M, s_off[E]);  // rows past offsets[E] are never read
+    const int n_chunks = (g_rows + kGatherRows - 1) / kGatherRows;
     const int H8 = p.g_H8;
     // the CTA's first GW chunks are gathered by the epilogue warps
     for (int q = GW * ((int)blockIdx.x + (int)gridDim.x) + gw; q < n_chunks; q += GW * (int)gridDim.x) {
-      const int r0 = q * kGatherRows, nrow = min(kGatherRows, p.M - r0);
+      const int r0 = q * kGatherRows, nrow = min(kGatherRows, g_rows - r0);
       int tl = -1;  // lane i < nrow: source token of row r0 + i
       if (lane < nrow) {
-        tl = __ldg(p.g_sp + r0 + lane) / p.g_k;
-        if ((unsigned)tl >= (unsigned)p.g_T) tl = -1;
+        const int sp = __ldg(p.g_sp + r0 + lane);
+        tl = sp / p.g_k;
+        if (sp < 0 || (unsigned)tl >= (unsigned)p.g_T) {
+          tl = -1;
+          set_status(p.status, DEV_ERR_BOUNDS);
+        }
       }
       for (int i = 0; i < nrow; i += 4) {
         int tr[4];
@@ -653,12 +669,16 @@ __global__ void __launch_bounds__(64 + 32 * (EPI + GW), 1)
   if (PAIR == 2) {
     cluster_sync();  // both CTAs have stopped issuing; the follower's load count has arrived
     if (rank == 0 && warp == 0 && lane == 0) {
-      // Drain: every stage's last fill, by either CTA, must have landed before either CTA exits.
+      // Drain: every stage's last fill, by either CTA, must have landed before either CTA exits
+      // (one deadline for all stages).
       const uint32_t pi = *peer_issued;
       const uint32_t n_all = issued > pi ? issued : pi;
+      const uint64_t deadline = globaltimer_ns() + p.timeout_ns;
       for (int s = 0; s < STAGES; ++s) {
         const uint32_t n = n_all / STAGES + ((uint32_t)s < n_all % STAGES ? 1u : 0u);
-        if (n) mbar_wait_bounded(&full[s], (n - 1u) & 1u, abort_flag, p.timeout_ns, p.status, false);
+        const uint64_t now = globaltimer_ns();
+        if (n) mbar_wait_bounded(&full[s], (n - 1u) & 1u, abort_flag, deadline > now ? deadline - now : 0, p.status,
+                                 false);
       }
     }
     cluster_sync();
@@ -845,8 +865,9 @@ cudaError_t launch_grouped_gemm(const GroupedGemmProblem& pr, cudaStream_t strea
   // while the GEMM runs (when asked to); the other instances have the rows gathered by a
   // separate kernel first.
   if (gather && !grouped_gemm_gathers_inline(pr.M, pr.E, has_shared, pr.T_s)) {
+    // rows past offsets[E] are never read by the GEMM: gather only the routed ones
     cudaError_t e = launch_expand_rows(pr.g_x, pr.g_sorted_pair, pr.M, pr.g_k, pr.K, const_cast<uint16_t*>(pr.a_rows),
-                                       stream, pdl);
+                                       stream, pdl, pr.offsets + pr.E, pr.g_T, pr.status);
     if (e != cudaSuccess) return e;
   }
   if (grouped_gemm_narrow(pr.M, pr.E, has_shared, pr.T_s))

@@ -24,9 +24,11 @@ cudaError_t launch_init_routing(const int32_t* topk_idx, int P, int E, int k, co
                                 bool pdl = false, unsigned* zero = nullptr, int n_zero = 0, int e0 = 0,
                                 int e1 = -1);
 // n_rows: optional device count of the rows to gather (the rest of x_exp is left alone).
+// T: token rows of x (< 0: P / k).  status: optional; a source index outside [0, T*k) skips its
+// row and sets DEV_ERR_BOUNDS there.
 cudaError_t launch_expand_rows(const uint16_t* x, const int32_t* sorted_pair, int P, int k, int H,
                                uint16_t* x_exp, cudaStream_t stream, bool pdl = false,
-                               const int32_t* n_rows = nullptr);
+                               const int32_t* n_rows = nullptr, int T = -1, unsigned* status = nullptr);
 
 // One grouped GEMM launch: routed experts (+ optionally one dense "shared" segment).
 struct GroupedGemmProblem {

@@ -208,20 +208,25 @@ constexpr int kExpandRows = 4;
 __global__ void __launch_bounds__(512) expand_rows_kernel(const uint4* __restrict__ x,
                                                           const int32_t* __restrict__ sorted_pair, int P, int k,
                                                           int T, int H8, uint4* __restrict__ x_exp,
-                                                          const int32_t* __restrict__ n_rows) {
+                                                          const int32_t* __restrict__ n_rows,
+                                                          unsigned* __restrict__ status) {
   pdl_wait();
   pdl_launch_dependents();
   if (n_rows) P = min(P, __ldg(n_rows));  // rows routed here (an expert range routes fewer than P)
   const int r0 = blockIdx.x * kExpandRows;
   const uint4* src[kExpandRows];
+  bool bad = false;
 #pragma unroll
   for (int u = 0; u < kExpandRows; ++u) {
     src[u] = nullptr;
     if (r0 + u < P) {
-      const int t = __ldg(sorted_pair + r0 + u) / k;
-      if ((unsigned)t < (unsigned)T) src[u] = x + (size_t)t * H8;
+      const int sp = __ldg(sorted_pair + r0 + u);
+      const int t = sp / k;
+      if (sp >= 0 && (unsigned)t < (unsigned)T) src[u] = x + (size_t)t * H8;
+      else bad = true;
     }
   }
+  if (bad && threadIdx.x == 0) set_status(status, DEV_ERR_BOUNDS);
   uint4* dst = x_exp + (size_t)r0 * H8;
   for (int c = threadIdx.x; c < H8; c += blockDim.x) {
     uint4 v[kExpandRows];
@@ -250,14 +255,15 @@ size_t routing_scratch_bytes(int P, int E) {
 }
 
 cudaError_t launch_expand_rows(const uint16_t* x, const int32_t* sorted_pair, int P, int k, int H,
-                               uint16_t* x_exp, cudaStream_t stream, bool pdl, const int32_t* n_rows) {
+                               uint16_t* x_exp, cudaStream_t stream, bool pdl, const int32_t* n_rows, int T,
+                               unsigned* status) {
   if (P == 0) return cudaSuccess;
-  const int T = P / k;
+  if (T < 0) T = P / k;
   const int H8 = H / 8;
   const int threads = H8 >= 512 ? 512 : (H8 + 31) / 32 * 32;
   return launch_kernel(expand_rows_kernel, dim3((unsigned)((P + kExpandRows - 1) / kExpandRows)), dim3(threads), 0,
                        stream, pdl, reinterpret_cast<const uint4*>(x), sorted_pair, P, k, T, H8,
-                       reinterpret_cast<uint4*>(x_exp), n_rows);
+                       reinterpret_cast<uint4*>(x_exp), n_rows, status);
 }
 
 cudaError_t launch_init_routing(const int32_t* topk_idx, int P, int E, int k, const uint16_t* x, int H,

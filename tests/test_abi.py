@@ -42,7 +42,7 @@ def test_every_declared_symbol_is_exported(L):
 
 
 def test_version_and_status_strings(L):
-    assert moe.lib().moe_abi_version() == 100
+    assert moe.lib().moe_abi_version() == 200
     assert moe.status_string(0) == "MOE_OK"
     assert moe.status_string(-1) == "MOE_ERR_INVALID_ARG"
     assert moe.status_string(-5) == "MOE_ERR_TIMEOUT"
@@ -99,8 +99,21 @@ def test_routing_and_gemm_validation(L):
         moe.MOE_ERR_WORKSPACE
     assert L.moe_init_routing(P16, 4, 8, 2, P16, 0, None, P16, P16, P16, P16, P16, small, None) == \
         moe.MOE_ERR_INVALID_ARG  # x without x_exp
-    assert L.moe_grouped_gemm_swiglu(P16, P16, P16, 8, 32, 100, 128, P16, P16, 256, None) == moe.MOE_ERR_UNSUPPORTED
-    assert L.moe_grouped_gemm_swiglu(P16, P16, P16, 8, 32, 256, 128, P16, P16, 255, None) == moe.MOE_ERR_WORKSPACE
+    # moe_grouped_gemm_swiglu(x, row_src, k, T, w13, offsets, E, M, H, I, act, ws, ws_bytes, stream)
+    assert L.moe_grouped_gemm_swiglu(P16, None, 1, 0, P16, P16, 8, 32, 100, 128, P16, P16, 256, None) == \
+        moe.MOE_ERR_UNSUPPORTED
+    assert L.moe_grouped_gemm_swiglu(P16, None, 1, 0, P16, P16, 8, 32, 256, 128, P16, P16, 255, None) == \
+        moe.MOE_ERR_WORKSPACE
+    # with row_src the workspace also holds the gathered rows and their flags
+    need = L.moe_grouped_gemm_swiglu_workspace_size(32, 256, 1)
+    assert need >= L.moe_status_bytes() + 32 * 256 * 2 + 8
+    assert L.moe_grouped_gemm_swiglu_workspace_size(32, 256, 0) == L.moe_status_bytes()
+    assert L.moe_grouped_gemm_swiglu(P16, P16, 8, 4, P16, P16, 8, 32, 256, 128, P16, P16, need - 1, None) == \
+        moe.MOE_ERR_WORKSPACE
+    assert L.moe_grouped_gemm_swiglu(P16, P16, 0, 4, P16, P16, 8, 32, 256, 128, P16, P16, need, None) == \
+        moe.MOE_ERR_INVALID_ARG  # k < 1
+    assert L.moe_grouped_gemm_swiglu(P16, P16 + 4, 8, 4, P16, P16, 8, 32, 256, 128, P16, P16, need, None) == \
+        moe.MOE_ERR_INVALID_ARG  # misaligned row_src
     assert L.moe_grouped_gemm(P16, P16, P16, P16, None, 8, 32, 256, 128, P16, P16, 256, None) == \
         moe.MOE_ERR_INVALID_ARG  # topk_w without sorted_pair
     assert L.moe_grouped_gemm(P16, P16, P16, None, None, 8, 0, 256, 128, P16, P16, 256, None) == moe.MOE_OK

@@ -162,6 +162,54 @@ def test_grouped_gemm_swiglu_parity(moe, counts, H, I):
     assert_bf16_rounding_close(got, ref, "act")
 
 
+# (T, k, E, H, I, zipf-like skew): the gate/up GEMM gathering its own rows through row_src, on
+# each instance family: decode (<= 32 rows per expert), weight-streaming CTA pairs (< 256 rows per
+# expert, a separate gather kernel first) and compute-bound CTA pairs (the gather inside the GEMM)
+GATHER_CASES = [(16, 2, 8, 256, 128, 0.0), (300, 4, 16, 512, 128, 0.0), (1000, 4, 8, 512, 256, 0.3),
+                (3000, 2, 6, 256, 128, 0.0), (37, 8, 64, 4096, 1536, 0.0)]
+
+
+@pytest.mark.parametrize("T,k,E,H,I,skew", GATHER_CASES)
+def test_grouped_gemm_swiglu_gathers_its_rows(moe, T, k, E, H, I, skew):
+    """act through row_src (the call gathers x[sorted_pair[pos] // k]) equals the oracle's GEMM on the
+    oracle's expanded rows, and equals the call on pre-expanded rows bit for bit."""
+    seed = T + E + H
+    rng = np.random.default_rng(seed)
+    p = np.exp(skew * rng.normal(size=E) * 3)
+    p /= p.sum()
+    idx = np.stack([rng.choice(E, size=k, replace=False, p=p) for _ in range(T)]).astype(np.int32)
+    counts, off, sp, _ = oracle.init_routing(idx, E)
+    x = mi.normal_bf16(seed, 1, (T, H))
+    w13 = mi.normal_bf16(seed, 2, (E, 2 * I, H), 0.0, 0.02)
+    ref = oracle.grouped_gemm_swiglu(oracle.expand_rows(x, sp, k), w13, off)
+    w13p = moe.moe_prepack_w13(dev_bf16(w13))
+    ws = _torch().zeros(moe.lib().moe_grouped_gemm_swiglu_workspace_size(T * k, H, 1), dtype=_torch().uint8,
+                        device="cuda")
+    act = moe.moe_grouped_gemm_swiglu(dev_bf16(x), w13p, dev(off), ws=ws, row_src=dev(sp), k=k)
+    assert moe.moe_get_device_status(ws) == moe.MOE_OK
+    got = host_bf16_f64(act)
+    assert_close(got, ref, "act (row_src)")
+    assert_bf16_rounding_close(got, ref, "act (row_src)")
+    pre = moe.moe_grouped_gemm_swiglu(dev_bf16(oracle.expand_rows(x, sp, k)), w13p, dev(off))
+    assert _torch().equal(act.view(_torch().int16), pre.view(_torch().int16))
+
+
+@pytest.mark.parametrize("T,k,E,H,I", [(8, 2, 4, 256, 128), (1000, 4, 8, 256, 128)])
+def test_grouped_gemm_swiglu_flags_bad_row_src(moe, T, k, E, H, I):
+    """A source row outside [0, T*k) is skipped and reported, by the separate gather kernel (the first
+    shape) and by the gather inside the GEMM (the second), without stalling the GEMM."""
+    torch = _torch()
+    idx = np.array([[e % E, (e + 1) % E] for e in range(T)], np.int32)
+    _, off, sp, _ = oracle.init_routing(idx, E)
+    sp = sp.copy()
+    sp[3] = T * k + 5  # outside [0, T*k)
+    x = mi.normal_bf16(3, 1, (T, H))
+    w13 = mi.normal_bf16(3, 2, (E, 2 * I, H), 0.0, 0.02)
+    ws = torch.zeros(moe.lib().moe_grouped_gemm_swiglu_workspace_size(T * k, H, 1), dtype=torch.uint8, device="cuda")
+    moe.moe_grouped_gemm_swiglu(dev_bf16(x), moe.moe_prepack_w13(dev_bf16(w13)), dev(off), ws=ws, row_src=dev(sp), k=k)
+    assert moe.moe_get_device_status(ws) == moe.MOE_ERR_DEVICE_CHECK
+
+
 @pytest.mark.parametrize("counts,H,I", GEMM_CASES)
 def test_grouped_gemm_down_parity(moe, counts, H, I):
     E = len(counts)
