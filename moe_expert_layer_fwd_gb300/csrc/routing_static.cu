@@ -21,6 +21,7 @@
 //  - the first call on a device looks up the array's device address
 //    (cudaGetSymbolAddress) with that device current and caches it; make that
 //    first call before any stream capture begins.
+#include <atomic>
 #include <mutex>
 
 #include "moe_common.cuh"
@@ -33,21 +34,28 @@ constexpr int kMaxDevices = 64;
 
 static __device__ __align__(256) int32_t g_routing_scratch[kStaticScratchBytes / sizeof(int32_t)];
 
+// Per device, the array's device address once it has been looked up.  Reads take no lock; the
+// mutex is taken only by a call that finds no address yet for its device.
+std::atomic<int32_t*> g_scratch_ptr[kMaxDevices] = {};
 std::mutex g_mutex;
-int32_t* g_scratch_ptr[kMaxDevices] = {};
 
 // Device address of g_routing_scratch on the current device (looked up once per device).
 int scratch_for_current_device(int32_t** out) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return MOE_ERR_CUDA;
   if (dev < 0 || dev >= kMaxDevices) return MOE_ERR_UNSUPPORTED;
-  std::lock_guard<std::mutex> lock(g_mutex);
-  if (g_scratch_ptr[dev] == nullptr) {
-    void* p = nullptr;
-    if (cudaGetSymbolAddress(&p, g_routing_scratch) != cudaSuccess || p == nullptr) return MOE_ERR_CUDA;
-    g_scratch_ptr[dev] = static_cast<int32_t*>(p);
+  int32_t* p = g_scratch_ptr[dev].load(std::memory_order_acquire);
+  if (p == nullptr) {
+    std::lock_guard<std::mutex> lock(g_mutex);
+    p = g_scratch_ptr[dev].load(std::memory_order_relaxed);
+    if (p == nullptr) {
+      void* a = nullptr;
+      if (cudaGetSymbolAddress(&a, g_routing_scratch) != cudaSuccess || a == nullptr) return MOE_ERR_CUDA;
+      p = static_cast<int32_t*>(a);
+      g_scratch_ptr[dev].store(p, std::memory_order_release);
+    }
   }
-  *out = g_scratch_ptr[dev];
+  *out = p;
   return MOE_OK;
 }
 

@@ -74,10 +74,44 @@ def test_static_scratch_matches_workspace_routing_twice_in_a_row(env):
             assert torch.equal(got[name], ref[name]), f"call {seed}: {name} differs"
 
 
-def test_static_scratch_rejects_problems_beyond_its_limit(env):
+# (T, E, k, H): the 1 MiB limit exactly (E = 1024 at T*k = 65536, and E = 512 at T*k = 131072),
+# a single token, and no row gather (H = 0)
+ORACLE_CASES = [(8192, 1024, 8, 64), (16384, 512, 8, 0), (1, 16, 4, 128), (777, 40, 5, 0)]
+
+
+@pytest.mark.parametrize("T,E,k,H", ORACLE_CASES)
+def test_static_scratch_matches_the_oracle(env, T, E, k, H):
+    """Counts, offsets, both permutations and the gathered rows bit for bit against the oracle's
+    counting sort and row expansion."""
     moe, torch = env
-    # E = 1024 needs 2 * n_chunks * 1024 * 4 bytes: over 1 MiB once T*k > 65536
-    T, E, k = 8200, 1024, 16
+    import oracle
+    idx, x = _routing_case(T + E, T, E, k, max(H, 64))
+    counts, offsets, sp, pp = oracle.init_routing(idx, E)
+    idx_d = torch.from_numpy(idx).cuda()
+    got = _outputs(torch, T, E, k, max(H, 64), 3)
+    stream = torch.cuda.current_stream().cuda_stream
+    x_d = torch.from_numpy(x).cuda() if H else None
+    st = moe.lib().moe_init_routing_static_scratch(
+        idx_d.data_ptr(), T, E, k, x_d.data_ptr() if H else None, H, got["x_exp"].data_ptr() if H else None,
+        got["counts"].data_ptr(), got["offsets"].data_ptr(), got["sorted_pair"].data_ptr(),
+        got["pair_pos"].data_ptr(), stream)
+    assert st == moe.MOE_OK
+    torch.cuda.synchronize()
+    assert (got["counts"].cpu().numpy() == counts).all()
+    assert (got["offsets"].cpu().numpy() == offsets).all()
+    assert (got["sorted_pair"].cpu().numpy() == sp).all()
+    assert (got["pair_pos"].cpu().numpy() == pp).all()
+    if H:
+        xe = got["x_exp"].cpu().numpy().view(np.uint16)
+        assert (xe == oracle.expand_rows(x.view(np.uint16), sp, k)).all()
+    else:
+        assert (got["x_exp"] == 3).all()  # no gather asked for: untouched
+
+
+@pytest.mark.parametrize("T,E,k", [(8200, 1024, 16), (65537, 1024, 1)])
+def test_static_scratch_rejects_problems_beyond_its_limit(env, T, E, k):
+    moe, torch = env
+    # E = 1024 needs 2 * n_chunks * 1024 * 4 bytes: over 1 MiB once T*k > 65536 (65537 is the first)
     stream = torch.cuda.current_stream().cuda_stream
     d = torch.zeros(16, dtype=torch.int32, device="cuda").data_ptr()
     st = moe.lib().moe_init_routing_static_scratch(d, T, E, k, None, 0, None, d, d, d, d, stream)
