@@ -125,6 +125,37 @@ def test_add_rms_norm_mxfp8_parity(moe, T, H, with_res):
     sat = np.abs(y_gpu) / x > 448
     assert (np.abs(back - y_gpu)[~sat] <= 2.0 ** -4 * np.abs(y_gpu)[~sat] + 2.0 ** -10 * x[~sat]).all()
     assert (np.abs(back[sat]) == 448 * x[sat]).all()
+    _end_to_end_mx_agreement(host(codes), host(scales), y_ref, f"T={T} H={H}")
+
+
+def _end_to_end_mx_agreement(codes, scales, y_ref, what):
+    """The GPU's codes against the oracle quantising its own float64 row (not the GPU's fp32 row).
+    The fp32 and float64 rows differ by ~1e-7 relative, so a code or a scale can differ only where
+    that decides a rounding: a scale byte only for a block whose amax lies within 1e-5 of a power of
+    two, a code only by one E4M3 step, for an element within 1e-5 of the midpoint of the two
+    neighbouring E4M3 values.  Reports the rate of differing codes."""
+    from oracle.mx import e4m3_decode, mx_quantize_e4m3
+    c_ref, s_ref = mx_quantize_e4m3(y_ref)
+    T, H = codes.shape
+    blk = y_ref.reshape(T, H // 32, 32)
+    amax = np.abs(blk).max(axis=-1)
+    s_diff = scales != s_ref
+    if s_diff.any():
+        frac = np.log2(amax[s_diff])
+        assert (np.abs(frac - np.rint(frac)) <= 1e-5).all(), f"{what}: scale differs away from a power of two"
+    same_scale = np.repeat(~s_diff, 32, axis=1)
+    mag, mag_ref = codes & 0x7F, c_ref & 0x7F
+    differ = (codes != c_ref) & ~((mag == 0) & (mag_ref == 0)) & same_scale
+    n = int(differ.sum())
+    if n:
+        assert (np.abs(mag[differ].astype(int) - mag_ref[differ].astype(int)) == 1).all(), \
+            f"{what}: a code differs by more than one E4M3 step"
+        x = np.exp2(scales.astype(np.float64) - 127.0).repeat(32, axis=1)
+        v = np.abs(y_ref[differ]) / x[differ]
+        mid = (np.abs(e4m3_decode(codes[differ])) + np.abs(e4m3_decode(c_ref[differ]))) / 2
+        assert (np.abs(v - mid) <= 1e-5 * v).all(), f"{what}: a differing code is not at a rounding boundary"
+    print(f"MXFP8 end to end ({what}): {n} of {codes.size} codes ({n / codes.size:.2e}) and "
+          f"{int(s_diff.sum())} of {scales.size} scales differ from the float64 oracle, each at a rounding boundary")
 
 
 def test_mxfp8_zero_rows_and_saturation(moe):

@@ -96,3 +96,30 @@ def test_partial_layers_of_an_expert_partition(moe, cfg, parts):
         acc += got
         assert moe.moe_get_device_status(o["ws"]) == 0
     assert_close(acc, full["y"], "sum of the partial outputs")
+
+
+def test_mxfp4_partial_layer_on_a_local_expert_range(moe):
+    """The 4-bit-weight GEMMs on a local expert slice: weights quantised and prepacked for all 16
+    experts, sliced to [4, 12) with Mxfp4Weights.experts (the pointer offsets include/moe.h states),
+    routed with moe_init_routing_range, both 4-bit GEMMs and finalize -> the range's partial output,
+    against the oracle's partial layer on the MXFP4-decoded weights."""
+    import torch
+    cfg = mi.CONFIGS["qwen3_decode"].with_(T=24, H=256, E=16, k=4, I=128)
+    e0, e1 = 4, 12
+    inp = mi.generate(cfg)
+    ref = oracle.moe_layer_forward_range(inp.x, inp.logits, cfg.k, cfg.gate, oracle.mxfp4_weights(inp.w13),
+                                         oracle.mxfp4_weights(inp.w2), e0, e1)
+    w13q = moe.moe_mxfp4_prepack(*moe.moe_mxfp4_quantize(dev_bf16(inp.w13)), gate_up=True).experts(e0, e1)
+    w2q = moe.moe_mxfp4_prepack(*moe.moe_mxfp4_quantize(dev_bf16(inp.w2)), gate_up=False).experts(e0, e1)
+    topk_w, topk_idx = moe.moe_gating_topk(dev(inp.logits), cfg.k, cfg.gate)
+    o = moe.moe_init_routing_range(topk_idx, cfg.E, e0, e1)
+    torch.cuda.synchronize()
+    n_loc = int(o["offsets"][-1].item())
+    assert (host(o["offsets"]) == ref["offsets"]).all() and (host(o["pair_pos"]) == ref["pair_pos"]).all()
+    x16 = moe.moe_gather_rows_f16(dev_bf16(inp.x), o["sorted_pair"], cfg.k, M=n_loc)
+    act = moe.moe_grouped_gemm_swiglu_mxfp4(x16, w13q, o["offsets"])
+    y_perm = moe.moe_grouped_gemm_mxfp4(act, w2q, o["offsets"], topk_w, o["sorted_pair"])
+    y = moe.moe_finalize_routing(y_perm, o["pair_pos"], cfg.T, cfg.k)
+    torch.cuda.synchronize()
+    assert moe.moe_get_device_status(o["ws"]) == 0
+    assert_close(host_bf16_f64(y), ref["y"], f"4-bit partial y [{e0},{e1})")
