@@ -70,6 +70,9 @@ def _args(argv=None):
                     help="plain moe_layer_forward loop only (for ncu launch lists)")
     ap.add_argument("--override", default="",
                     help="shape overrides of the workload for small profiling captures, e.g. E=32,T=16")
+    ap.add_argument("--per-config", default="auto",
+                    help="workloads measured beside the headline one, each in its own record: 'auto' (all other "
+                         "workloads when the headline is the default one), 'none', or a comma-separated list")
     a = ap.parse_args(argv)
     if a.warmup < 3:
         ap.error("--warmup must be >= 3")
@@ -216,15 +219,35 @@ def workload(args):
     return cfg
 
 
-def cpu_baseline_child(args):
-    """Runs in a subprocess with the BLAS thread count fixed: times the oracle on a token sample."""
+def oracle_inputs(cfg, tokens):
+    """The workload's inputs for the oracle on `tokens`: x, logits and bias in full, and the expert
+    weights of the experts those tokens are routed to (the oracle's own routing), each generated from
+    its slice of the seeded weight stream; the other experts' rows are never touched (the arrays are
+    allocated, not filled)."""
     import numpy as np
     import moe_inputs as mi
     import oracle
+    inp = mi.generate(cfg, weights=False)
+    _, idx = oracle.gating_topk(inp.logits, cfg.k, cfg.gate, inp.bias, cfg.routed_scaling_factor, cfg.eps)
+    w13 = np.empty((cfg.E, 2 * cfg.I, cfg.H), np.uint16)
+    w2 = np.empty((cfg.E, cfg.H, cfg.I), np.uint16)
+    for e in np.unique(idx[np.asarray(tokens)]):
+        w13[e], w2[e] = mi.expert_weights(cfg, int(e))
+    inp.w13, inp.w2 = w13, w2
+    if cfg.n_shared:
+        full = mi.generate(cfg.with_(E=1, T=1))  # the shared expert's streams do not depend on E or T
+        inp.w13_s, inp.w2_s = full.w13_s, full.w2_s
+    return inp
+
+
+def cpu_baseline_child(args):
+    """Runs in a subprocess with the BLAS thread count fixed: times the oracle on a token sample."""
+    import numpy as np
+    import oracle
     cfg = workload(args)
-    inp = mi.generate(cfg)
     n = min(args.sample_tokens, cfg.T)
     toks = np.arange(n)
+    inp = oracle_inputs(cfg, toks)
     t0 = time.perf_counter()
     oracle.moe_layer_forward_tokens(toks, inp.x, inp.logits, cfg.k, cfg.gate, inp.w13, inp.w2, inp.bias,
                                     cfg.routed_scaling_factor, cfg.eps, inp.w13_s, inp.w2_s)
@@ -232,20 +255,24 @@ def cpu_baseline_child(args):
     print(json.dumps({"tokens": n, "seconds": dt}))
 
 
-def cpu_baseline(args, cores=None):
+def cpu_baseline(args, cores=None, workload_name=None, override=None):
+    """The oracle timed on `args.sample_tokens` tokens of a workload, in a child process on `cores`
+    host threads (default: all of this process's affinity set)."""
+    workload_name = workload_name or args.workload
+    override = args.override if override is None else override
     cores = cores or len(os.sched_getaffinity(0))
     env = dict(os.environ, OMP_NUM_THREADS=str(cores), OPENBLAS_NUM_THREADS=str(cores), MKL_NUM_THREADS=str(cores))
     for k in ("RANK", "WORLD_SIZE", "LOCAL_RANK", "MASTER_ADDR", "MASTER_PORT"):
         env.pop(k, None)
-    cmd = [sys.executable, os.path.join(ROOT, "bench.py"), "--cpu-baseline-child", "--workload", args.workload,
-           "--sample-tokens", str(args.sample_tokens), "--override", args.override]
+    cmd = [sys.executable, os.path.join(ROOT, "bench.py"), "--cpu-baseline-child", "--workload", workload_name,
+           "--sample-tokens", str(args.sample_tokens), "--override", override]
     r = subprocess.run(cmd, env=env, capture_output=True, text=True, timeout=900)
     if r.returncode != 0:
         return {"value": None, "unit": "tokens/s", "cores": cores, "kind": "oracle",
                 "error": r.stderr.strip().splitlines()[-1:] }
     d = json.loads(r.stdout.strip().splitlines()[-1])
     return {"value": d["tokens"] / d["seconds"], "unit": "tokens/s", "cores": cores, "kind": "oracle",
-            "sample": f"{d['tokens']} tokens of the {args.workload} workload (routing of all tokens, expert FFNs of the "
+            "sample": f"{d['tokens']} tokens of the {workload_name} workload (routing of all tokens, expert FFNs of the "
                       f"sampled tokens, float64 numpy with BLAS on {cores} thread{'s' if cores > 1 else ''}): "
                       f"{d['seconds']:.2f} s"}
 
@@ -258,7 +285,7 @@ def run_reference(args, rank, world):
     import moe_inputs as mi
     import oracle
     cfg = workload(args)
-    inp = mi.generate(cfg)
+    inp = oracle_inputs(cfg, np.arange(args.warmup + args.steps) % cfg.T)
     cores = len(os.sched_getaffinity(0))
 
     def step(i):
@@ -405,55 +432,58 @@ def mxfp4_leg(args, cfg, K, W, moe, inp, t, d16, peaks, peak_src, y_bf16):
 
 
 # ------------------------------------------------------------------ GB300 arm
-def run_gb300(args, rank, world, local):
+# the workloads measured beside the default one (hy3_decode and hy3_prefill share their weights)
+OTHER_WORKLOADS = ["tiny", "hy3_decode", "hy3_prefill", "long_prefill"]
+
+
+def per_config_names(args):
+    if args.per_config == "none":
+        return []
+    if args.per_config == "auto":
+        if args.workload != DEFAULT_WORKLOAD or args.override:
+            return []
+        return [n for n in OTHER_WORKLOADS if n != args.workload]
+    return [n for n in args.per_config.split(",") if n and n != args.workload]
+
+
+class DeviceWeights:
+    """Expert weights resident in HBM, kept for the next workload when it has the same weights
+    (the weights depend only on the seed, E, H, I, the shared expert and their spread)."""
+
+    def __init__(self):
+        self.key = None
+        self.t = None
+
+    def get(self, cfg, moe, mi, d16):
+        import torch
+        key = (cfg.seed, cfg.E, cfg.H, cfg.I, cfg.w_std, cfg.n_shared, cfg.I_s)
+        if key != self.key:
+            self.t = None
+            torch.cuda.empty_cache()
+            inp = mi.generate(cfg)
+            # weights are loaded once: w13 goes through the one-time gate/up packing (not timed)
+            w13_raw = d16(inp.w13)
+            self.t = dict(w13=moe.moe_prepack_w13(w13_raw), w2=d16(inp.w2),
+                          w13_s=moe.moe_prepack_w13(d16(inp.w13_s)) if inp.w13_s is not None else None,
+                          w2_s=d16(inp.w2_s) if inp.w2_s is not None else None)
+            del w13_raw, inp
+            self.key = key
+        return self.t
+
+
+def measure(args, cfg, K, W, world, rank, local, moe, mi, d16, weights, peaks, peak_src, dev_id):
+    """One workload: the headline timed loop, per-step events, e2e, clocks, roofline, CPU baseline."""
     import numpy as np
     import torch
 
-    import moe_expert_layer_fwd_gb300 as moe
-    import moe_inputs as mi
-    from moe_expert_layer_fwd_gb300 import build as moe_build
-
-    if not torch.cuda.is_available():
-        raise SystemExit("bench.py needs a CUDA GPU for --impl gb300")
-    torch.cuda.set_device(local)
-    moe_build.build()
-    cfg = workload(args)
-    inp = mi.generate(cfg)
-
-    def d16(u):
-        return torch.from_numpy(np.ascontiguousarray(u).view(np.int16)).cuda().view(torch.bfloat16)
-
-    # weights are loaded once: w13 goes through the one-time gate/up packing (not timed)
-    w13_raw = d16(inp.w13)
-    w13p = moe.moe_prepack_w13(w13_raw)
-    del w13_raw
-    t = dict(x=d16(inp.x), logits=torch.from_numpy(inp.logits).cuda(), w13=w13p, w2=d16(inp.w2),
-             bias=torch.from_numpy(inp.bias).cuda() if inp.bias is not None else None,
-             w13_s=moe.moe_prepack_w13(d16(inp.w13_s)) if inp.w13_s is not None else None,
-             w2_s=d16(inp.w2_s) if inp.w2_s is not None else None)
+    inp = mi.generate(cfg, weights=False)
+    t = dict(weights.get(cfg, moe, mi, d16))
+    t.update(x=d16(inp.x), logits=torch.from_numpy(inp.logits).cuda(),
+             bias=torch.from_numpy(inp.bias).cuda() if inp.bias is not None else None)
     layer = moe.MoELayer(cfg.T, cfg.H, cfg.E, cfg.k, cfg.I, cfg.gate, cfg.routed_scaling_factor, cfg.eps,
                          cfg.n_shared, cfg.I_s)
     launches = moe.moe_layer_kernel_launches(layer.desc)
-    K, W = args.steps, args.warmup
 
-    if args.profile_steps:
-        if args.profile_mxfp4:
-            w13q = moe.moe_mxfp4_prepack(*moe.moe_mxfp4_quantize(d16(inp.w13)), gate_up=True)
-            w2q = moe.moe_mxfp4_prepack(*moe.moe_mxfp4_quantize(t["w2"]), gate_up=False)
-            l4 = moe.Mxfp4Layer(cfg.T, cfg.H, cfg.E, cfg.k, cfg.I, cfg.gate, cfg.routed_scaling_factor, cfg.eps)
-            for _ in range(W + K):
-                l4.forward(t["x"], t["logits"], w13q, w2q, t["bias"])
-        else:
-            for _ in range(W + K):
-                layer.forward(**t)
-        torch.cuda.synchronize()
-        return
-
-    dev_id = str(local)
-    try:
-        dev_id = "GPU-" + str(torch.cuda.get_device_properties(local).uuid)
-    except Exception:
-        pass
     clocks = Clocks(dev_id) if rank == 0 else None
     if clocks:
         clocks.start()
@@ -470,9 +500,9 @@ def run_gb300(args, rank, world, local):
     torch.cuda.synchronize()
     status = moe.moe_get_device_status(layer.ws)
     if status != moe.MOE_OK:
-        raise SystemExit(f"device status after warm-up: {moe.status_string(status)}")
+        raise SystemExit(f"{cfg.name}: device status after warm-up: {moe.status_string(status)}")
     counts = layer.counts.cpu().numpy()
-    # timed region 1 (the headline value): K plain moe_layer_forward calls
+    # timed region 1 (the value): K plain moe_layer_forward calls
     start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     torch.cuda.synchronize()
     _barrier(world)
@@ -490,7 +520,7 @@ def run_gb300(args, rank, world, local):
     ms_total = _max_over_ranks(start.elapsed_time(end), world)
     status = moe.moe_get_device_status(layer.ws)
     if status != moe.MOE_OK:
-        raise SystemExit(f"device status after the timed region: {moe.status_string(status)}")
+        raise SystemExit(f"{cfg.name}: device status after the timed region: {moe.status_string(status)}")
     # timed region 2 (per-kernel durations): K moe_layer_forward_events calls, six events
     # recorded on the launching stream around the steps of every call
     evs = [[torch.cuda.Event(enable_timing=True) for _ in range(6)] for _ in range(K)]
@@ -505,13 +535,6 @@ def run_gb300(args, rank, world, local):
     kern_ms = {n: statistics.mean(evs[i][j].elapsed_time(evs[i][j + 1]) for i in range(K))
                for j, n in enumerate(names)}
     step_ms = sorted(evs[i][0].elapsed_time(evs[i][5]) for i in range(K))
-
-    front = None if args.no_front_end else front_end(args, cfg, K, W, moe, mi, d16)
-    peaks, src = _peaks()
-    # the 4-bit-weight layer: decode-sized routed-only workloads (the 4-bit GEMMs walk 32 token columns)
-    w4 = None
-    if not args.no_mxfp4 and cfg.n_shared == 0 and cfg.T * cfg.k <= 32 * cfg.E:
-        w4 = mxfp4_leg(args, cfg, K, W, moe, inp, t, d16, peaks, src, layer.y.float())
 
     # end to end: pinned host inputs -> device, forward, result -> pinned host, every step.  Served
     # as a pipeline: two buffer sets (inputs, layer outputs, pinned results) and three streams, so
@@ -586,12 +609,10 @@ def run_gb300(args, rank, world, local):
         ref_y = layer.y.view(torch.int16).cpu().numpy()
         for b in range(NB):
             if not np.array_equal(hys[b].numpy(), ref_y):
-                raise SystemExit("end-to-end result differs from the device-resident run")
+                raise SystemExit(f"{cfg.name}: end-to-end result differs from the device-resident run")
         del layers, dxs, dls
 
     clk = clocks.stop() if clocks else None
-    if rank != 0:
-        return
 
     work = layer_work(cfg, counts)
     ms = ms_total / K
@@ -610,7 +631,7 @@ def run_gb300(args, rank, world, local):
         roof = {"bound": "tensor", "achieved": tf, "peak": peaks["bf16_tflops_sustained"], "unit": "TFLOP/s",
                 "frac": tf / peaks["bf16_tflops_sustained"]}
     roof["traffic"] = _traffic(cfg.name, dom)
-    roof.update(kernel=dom, peak_source=f"{src} ({'hbm_gbs' if roof['bound'] == 'hbm' else 'bf16_tflops_sustained'})",
+    roof.update(kernel=dom, peak_source=f"{peak_src} ({'hbm_gbs' if roof['bound'] == 'hbm' else 'bf16_tflops_sustained'})",
                 algorithmic_bytes_per_launch=dom_work["bytes"], flops_per_launch=dom_work["flops"],
                 per_unit=f"{2 * cfg.I * cfg.H * 2} weight bytes per active expert "
                          f"(x {work['active_experts']} active experts" + (" + the shared expert)" if cfg.n_shared else ")"),
@@ -619,19 +640,17 @@ def run_gb300(args, rank, world, local):
     tot_f = work["gemm_w13"]["flops"] + work["gemm_down"]["flops"]
     layer_roof = {"weight_bytes": tot_b, "flops": tot_f,
                   "hbm_frac_of_measured": tot_b / (ms * 1e-3) / 1e9 / peaks["hbm_gbs"],
-                  "tc_frac_of_measured_burst": tot_f / (ms * 1e-3) / 1e12 / peaks["bf16_tflops"]}
+                  "tc_frac_of_measured_burst": tot_f / (ms * 1e-3) / 1e12 / peaks["bf16_tflops"],
+                  "tc_frac_of_measured_sustained": tot_f / (ms * 1e-3) / 1e12 / peaks["bf16_tflops_sustained"],
+                  "how": "the two grouped GEMMs' weight bytes and FLOPs over ms_per_step (the whole layer)"}
     t_down = kern_ms["gemm_down"] * 1e-3
-    line = {
-        "metric": METRIC,
+    rec = {
         "value": world * cfg.T * K / (ms_total * 1e-3),
         "unit": "tokens/s",
-        "n_gpus": world, "steps": K, "warmup": W, "ms_per_step": ms,
+        "ms_per_step": ms,
         "step_ms": {"median": statistics.median(step_ms), "min": step_ms[0], "cold_first_call": cold_ms,
                     "how": "median and minimum of the K per-call durations of the events loop; the first call "
                            "of the process timed alone"},
-        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-        "dtype": "bf16", "data": "synthetic (seeded Philox inputs, random-init weights)",
-        "config": _config(cfg, world),
         "roofline": roof,
         "roofline_layer": layer_roof,
         "roofline_gemm_down": {"achieved_gbs": work["gemm_down"]["bytes"] / t_down / 1e9,
@@ -643,10 +662,98 @@ def run_gb300(args, rank, world, local):
         "clocks": clk,
     }
     if e2e:
-        line["e2e"] = e2e
+        rec["e2e"] = e2e
+    rec["_y"] = layer.y.float()
+    rec["_t"] = t
+    rec["_inp"] = inp
+    return rec
+
+
+def run_gb300(args, rank, world, local):
+    import numpy as np
+    import torch
+
+    import moe_expert_layer_fwd_gb300 as moe
+    import moe_inputs as mi
+    from moe_expert_layer_fwd_gb300 import build as moe_build
+
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py needs a CUDA GPU for --impl gb300")
+    torch.cuda.set_device(local)
+    moe_build.build()
+    cfg = workload(args)
+    K, W = args.steps, args.warmup
+
+    def d16(u):
+        return torch.from_numpy(np.ascontiguousarray(u).view(np.int16)).cuda().view(torch.bfloat16)
+
+    weights = DeviceWeights()
+    if args.profile_steps:
+        inp = mi.generate(cfg, weights=False)
+        t = dict(weights.get(cfg, moe, mi, d16))
+        t.update(x=d16(inp.x), logits=torch.from_numpy(inp.logits).cuda(),
+                 bias=torch.from_numpy(inp.bias).cuda() if inp.bias is not None else None)
+        if args.profile_mxfp4:
+            full = mi.generate(cfg)
+            w13q = moe.moe_mxfp4_prepack(*moe.moe_mxfp4_quantize(d16(full.w13)), gate_up=True)
+            w2q = moe.moe_mxfp4_prepack(*moe.moe_mxfp4_quantize(t["w2"]), gate_up=False)
+            l4 = moe.Mxfp4Layer(cfg.T, cfg.H, cfg.E, cfg.k, cfg.I, cfg.gate, cfg.routed_scaling_factor, cfg.eps)
+            for _ in range(W + K):
+                l4.forward(t["x"], t["logits"], w13q, w2q, t["bias"])
+        else:
+            layer = moe.MoELayer(cfg.T, cfg.H, cfg.E, cfg.k, cfg.I, cfg.gate, cfg.routed_scaling_factor, cfg.eps,
+                                 cfg.n_shared, cfg.I_s)
+            for _ in range(W + K):
+                layer.forward(**t)
+        torch.cuda.synchronize()
+        return
+
+    dev_id = str(local)
+    try:
+        dev_id = "GPU-" + str(torch.cuda.get_device_properties(local).uuid)
+    except Exception:
+        pass
+    peaks, src = _peaks()
+    rec = measure(args, cfg, K, W, world, rank, local, moe, mi, d16, weights, peaks, src, dev_id)
+    y_bf16, t, inp = rec.pop("_y"), rec.pop("_t"), rec.pop("_inp")
+
+    front = None if args.no_front_end else front_end(args, cfg, K, W, moe, mi, d16)
+    # the 4-bit-weight layer: decode-sized routed-only workloads (the 4-bit GEMMs walk 32 token columns)
+    w4 = None
+    if not args.no_mxfp4 and cfg.n_shared == 0 and cfg.T * cfg.k <= 32 * cfg.E:
+        inp.w13 = mi.normal_bf16(cfg.seed, mi.TID_W13, (cfg.E, 2 * cfg.I, cfg.H), 0.0, cfg.w_std)
+        w4 = mxfp4_leg(args, cfg, K, W, moe, inp, t, d16, peaks, src, y_bf16)
+        inp.w13 = None
+    del t, y_bf16
+
+    others = {}
+    for name in per_config_names(args):
+        c = mi.CONFIGS[name]
+        r = measure(args, c, K, W, world, rank, local, moe, mi, d16, weights, peaks, src, dev_id)
+        for key in ("_y", "_t", "_inp"):
+            r.pop(key)
+        r["config"] = _config(c, world)
+        others[name] = r
+    weights.t = None
+    torch.cuda.empty_cache()
+
+    if rank != 0:
+        return
+
+    line = {
+        "metric": METRIC,
+        "value": rec.pop("value"),
+        "unit": rec.pop("unit"),
+        "n_gpus": world, "steps": K, "warmup": W, "ms_per_step": rec.pop("ms_per_step"),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "bf16", "data": "synthetic (seeded Philox inputs, random-init weights)",
+        "config": _config(cfg, world),
+    }
+    line.update(rec)
     if w4:
         line["mxfp4_weights"] = w4
     if front:
+        clk = rec.get("clocks")
         sm_mhz = (clk or {}).get("sm_mhz") or peaks.get("sm_max_mhz", 2070.0)
         fp32_tflops = torch.cuda.get_device_properties(local).multi_processor_count * 128 * 2 * sm_mhz * 1e6 / 1e12
         nb = front.pop("norm_bytes")
@@ -668,6 +775,10 @@ def run_gb300(args, rank, world, local):
         line["cpu_baseline"] = cpu_baseline(args)
         if cfg.T * cfg.k <= 32 * cfg.E:  # the small and decode configs: the oracle on one core as well
             line["cpu_baseline_1core"] = cpu_baseline(args, cores=1)
+        for name, r in others.items():
+            r["cpu_baseline"] = cpu_baseline(args, workload_name=name, override="")
+    if others:
+        line["per_config"] = others
     print(json.dumps(line), flush=True)
 
 

@@ -60,9 +60,11 @@ def _load():
             lib.moe_inputs_philox4x32_10.argtypes = [vp, vp, vp]
             lib.moe_inputs_u32.argtypes = [u64, u32, i64, vp]
             lib.moe_inputs_normal_bf16.argtypes = [u64, u32, i64, dbl, dbl, vp]
+            lib.moe_inputs_normal_bf16_range.argtypes = [u64, u32, i64, i64, dbl, dbl, vp]
             lib.moe_inputs_normal_f32.argtypes = [u64, u32, i64, dbl, dbl, vp]
             lib.moe_inputs_grid_logits.argtypes = [u64, u32, i64, i64, vp, ctypes.c_int, vp]
             for f in ("moe_inputs_philox4x32_10", "moe_inputs_u32", "moe_inputs_normal_bf16",
+                      "moe_inputs_normal_bf16_range",
                       "moe_inputs_normal_f32", "moe_inputs_grid_logits"):
                 getattr(lib, f).restype = None
             _lib = lib
@@ -93,6 +95,21 @@ def normal_bf16(seed: int, tid: int, shape, mean=0.0, std=1.0) -> np.ndarray:
     out = np.empty(shape, np.uint16)
     _load().moe_inputs_normal_bf16(seed, tid, out.size, float(mean), float(std), _ptr(out))
     return out
+
+
+def normal_bf16_slice(seed: int, tid: int, start: int, shape, mean=0.0, std=1.0) -> np.ndarray:
+    """Elements [start, start + prod(shape)) of the stream normal_bf16 draws for the same tensor id:
+    normal_bf16(seed, tid, full_shape).reshape(-1)[start:start + n], without the rest."""
+    out = np.empty(shape, np.uint16)
+    _load().moe_inputs_normal_bf16_range(seed, tid, int(start), out.size, float(mean), float(std), _ptr(out))
+    return out
+
+
+def expert_weights(cfg: "MoEConfig", e: int):
+    """(w13[e] [2I,H], w2[e] [H,I]) of generate(cfg): expert e's slices of the weight streams."""
+    n13, n2 = 2 * cfg.I * cfg.H, cfg.H * cfg.I
+    return (normal_bf16_slice(cfg.seed, TID_W13, e * n13, (2 * cfg.I, cfg.H), 0.0, cfg.w_std),
+            normal_bf16_slice(cfg.seed, TID_W2, e * n2, (cfg.H, cfg.I), 0.0, cfg.w_std))
 
 
 def normal_f32(seed: int, tid: int, shape, mean=0.0, std=1.0) -> np.ndarray:

@@ -86,13 +86,40 @@ void moe_inputs_u32(uint64_t seed, uint32_t tensor_id, int64_t n, uint32_t* out)
   }
 }
 
+/* The four normals of counter block blk: z[j] = normal_at(seed, tensor_id, 4*blk + j), one Philox
+ * block and one Box-Muller pair per two elements instead of one each per element. */
+static inline void normal4_at(uint64_t seed, uint32_t tensor_id, uint64_t blk, double z[4]) {
+  uint32_t r[4];
+  block_for(seed, tensor_id, blk, r);
+  for (unsigned pair = 0; pair < 4; pair += 2) {
+    double u1 = u01(r[pair]), u2 = u01(r[pair + 1]);
+    double rad = sqrt(-2.0 * log(u1));
+    double th = 6.283185307179586476925286766559 * u2;
+    z[pair] = rad * cos(th);
+    z[pair + 1] = rad * sin(th);
+  }
+}
+
+/* out[i - start] = bf16(mean + std * z_i), z_i ~ N(0,1), for start <= i < start + n: a slice of the
+ * tensor's stream (element i always uses counter block i/4, lane i%4). */
+void moe_inputs_normal_bf16_range(uint64_t seed, uint32_t tensor_id, int64_t start, int64_t n, double mean,
+                                  double stdv, uint16_t* out) {
+  const int64_t b0 = start / 4, b1 = (start + n + 3) / 4;
+#pragma omp parallel for schedule(static)
+  for (int64_t b = b0; b < b1; ++b) {
+    double z[4];
+    normal4_at(seed, tensor_id, (uint64_t)b, z);
+    for (int j = 0; j < 4; ++j) {
+      const int64_t i = b * 4 + j;
+      if (i >= start && i < start + n) out[i - start] = f32_to_bf16_rne((float)(mean + stdv * z[j]));
+    }
+  }
+}
+
 /* out[i] = bf16(mean + std * z_i), z_i ~ N(0,1). */
 void moe_inputs_normal_bf16(uint64_t seed, uint32_t tensor_id, int64_t n, double mean, double stdv,
                             uint16_t* out) {
-#pragma omp parallel for schedule(static)
-  for (int64_t i = 0; i < n; ++i) {
-    out[i] = f32_to_bf16_rne((float)(mean + stdv * normal_at(seed, tensor_id, (uint64_t)i)));
-  }
+  moe_inputs_normal_bf16_range(seed, tensor_id, 0, n, mean, stdv, out);
 }
 
 /* out[i] = float(mean + std * z_i). */

@@ -31,9 +31,16 @@ def test_layer_work_closed_forms():
 
 
 def test_traffic_lookup_is_keyed_to_the_kernel_source(tmp_path, monkeypatch):
-    # the committed records match the committed sources
-    assert bench._traffic("qwen3_decode", "gemm_w13_swiglu") is not None
-    assert bench._traffic("qwen3_decode", "gemm_w13_swiglu_mxfp4", "grouped_gemm_mxfp4.cu") is not None
+    # a committed record is used exactly when it was taken on the current kernel source
+    import hashlib
+    recs = json.load(open(os.path.join(bench.ROOT, "profiles", "dram_traffic.json")))
+    for wl, kernels in recs.items():
+        for kern, rec in kernels.items():
+            src = rec.get("src", "grouped_gemm.cu")
+            with open(os.path.join(bench.ROOT, "moe_expert_layer_fwd_gb300", "csrc", src), "rb") as f:
+                sha = hashlib.sha256(f.read()).hexdigest()[:16]
+            want = rec["bytes_per_launch"] if rec["src_sha"] == sha else None
+            assert bench._traffic(wl, kern, src) == want
     assert bench._traffic("qwen3_decode", "no_such_kernel") is None
     assert bench._traffic("no_such_workload", "gemm_w13_swiglu") is None
     # an edited kernel source voids the record
@@ -46,6 +53,9 @@ def test_traffic_lookup_is_keyed_to_the_kernel_source(tmp_path, monkeypatch):
     shutil.copy(src, dst)
     monkeypatch.setattr(bench, "ROOT", str(root))
     rec = json.load(open(root / "profiles" / "dram_traffic.json"))["qwen3_decode"]["gemm_w13_swiglu"]
+    with open(dst, "rb") as f:
+        rec["src_sha"] = hashlib.sha256(f.read()).hexdigest()[:16]
+    json.dump({"qwen3_decode": {"gemm_w13_swiglu": rec}}, open(root / "profiles" / "dram_traffic.json", "w"))
     assert bench._traffic("qwen3_decode", "gemm_w13_swiglu") == rec["bytes_per_launch"]
     with open(dst, "a") as f:
         f.write("\n// edited\n")
@@ -67,3 +77,33 @@ def test_arguments():
         bench._args(["--warmup", "2"])
     a = bench._args([])
     assert a.workload == bench.DEFAULT_WORKLOAD and a.warmup >= 3 and a.impl == "gb300"
+
+
+def test_per_config_selection():
+    a = bench._args([])
+    assert bench.per_config_names(a) == ["tiny", "hy3_decode", "hy3_prefill", "long_prefill"]
+    assert bench.per_config_names(bench._args(["--workload", "long_prefill"])) == []
+    assert bench.per_config_names(bench._args(["--override", "E=32"])) == []
+    assert bench.per_config_names(bench._args(["--per-config", "none"])) == []
+    assert bench.per_config_names(bench._args(["--per-config", "tiny,qwen3_decode"])) == ["tiny"]
+
+
+def test_oracle_inputs_generate_exactly_the_needed_experts():
+    """The CPU legs' inputs: the sampled tokens' experts carry the generated weights (bit for bit
+    those of the full generation), and the oracle's result on them equals the one on full inputs."""
+    import oracle
+    cfg = mi.CONFIGS["hy3_decode"].with_(T=6, H=128, E=12, k=3, I=64, I_s=64)
+    full = mi.generate(cfg)
+    toks = np.arange(4)
+    lazy = bench.oracle_inputs(cfg, toks)
+    _, idx = oracle.gating_topk(full.logits, cfg.k, cfg.gate, full.bias, cfg.routed_scaling_factor, cfg.eps)
+    for e in np.unique(idx[toks]):
+        assert (lazy.w13[e] == full.w13[e]).all() and (lazy.w2[e] == full.w2[e]).all()
+    assert (lazy.w13_s == full.w13_s).all() and (lazy.w2_s == full.w2_s).all()
+    args = (cfg.k, cfg.gate)
+    kw = dict(routed_scaling_factor=cfg.routed_scaling_factor, eps=cfg.eps)
+    a = oracle.moe_layer_forward_tokens(toks, full.x, full.logits, *args, full.w13, full.w2, full.bias,
+                                        w13_s=full.w13_s, w2_s=full.w2_s, **kw)
+    b = oracle.moe_layer_forward_tokens(toks, lazy.x, lazy.logits, *args, lazy.w13, lazy.w2, lazy.bias,
+                                        w13_s=lazy.w13_s, w2_s=lazy.w2_s, **kw)
+    assert (a["y"] == b["y"]).all()

@@ -45,3 +45,14 @@ def test_zipf_workloads_have_hot_and_empty_experts(name):
     ratio = c.max() / c.mean()
     assert 5.0 <= ratio <= 10.0, ratio
     assert (c == 0).sum() >= 1
+
+
+def test_stream_slices_equal_the_full_stream():
+    full = mi.normal_bf16(3, 2, (4099,), 0.0, 0.02)
+    for start, n in ((0, 4099), (1, 5), (3, 1), (4, 8), (1001, 2000), (4098, 1)):
+        assert (mi.normal_bf16_slice(3, 2, start, (n,), 0.0, 0.02) == full[start:start + n]).all()
+    cfg = mi.CONFIGS["tiny"].with_(E=5)
+    inp = mi.generate(cfg)
+    for e in range(cfg.E):
+        w13, w2 = mi.expert_weights(cfg, e)
+        assert (w13 == inp.w13[e]).all() and (w2 == inp.w2[e]).all()
