@@ -61,7 +61,9 @@ def _args(argv=None):
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-front-end", action="store_true", help="skip timing the front end (norm + router GEMM)")
-    ap.add_argument("--no-mxfp4", action="store_true", help="skip timing the layer on MXFP4 expert weights")
+    ap.add_argument("--no-mxfp4", action="store_true", help="skip timing the W4A8 layer (MXFP8 x MXFP4 weights)")
+    ap.add_argument("--mxfp4-f16", action="store_true",
+                    help="also time the 4-bit-weight layer on f16 operands (software-decoded weights)")
     ap.add_argument("--profile-mxfp4", action="store_true",
                     help="with --profile-steps: the MXFP4-weight layer loop instead (for ncu launch lists)")
     ap.add_argument("--cpu-baseline-child", action="store_true", help=argparse.SUPPRESS)
@@ -431,9 +433,82 @@ def mxfp4_leg(args, cfg, K, W, moe, inp, t, d16, peaks, peak_src, y_bf16):
     }
 
 
+# ------------------------------------------------------------------ the W4A8 layer (MXFP8 x MXFP4)
+def w4a8_leg(args, cfg, K, W, moe, mi, d16, t, peaks, peak_src, y_bf16):
+    """Times moe_layer_forward_w4a8 (gating, routing, MXFP8 row gather, the two block-scaled W4A8 GEMMs,
+    finalize; the shared expert as one more GEMM segment) on the workload: the expert weights quantised
+    to MXFP4 on the GPU and the hidden state to MXFP8 by the fused RMSNorm + MX quantisation (both
+    one-time, not timed).  Reported beside the bf16 layer (a lower precision), not part of its value."""
+    import torch
+    w13_raw = d16(mi.normal_bf16(cfg.seed, mi.TID_W13, (cfg.E, 2 * cfg.I, cfg.H), 0.0, cfg.w_std))
+    w13 = moe.moe_w4a8_prepack(*moe.moe_mxfp4_quantize(w13_raw), gate_up=True)
+    del w13_raw
+    w2 = moe.moe_w4a8_prepack(*moe.moe_mxfp4_quantize(t["w2"]), gate_up=False)
+    w13_s = w2_s = None
+    if cfg.n_shared:
+        sh = mi.generate(cfg.with_(E=1, T=1))
+        w13_s = moe.moe_w4a8_prepack(*moe.moe_mxfp4_quantize(d16(sh.w13_s)), gate_up=True)
+        w2_s = moe.moe_w4a8_prepack(*moe.moe_mxfp4_quantize(d16(sh.w2_s)), gate_up=False)
+    torch.cuda.empty_cache()
+    ones = torch.ones(cfg.H, dtype=torch.bfloat16, device="cuda")
+    xc, xs, _, _ = moe.moe_add_rms_norm_mxfp8(t["x"], None, ones, 1e-6, with_fp32=False)
+    layer = moe.W4a8Layer(cfg.T, cfg.H, cfg.E, cfg.k, cfg.I, cfg.gate, cfg.routed_scaling_factor, cfg.eps,
+                          cfg.n_shared, cfg.I_s)
+    fw = dict(x_codes=xc, x_scales=xs, logits=t["logits"], w13=w13, w2=w2, bias=t["bias"], w13_s=w13_s, w2_s=w2_s)
+    for _ in range(W):
+        layer.forward(**fw)
+    torch.cuda.synchronize()
+    s0, s1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    s0.record()
+    for _ in range(K):
+        layer.forward(**fw)
+    s1.record()
+    torch.cuda.synchronize()
+    ms = s0.elapsed_time(s1) / K
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(6)] for _ in range(K)]
+    for i in range(K):
+        layer.forward_events(evs[i], **fw)
+    torch.cuda.synchronize()
+    st = moe.moe_get_device_status(layer.ws)
+    if st != moe.MOE_OK:
+        raise SystemExit(f"{cfg.name}: W4A8 layer device status: {moe.status_string(st)}")
+    names = ["gating", "init_routing_and_row_gather", "gemm_w13_swiglu_w4a8", "gemm_down_w4a8", "finalize"]
+    kern = {n: statistics.mean(evs[i][j].elapsed_time(evs[i][j + 1]) for i in range(K)) for j, n in enumerate(names)}
+    A = int((layer.counts.cpu() > 0).sum())
+    per_w = 0.5 + 1.0 / 32  # code + scale bytes per weight
+    n_units = A + (1 if cfg.n_shared else 0)
+    b1 = n_units * 2 * cfg.I * cfg.H * per_w
+    b2 = n_units * cfg.H * cfg.I * per_w
+    t1 = kern["gemm_w13_swiglu_w4a8"] * 1e-3
+    t2 = kern["gemm_down_w4a8"] * 1e-3
+    y = layer.y.float()
+    return {
+        "value": cfg.T / (ms * 1e-3), "unit": "tokens/s", "ms_per_step": ms, "kernels_ms": kern,
+        "gpu_launches": layer.launches * K,
+        "precision": "W4A8: MXFP8 hidden state and act (E4M3, E8M0 scale per 32), MXFP4 expert weights (E2M1, E8M0 "
+                     "scale per 32) quantised on the GPU from the bf16 weights; block-scaled tcgen05 MMA "
+                     "(kind::mxf8f6f4), fp32 accumulation",
+        "roofline": {"bound": "hbm", "kernel": "gemm_w13_swiglu_w4a8", "achieved": b1 / t1 / 1e9,
+                     "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": b1 / t1 / 1e9 / peaks["hbm_gbs"],
+                     "peak_source": f"{peak_src} (hbm_gbs)", "algorithmic_bytes_per_launch": b1,
+                     "per_unit": f"{2 * cfg.I * cfg.H} weights x {per_w} B per streamed expert (x {A} active"
+                                 + (" + the shared expert)" if cfg.n_shared else ")"),
+                     "traffic": _traffic(cfg.name, "gemm_w13_swiglu_w4a8", "grouped_gemm_w4a8.cu")},
+        "gemm_down_w4a8": {"achieved_gbs": b2 / t2 / 1e9, "frac": b2 / t2 / 1e9 / peaks["hbm_gbs"]},
+        "layer_hbm_frac_of_measured": (b1 + b2) / (ms * 1e-3) / 1e9 / peaks["hbm_gbs"],
+        "max_rel_diff_vs_bf16_layer": float((y - y_bf16).abs().max() / y_bf16.abs().max()),
+    }
+
+
 # ------------------------------------------------------------------ GB300 arm
 # the workloads measured beside the default one (hy3_decode and hy3_prefill share their weights)
 OTHER_WORKLOADS = ["tiny", "hy3_decode", "hy3_prefill", "long_prefill"]
+
+
+def _decode_sized(cfg):
+    """Decode-shaped problems (at most 32 token rows per expert on average, no more than 32 tokens for a
+    shared expert), the shapes the 4-bit layers' 32-column tiles are built for."""
+    return cfg.T * cfg.k <= 32 * cfg.E and cfg.T <= 64 and cfg.E >= 16
 
 
 def per_config_names(args):
@@ -718,9 +793,13 @@ def run_gb300(args, rank, world, local):
     y_bf16, t, inp = rec.pop("_y"), rec.pop("_t"), rec.pop("_inp")
 
     front = None if args.no_front_end else front_end(args, cfg, K, W, moe, mi, d16)
-    # the 4-bit-weight layer: decode-sized routed-only workloads (the 4-bit GEMMs walk 32 token columns)
+    # the W4A8 layer on decode-sized workloads (its GEMMs walk 32 token columns per tile)
+    w8 = None
+    if not args.no_mxfp4 and _decode_sized(cfg):
+        w8 = w4a8_leg(args, cfg, K, W, moe, mi, d16, t, peaks, src, y_bf16)
+    # the 4-bit-weight layer on f16 operands (routed experts only), on request
     w4 = None
-    if not args.no_mxfp4 and cfg.n_shared == 0 and cfg.T * cfg.k <= 32 * cfg.E:
+    if args.mxfp4_f16 and cfg.n_shared == 0 and _decode_sized(cfg):
         inp.w13 = mi.normal_bf16(cfg.seed, mi.TID_W13, (cfg.E, 2 * cfg.I, cfg.H), 0.0, cfg.w_std)
         w4 = mxfp4_leg(args, cfg, K, W, moe, inp, t, d16, peaks, src, y_bf16)
         inp.w13 = None
@@ -730,8 +809,11 @@ def run_gb300(args, rank, world, local):
     for name in per_config_names(args):
         c = mi.CONFIGS[name]
         r = measure(args, c, K, W, world, rank, local, moe, mi, d16, weights, peaks, src, dev_id)
-        for key in ("_y", "_t", "_inp"):
-            r.pop(key)
+        y_c, t_c = r.pop("_y"), r.pop("_t")
+        r.pop("_inp")
+        if not args.no_mxfp4 and _decode_sized(c):
+            r["w4a8"] = w4a8_leg(args, c, K, W, moe, mi, d16, t_c, peaks, src, y_c)
+        del y_c, t_c
         r["config"] = _config(c, world)
         others[name] = r
     weights.t = None
@@ -750,6 +832,8 @@ def run_gb300(args, rank, world, local):
         "config": _config(cfg, world),
     }
     line.update(rec)
+    if w8:
+        line["w4a8"] = w8
     if w4:
         line["mxfp4_weights"] = w4
     if front:

@@ -17,8 +17,11 @@
  * and around it: moe_add_rms_norm_cast / moe_add_rms_norm_mxfp8 and
  * moe_router_logits (the step before gating), moe_init_routing_range (routing
  * restricted to a local expert range), moe_prepack_w13 (one-time weight layout),
- * and the 4-bit-weight decode GEMMs (moe_mxfp4_quantize, moe_mxfp4_prepack,
- * moe_gather_rows_f16, moe_grouped_gemm_swiglu_mxfp4, moe_grouped_gemm_mxfp4).
+ * the 4-bit-weight decode GEMMs on f16 operands (moe_mxfp4_quantize,
+ * moe_mxfp4_prepack, moe_gather_rows_f16, moe_grouped_gemm_swiglu_mxfp4,
+ * moe_grouped_gemm_mxfp4) and the W4A8 path on the block-scaled MMA
+ * (moe_w4a8_prepack, moe_gather_rows_mx, moe_grouped_gemm_swiglu_w4a8,
+ * moe_grouped_gemm_w4a8, moe_layer_forward_w4a8).
  *
  * Sources (page titles and sections):
  *  [Q3]  "Qwen3-MoE low-latency inference practice on Atlas A3/950 clusters"
@@ -397,6 +400,81 @@ MOE_API int moe_grouped_gemm_mxfp4(const uint16_t* a16, const uint8_t* w_codes, 
                                    const float* w_omega, const int32_t* offsets, const float* topk_w,
                                    const int32_t* sorted_pair, int E, int M, int N, int K, uint16_t* out, void* ws,
                                    size_t ws_bytes, void* stream);
+
+/*
+ * W4A8: MXFP8 activations x MXFP4 expert weights on the block-scaled tensor-core MMA
+ * (tcgen05.mma kind::mxf8f6f4 with the E8M0 scale factors of both operands applied by the
+ * hardware).  [Q3] MoE EP section, "computation decomposition (AllGather scheme, W4A8)": the hidden
+ * state is quantised to MXFP8 (data + scale), routed, and the grouped matmuls run on it with MXFP4
+ * expert weights; [HY3] 5.2: on the quantised path the SwiGLU is fused with a group quantisation, so
+ * act enters the down projection as MXFP8 too.  Formats as above (MXFP8: E4M3 codes, E8M0 scale per
+ * 32 along K, the rule of moe_add_rms_norm_mxfp8; MXFP4: the codes and scales moe_mxfp4_quantize
+ * writes).  Products are exact; accumulation in fp32.
+ *
+ * Token-row scales inside this path are "padded scale rows": [rows, K/128, 16] bytes, per row and
+ * 128-K chunk the chunk's four E8M0 scales followed by twelve zero bytes.
+ *
+ * moe_w4a8_prepack: one-time layout.  codes [E,n_out,K/2] and scales [E,n_out,K/32] of MXFP4
+ *   weights -> codes_p [E*n_out,K/2] and sf_p [E*n_out/128][K/128][512] (E*n_out*K/32 bytes).
+ *   gate_up = 1 (w13, n_out = 2I, I % 128 == 0): packed row R of an expert is the gate (R % 32 < 16)
+ *   or up row of feature 128*(R/256) + 32*((R/32)%4) + 16*((R/128)%2) + R%16, so every 256-row tile
+ *   holds 128 whole features.  gate_up = 0: rows unchanged (n_out % 128 == 0).  sf_p: per 128-row
+ *   tile and 128-K chunk a 512-byte atom, byte (r%32)*16 + (r/32)*4 + b = the scale of tile row r,
+ *   block b of the chunk.  K % 128 == 0.  Not in place.  Local expert range [e0, e1): codes_p +
+ *   e0*n_out*K/2 and sf_p + e0*n_out*K/32.
+ *
+ * moe_gather_rows_mx: out_codes[pos] = x_codes[t], out_sf[pos] = the padded scale row of
+ *   x_scales[t], t = sorted_pair[pos] / k, for pos < M (x_codes [T,H], x_scales [T,H/32]; H % 128
+ *   == 0).  sorted_pair NULL: t = pos (M <= T), only out_sf written (out_codes may be NULL).  A
+ *   pair index outside [0, T*k) skips its row and raises MOE_ERR_DEVICE_CHECK in ws's status word.
+ *
+ * moe_grouped_gemm_swiglu_w4a8: act = SiLU(g) * u of (g, u) = row(pos) . w13[e]^T in fp32, then
+ *   MXFP8 along I: act [M,I] E4M3 codes and act_sf [M,I/128,16] padded scale rows (block scale
+ *   2^(floor(log2 amax) - 8), E4M3 nearest-even, saturating at 448).  x [M,H] E4M3 codes in
+ *   expert-sorted order with x_sf [M,H/128,16]; w13 prepacked with gate_up = 1.  H % 128 == 0,
+ *   I % 128 == 0.  Rows >= offsets[E] untouched.
+ * moe_grouped_gemm_w4a8: out [M,N] bf16 = topk_w[sorted_pair[pos]] (optional) *
+ *   (a[pos] . w[e]^T), a [M,K] E4M3 with a_sf [M,K/128,16], w prepacked with gate_up = 0;
+ *   N % 128 == 0, K % 128 == 0.
+ * Both walk 32 token columns per tile (a decode-shaped instance; correct for any M).  ws: at least
+ * moe_grouped_gemm_workspace_size() bytes.
+ *
+ * moe_layer_forward_w4a8: the whole layer a1 -> a6 on MXFP8 x (x_codes [T,H], x_scales [T,H/32],
+ *   e.g. from moe_add_rms_norm_mxfp8): gating, routing, the MXFP8 row gather, the W4A8 gate/up GEMM
+ *   (+ the shared expert as one more segment, act_s in MXFP8 as well), the W4A8 down GEMM
+ *   (+ shared), finalize; y [T,H] bf16.  Weights prepacked by moe_w4a8_prepack (w13 with gate_up = 1,
+ *   w2 with 0; the shared expert's likewise with E = 1, or all four NULL when d->n_shared == 0).
+ *   H, I, I_s multiples of 128.  ws: moe_w4a8_layer_workspace_size(d) bytes.
+ *   moe_layer_forward_w4a8_events records six caller events as moe_layer_forward_events does (before
+ *   gating, routing, the gate/up GEMM (after the row gather), the down GEMM, finalize; after it).
+ *   moe_w4a8_layer_kernel_launches: kernels per call.
+ */
+MOE_API int moe_w4a8_prepack(const uint8_t* codes, const uint8_t* scales, int E, int n_out, int K, int gate_up,
+                             uint8_t* codes_p, uint8_t* sf_p, void* stream);
+MOE_API int moe_gather_rows_mx(const uint8_t* x_codes, const uint8_t* x_scales, const int32_t* sorted_pair, int T,
+                               int k, int H, int M, uint8_t* out_codes, uint8_t* out_sf, void* ws, size_t ws_bytes,
+                               void* stream);
+MOE_API int moe_grouped_gemm_swiglu_w4a8(const uint8_t* x, const uint8_t* x_sf, const uint8_t* w13_codes,
+                                         const uint8_t* w13_sf, const int32_t* offsets, int E, int M, int H, int I,
+                                         uint8_t* act, uint8_t* act_sf, void* ws, size_t ws_bytes, void* stream);
+MOE_API int moe_grouped_gemm_w4a8(const uint8_t* a, const uint8_t* a_sf, const uint8_t* w_codes, const uint8_t* w_sf,
+                                  const int32_t* offsets, const float* topk_w, const int32_t* sorted_pair, int E,
+                                  int M, int N, int K, uint16_t* out, void* ws, size_t ws_bytes, void* stream);
+MOE_API size_t moe_w4a8_layer_workspace_size(const moe_layer_desc* d);
+MOE_API int moe_layer_forward_w4a8(const moe_layer_desc* d, const uint8_t* x_codes, const uint8_t* x_scales,
+                                   const float* logits, const float* bias, const uint8_t* w13_codes,
+                                   const uint8_t* w13_sf, const uint8_t* w2_codes, const uint8_t* w2_sf,
+                                   const uint8_t* w13s_codes, const uint8_t* w13s_sf, const uint8_t* w2s_codes,
+                                   const uint8_t* w2s_sf, uint16_t* y, float* topk_w, int32_t* topk_idx,
+                                   int32_t* counts, void* ws, size_t ws_bytes, void* stream);
+MOE_API int moe_layer_forward_w4a8_events(const moe_layer_desc* d, const uint8_t* x_codes, const uint8_t* x_scales,
+                                          const float* logits, const float* bias, const uint8_t* w13_codes,
+                                          const uint8_t* w13_sf, const uint8_t* w2_codes, const uint8_t* w2_sf,
+                                          const uint8_t* w13s_codes, const uint8_t* w13s_sf,
+                                          const uint8_t* w2s_codes, const uint8_t* w2s_sf, uint16_t* y,
+                                          float* topk_w, int32_t* topk_idx, int32_t* counts, void* ws,
+                                          size_t ws_bytes, void* stream, void* const* events, int n_events);
+MOE_API int moe_w4a8_layer_kernel_launches(const moe_layer_desc* d);
 
 /*
  * a6. Finalize-routing.  [Q3] "GMM enablement and routing optimisation"

@@ -84,6 +84,23 @@ _SIGS = {
                                               ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int,
                                               ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_void_p,
                                               ctypes.c_void_p, ctypes.c_size_t, ctypes.c_void_p]),
+    "moe_w4a8_prepack": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                                        ctypes.c_int, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p]),
+    "moe_gather_rows_mx": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int,
+                                          ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_void_p, ctypes.c_void_p,
+                                          ctypes.c_void_p, ctypes.c_size_t, ctypes.c_void_p]),
+    "moe_grouped_gemm_swiglu_w4a8": (ctypes.c_int, [ctypes.c_void_p] * 5 + [ctypes.c_int] * 4 +
+                                     [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_size_t,
+                                      ctypes.c_void_p]),
+    "moe_grouped_gemm_w4a8": (ctypes.c_int, [ctypes.c_void_p] * 7 + [ctypes.c_int] * 4 +
+                              [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_size_t, ctypes.c_void_p]),
+    "moe_w4a8_layer_workspace_size": (ctypes.c_size_t, [ctypes.POINTER(moe_layer_desc)]),
+    "moe_layer_forward_w4a8": (ctypes.c_int, [ctypes.POINTER(moe_layer_desc)] + [ctypes.c_void_p] * 17 +
+                               [ctypes.c_size_t, ctypes.c_void_p]),
+    "moe_layer_forward_w4a8_events": (ctypes.c_int, [ctypes.POINTER(moe_layer_desc)] + [ctypes.c_void_p] * 17 +
+                                      [ctypes.c_size_t, ctypes.c_void_p, ctypes.POINTER(ctypes.c_void_p),
+                                       ctypes.c_int]),
+    "moe_w4a8_layer_kernel_launches": (ctypes.c_int, [ctypes.POINTER(moe_layer_desc)]),
     "moe_debug_set": (ctypes.c_int, [ctypes.c_int, ctypes.c_ulonglong]),
     "moe_add_rms_norm_cast": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int,
                                              ctypes.c_int, ctypes.c_float, ctypes.c_void_p, ctypes.c_void_p,
@@ -497,6 +514,130 @@ class Mxfp4Layer:
         ev(3)
         moe_finalize_routing(self.y_perm, r["pair_pos"], self.T, self.k, y=self.y, stream=s)
         ev(4)
+        return self.y
+
+
+# ------------------------------------------------------------------ W4A8: MXFP8 x MXFP4 on the block-scaled MMA
+class W4a8Weights(NamedTuple):
+    """Expert weights [E, n_out, K] in the layout of moe_w4a8_prepack."""
+    codes: object    # [E*n_out, K/2] uint8 E2M1 codes (gate/up rows regrouped when packed for w13)
+    sf: object       # [E*n_out/128, K/128, 512] uint8 scale atoms
+    E: int
+    n_out: int
+    K: int
+
+    def experts(self, e0: int, e1: int) -> "W4a8Weights":
+        """The local experts [e0, e1) as views (every expert owns whole 128-row tiles)."""
+        if not 0 <= e0 < e1 <= self.E:
+            raise ValueError(f"expert range [{e0}, {e1}) outside [0, {self.E})")
+        r0, r1 = e0 * self.n_out, e1 * self.n_out
+        return W4a8Weights(self.codes[r0:r1], self.sf[r0 // 128:r1 // 128], e1 - e0, self.n_out, self.K)
+
+
+def moe_w4a8_prepack(codes, scales, gate_up: bool, stream=None) -> W4a8Weights:
+    """codes [E,n_out,K/2], scales [E,n_out,K/32] (moe_mxfp4_quantize) -> the W4A8 GEMMs' layout."""
+    torch = _torch()
+    if codes.dim() == 2:
+        codes, scales = codes.unsqueeze(0), scales.unsqueeze(0)
+    E, n_out, K2 = codes.shape
+    K = 2 * K2
+    dev = codes.device
+    cp = torch.empty((E * n_out, K2), dtype=torch.uint8, device=dev)
+    sf = torch.empty((E * n_out // 128, K // 128, 512), dtype=torch.uint8, device=dev)
+    _check(lib().moe_w4a8_prepack(_ptr(codes), _ptr(scales), E, n_out, K, int(bool(gate_up)), _ptr(cp), _ptr(sf),
+                                  _stream(stream)), "moe_w4a8_prepack")
+    return W4a8Weights(cp, sf, E, n_out, K)
+
+
+def moe_gather_rows_mx(x_codes, x_scales, sorted_pair=None, k: int = 1, M: Optional[int] = None, out_codes=None,
+                       out_sf=None, ws=None, stream=None):
+    """(out_codes [M,H] E4M3, out_sf [M,H/128,16] padded scale rows) of rows x[sorted_pair[pos] // k]
+    (sorted_pair None: the first M token rows, scale rows only)."""
+    torch = _torch()
+    T, H = x_codes.shape
+    if M is None:
+        M = sorted_pair.numel() if sorted_pair is not None else T
+    dev = x_codes.device
+    if out_codes is None and sorted_pair is not None:
+        out_codes = torch.empty((M, H), dtype=torch.uint8, device=dev)
+    if out_sf is None:
+        out_sf = torch.empty((M, H // 128, 16), dtype=torch.uint8, device=dev)
+    ws = _ws(lib().moe_grouped_gemm_workspace_size(), dev, ws)
+    _check(lib().moe_gather_rows_mx(_ptr(x_codes), _ptr(x_scales), _ptr(sorted_pair), T, k, H, M, _ptr(out_codes),
+                                    _ptr(out_sf), _ptr(ws), ws.numel(), _stream(stream)), "moe_gather_rows_mx")
+    return out_codes, out_sf
+
+
+def moe_grouped_gemm_swiglu_w4a8(x, x_sf, w13: W4a8Weights, offsets, act=None, act_sf=None, ws=None, stream=None):
+    """a3 in W4A8: (act [M,I] E4M3, act_sf [M,I/128,16]) = MXFP8(SwiGLU(x . w13[e]^T))."""
+    torch = _torch()
+    M, H = x.shape
+    I = w13.n_out // 2
+    if act is None:
+        act = torch.empty((M, I), dtype=torch.uint8, device=x.device)
+    if act_sf is None:
+        act_sf = torch.empty((M, I // 128, 16), dtype=torch.uint8, device=x.device)
+    ws = _ws(lib().moe_grouped_gemm_workspace_size(), x.device, ws)
+    _check(lib().moe_grouped_gemm_swiglu_w4a8(_ptr(x), _ptr(x_sf), _ptr(w13.codes), _ptr(w13.sf), _ptr(offsets),
+                                              w13.E, M, H, I, _ptr(act), _ptr(act_sf), _ptr(ws), ws.numel(),
+                                              _stream(stream)), "moe_grouped_gemm_swiglu_w4a8")
+    return act, act_sf
+
+
+def moe_grouped_gemm_w4a8(a, a_sf, w: W4a8Weights, offsets, topk_w=None, sorted_pair=None, out=None, ws=None,
+                          stream=None):
+    """a4 in W4A8: out [M,N] bf16 = scale * (a . w[e]^T)."""
+    torch = _torch()
+    M, K = a.shape
+    if out is None:
+        out = torch.empty((M, w.n_out), dtype=torch.bfloat16, device=a.device)
+    ws = _ws(lib().moe_grouped_gemm_workspace_size(), a.device, ws)
+    _check(lib().moe_grouped_gemm_w4a8(_ptr(a), _ptr(a_sf), _ptr(w.codes), _ptr(w.sf), _ptr(offsets), _ptr(topk_w),
+                                       _ptr(sorted_pair), w.E, M, w.n_out, K, _ptr(out), _ptr(ws), ws.numel(),
+                                       _stream(stream)), "moe_grouped_gemm_w4a8")
+    return out
+
+
+class W4a8Layer:
+    """One W4A8 layer shape (moe_layer_forward_w4a8) with its own workspace and output buffers."""
+
+    def __init__(self, T, H, E, k, I, gate="softmax", routed_scaling_factor=1.0, eps=1e-20, n_shared=0, I_s=0,
+                 device="cuda"):
+        torch = _torch()
+        self.desc = make_desc(T, H, E, k, I, gate, routed_scaling_factor, eps, n_shared, I_s)
+        n = lib().moe_w4a8_layer_workspace_size(ctypes.byref(self.desc))
+        if n == 0:
+            raise MoEError(MOE_ERR_UNSUPPORTED, "moe_w4a8_layer_workspace_size")
+        self.ws = torch.zeros(n, dtype=torch.uint8, device=device)
+        self.y = torch.empty((T, H), dtype=torch.bfloat16, device=device)
+        self.topk_w = torch.empty((T, k), dtype=torch.float32, device=device)
+        self.topk_idx = torch.empty((T, k), dtype=torch.int32, device=device)
+        self.counts = torch.empty(E, dtype=torch.int32, device=device)
+        self.launches = lib().moe_w4a8_layer_kernel_launches(ctypes.byref(self.desc))
+
+    def _args(self, x_codes, x_scales, logits, w13, w2, bias, w13_s, w2_s):
+        return [_ptr(x_codes), _ptr(x_scales), _ptr(logits), _ptr(bias), _ptr(w13.codes), _ptr(w13.sf),
+                _ptr(w2.codes), _ptr(w2.sf), _ptr(w13_s.codes) if w13_s else None, _ptr(w13_s.sf) if w13_s else None,
+                _ptr(w2_s.codes) if w2_s else None, _ptr(w2_s.sf) if w2_s else None, _ptr(self.y),
+                _ptr(self.topk_w), _ptr(self.topk_idx), _ptr(self.counts), _ptr(self.ws), self.ws.numel()]
+
+    def forward(self, x_codes, x_scales, logits, w13: W4a8Weights, w2: W4a8Weights, bias=None, w13_s=None,
+                w2_s=None, stream=None):
+        _check(lib().moe_layer_forward_w4a8(ctypes.byref(self.desc),
+                                            *self._args(x_codes, x_scales, logits, w13, w2, bias, w13_s, w2_s),
+                                            _stream(stream)), "moe_layer_forward_w4a8")
+        return self.y
+
+    def forward_events(self, events, x_codes, x_scales, logits, w13, w2, bias=None, w13_s=None, w2_s=None,
+                       stream=None):
+        handles = (ctypes.c_void_p * 6)()
+        for i, ev in enumerate(events):
+            if ev.cuda_event == 0:
+                ev.record()
+            handles[i] = ev.cuda_event
+        _check(lib().moe_layer_forward_w4a8_events(ctypes.byref(self.desc),
+                                                   *self._args(x_codes, x_scales, logits, w13, w2, bias, w13_s, w2_s),
+                                                   _stream(stream), handles, 6), "moe_layer_forward_w4a8_events")
         return self.y
 
 

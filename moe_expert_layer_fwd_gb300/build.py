@@ -20,7 +20,7 @@ ROOT = os.path.dirname(HERE)
 CSRC = os.path.join(HERE, "csrc")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libmoe_gb300.so")
-SOURCES = ["gating.cu", "routing.cu", "routing_static.cu", "grouped_gemm.cu", "grouped_gemm_mxfp4.cu",
+SOURCES = ["gating.cu", "routing.cu", "routing_static.cu", "grouped_gemm.cu", "grouped_gemm_mxfp4.cu", "grouped_gemm_w4a8.cu",
            "finalize.cu", "frontend.cu", "api.cu"]
 HEADERS = ["moe_common.cuh", "moe_internal.h"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]

@@ -426,6 +426,86 @@ int moe_grouped_gemm_mxfp4(const uint16_t* a16, const uint8_t* w_codes, const ui
                     stream);
 }
 
+// ---------------------------------------------------------------- W4A8 (MXFP8 x MXFP4, block-scaled MMA)
+int moe_w4a8_prepack(const uint8_t* codes, const uint8_t* scales, int E, int n_out, int K, int gate_up,
+                     uint8_t* codes_p, uint8_t* sf_p, void* stream) {
+  if (E < 1 || n_out <= 0 || K <= 0) return MOE_ERR_INVALID_ARG;
+  if (n_out % (gate_up ? 256 : 128) != 0 || K % 128 != 0 || (long long)E * n_out * K >= (1LL << 40))
+    return MOE_ERR_UNSUPPORTED;
+  if (!codes || !scales || !codes_p || !sf_p || codes == codes_p) return MOE_ERR_INVALID_ARG;
+  if (!aligned16(codes) || !aligned16(codes_p) || !aligned16(sf_p)) return MOE_ERR_INVALID_ARG;
+  return cuda_status(moe::launch_w4a8_prepack(codes, scales, E, n_out, K, gate_up ? 1 : 0, codes_p, sf_p,
+                                              as_stream(stream)));
+}
+
+int moe_gather_rows_mx(const uint8_t* x_codes, const uint8_t* x_scales, const int32_t* sorted_pair, int T, int k,
+                       int H, int M, uint8_t* out_codes, uint8_t* out_sf, void* ws, size_t ws_bytes, void* stream) {
+  if (T < 0 || k < 1 || M < 0 || H <= 0) return MOE_ERR_INVALID_ARG;
+  if (H % 128 != 0 || (long long)T * k >= (1LL << 31) || (long long)M * H >= (1LL << 40)) return MOE_ERR_UNSUPPORTED;
+  if (!ws || ws_bytes < kHeader || !aligned16(ws)) return MOE_ERR_WORKSPACE;
+  if (!sorted_pair && M > T) return MOE_ERR_INVALID_ARG;  // identity rows: at most the T token rows
+  if (M == 0) return MOE_OK;
+  if (!x_codes || !x_scales || !out_sf || (sorted_pair && !out_codes)) return MOE_ERR_INVALID_ARG;
+  if (!aligned16(x_codes) || !aligned16(out_sf) || (out_codes && !aligned16(out_codes)) ||
+      (reinterpret_cast<uintptr_t>(x_scales) & 3u))
+    return MOE_ERR_INVALID_ARG;
+  return cuda_status(moe::launch_gather_rows_mx(x_codes, x_scales, sorted_pair, M, k, T, H,
+                                                sorted_pair ? out_codes : nullptr, out_sf, nullptr, status_word(ws),
+                                                as_stream(stream)));
+}
+
+namespace {
+int w4a8_gemm(int mode, const uint8_t* a, const uint8_t* a_sf, const uint8_t* codes, const uint8_t* sf,
+              const int32_t* offsets, const float* topk_w, const int32_t* sorted_pair, int E, int M, int n_out, int K,
+              uint8_t* act, uint8_t* act_sf, uint16_t* out, void* ws, size_t ws_bytes, void* stream) {
+  if (E < 1 || M < 0 || n_out <= 0 || K <= 0) return MOE_ERR_INVALID_ARG;
+  if (E > 1024) return MOE_ERR_UNSUPPORTED;
+  if (K % 128 != 0 || n_out % (mode == 0 ? 256 : 128) != 0) return MOE_ERR_UNSUPPORTED;
+  if ((long long)M * (n_out > K ? n_out : K) >= (1LL << 40)) return MOE_ERR_UNSUPPORTED;
+  if ((topk_w == nullptr) != (sorted_pair == nullptr)) return MOE_ERR_INVALID_ARG;
+  if (!codes || !sf || !offsets || !ws) return MOE_ERR_INVALID_ARG;
+  if (ws_bytes < kHeader) return MOE_ERR_WORKSPACE;
+  if (M == 0) return MOE_OK;
+  if (!a || !a_sf || (mode == 0 && (!act || !act_sf)) || (mode == 1 && !out)) return MOE_ERR_INVALID_ARG;
+  const void* ptrs[] = {a, a_sf, codes, sf, offsets, ws, act, act_sf, out, topk_w, sorted_pair};
+  for (const void* p : ptrs)
+    if (p && !aligned16(p)) return MOE_ERR_INVALID_ARG;
+  moe::W4a8GemmProblem p{};
+  p.mode = mode;
+  p.a_rows = a;
+  p.a_sf = a_sf;
+  p.codes = codes;
+  p.sf = sf;
+  p.offsets = offsets;
+  p.E = E;
+  p.M = M;
+  p.K = K;
+  p.n_out = n_out;
+  p.act = act;
+  p.act_sf = act_sf;
+  p.out = out;
+  p.topk_w = topk_w;
+  p.sorted_pair = sorted_pair;
+  p.status = status_word(ws);
+  return cuda_status(moe::launch_grouped_gemm_w4a8(p, as_stream(stream)));
+}
+}  // namespace
+
+int moe_grouped_gemm_swiglu_w4a8(const uint8_t* x, const uint8_t* x_sf, const uint8_t* w13_codes,
+                                 const uint8_t* w13_sf, const int32_t* offsets, int E, int M, int H, int I,
+                                 uint8_t* act, uint8_t* act_sf, void* ws, size_t ws_bytes, void* stream) {
+  if (I <= 0) return MOE_ERR_INVALID_ARG;
+  return w4a8_gemm(0, x, x_sf, w13_codes, w13_sf, offsets, nullptr, nullptr, E, M, 2 * I, H, act, act_sf, nullptr, ws,
+                   ws_bytes, stream);
+}
+
+int moe_grouped_gemm_w4a8(const uint8_t* a, const uint8_t* a_sf, const uint8_t* w_codes, const uint8_t* w_sf,
+                          const int32_t* offsets, const float* topk_w, const int32_t* sorted_pair, int E, int M, int N,
+                          int K, uint16_t* out, void* ws, size_t ws_bytes, void* stream) {
+  return w4a8_gemm(1, a, a_sf, w_codes, w_sf, offsets, topk_w, sorted_pair, E, M, N, K, nullptr, nullptr, out, ws,
+                   ws_bytes, stream);
+}
+
 int moe_finalize_routing(const uint16_t* y_perm, const int32_t* pair_pos, const uint16_t* shared, int T, int k,
                          int H, uint16_t* y, void* stream) {
   if (T < 0 || k < 1 || H <= 0) return MOE_ERR_INVALID_ARG;
@@ -619,6 +699,223 @@ int moe_layer_kernel_launches(const moe_layer_desc* d) {
   const bool sh = d->n_shared > 0;
   const bool gather_kernel = !moe::grouped_gemm_gathers_inline(d->T * d->k, d->E, sh, d->T);
   return 7 + (gather_kernel ? 1 : 0) + ((sh && d->I_s != d->I) ? 1 : 0);
+}
+
+}  // extern "C"
+
+namespace {
+
+// Layout of the moe_layer_forward_w4a8 workspace.
+struct W8Ws {
+  size_t offsets, scratch, sorted_pair, pair_pos, x8, x8_sf, act, act_sf, y_perm, x_sf_tok, act_s, act_sf_s, shared,
+      total;
+};
+
+W8Ws w8_ws(const moe_layer_desc* d) {
+  W8Ws w{};
+  const size_t P = (size_t)d->T * d->k, T = (size_t)d->T, H = (size_t)d->H, I = (size_t)d->I;
+  const bool sh = d->n_shared > 0;
+  const size_t Is = sh ? (size_t)d->I_s : 0;
+  size_t o = kHeader;
+  w.offsets = o;     o = align_up(o + (size_t)(d->E + 1) * 4);
+  w.scratch = o;     o = align_up(o + moe::routing_scratch_bytes((int)P, d->E));
+  w.sorted_pair = o; o = align_up(o + P * 4);
+  w.pair_pos = o;    o = align_up(o + P * 4);
+  w.x8 = o;          o = align_up(o + P * H);
+  w.x8_sf = o;       o = align_up(o + P * (H / 128) * 16);
+  w.act = o;         o = align_up(o + P * I);
+  w.act_sf = o;      o = align_up(o + P * (I / 128) * 16);
+  w.y_perm = o;      o = align_up(o + P * H * 2);
+  w.x_sf_tok = o;    o = align_up(o + (sh ? T * (H / 128) * 16 : 0));
+  w.act_s = o;       o = align_up(o + T * Is);
+  w.act_sf_s = o;    o = align_up(o + T * (Is / 128) * 16);
+  w.shared = o;      o = align_up(o + (sh ? T * H * 2 : 0));
+  w.total = o;
+  return w;
+}
+
+int check_desc_w4a8(const moe_layer_desc* d) {
+  int s = check_desc(d);
+  if (s) return s;
+  if (d->H % 128 != 0 || d->I % 128 != 0 || (d->n_shared && d->I_s % 128 != 0)) return MOE_ERR_UNSUPPORTED;
+  return MOE_OK;
+}
+
+int layer_forward_w4a8_impl(const moe_layer_desc* d, const uint8_t* x_codes, const uint8_t* x_scales,
+                            const float* logits, const float* bias, const uint8_t* w13_codes, const uint8_t* w13_sf,
+                            const uint8_t* w2_codes, const uint8_t* w2_sf, const uint8_t* w13s_codes,
+                            const uint8_t* w13s_sf, const uint8_t* w2s_codes, const uint8_t* w2s_sf, uint16_t* y,
+                            float* topk_w, int32_t* topk_idx, int32_t* counts, void* ws, size_t ws_bytes,
+                            void* stream, void* const* events) {
+  int s = check_desc_w4a8(d);
+  if (s) return s;
+  if (d->gate == MOE_GATE_SOFTMAX && bias) return MOE_ERR_INVALID_ARG;
+  if (!ws || !counts) return MOE_ERR_INVALID_ARG;
+  const W8Ws L = w8_ws(d);
+  if (ws_bytes < L.total) return MOE_ERR_WORKSPACE;
+  if (d->T == 0) return MOE_OK;
+  if (!x_codes || !x_scales || !logits || !w13_codes || !w13_sf || !w2_codes || !w2_sf || !y || !topk_w || !topk_idx)
+    return MOE_ERR_INVALID_ARG;
+  const bool sh = d->n_shared > 0;
+  if (sh && (!w13s_codes || !w13s_sf || !w2s_codes || !w2s_sf)) return MOE_ERR_INVALID_ARG;
+  const void* ptrs[] = {x_codes, logits, w13_codes, w13_sf, w2_codes, w2_sf, y, topk_w, topk_idx, counts, ws,
+                        bias, w13s_codes, w13s_sf, w2s_codes, w2s_sf};
+  for (const void* p : ptrs)
+    if (p && !aligned16(p)) return MOE_ERR_INVALID_ARG;
+  if (reinterpret_cast<uintptr_t>(x_scales) & 3u) return MOE_ERR_INVALID_ARG;
+
+  cudaStream_t st = as_stream(stream);
+  char* base = static_cast<char*>(ws);
+  unsigned* status = status_word(ws);
+  int32_t* offsets = reinterpret_cast<int32_t*>(base + L.offsets);
+  int32_t* scratch = reinterpret_cast<int32_t*>(base + L.scratch);
+  int32_t* sorted_pair = reinterpret_cast<int32_t*>(base + L.sorted_pair);
+  int32_t* pair_pos = reinterpret_cast<int32_t*>(base + L.pair_pos);
+  uint8_t* x8 = reinterpret_cast<uint8_t*>(base + L.x8);
+  uint8_t* x8_sf = reinterpret_cast<uint8_t*>(base + L.x8_sf);
+  uint8_t* act = reinterpret_cast<uint8_t*>(base + L.act);
+  uint8_t* act_sf = reinterpret_cast<uint8_t*>(base + L.act_sf);
+  uint16_t* y_perm = reinterpret_cast<uint16_t*>(base + L.y_perm);
+  uint8_t* x_sf_tok = reinterpret_cast<uint8_t*>(base + L.x_sf_tok);
+  uint8_t* act_s = reinterpret_cast<uint8_t*>(base + L.act_s);
+  uint8_t* act_sf_s = reinterpret_cast<uint8_t*>(base + L.act_sf_s);
+  uint16_t* shared = reinterpret_cast<uint16_t*>(base + L.shared);
+  const int T = d->T, E = d->E, k = d->k, H = d->H, I = d->I, P = T * k;
+
+  auto mark = [&](int i) {
+    return events ? cudaEventRecord(reinterpret_cast<cudaEvent_t>(events[i]), st) : cudaSuccess;
+  };
+  constexpr bool kPdl = true;
+  if (mark(0) != cudaSuccess) return MOE_ERR_CUDA;
+  if (moe::launch_gating_topk(logits, bias, T, E, k, d->gate, d->routed_scaling_factor, d->eps, topk_w, topk_idx,
+                              st) != cudaSuccess)
+    return MOE_ERR_CUDA;
+  if (mark(1) != cudaSuccess) return MOE_ERR_CUDA;
+  if (moe::launch_init_routing(topk_idx, P, E, k, nullptr, H, nullptr, counts, offsets, sorted_pair, pair_pos,
+                               scratch, status, st, kPdl) != cudaSuccess)
+    return MOE_ERR_CUDA;
+  // the routed MXFP8 rows in expert order, and (shared expert) the padded scale rows of x itself
+  if (moe::launch_gather_rows_mx(x_codes, x_scales, sorted_pair, P, k, T, H, x8, x8_sf, nullptr, status, st,
+                                 kPdl) != cudaSuccess)
+    return MOE_ERR_CUDA;
+  if (sh && moe::launch_gather_rows_mx(x_codes, x_scales, nullptr, T, 1, T, H, nullptr, x_sf_tok, nullptr, status,
+                                       st, kPdl) != cudaSuccess)
+    return MOE_ERR_CUDA;
+  if (mark(2) != cudaSuccess) return MOE_ERR_CUDA;
+  moe::W4a8GemmProblem g1{};
+  g1.mode = 0;
+  g1.a_rows = x8;
+  g1.a_sf = x8_sf;
+  g1.codes = w13_codes;
+  g1.sf = w13_sf;
+  g1.offsets = offsets;
+  g1.E = E;
+  g1.M = P;
+  g1.K = H;
+  g1.n_out = 2 * I;
+  g1.act = act;
+  g1.act_sf = act_sf;
+  if (sh) {
+    g1.s_rows = x_codes;
+    g1.s_rows_sf = x_sf_tok;
+    g1.s_codes = w13s_codes;
+    g1.s_sf = w13s_sf;
+    g1.T_s = T;
+    g1.n_out_s = 2 * d->I_s;
+    g1.s_act = act_s;
+    g1.s_act_sf = act_sf_s;
+  }
+  g1.status = status;
+  if (moe::launch_grouped_gemm_w4a8(g1, st, kPdl) != cudaSuccess) return MOE_ERR_CUDA;
+  if (mark(3) != cudaSuccess) return MOE_ERR_CUDA;
+  // the down projection's K is I for routed experts and I_s for the shared one: one launch covers
+  // both only when they agree
+  moe::W4a8GemmProblem g2{};
+  g2.mode = 1;
+  g2.a_rows = act;
+  g2.a_sf = act_sf;
+  g2.codes = w2_codes;
+  g2.sf = w2_sf;
+  g2.offsets = offsets;
+  g2.E = E;
+  g2.M = P;
+  g2.K = I;
+  g2.n_out = H;
+  g2.out = y_perm;
+  g2.topk_w = topk_w;
+  g2.sorted_pair = sorted_pair;
+  g2.status = status;
+  moe::W4a8GemmProblem g2s{};
+  const bool fused_shared = sh && d->I_s == I;
+  if (sh) {
+    moe::W4a8GemmProblem& gs = fused_shared ? g2 : g2s;
+    gs.s_rows = act_s;
+    gs.s_rows_sf = act_sf_s;
+    gs.s_codes = w2s_codes;
+    gs.s_sf = w2s_sf;
+    gs.T_s = T;
+    gs.n_out_s = H;
+    gs.s_out = shared;
+  }
+  if (moe::launch_grouped_gemm_w4a8(g2, st, kPdl) != cudaSuccess) return MOE_ERR_CUDA;
+  if (sh && !fused_shared) {
+    g2s.mode = 1;
+    g2s.codes = w2s_codes;
+    g2s.sf = w2s_sf;
+    g2s.E = 1;
+    g2s.M = 0;
+    g2s.K = d->I_s;
+    g2s.n_out = H;
+    g2s.status = status;
+    if (moe::launch_grouped_gemm_w4a8(g2s, st, kPdl) != cudaSuccess) return MOE_ERR_CUDA;
+  }
+  if (mark(4) != cudaSuccess) return MOE_ERR_CUDA;
+  if (moe::launch_finalize(y_perm, pair_pos, sh ? shared : nullptr, T, k, H, y, st, kPdl) != cudaSuccess)
+    return MOE_ERR_CUDA;
+  return cuda_status(mark(5));
+}
+
+}  // namespace
+
+extern "C" {
+
+size_t moe_w4a8_layer_workspace_size(const moe_layer_desc* d) {
+  if (check_desc_w4a8(d)) return 0;
+  return w8_ws(d).total;
+}
+
+int moe_layer_forward_w4a8(const moe_layer_desc* d, const uint8_t* x_codes, const uint8_t* x_scales,
+                           const float* logits, const float* bias, const uint8_t* w13_codes, const uint8_t* w13_sf,
+                           const uint8_t* w2_codes, const uint8_t* w2_sf, const uint8_t* w13s_codes,
+                           const uint8_t* w13s_sf, const uint8_t* w2s_codes, const uint8_t* w2s_sf, uint16_t* y,
+                           float* topk_w, int32_t* topk_idx, int32_t* counts, void* ws, size_t ws_bytes,
+                           void* stream) {
+  return layer_forward_w4a8_impl(d, x_codes, x_scales, logits, bias, w13_codes, w13_sf, w2_codes, w2_sf, w13s_codes,
+                                 w13s_sf, w2s_codes, w2s_sf, y, topk_w, topk_idx, counts, ws, ws_bytes, stream,
+                                 nullptr);
+}
+
+int moe_layer_forward_w4a8_events(const moe_layer_desc* d, const uint8_t* x_codes, const uint8_t* x_scales,
+                                  const float* logits, const float* bias, const uint8_t* w13_codes,
+                                  const uint8_t* w13_sf, const uint8_t* w2_codes, const uint8_t* w2_sf,
+                                  const uint8_t* w13s_codes, const uint8_t* w13s_sf, const uint8_t* w2s_codes,
+                                  const uint8_t* w2s_sf, uint16_t* y, float* topk_w, int32_t* topk_idx,
+                                  int32_t* counts, void* ws, size_t ws_bytes, void* stream, void* const* events,
+                                  int n_events) {
+  if (!events || n_events != 6) return MOE_ERR_INVALID_ARG;
+  for (int i = 0; i < 6; ++i)
+    if (!events[i]) return MOE_ERR_INVALID_ARG;
+  return layer_forward_w4a8_impl(d, x_codes, x_scales, logits, bias, w13_codes, w13_sf, w2_codes, w2_sf, w13s_codes,
+                                 w13s_sf, w2s_codes, w2s_sf, y, topk_w, topk_idx, counts, ws, ws_bytes, stream,
+                                 events);
+}
+
+int moe_w4a8_layer_kernel_launches(const moe_layer_desc* d) {
+  if (check_desc_w4a8(d) || d->T == 0) return 0;
+  // gating 1 + routing 3 + MXFP8 row gather 1 (+1 for the shared expert's scale rows) + gate/up GEMM 1
+  // + down GEMM 1 (+1 when I_s != I) + finalize 1
+  const bool sh = d->n_shared > 0;
+  return 8 + (sh ? 1 : 0) + ((sh && d->I_s != d->I) ? 1 : 0);
 }
 
 }  // extern "C"

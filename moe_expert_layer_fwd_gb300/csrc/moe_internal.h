@@ -113,4 +113,40 @@ cudaError_t launch_mxfp4_prepack(const uint8_t* codes, const uint8_t* scales, in
 cudaError_t launch_gather_rows_f16(const uint16_t* x, const int32_t* sorted_pair, int M, int k, int T, int H,
                                    uint16_t* out, unsigned* status, cudaStream_t stream, bool pdl = false);
 
+// W4A8: MXFP8 token rows x MXFP4 expert weights on the block-scaled MMA.  Token rows: E4M3 codes
+// [rows, K] with padded scale rows [rows, K/128, 16] (four E8M0 scales, twelve zero bytes).  Weights
+// prepacked by launch_w4a8_prepack.  Mode 0: act codes [M, n_out/2] + padded scale rows; mode 1: bf16
+// out [M, n_out] times the routing weight.  K % 128 == 0; n_out % 256 (mode 0) or % 128 (mode 1).
+struct W4a8GemmProblem {
+  int mode;
+  const uint8_t* a_rows;     // [M, K] E4M3 codes in expert-sorted order
+  const uint8_t* a_sf;       // [M, K/128, 16] padded scale rows
+  const uint8_t* codes;      // [E*n_out, K/2] prepacked E2M1 codes
+  const uint8_t* sf;         // scale atoms [E*n_out/128][K/128][512]
+  const int32_t* offsets;    // [E+1] device
+  int E, M, K, n_out;
+  uint8_t* act;              // mode 0 out: [M, n_out/2] E4M3
+  uint8_t* act_sf;           // mode 0 out: [M, n_out/256, 16]
+  uint16_t* out;             // mode 1 out: [M, n_out] bf16
+  const float* topk_w;       // mode 1, optional (with sorted_pair)
+  const int32_t* sorted_pair;
+  // optional shared segment (weight 1, token rows 0..T_s-1 of s_rows)
+  const uint8_t* s_rows;
+  const uint8_t* s_rows_sf;
+  const uint8_t* s_codes;
+  const uint8_t* s_sf;
+  int T_s, n_out_s;
+  uint8_t* s_act;
+  uint8_t* s_act_sf;
+  uint16_t* s_out;
+  unsigned* status;
+};
+cudaError_t launch_grouped_gemm_w4a8(const W4a8GemmProblem& p, cudaStream_t stream, bool pdl = false);
+cudaError_t launch_w4a8_prepack(const uint8_t* codes, const uint8_t* scales, int E, int n_out, int K, int gate_up,
+                                uint8_t* codes_p, uint8_t* sf_p, cudaStream_t stream);
+// sorted_pair NULL: identity rows and no codes written (the padded scale rows of x itself).
+cudaError_t launch_gather_rows_mx(const uint8_t* x_codes, const uint8_t* x_scales, const int32_t* sorted_pair, int M,
+                                  int k, int T, int H, uint8_t* out_codes, uint8_t* out_sf, const int32_t* n_rows,
+                                  unsigned* status, cudaStream_t stream, bool pdl = false);
+
 }  // namespace moe

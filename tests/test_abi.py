@@ -209,3 +209,39 @@ def test_mxfp4_weights_expert_slice_is_a_view_of_the_local_rows():
         w.experts(3, 3)
     with pytest.raises(ValueError):
         w.experts(0, 6)
+
+
+def test_w4a8_validation_returns_before_launch(L):
+    P16 = 1 << 20
+    E = moe.MOE_ERR_INVALID_ARG
+    U = moe.MOE_ERR_UNSUPPORTED
+    # moe_w4a8_prepack(codes, scales, E, n_out, K, gate_up, codes_p, sf_p, stream)
+    assert L.moe_w4a8_prepack(P16, P16, 2, 128, 256, 1, P16 * 2, P16 * 3, None) == U   # gate/up: n_out % 256
+    assert L.moe_w4a8_prepack(P16, P16, 2, 128, 192, 0, P16 * 2, P16 * 3, None) == U   # K % 128
+    assert L.moe_w4a8_prepack(P16, P16, 2, 128, 256, 0, P16, P16 * 3, None) == E       # in place
+    # moe_gather_rows_mx(x_codes, x_scales, sorted_pair, T, k, H, M, out_codes, out_sf, ws, ws_bytes, stream)
+    assert L.moe_gather_rows_mx(P16, P16, P16, 4, 2, 192, 8, P16, P16, P16, 256, None) == U        # H % 128
+    assert L.moe_gather_rows_mx(P16, P16, None, 4, 1, 256, 8, None, P16, P16, 256, None) == E      # M > T, identity
+    assert L.moe_gather_rows_mx(P16, P16, P16, 4, 2, 256, 8, P16, P16, P16, 16, None) == moe.MOE_ERR_WORKSPACE
+    # moe_grouped_gemm_swiglu_w4a8(x, x_sf, codes, sf, offsets, E, M, H, I, act, act_sf, ws, ws_bytes, stream)
+    assert L.moe_grouped_gemm_swiglu_w4a8(P16, P16, P16, P16, P16, 8, 32, 192, 128, P16, P16, P16, 256, None) == U
+    assert L.moe_grouped_gemm_swiglu_w4a8(P16, P16, P16, P16, P16, 8, 32, 256, 64, P16, P16, P16, 256, None) == U
+    assert L.moe_grouped_gemm_swiglu_w4a8(P16, P16, P16, P16, P16, 8, 32, 256, 128, None, P16, P16, 256, None) == E
+    # moe_grouped_gemm_w4a8(a, a_sf, codes, sf, offsets, topk_w, sorted_pair, E, M, N, K, out, ws, ws_bytes, stream)
+    assert L.moe_grouped_gemm_w4a8(P16, P16, P16, P16, P16, P16, None, 8, 32, 256, 128, P16, P16, 256, None) == E
+    assert L.moe_grouped_gemm_w4a8(P16, P16, P16, P16, P16, None, None, 8, 32, 192, 128, P16, P16, 256, None) == U
+    assert L.moe_grouped_gemm_w4a8(P16, P16, P16, P16, P16, None, None, 8, 0, 256, 128, None, P16, 256, None) == \
+        moe.MOE_OK
+    # the layer: H, I, I_s multiples of 128
+    d = moe.make_desc(16, 256, 8, 2, 192)
+    assert L.moe_w4a8_layer_workspace_size(ctypes.byref(d)) == 0
+    d = moe.make_desc(16, 256, 8, 2, 128, gate="sigmoid", n_shared=1, I_s=128)
+    need = L.moe_w4a8_layer_workspace_size(ctypes.byref(d))
+    assert need > 16 * 2 * (256 + 128 + 512)
+    assert L.moe_w4a8_layer_kernel_launches(ctypes.byref(d)) == 9
+    args = [P16] * 16  # x_codes ... counts (the workspace pointer follows)
+    args[3] = None  # no bias
+    assert L.moe_layer_forward_w4a8(ctypes.byref(d), *args, P16, need - 1, None) == moe.MOE_ERR_WORKSPACE
+    a = list(args)
+    a[8] = None  # shared expert weights missing
+    assert L.moe_layer_forward_w4a8(ctypes.byref(d), *a, P16, need, None) == E
