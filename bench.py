@@ -65,7 +65,9 @@ def _args(argv=None):
     ap.add_argument("--mxfp4-f16", action="store_true",
                     help="also time the 4-bit-weight layer on f16 operands (software-decoded weights)")
     ap.add_argument("--profile-mxfp4", action="store_true",
-                    help="with --profile-steps: the MXFP4-weight layer loop instead (for ncu launch lists)")
+                    help="with --profile-steps: the MXFP4-weight layer loop on f16 operands instead")
+    ap.add_argument("--profile-w4a8", action="store_true",
+                    help="with --profile-steps: the W4A8 layer loop instead (for ncu launch lists and captures)")
     ap.add_argument("--cpu-baseline-child", action="store_true", help=argparse.SUPPRESS)
     ap.add_argument("--sample-tokens", type=int, default=8)
     ap.add_argument("--profile-steps", action="store_true",
@@ -768,7 +770,23 @@ def run_gb300(args, rank, world, local):
         t = dict(weights.get(cfg, moe, mi, d16))
         t.update(x=d16(inp.x), logits=torch.from_numpy(inp.logits).cuda(),
                  bias=torch.from_numpy(inp.bias).cuda() if inp.bias is not None else None)
-        if args.profile_mxfp4:
+        if args.profile_w4a8:
+            w13_raw = d16(mi.normal_bf16(cfg.seed, mi.TID_W13, (cfg.E, 2 * cfg.I, cfg.H), 0.0, cfg.w_std))
+            w13 = moe.moe_w4a8_prepack(*moe.moe_mxfp4_quantize(w13_raw), gate_up=True)
+            del w13_raw
+            w2 = moe.moe_w4a8_prepack(*moe.moe_mxfp4_quantize(t["w2"]), gate_up=False)
+            w13_s = w2_s = None
+            if cfg.n_shared:
+                sh = mi.generate(cfg.with_(E=1, T=1))
+                w13_s = moe.moe_w4a8_prepack(*moe.moe_mxfp4_quantize(d16(sh.w13_s)), gate_up=True)
+                w2_s = moe.moe_w4a8_prepack(*moe.moe_mxfp4_quantize(d16(sh.w2_s)), gate_up=False)
+            ones = torch.ones(cfg.H, dtype=torch.bfloat16, device="cuda")
+            xc, xs, _, _ = moe.moe_add_rms_norm_mxfp8(t["x"], None, ones, 1e-6, with_fp32=False)
+            l8 = moe.W4a8Layer(cfg.T, cfg.H, cfg.E, cfg.k, cfg.I, cfg.gate, cfg.routed_scaling_factor, cfg.eps,
+                               cfg.n_shared, cfg.I_s)
+            for _ in range(W + K):
+                l8.forward(xc, xs, t["logits"], w13, w2, t["bias"], w13_s, w2_s)
+        elif args.profile_mxfp4:
             full = mi.generate(cfg)
             w13q = moe.moe_mxfp4_prepack(*moe.moe_mxfp4_quantize(d16(full.w13)), gate_up=True)
             w2q = moe.moe_mxfp4_prepack(*moe.moe_mxfp4_quantize(t["w2"]), gate_up=False)

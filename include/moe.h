@@ -415,13 +415,15 @@ MOE_API int moe_grouped_gemm_mxfp4(const uint16_t* a16, const uint8_t* w_codes, 
  * 128-K chunk the chunk's four E8M0 scales followed by twelve zero bytes.
  *
  * moe_w4a8_prepack: one-time layout.  codes [E,n_out,K/2] and scales [E,n_out,K/32] of MXFP4
- *   weights -> codes_p [E*n_out,K/2] and sf_p [E*n_out/128][K/128][512] (E*n_out*K/32 bytes).
+ *   weights -> codes_p [E*n_out/256][K/128][256][64] (per 256-row tile and 128-K chunk the 64 code
+ *   bytes of the chunk for each of the tile's rows, so every block the GEMM loads is one contiguous
+ *   16 KB; E*n_out*K/2 bytes) and sf_p [E*n_out/256][K/128][2][512] (E*n_out*K/32 bytes).
  *   gate_up = 1 (w13, n_out = 2I, I % 128 == 0): packed row R of an expert is the gate (R % 32 < 16)
  *   or up row of feature 128*(R/256) + 32*((R/32)%4) + 16*((R/128)%2) + R%16, so every 256-row tile
- *   holds 128 whole features.  gate_up = 0: rows unchanged (n_out % 128 == 0).  sf_p: per 128-row
- *   tile and 128-K chunk a 512-byte atom, byte (r%32)*16 + (r/32)*4 + b = the scale of tile row r,
- *   block b of the chunk.  K % 128 == 0.  Not in place.  Local expert range [e0, e1): codes_p +
- *   e0*n_out*K/2 and sf_p + e0*n_out*K/32.
+ *   holds 128 whole features.  gate_up = 0: rows unchanged.  n_out % 256 == 0.  sf_p: per 256-row
+ *   tile, 128-K chunk and 128-row half a 512-byte atom, byte (r%32)*16 + (r/32)*4 + b = the scale of
+ *   half row r, block b of the chunk.  K % 128 == 0.  Not in place.  Local expert range [e0, e1):
+ *   codes_p + e0*n_out*K/2 and sf_p + e0*n_out*K/32.
  *
  * moe_gather_rows_mx: out_codes[pos] = x_codes[t], out_sf[pos] = the padded scale row of
  *   x_scales[t], t = sorted_pair[pos] / k, for pos < M (x_codes [T,H], x_scales [T,H/32]; H % 128
@@ -435,7 +437,7 @@ MOE_API int moe_grouped_gemm_mxfp4(const uint16_t* a16, const uint8_t* w_codes, 
  *   I % 128 == 0.  Rows >= offsets[E] untouched.
  * moe_grouped_gemm_w4a8: out [M,N] bf16 = topk_w[sorted_pair[pos]] (optional) *
  *   (a[pos] . w[e]^T), a [M,K] E4M3 with a_sf [M,K/128,16], w prepacked with gate_up = 0;
- *   N % 128 == 0, K % 128 == 0.
+ *   N % 256 == 0, K % 128 == 0.
  * Both walk 32 token columns per tile (a decode-shaped instance; correct for any M).  ws: at least
  * moe_grouped_gemm_workspace_size() bytes.
  *
@@ -444,7 +446,7 @@ MOE_API int moe_grouped_gemm_mxfp4(const uint16_t* a16, const uint8_t* w_codes, 
  *   (+ the shared expert as one more segment, act_s in MXFP8 as well), the W4A8 down GEMM
  *   (+ shared), finalize; y [T,H] bf16.  Weights prepacked by moe_w4a8_prepack (w13 with gate_up = 1,
  *   w2 with 0; the shared expert's likewise with E = 1, or all four NULL when d->n_shared == 0).
- *   H, I, I_s multiples of 128.  ws: moe_w4a8_layer_workspace_size(d) bytes.
+ *   H % 256 == 0; I, I_s multiples of 128.  ws: moe_w4a8_layer_workspace_size(d) bytes.
  *   moe_layer_forward_w4a8_events records six caller events as moe_layer_forward_events does (before
  *   gating, routing, the gate/up GEMM (after the row gather), the down GEMM, finalize; after it).
  *   moe_w4a8_layer_kernel_launches: kernels per call.

@@ -520,18 +520,19 @@ class Mxfp4Layer:
 # ------------------------------------------------------------------ W4A8: MXFP8 x MXFP4 on the block-scaled MMA
 class W4a8Weights(NamedTuple):
     """Expert weights [E, n_out, K] in the layout of moe_w4a8_prepack."""
-    codes: object    # [E*n_out, K/2] uint8 E2M1 codes (gate/up rows regrouped when packed for w13)
-    sf: object       # [E*n_out/128, K/128, 512] uint8 scale atoms
+    codes: object    # [E*n_out/256, K/128, 256, 64] uint8 E2M1 codes (gate/up rows regrouped for w13)
+    sf: object       # [E*n_out/256, K/128, 2, 512] uint8 scale atoms
     E: int
     n_out: int
     K: int
 
     def experts(self, e0: int, e1: int) -> "W4a8Weights":
-        """The local experts [e0, e1) as views (every expert owns whole 128-row tiles)."""
+        """The local experts [e0, e1) as views (every expert owns whole 256-row tiles)."""
         if not 0 <= e0 < e1 <= self.E:
             raise ValueError(f"expert range [{e0}, {e1}) outside [0, {self.E})")
         r0, r1 = e0 * self.n_out, e1 * self.n_out
-        return W4a8Weights(self.codes[r0:r1], self.sf[r0 // 128:r1 // 128], e1 - e0, self.n_out, self.K)
+        return W4a8Weights(self.codes[r0 // 256:r1 // 256], self.sf[r0 // 256:r1 // 256], e1 - e0, self.n_out,
+                           self.K)
 
 
 def moe_w4a8_prepack(codes, scales, gate_up: bool, stream=None) -> W4a8Weights:
@@ -542,8 +543,8 @@ def moe_w4a8_prepack(codes, scales, gate_up: bool, stream=None) -> W4a8Weights:
     E, n_out, K2 = codes.shape
     K = 2 * K2
     dev = codes.device
-    cp = torch.empty((E * n_out, K2), dtype=torch.uint8, device=dev)
-    sf = torch.empty((E * n_out // 128, K // 128, 512), dtype=torch.uint8, device=dev)
+    cp = torch.empty((E * n_out // 256, K // 128, 256, 64), dtype=torch.uint8, device=dev)
+    sf = torch.empty((E * n_out // 256, K // 128, 2, 512), dtype=torch.uint8, device=dev)
     _check(lib().moe_w4a8_prepack(_ptr(codes), _ptr(scales), E, n_out, K, int(bool(gate_up)), _ptr(cp), _ptr(sf),
                                   _stream(stream)), "moe_w4a8_prepack")
     return W4a8Weights(cp, sf, E, n_out, K)

@@ -430,8 +430,7 @@ int moe_grouped_gemm_mxfp4(const uint16_t* a16, const uint8_t* w_codes, const ui
 int moe_w4a8_prepack(const uint8_t* codes, const uint8_t* scales, int E, int n_out, int K, int gate_up,
                      uint8_t* codes_p, uint8_t* sf_p, void* stream) {
   if (E < 1 || n_out <= 0 || K <= 0) return MOE_ERR_INVALID_ARG;
-  if (n_out % (gate_up ? 256 : 128) != 0 || K % 128 != 0 || (long long)E * n_out * K >= (1LL << 40))
-    return MOE_ERR_UNSUPPORTED;
+  if (n_out % 256 != 0 || K % 128 != 0 || (long long)E * n_out * K >= (1LL << 40)) return MOE_ERR_UNSUPPORTED;
   if (!codes || !scales || !codes_p || !sf_p || codes == codes_p) return MOE_ERR_INVALID_ARG;
   if (!aligned16(codes) || !aligned16(codes_p) || !aligned16(sf_p)) return MOE_ERR_INVALID_ARG;
   return cuda_status(moe::launch_w4a8_prepack(codes, scales, E, n_out, K, gate_up ? 1 : 0, codes_p, sf_p,
@@ -460,7 +459,7 @@ int w4a8_gemm(int mode, const uint8_t* a, const uint8_t* a_sf, const uint8_t* co
               uint8_t* act, uint8_t* act_sf, uint16_t* out, void* ws, size_t ws_bytes, void* stream) {
   if (E < 1 || M < 0 || n_out <= 0 || K <= 0) return MOE_ERR_INVALID_ARG;
   if (E > 1024) return MOE_ERR_UNSUPPORTED;
-  if (K % 128 != 0 || n_out % (mode == 0 ? 256 : 128) != 0) return MOE_ERR_UNSUPPORTED;
+  if (K % 128 != 0 || n_out % 256 != 0) return MOE_ERR_UNSUPPORTED;
   if ((long long)M * (n_out > K ? n_out : K) >= (1LL << 40)) return MOE_ERR_UNSUPPORTED;
   if ((topk_w == nullptr) != (sorted_pair == nullptr)) return MOE_ERR_INVALID_ARG;
   if (!codes || !sf || !offsets || !ws) return MOE_ERR_INVALID_ARG;
@@ -737,7 +736,7 @@ W8Ws w8_ws(const moe_layer_desc* d) {
 int check_desc_w4a8(const moe_layer_desc* d) {
   int s = check_desc(d);
   if (s) return s;
-  if (d->H % 128 != 0 || d->I % 128 != 0 || (d->n_shared && d->I_s % 128 != 0)) return MOE_ERR_UNSUPPORTED;
+  if (d->H % 256 != 0 || d->I % 128 != 0 || (d->n_shared && d->I_s % 128 != 0)) return MOE_ERR_UNSUPPORTED;
   return MOE_OK;
 }
 

@@ -12,35 +12,44 @@
 //   weights  E2M1 codes, two per byte (element 2j in the low nibble of byte j), prepacked by
 //            moe_w4a8_prepack: rows of the gate/up weight regrouped so that a 256-row tile holds
 //            128 whole features (below), and the scales rearranged into 512-byte atoms, one per
-//            (128-row tile, 128-K chunk): byte (r % 32) * 16 + (r / 32) * 4 + b holds the scale of
-//            row r, block b -- the layout tcgen05.cp .32x128b.warpx4 turns into the tensor-memory
-//            scale-factor layout of an M = 128 block-scaled MMA (row r at lane r % 32 of every lane
-//            quarter, column r / 32, byte b = the MMA's scale-factor id).
+//            (128-row half of a 256-row tile, 128-K chunk), the two halves' atoms of a chunk side by
+//            side: byte (r % 32) * 16 + (r / 32) * 4 + b holds the scale of half-tile row r, block b --
+//            the layout tcgen05.cp .32x128b.warpx4 turns into the tensor-memory scale-factor layout of
+//            an M = 128 block-scaled MMA (row r at lane r % 32 of every lane quarter, column r / 32,
+//            byte b = the MMA's scale-factor id).
 //   tokens   E4M3 codes [rows, K] and "padded scale rows" [rows, K/128, 16]: per row and 128-K
 //            chunk, 16 bytes whose first four are the chunk's four block scales (the rest zero).  A
-//            32-row TMA box of them is the 32 x 16-byte source of one tcgen05.cp for the token
+//            32-row slice of one chunk is the 32 x 16-byte source of one tcgen05.cp for the token
 //            operand's scale factors (token n at lane n, column 0).
 //
-// Product (swap-AB, as the bf16 decode instances): weight rows are the MMA's M = 128 operand A,
-// read from shared memory in the padded E2M1 layout that TMA writes for
-// CU_TENSOR_MAP_DATA_TYPE_16U4_ALIGN16B (each 16 codes = 8 bytes followed by 8 zero bytes, so a
-// 128-code row is a 128-byte swizzled row); the expert's token rows are the N = 32 operand B
-// (E4M3, 128-byte swizzled rows).  One 128-K stage = 4 MMAs of K = 32, each naming its block with
-// the scale-factor ids of the instruction descriptor; both operands' scale factors are copied into
-// a per-stage tensor-memory slot by the MMA thread (tcgen05.cp, which the MMAs issued after it by
-// the same thread are ordered behind).
+// Product (swap-AB, as the bf16 decode instances): weight rows are the MMA's operand A, two M = 128
+// halves of a 256-row tile into two accumulators, read from shared memory in the padded E2M1 layout
+// that TMA writes for CU_TENSOR_MAP_DATA_TYPE_16U4_ALIGN16B (each 16 codes = 8 bytes followed by 8
+// zero bytes, so a 128-code row is a 128-byte swizzled row); the expert's token rows are the N = 32
+// operand B (E4M3, 128-byte swizzled rows).  One 128-K chunk = 4 MMAs of K = 32 per half, each
+// naming its block with the scale-factor ids of the instruction descriptor; the scale factors are
+// copied into a per-stage tensor-memory slot by the MMA thread (tcgen05.cp, which the MMAs issued
+// after it by the same thread are ordered behind).
 //
-// Mode 0 (gate/up + SwiGLU + MXFP8 of act): two 128-row weight boxes per stage, each into its own
-// accumulator.  The prepacked gate/up tile of 256 rows holds features [128 f, 128 f + 128): box p,
-// lane quarter q, lane l holds the gate (l < 16) or up (l >= 16) row of feature
-// 128 f + 32 q + 16 p + (l % 16), so one epilogue warp ends up with a whole 32-feature block of act
-// for each token column: the block maximum is a 4-step shuffle reduction, and the warp writes the
-// E4M3 codes and the E8M0 scale byte of that block for the down GEMM.
-// Mode 1 (down + routing weight): one 128-row box, bf16 output times topk_w[sorted_pair[pos]].
+// Loads.  Each SM's TMA engine works through its copies one after another (about 0.33 us per 16 KB),
+// so it carries only the weights: one 16-KB copy per 128-K chunk of the tile's 256 weight rows (A ring,
+// 32 KB in shared memory in the padded layout; the prepacked codes of a (tile, chunk) are one contiguous
+// block) and one bulk copy of the weight scale atoms per 512-K window (4 chunks).  The window's 32 token
+// rows and their scale rows, read from L2 again by every feature tile of an expert, are copied by two
+// loader warps with cp.async (T ring).  Two MMA-issuing threads, one per 128-row weight half, keep the
+// tensor pipe fed: an N = 32 block-scaled MMA takes about as long to issue as a wide one.
 //
-// Warp roles (64 + 32 * 4 threads, one persistent CTA per SM, static round-robin tiles; an expert's
-// token tiles that reuse a weight tile run next to each other): warp 0 TMA producer, warp 1 TMEM
-// allocator + MMA issuer, warps 2-5 epilogue (one per TMEM lane quarter).  Every wait is bounded
+// Mode 0 (gate/up + SwiGLU + MXFP8 of act): the prepacked gate/up tile of 256 rows holds features
+// [128 f, 128 f + 128): half p, lane quarter q, lane l holds the gate (l < 16) or up (l >= 16) row
+// of feature 128 f + 32 q + 16 p + (l % 16), so one epilogue warp ends up with a whole 32-feature
+// block of act for each token column: the block maximum is a 4-step shuffle reduction, and the warp
+// writes the E4M3 codes and the E8M0 scale byte of that block for the down GEMM.
+// Mode 1 (down + routing weight): 256 output features per tile, bf16 times topk_w[sorted_pair[pos]].
+//
+// Warp roles (288 threads, one persistent CTA per SM, static round-robin tiles; an expert's token
+// tiles that reuse a weight tile run next to each other): warp 0 TMA producer, warp 1 TMEM allocator +
+// MMA issuer of weight half 0, warps 2-5 epilogue (one per TMEM lane quarter), warp 6 MMA issuer of
+// half 1, warps 7-8 token loaders.  Every wait is bounded
 // (2 s): on expiry the CTA raises its abort flag, records DEV_ERR_TIMEOUT, lets its copies land,
 // drains its MMAs and frees TMEM.
 #include "moe_common.cuh"
@@ -54,42 +63,45 @@
 namespace moe {
 namespace {
 
-constexpr int kBM = 128;                  // weight rows per box (MMA M)
+constexpr int kBM = 128;                  // weight rows per MMA (M), one half of a tile
+constexpr int kTR = 256;                  // weight rows per tile and per A copy
 constexpr int kNT = 32;                   // token columns per tile (MMA N)
-constexpr int kKC = 128;                  // K per stage: 4 MMAs of K = 32
-constexpr int kABox = kBM * 128;          // shared-memory bytes of one weight box (padded codes): 16 KB
-constexpr int kATx = kBM * kKC / 2;       // bytes the weight box moves (and counts on the barrier): 8 KB
-constexpr int kBBox = kNT * kKC;          // 32 token rows x 128 E4M3 codes: 4 KB
-constexpr int kSF = 512;                  // one scale-factor atom / one 32-row box of padded scale rows
-constexpr int kEPI = 4;                   // epilogue warps, one per TMEM lane quarter
-constexpr int kThreads = 64 + 32 * kEPI;
+constexpr int kKC = 128;                  // K per chunk: 4 MMAs of K = 32 per half
+constexpr int kWin = 4;                   // chunks per T-ring window (512 K)
+constexpr int kABox = kTR * 128;          // shared-memory bytes of one A copy (padded codes): 32 KB
+constexpr int kATx = kTR * kKC / 2;       // bytes the A copy moves (and counts on the barrier): 16 KB
+constexpr int kSF = 512;                  // one scale-factor atom (128 rows) / 32 token scale rows
+constexpr int kTB = kWin * kNT * kKC;     // token rows of a window: 16 KB
+constexpr int kTSB = kWin * kSF;          // their padded scale rows: 2 KB
+constexpr int kTSA = kWin * 2 * kSF;      // the window's weight scale atoms: 4 KB
+constexpr int kTSlot = kTB + kTSB + kTSA; // 22 KB
+constexpr int kEPI = 4;                   // epilogue warps (2-5), one per TMEM lane quarter
+constexpr int kMMA2 = 2 + kEPI;           // warp of the second MMA issuer (weight half 1)
+constexpr int kLD0 = kMMA2 + 1;           // first of the two token-loader warps
+constexpr int kLoaders = 64;              // token-loader threads
+constexpr int kThreads = 32 * (kLD0 + 2);
 constexpr int kMaxDynSmem = 232448;
 constexpr unsigned long long kTimeoutNs = 2000000000ull;
 
-template <int MODE, int STAGES>
+template <int MODE, int STAGES, int TSLOTS>
 struct W8Layout {
-  static constexpr int kParts = MODE == 0 ? 2 : 1;                 // weight boxes per stage
-  static constexpr int kAOff = 0;
-  static constexpr int kBOff = kParts * kABox;
-  static constexpr int kSFAOff = kBOff + kBBox;
-  static constexpr int kSFBOff = kSFAOff + kParts * kSF;
-  static constexpr int kStageBytes = (kSFBOff + kSF + 1023) / 1024 * 1024;
-  static constexpr int kBarOff = STAGES * kStageBytes;
-  static constexpr int kNumBars = 2 * STAGES + 5;
+  static constexpr int kAOff = 0;                                  // STAGES x 32 KB
+  static constexpr int kTOff = STAGES * kABox;                     // TSLOTS x 22 KB
+  static constexpr int kBarOff = kTOff + TSLOTS * kTSlot;
+  static constexpr int kNumBars = 2 * STAGES + 2 * TSLOTS + 6;
   static constexpr int kMiscOff = kBarOff + kNumBars * 8;
   static constexpr int kScaleOff = kMiscOff + 16;                  // mode 1: routing weights per epilogue warp
   static constexpr int kTabOff = kScaleOff + kEPI * kNT * 4;
-  static constexpr uint32_t kTx = kParts * (kATx + kSF) + kBBox + kSF;
-  // tensor memory: two accumulator buffers of kParts x 32 columns, then a scale-factor slot per
-  // stage (4 columns per weight box, 4 for the tokens)
-  static constexpr int kAccCols = kParts * kNT;
+  // tensor memory: two accumulator buffers of 2 x 32 columns, then a scale-factor slot per A stage:
+  // per weight half (one per MMA issuer) 4 columns of weight scales and 4 of token scales
+  static constexpr int kAccCols = 2 * kNT;
   static constexpr int kSFCol0 = 2 * kAccCols;
-  static constexpr int kSFColsPerStage = 4 * (kParts + 1);
+  static constexpr int kSFColsPerStage = 16;
   static constexpr int kColsNeeded = kSFCol0 + STAGES * kSFColsPerStage;
   static constexpr uint32_t kTmemCols = kColsNeeded <= 64 ? 64 : (kColsNeeded <= 128 ? 128 : (kColsNeeded <= 256 ? 256 : 512));
-  static constexpr int kFeatPerTile = 128;
+  static constexpr int kFeatPerTile = MODE == 0 ? 128 : 256;
   static_assert(kColsNeeded <= 512, "TMEM");
-  static_assert(kABox % 1024 == 0 && kBOff % 1024 == 0 && kSFAOff % 16 == 0, "alignment");
+  static_assert(kABox % 1024 == 0 && kTOff % 1024 == 0 && kTSlot % 1024 == 0 && kTB % 1024 == 0, "alignment");
   static_assert(1024 + kTabOff + 2 * 1025 * 4 <= kMaxDynSmem, "shared memory");
   static size_t bytes(int E) { return 1024 + kTabOff + 2 * (size_t)(E + 1) * 4; }
 };
@@ -97,8 +109,12 @@ struct W8Layout {
 struct W8Params {
   const int32_t* offsets;
   int E, M, K;
-  int n_out, n_ftiles, n_feat;      // routed: weight rows per expert, feature tiles per expert, features
-  const uint8_t* sfa;               // weight scale atoms
+  int n_out, n_ftiles, n_feat;      // routed: weight rows per expert, 256-row tiles per expert, features
+  const uint8_t* b_rows;            // token rows [M, K] E4M3 (read by the loader warps)
+  const uint8_t* b_sf;              // their padded scale rows [M, K/128, 16]
+  const uint8_t* bs_rows;           // shared segment: [T_s, K] and [T_s, K/128, 16]
+  const uint8_t* bs_sf;
+  const uint8_t* sfa;               // weight scale atoms [E*n_out/256][K/128][2][512]
   uint8_t* act;                     // mode 0: [M, n_feat] E4M3 codes
   uint8_t* act_sf;                  // mode 0: [M, n_feat/128, 16] padded scale rows
   uint16_t* out;                    // mode 1: [M, n_feat] bf16
@@ -207,6 +223,13 @@ __device__ __forceinline__ void bulk_load(void* smem_dst, const void* src, uint3
       : "memory");
 }
 
+// cp.async of 16 bytes global -> shared (zero-filled when src_bytes is 0).
+__device__ __forceinline__ void cp_async16(void* smem_dst, const void* src, uint32_t src_bytes) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(smem_u32(smem_dst)),
+               "l"(reinterpret_cast<uint64_t>(src)), "r"(src_bytes)
+               : "memory");
+}
+
 // floor(log2 m) - 8 clamped to the E8M0 range (m == 0 -> -127): the block's shared exponent.
 __device__ __forceinline__ int mx_shared_exponent(float m) {
   const uint32_t b = __float_as_uint(m);
@@ -237,21 +260,20 @@ __device__ __forceinline__ void store_pairs16_bf16(const float* v, int lane, uin
   }
 }
 
-template <int MODE, int STAGES>
+template <int MODE, int STAGES, int TSLOTS>
 __global__ void __launch_bounds__(kThreads, 1)
-    grouped_gemm_w4a8_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                             const __grid_constant__ CUtensorMap tmSB, const __grid_constant__ CUtensorMap tmAs,
-                             const __grid_constant__ CUtensorMap tmBs, const __grid_constant__ CUtensorMap tmSBs,
+    grouped_gemm_w4a8_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmAs,
                              const W8Params p) {
-  using L = W8Layout<MODE, STAGES>;
-  constexpr int P = L::kParts;
+  using L = W8Layout<MODE, STAGES, TSLOTS>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem + L::kBarOff);
-  uint64_t* empty = full + STAGES;
-  uint64_t* tfull = empty + STAGES;
+  uint64_t* afull = reinterpret_cast<uint64_t*>(smem + L::kBarOff);
+  uint64_t* aempty = afull + STAGES;
+  uint64_t* wfull = aempty + STAGES;     // T ring (512-K windows)
+  uint64_t* wempty = wfull + TSLOTS;
+  uint64_t* tfull = wempty + TSLOTS;     // accumulators
   uint64_t* tempty = tfull + 2;
-  uint64_t* done = tempty + 2;
+  uint64_t* done = tempty + 2;           // one per MMA issuer
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::kMiscOff);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::kMiscOff + 4);
   volatile int* cfg_bad = reinterpret_cast<volatile int*>(smem + L::kMiscOff + 8);
@@ -264,27 +286,26 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
-      mbar_init(&full[s], 1);
-      mbar_init(&empty[s], 1);
+      mbar_init(&afull[s], 1);
+      mbar_init(&aempty[s], 2);                // both MMA issuers release a stage
+    }
+    for (int s = 0; s < TSLOTS; ++s) {
+      mbar_init(&wfull[s], 1 + kLoaders);      // the producer (scale atoms) and every loader thread
+      mbar_init(&wempty[s], 2);
     }
     for (int b = 0; b < 2; ++b) {
-      mbar_init(&tfull[b], 1);
+      mbar_init(&tfull[b], 2);
       mbar_init(&tempty[b], kEPI);
     }
-    mbar_init(done, 1);
+    mbar_init(&done[0], 1);
+    mbar_init(&done[1], 1);
     *abort_flag = 0;
     *cfg_bad = 0;
     fence_mbar_init();
   }
   if (warp == 0 && lane == 0) {
     tma_prefetch_desc(&tmA);
-    tma_prefetch_desc(&tmB);
-    tma_prefetch_desc(&tmSB);
-    if (p.has_shared) {
-      tma_prefetch_desc(&tmAs);
-      tma_prefetch_desc(&tmBs);
-      tma_prefetch_desc(&tmSBs);
-    }
+    if (p.has_shared) tma_prefetch_desc(&tmAs);
   }
   if (warp == 1) tmem_alloc(tmem_slot, L::kTmemCols);
   for (int i = threadIdx.x; i <= E; i += kThreads) s_off[i] = p.offsets ? __ldg(p.offsets + i) : 0;
@@ -326,130 +347,202 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int routed_total = *cfg_bad ? 0 : s_tt[E] * p.n_ftiles;
   const int shared_total = (*cfg_bad || !p.has_shared) ? 0 : ((p.T_s + kNT - 1) / kNT) * p.n_ftiles_s;
   const int total = routed_total + shared_total;
-  const int KB = p.K / kKC;  // stages per tile (K is a multiple of 128)
+  const int KB = p.K / kKC;  // chunks per tile (K is a multiple of 128)
 
   if (warp == 0) {
-    // ------------------------------------------------------------ producer
-    const uint64_t pol_first = policy_evict_first();
-    const uint64_t pol_last = policy_evict_last();
-    int stage = 0;
-    uint32_t phase = 0;
-    uint32_t issued = 0;
-    bool ok = true;
-    // Inside a layer forward this kernel may start while its predecessor finishes (programmatic
-    // dependent launch): wait for it before reading the rows it writes, then let the next launch.
-    pdl_wait();
-    pdl_launch_dependents();
-    for (int tile = blockIdx.x; ok && tile < total; tile += gridDim.x) {
-      const W8Tile t = w8_tile(tile, routed_total, s_off, s_tt, p);
-      const CUtensorMap* mA = t.shared ? &tmAs : &tmA;
-      const CUtensorMap* mB = t.shared ? &tmBs : &tmB;
-      const CUtensorMap* mSB = t.shared ? &tmSBs : &tmSB;
-      const int n_out = t.shared ? p.n_out_s : p.n_out;
-      // first 128-row box of this tile, counted in rows of the prepacked weight
-      const int a_row = (t.shared ? 0 : t.e * n_out) + t.f * (kBM * P);
-      const uint8_t* sfa = (t.shared ? p.sfa_s : p.sfa) + (size_t)(a_row / kBM) * KB * kSF;
-      const uint64_t pol_a = t.nt > 1 ? pol_last : pol_first;  // weight tiles read again stay in L2
-      for (int kb = 0; kb < KB; ++kb) {
-        bool w = (lane == 0) ? mbar_wait_bounded(&empty[stage], phase ^ 1u, abort_flag, p.timeout_ns, p.status)
-                             : false;
-        w = __shfl_sync(0xffffffffu, w, 0);
-        if (!w) {
-          ok = false;
-          break;
-        }
-        if (lane == 0) mbar_arrive_expect_tx(&full[stage], L::kTx);
-        __syncwarp();
-        uint8_t* st = smem + stage * L::kStageBytes;
-        if (lane < P) {
-          tma_load_2d(st + L::kAOff + lane * kABox, mA, kb * kKC, a_row + lane * kBM, &full[stage], pol_a);
-        } else if (lane == 8) {
-          tma_load_2d(st + L::kBOff, mB, kb * kKC, t.row_base, &full[stage], pol_last);
-        } else if (lane >= 16 && lane < 16 + P) {
-          const int part = lane - 16;
-          bulk_load(st + L::kSFAOff + part * kSF, sfa + ((size_t)part * KB + kb) * kSF, kSF, &full[stage], pol_a);
-        } else if (lane == 24) {
-          tma_load_2d(st + L::kSFBOff, mSB, kb * 16, t.row_base, &full[stage], pol_last);
-        }
-        __syncwarp();
-        ++issued;
-        if (++stage == STAGES) {
-          stage = 0;
-          phase ^= 1u;
+    // ------------------------------------------------------------ producer (one lane)
+    if (lane == 0) {
+      const uint64_t pol_first = policy_evict_first();
+      const uint64_t pol_last = policy_evict_last();
+      int as = 0, ws = 0;
+      uint32_t aph = 0, wph = 0;
+      uint32_t a_issued = 0, w_issued = 0;
+      bool ok = true;
+      // Inside a layer forward this kernel may start while its predecessor finishes (programmatic
+      // dependent launch): wait for it before reading the rows it writes, then let the next launch.
+      pdl_wait();
+      pdl_launch_dependents();
+      for (int tile = blockIdx.x; ok && tile < total; tile += gridDim.x) {
+        const W8Tile t = w8_tile(tile, routed_total, s_off, s_tt, p);
+        const CUtensorMap* mA = t.shared ? &tmAs : &tmA;
+        const int n_out = t.shared ? p.n_out_s : p.n_out;
+        const int a_tile = ((t.shared ? 0 : t.e * n_out) + t.f * kTR) / kTR;  // 256-row tile of the weights
+        const uint8_t* sfa = (t.shared ? p.sfa_s : p.sfa) + (size_t)a_tile * KB * 2 * kSF;
+        const uint64_t pol_a = t.nt > 1 ? pol_last : pol_first;  // weight tiles read again stay in L2
+        for (int kb = 0; kb < KB && ok; ++kb) {
+          if (kb % kWin == 0) {
+            // the window's weight scale atoms (the loader warps copy its token rows and their scales)
+            if (!mbar_wait_bounded(&wempty[ws], wph ^ 1u, abort_flag, p.timeout_ns, p.status)) {
+              ok = false;
+              break;
+            }
+            const int nch = min(kWin, KB - kb);
+            uint8_t* slot = smem + L::kTOff + ws * kTSlot;
+            mbar_arrive_expect_tx(&wfull[ws], (uint32_t)(nch * 2 * kSF));
+            bulk_load(slot + kTB + kTSB, sfa + (size_t)kb * 2 * kSF, (uint32_t)(nch * 2 * kSF), &wfull[ws], pol_a);
+            ++w_issued;
+            if (++ws == TSLOTS) {
+              ws = 0;
+              wph ^= 1u;
+            }
+          }
+          if (!mbar_wait_bounded(&aempty[as], aph ^ 1u, abort_flag, p.timeout_ns, p.status)) {
+            ok = false;
+            break;
+          }
+          mbar_arrive_expect_tx(&afull[as], (uint32_t)kATx);
+          tma_load_2d(smem + L::kAOff + as * kABox, mA, 0, ((int)a_tile * KB + kb) * kTR, &afull[as], pol_a);
+          ++a_issued;
+          if (++as == STAGES) {
+            as = 0;
+            aph ^= 1u;
+          }
         }
       }
-    }
-    // Drain: the last fill of every stage must have landed before the CTA exits (one deadline).
-    if (lane == 0) {
+      // Drain: the last fill of every stage and window slot must have landed before the CTA exits
+      // (one deadline for all).
       const uint64_t deadline = globaltimer_ns() + p.timeout_ns;
-      for (int s = 0; s < STAGES; ++s) {
-        const uint32_t n = issued / STAGES + ((uint32_t)s < issued % STAGES ? 1u : 0u);
+      for (int s = 0; s < STAGES + TSLOTS; ++s) {
+        const bool is_a = s < STAGES;
+        const uint32_t issued = is_a ? a_issued : w_issued;
+        const int nst = is_a ? STAGES : TSLOTS;
+        const int k = is_a ? s : s - STAGES;
+        const uint32_t n = issued / nst + ((uint32_t)k < issued % nst ? 1u : 0u);
         const uint64_t now = globaltimer_ns();
-        if (n) mbar_wait_bounded(&full[s], (n - 1u) & 1u, abort_flag, deadline > now ? deadline - now : 0,
-                                 p.status, false);
+        if (n) mbar_wait_bounded(is_a ? &afull[k] : &wfull[k], (n - 1u) & 1u, abort_flag,
+                                 deadline > now ? deadline - now : 0, p.status, false);
       }
     }
     __syncwarp();
-  } else if (warp == 1) {
-    // ------------------------------------------------------------ MMA issuer
+  } else if (warp == 1 || warp == kMMA2) {
+    // ------------------------------------------------------------ MMA issuers, one per weight half
+    // Each issues its half's MMAs into its own accumulator and copies the scale factors it needs into
+    // its own tensor-memory columns (tcgen05 operations of different threads are not ordered).
     if (lane == 0) {
-      int stage = 0;
-      uint32_t phase = 0;
+      const int half = warp == 1 ? 0 : 1;
+      int as = 0, ws = 0;
+      uint32_t aph = 0, wph = 0;
       bool ok = true;
       int it = 0;
       const uint64_t desc0 = umma_desc_sw128(smem_u32(smem));
       const uint64_t sfd0 = sf_src_desc(smem_u32(smem));
       for (int tile = blockIdx.x; ok && tile < total; tile += gridDim.x, ++it) {
         const int buf = it & 1;
-        const uint32_t aph = (uint32_t)(it >> 1) & 1u;
-        if (!mbar_wait_bounded(&tempty[buf], aph ^ 1u, abort_flag, p.timeout_ns, p.status)) break;
+        const uint32_t acc_ph = (uint32_t)(it >> 1) & 1u;
+        if (!mbar_wait_bounded(&tempty[buf], acc_ph ^ 1u, abort_flag, p.timeout_ns, p.status)) break;
         tc_fence_after();
-        const uint32_t d = tmem_base + (uint32_t)(buf * L::kAccCols);
+        const uint32_t d = tmem_base + (uint32_t)(buf * L::kAccCols + half * kNT);
         for (int kb = 0; kb < KB; ++kb) {
-          if (!mbar_wait_bounded(&full[stage], phase, abort_flag, p.timeout_ns, p.status)) {
+          const int ci = kb % kWin;  // chunk inside the window
+          if (ci == 0) {
+            if (!mbar_wait_bounded(&wfull[ws], wph, abort_flag, p.timeout_ns, p.status)) {
+              ok = false;
+              break;
+            }
+          }
+          if (!mbar_wait_bounded(&afull[as], aph, abort_flag, p.timeout_ns, p.status)) {
             ok = false;
             break;
           }
           tc_fence_after();
-          const uint32_t soff = (uint32_t)(stage * L::kStageBytes);
-          const uint32_t sf_slot = tmem_base + (uint32_t)(L::kSFCol0 + stage * L::kSFColsPerStage);
-          const uint32_t sfb_t = sf_slot + 4u * P;
+          const uint32_t woff = (uint32_t)(L::kTOff + ws * kTSlot);
+          const uint32_t sfa_t = tmem_base + (uint32_t)(L::kSFCol0 + as * L::kSFColsPerStage + 8 * half);
+          const uint32_t sfb_t = sfa_t + 4u;
+          tmem_cp_32x128_x4(sfa_t, sfd0 + (uint64_t)((woff + kTB + kTSB + (ci * 2 + half) * kSF) >> 4));
+          tmem_cp_32x128_x4(sfb_t, sfd0 + (uint64_t)((woff + kTB + ci * kSF) >> 4));
+          const uint64_t ad0 = desc0 + (uint64_t)((L::kAOff + as * kABox + half * kBM * 128) >> 4);
+          const uint64_t bd0 = desc0 + (uint64_t)((woff + ci * kNT * kKC) >> 4);
 #pragma unroll
-          for (int part = 0; part < P; ++part)
-            tmem_cp_32x128_x4(sf_slot + 4u * part, sfd0 + (uint64_t)((soff + L::kSFAOff + part * kSF) >> 4));
-          tmem_cp_32x128_x4(sfb_t, sfd0 + (uint64_t)((soff + L::kSFBOff) >> 4));
-          const uint64_t ad0 = desc0 + (uint64_t)((soff + L::kAOff) >> 4);
-          const uint64_t bd0 = desc0 + (uint64_t)((soff + L::kBOff) >> 4);
-#pragma unroll
-          for (int kk = 0; kk < kKC / 32; ++kk) {
-            const uint32_t idesc = w4a8_idesc((uint32_t)kk);
-#pragma unroll
-            for (int part = 0; part < P; ++part)
-              umma_w4a8(d + part * kNT, ad0 + (uint64_t)((part * kABox + kk * 32) >> 4), bd0 + (uint64_t)((kk * 32) >> 4),
-                        idesc, sf_slot + 4u * part, sfb_t, (kb | kk) != 0);
+          for (int kk = 0; kk < kKC / 32; ++kk)
+            umma_w4a8(d, ad0 + (uint64_t)((kk * 32) >> 4), bd0 + (uint64_t)((kk * 32) >> 4), w4a8_idesc((uint32_t)kk),
+                      sfa_t, sfb_t, (kb | kk) != 0);
+          umma_commit(&aempty[as]);
+          if (++as == STAGES) {
+            as = 0;
+            aph ^= 1u;
           }
-          umma_commit(&empty[stage]);
-          if (++stage == STAGES) {
-            stage = 0;
-            phase ^= 1u;
+          if (ci == kWin - 1 || kb == KB - 1) {
+            umma_commit(&wempty[ws]);  // the window's token rows and scales are no longer read
+            if (++ws == TSLOTS) {
+              ws = 0;
+              wph ^= 1u;
+            }
           }
         }
         if (!ok) break;
         umma_commit(&tfull[buf]);
       }
       // Drain: every MMA issued by this thread must be complete before TMEM is freed.
-      umma_commit(done);
-      mbar_wait_bounded(done, 0, abort_flag, p.timeout_ns, p.status, false);
+      umma_commit(&done[half]);
+      mbar_wait_bounded(&done[half], 0, abort_flag, p.timeout_ns, p.status, false);
     }
     __syncwarp();
+  } else if (warp >= kLD0) {
+    // ------------------------------------------------------------ token loaders (cp.async)
+    // The window's 32 token rows x 4 chunks (128 bytes each, written in the 128-byte swizzle the MMA's
+    // operand descriptor expects: 16-byte unit j of row r at j ^ (r % 8)) and their padded scale rows;
+    // rows and chunks past the end are zero-filled.  Each thread waits for its own copies and fences
+    // them to the async proxy before arriving, one window behind the copies it issues.
+    const int lt = (warp - kLD0) * 32 + lane;
+    pdl_wait();  // the token rows come from the previous kernel
+    int ws = 0, prev = -1;
+    uint32_t wph = 0;
+    bool ok = true;
+    for (int tile = blockIdx.x; ok && tile < total; tile += gridDim.x) {
+      const W8Tile t = w8_tile(tile, routed_total, s_off, s_tt, p);
+      const uint8_t* rows = t.shared ? p.bs_rows : p.b_rows;
+      const uint8_t* sfr = t.shared ? p.bs_sf : p.b_sf;
+      const int nrows = t.shared ? p.T_s : p.M;
+      for (int kb0 = 0; kb0 < KB; kb0 += kWin) {
+        bool w = (lane == 0) ? mbar_wait_bounded(&wempty[ws], wph ^ 1u, abort_flag, p.timeout_ns, p.status) : false;
+        w = __shfl_sync(0xffffffffu, w, 0);
+        if (!w) {
+          ok = false;
+          break;
+        }
+        uint8_t* slot = smem + L::kTOff + ws * kTSlot;
+#pragma unroll 4
+        for (int i = 0; i < kTB / 16 / kLoaders; ++i) {
+          const int piece = lt + i * kLoaders;  // (chunk, row, 16-byte unit)
+          const int c = piece >> 8, r = (piece >> 3) & 31, j = piece & 7;
+          const int row = t.row_base + r, kc = kb0 + c;
+          const bool valid = row < nrows && kc < KB;
+          const uint8_t* src = valid ? rows + (size_t)row * p.K + kc * kKC + j * 16 : rows;
+          cp_async16(slot + c * (kNT * kKC) + r * kKC + ((j ^ (r & 7)) << 4), src, valid ? 16u : 0u);
+        }
+#pragma unroll
+        for (int i = 0; i < kTSB / 16 / kLoaders; ++i) {
+          const int piece = lt + i * kLoaders;  // (chunk, row)
+          const int c = piece >> 5, r = piece & 31;
+          const int row = t.row_base + r, kc = kb0 + c;
+          const bool valid = row < nrows && kc < KB;
+          const uint8_t* src = valid ? sfr + ((size_t)row * KB + kc) * 16 : sfr;
+          cp_async16(slot + kTB + c * kSF + r * 16, src, valid ? 16u : 0u);
+        }
+        asm volatile("cp.async.commit_group;" ::: "memory");
+        if (prev >= 0) {
+          asm volatile("cp.async.wait_group 1;" ::: "memory");
+          asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+          mbar_arrive(&wfull[prev]);
+        }
+        prev = ws;
+        if (++ws == TSLOTS) {
+          ws = 0;
+          wph ^= 1u;
+        }
+      }
+    }
+    asm volatile("cp.async.wait_group 0;" ::: "memory");
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+    if (prev >= 0) mbar_arrive(&wfull[prev]);
   } else {
-    // ------------------------------------------------------------ epilogue
+    // ------------------------------------------------------------ epilogue (warps 2-5)
     const int qw = warp & 3;  // TMEM lane quarter this warp may access
     int it = 0;
     for (int tile = blockIdx.x; tile < total; tile += gridDim.x, ++it) {
       const W8Tile t = w8_tile(tile, routed_total, s_off, s_tt, p);
       const int buf = it & 1;
-      const uint32_t aph = (uint32_t)(it >> 1) & 1u;
+      const uint32_t acc_ph = (uint32_t)(it >> 1) & 1u;
       float* wsc = s_scale + (warp - 2) * kNT;
       const bool scale = MODE == 1 && !t.shared && p.topk_w != nullptr;
       if (scale) {
@@ -458,35 +551,35 @@ __global__ void __launch_bounds__(kThreads, 1)
         wsc[lane] = pr >= 0 ? __ldg(p.topk_w + pr) : 0.0f;
         __syncwarp();
       }
-      bool w = (lane == 0) ? mbar_wait_sleep(&tfull[buf], aph, abort_flag, p.timeout_ns, p.status) : false;
+      bool w = (lane == 0) ? mbar_wait_sleep(&tfull[buf], acc_ph, abort_flag, p.timeout_ns, p.status) : false;
       w = __shfl_sync(0xffffffffu, w, 0);
       if (!w) break;
       tc_fence_after();
       const uint32_t tb = tmem_base + ((uint32_t)(qw * 32) << 16) + (uint32_t)(buf * L::kAccCols);
+      uint32_t v[2][32];
+      tmem_ld32_async(tb, v[0]);
+      tmem_ld32_async(tb + kNT, v[1]);
+      tmem_wait_ld();
+      // release the accumulator at once: everything below works on registers
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&tempty[buf]);
       if (MODE == 0) {
-        uint32_t v[2][32];
-        tmem_ld32_async(tb, v[0]);
-        tmem_ld32_async(tb + kNT, v[1]);
-        tmem_wait_ld();
-        // release the accumulator early: everything below works on registers
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&tempty[buf]);
         // SwiGLU: lanes 0-15 hold gate rows, lanes 16-31 the up rows of the same features; the gate
         // lanes finish token columns 0-15, the up lanes columns 16-31
         const bool is_gate = lane < 16;
         float a[2][16];
 #pragma unroll
-        for (int part = 0; part < 2; ++part)
+        for (int half = 0; half < 2; ++half)
 #pragma unroll
           for (int i = 0; i < 16; ++i) {
-            const float send = __uint_as_float(is_gate ? v[part][16 + i] : v[part][i]);
+            const float send = __uint_as_float(is_gate ? v[half][16 + i] : v[half][i]);
             const float recv = __shfl_xor_sync(0xffffffffu, send, 16);
-            const float g = is_gate ? __uint_as_float(v[part][i]) : recv;
-            const float u = is_gate ? recv : __uint_as_float(v[part][16 + i]);
-            a[part][i] = __fdividef(g, 1.0f + __expf(-g)) * u;
+            const float g = is_gate ? __uint_as_float(v[half][i]) : recv;
+            const float u = is_gate ? recv : __uint_as_float(v[half][16 + i]);
+            a[half][i] = __fdividef(g, 1.0f + __expf(-g)) * u;
           }
-        // MXFP8 of act: per token column, the 32 features of this warp's block are 16 lanes x 2 parts
+        // MXFP8 of act: per token column, the 32 features of this warp's block are 16 lanes x 2 halves
         uint8_t* act = t.shared ? p.act_s : p.act;
         uint8_t* act_sf = t.shared ? p.act_sf_s : p.act_sf;
         const int n_feat = t.shared ? p.n_feat_s : p.n_feat;
@@ -525,21 +618,18 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
       } else {
-        uint32_t v[32];
-        tmem_ld32_async(tb, v);
-        tmem_wait_ld();
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&tempty[buf]);
         uint16_t* out = t.shared ? p.out_s : p.out;
         const int n_feat = t.shared ? p.n_feat_s : p.n_feat;
-        const int feat = t.f * L::kFeatPerTile + qw * 32 + lane;
-        float o[32];
 #pragma unroll
-        for (int i = 0; i < 32; ++i) o[i] = __uint_as_float(v[i]) * (scale ? wsc[i] : 1.0f);
-        uint16_t* orow = out + (size_t)t.row_base * n_feat + feat;
-        store_pairs16_bf16(o, lane, orow, (size_t)n_feat, 0, t.rows, feat < n_feat);
-        store_pairs16_bf16(o + 16, lane, orow, (size_t)n_feat, 16, t.rows, feat < n_feat);
+        for (int half = 0; half < 2; ++half) {
+          const int feat = t.f * L::kFeatPerTile + half * kBM + qw * 32 + lane;
+          float o[32];
+#pragma unroll
+          for (int i = 0; i < 32; ++i) o[i] = __uint_as_float(v[half][i]) * (scale ? wsc[i] : 1.0f);
+          uint16_t* orow = out + (size_t)t.row_base * n_feat + feat;
+          store_pairs16_bf16(o, lane, orow, (size_t)n_feat, 0, t.rows, feat < n_feat);
+          store_pairs16_bf16(o + 16, lane, orow, (size_t)n_feat, 16, t.rows, feat < n_feat);
+        }
         __syncwarp();  // the next tile rewrites this warp's routing weights
       }
     }
@@ -554,8 +644,10 @@ __global__ void __launch_bounds__(kThreads, 1)
 }
 
 // ---------------------------------------------------------------- one-time weight layout
-// codes [E, n_out, K/2], scales [E, n_out, K/32] (moe_mxfp4_quantize) -> codes_p [E*n_out, K/2]
-// (gate/up rows regrouped when gate_up) and the scale atoms sf_p [E*n_out/128][K/128][512].
+// codes [E, n_out, K/2], scales [E, n_out, K/32] (moe_mxfp4_quantize) -> codes_p
+// [E*n_out/256][K/128][256][64] (per 256-row tile and 128-K chunk, the tile's rows' 64 code bytes of
+// the chunk: every block the GEMM loads is one contiguous 16 KB; gate/up rows regrouped when gate_up)
+// and the scale atoms sf_p [E*n_out/256][K/128][2][512].
 // Gate/up (n_out = 2I, I % 128 == 0): packed row R of an expert, with tile = R / 256,
 // p = (R / 128) % 2, q = (R / 32) % 4, l = R % 32, is the gate (l < 16) or up (l >= 16) row of
 // feature 128 tile + 32 q + 16 p + l % 16.  One warp per packed row.
@@ -576,14 +668,20 @@ __global__ void __launch_bounds__(256) w4a8_prepack_kernel(const uint8_t* __rest
   }
   const long long srow = (long long)e * n_out + src;
   const uint4* cs = reinterpret_cast<const uint4*>(codes + srow * (K / 2));
-  uint4* cd = reinterpret_cast<uint4*>(codes_p + row * (K / 2));
-  for (int c = lane; c < K / 32; c += 32) cd[c] = __ldg(cs + c);
+  const long long tile256 = row / kTR;
+  const int r256 = (int)(row % kTR);
+  for (int c = lane; c < K / 32; c += 32) {  // 16-byte piece c of the row: K chunk c / 4
+    const long long blk = tile256 * (K / kKC) + c / 4;
+    uint4* cd = reinterpret_cast<uint4*>(codes_p + (blk * kTR + r256) * (kKC / 2));
+    cd[c % 4] = __ldg(cs + c);
+  }
   const int nb = K / 32;
-  const long long tile128 = row / kBM;
+  const int half = (int)((row / kBM) % 2);
   const int r = (int)(row % kBM);
   for (int b = lane; b < nb; b += 32) {
     const int chunk = b >> 2, kb = b & 3;
-    sf_p[(tile128 * (K / kKC) + chunk) * kSF + (r % 32) * 16 + (r / 32) * 4 + kb] = __ldg(scales + srow * nb + b);
+    sf_p[((tile256 * (K / kKC) + chunk) * 2 + half) * kSF + (r % 32) * 16 + (r / 32) * 4 + kb] =
+        __ldg(scales + srow * nb + b);
   }
 }
 
@@ -637,69 +735,40 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn_w8() {
   return fn;
 }
 
-// E2M1 codes [rows, K] (K/2 bytes per row) in 128-row x 128-code boxes, each 16 codes landing as 8
-// bytes followed by 8 zero bytes (the operand layout of the block-scaled MMA for 4-bit A), 128-byte
-// swizzle.
+// E2M1 codes in 256-row x 128-code boxes, each 16 codes landing as 8 bytes followed by 8 zero bytes
+// (the operand layout of the block-scaled MMA for 4-bit A), 128-byte swizzle.
+// The prepacked codes are seen as one matrix of (rows * K/128) rows of 128 codes (the chunk-major
+// blocks stacked): block (tile, chunk) starts at row (tile * K/128 + chunk) * 256.
 bool make_map_e2m1(CUtensorMap* m, const void* base, int K, long long rows) {
   auto fn = encode_fn_w8();
   if (!fn) return false;
-  cuuint64_t dims[2] = {(cuuint64_t)K, (cuuint64_t)rows};
-  cuuint64_t strides[1] = {(cuuint64_t)K / 2};
-  cuuint32_t box[2] = {(cuuint32_t)kKC, (cuuint32_t)kBM};
+  cuuint64_t dims[2] = {(cuuint64_t)kKC, (cuuint64_t)rows * (K / kKC)};
+  cuuint64_t strides[1] = {(cuuint64_t)kKC / 2};
+  cuuint32_t box[2] = {(cuuint32_t)kKC, (cuuint32_t)kTR};
   cuuint32_t estr[2] = {1, 1};
   return fn(m, CU_TENSOR_MAP_DATA_TYPE_16U4_ALIGN16B, 2, const_cast<void*>(base), dims, strides, box, estr,
             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// bytes [rows, width] in boxes of box_w x box_h (128-byte swizzle or none); rows past the end read as zeros.
-bool make_map_bytes(CUtensorMap* m, const void* base, long long width, long long rows, int box_w, int box_h,
-                    bool swizzle) {
-  auto fn = encode_fn_w8();
-  if (!fn) return false;
-  cuuint64_t dims[2] = {(cuuint64_t)width, (cuuint64_t)rows};
-  cuuint64_t strides[1] = {(cuuint64_t)width};
-  cuuint32_t box[2] = {(cuuint32_t)box_w, (cuuint32_t)box_h};
-  cuuint32_t estr[2] = {1, 1};
-  return fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box, estr,
-            CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
-            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
-
-template <int MODE, int STAGES>
+template <int MODE, int STAGES, int TSLOTS>
 cudaError_t launch_w8(const W4a8GemmProblem& pr, W8Params gp, cudaStream_t stream, bool pdl) {
-  using L = W8Layout<MODE, STAGES>;
+  using L = W8Layout<MODE, STAGES, TSLOTS>;
   const bool has_shared = gp.has_shared != 0;
-  CUtensorMap ta, tb, tsb, tas, tbs, tsbs;
-  if (pr.M > 0) {
-    if (!make_map_e2m1(&ta, pr.codes, pr.K, (long long)pr.E * pr.n_out)) return cudaErrorInvalidValue;
-    if (!make_map_bytes(&tb, pr.a_rows, pr.K, pr.M, kKC, kNT, true)) return cudaErrorInvalidValue;
-    if (!make_map_bytes(&tsb, pr.a_sf, pr.K / kKC * 16, pr.M, 16, kNT, false)) return cudaErrorInvalidValue;
-  }
-  if (has_shared) {
-    if (!make_map_e2m1(&tas, pr.s_codes, pr.K, pr.n_out_s)) return cudaErrorInvalidValue;
-    if (!make_map_bytes(&tbs, pr.s_rows, pr.K, pr.T_s, kKC, kNT, true)) return cudaErrorInvalidValue;
-    if (!make_map_bytes(&tsbs, pr.s_rows_sf, pr.K / kKC * 16, pr.T_s, 16, kNT, false)) return cudaErrorInvalidValue;
-  }
-  // With no routed rows the routed maps are never read (and vice versa): alias them.
-  if (pr.M <= 0) {
-    ta = tas;
-    tb = tbs;
-    tsb = tsbs;
-  } else if (!has_shared) {
-    tas = ta;
-    tbs = tb;
-    tsbs = tsb;
-  }
-  auto kern = grouped_gemm_w4a8_kernel<MODE, STAGES>;
+  CUtensorMap ta, tas;
+  if (pr.M > 0 && !make_map_e2m1(&ta, pr.codes, pr.K, (long long)pr.E * pr.n_out)) return cudaErrorInvalidValue;
+  if (has_shared && !make_map_e2m1(&tas, pr.s_codes, pr.K, pr.n_out_s)) return cudaErrorInvalidValue;
+  // with no routed rows the routed map is never read (and vice versa): alias them
+  if (pr.M <= 0) ta = tas;
+  else if (!has_shared) tas = ta;
+  auto kern = grouped_gemm_w4a8_kernel<MODE, STAGES, TSLOTS>;
   const size_t smem = L::bytes(gp.E);
   cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (err != cudaSuccess) return err;
   int dev = 0, n_sms = 0;
   cudaGetDevice(&dev);
   cudaDeviceGetAttribute(&n_sms, cudaDevAttrMultiProcessorCount, dev);
-  return launch_kernel(kern, dim3(n_sms > 0 ? n_sms : 1), dim3(kThreads), smem, stream, pdl, ta, tb, tsb, tas, tbs,
-                       tsbs, gp);
+  return launch_kernel(kern, dim3(n_sms > 0 ? n_sms : 1), dim3(kThreads), smem, stream, pdl, ta, tas, gp);
 }
 
 }  // namespace
@@ -714,7 +783,9 @@ cudaError_t launch_grouped_gemm_w4a8(const W4a8GemmProblem& pr, cudaStream_t str
   gp.K = pr.K;
   gp.n_out = pr.n_out;
   gp.n_feat = pr.mode == 0 ? pr.n_out / 2 : pr.n_out;
-  gp.n_ftiles = pr.mode == 0 ? pr.n_out / 256 : pr.n_out / 128;
+  gp.n_ftiles = pr.n_out / kTR;
+  gp.b_rows = pr.a_rows;
+  gp.b_sf = pr.a_sf;
   gp.sfa = pr.sf;
   gp.act = pr.act;
   gp.act_sf = pr.act_sf;
@@ -726,7 +797,9 @@ cudaError_t launch_grouped_gemm_w4a8(const W4a8GemmProblem& pr, cudaStream_t str
     gp.T_s = pr.T_s;
     gp.n_out_s = pr.n_out_s;
     gp.n_feat_s = pr.mode == 0 ? pr.n_out_s / 2 : pr.n_out_s;
-    gp.n_ftiles_s = pr.mode == 0 ? pr.n_out_s / 256 : pr.n_out_s / 128;
+    gp.n_ftiles_s = pr.n_out_s / kTR;
+    gp.bs_rows = pr.s_rows;
+    gp.bs_sf = pr.s_rows_sf;
     gp.sfa_s = pr.s_sf;
     gp.act_s = pr.s_act;
     gp.act_sf_s = pr.s_act_sf;
@@ -734,7 +807,7 @@ cudaError_t launch_grouped_gemm_w4a8(const W4a8GemmProblem& pr, cudaStream_t str
   }
   gp.status = pr.status;
   gp.timeout_ns = kTimeoutNs;
-  return pr.mode == 0 ? launch_w8<0, 5>(pr, gp, stream, pdl) : launch_w8<1, 10>(pr, gp, stream, pdl);
+  return pr.mode == 0 ? launch_w8<0, 4, 3>(pr, gp, stream, pdl) : launch_w8<1, 4, 3>(pr, gp, stream, pdl);
 }
 
 cudaError_t launch_w4a8_prepack(const uint8_t* codes, const uint8_t* scales, int E, int n_out, int K, int gate_up,

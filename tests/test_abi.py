@@ -216,9 +216,9 @@ def test_w4a8_validation_returns_before_launch(L):
     E = moe.MOE_ERR_INVALID_ARG
     U = moe.MOE_ERR_UNSUPPORTED
     # moe_w4a8_prepack(codes, scales, E, n_out, K, gate_up, codes_p, sf_p, stream)
-    assert L.moe_w4a8_prepack(P16, P16, 2, 128, 256, 1, P16 * 2, P16 * 3, None) == U   # gate/up: n_out % 256
-    assert L.moe_w4a8_prepack(P16, P16, 2, 128, 192, 0, P16 * 2, P16 * 3, None) == U   # K % 128
-    assert L.moe_w4a8_prepack(P16, P16, 2, 128, 256, 0, P16, P16 * 3, None) == E       # in place
+    assert L.moe_w4a8_prepack(P16, P16, 2, 128, 256, 1, P16 * 2, P16 * 3, None) == U   # n_out % 256
+    assert L.moe_w4a8_prepack(P16, P16, 2, 256, 192, 0, P16 * 2, P16 * 3, None) == U   # K % 128
+    assert L.moe_w4a8_prepack(P16, P16, 2, 256, 256, 0, P16, P16 * 3, None) == E       # in place
     # moe_gather_rows_mx(x_codes, x_scales, sorted_pair, T, k, H, M, out_codes, out_sf, ws, ws_bytes, stream)
     assert L.moe_gather_rows_mx(P16, P16, P16, 4, 2, 192, 8, P16, P16, P16, 256, None) == U        # H % 128
     assert L.moe_gather_rows_mx(P16, P16, None, 4, 1, 256, 8, None, P16, P16, 256, None) == E      # M > T, identity

@@ -63,7 +63,7 @@ def _mx4(w):
 
 
 # ---------------------------------------------------------------- layout kernels
-@pytest.mark.parametrize("gate_up,E,n_out,K", [(True, 2, 256, 256), (True, 1, 512, 128), (False, 3, 128, 384)])
+@pytest.mark.parametrize("gate_up,E,n_out,K", [(True, 2, 256, 256), (True, 1, 512, 128), (False, 3, 256, 384)])
 def test_w4a8_prepack_layout(moe, gate_up, E, n_out, K):
     rng = np.random.default_rng(E + n_out + K)
     codes = rng.integers(0, 256, size=(E, n_out, K // 2), dtype=np.uint8)
@@ -76,14 +76,16 @@ def test_w4a8_prepack_layout(moe, gate_up, E, n_out, K):
         src = np.where(R % 32 < 16, f, I + f)
     else:
         src = R
-    want_codes = codes[:, src, :].reshape(E * n_out, K // 2)
+    rows = codes[:, src, :].reshape(E * n_out // 256, 256, K // 128, 64)
+    want_codes = rows.transpose(0, 2, 1, 3)  # [tile, chunk, row, 64 bytes]
     assert (host(w.codes) == want_codes).all()
     sc = scales[:, src, :].reshape(E * n_out, K // 32)
-    want_sf = np.zeros((E * n_out // 128, K // 128, 512), np.uint8)
+    want_sf = np.zeros((E * n_out // 256, K // 128, 2, 512), np.uint8)
     for row in range(E * n_out):
-        t, r = divmod(row, 128)
+        t, r = divmod(row, 256)
+        half, r = divmod(r, 128)
         for b in range(K // 32):
-            want_sf[t, b // 4, (r % 32) * 16 + (r // 32) * 4 + b % 4] = sc[row, b]
+            want_sf[t, b // 4, half, (r % 32) * 16 + (r // 32) * 4 + b % 4] = sc[row, b]
     assert (host(w.sf) == want_sf).all()
 
 
@@ -113,7 +115,8 @@ GEMM_CASES = [
     # tiles in one expert), K of one and of several 128-K stages
     ([3, 0, 1, 32, 33, 0, 70, 5], 256, 128),
     ([1] * 12 + [0] * 4, 512, 256),
-    ([40, 2, 0, 9], 1024, 384),
+    ([40, 2, 0, 9], 1024, 384),          # I = 384: a window of 3 chunks in the down GEMM
+    ([2, 0, 65, 7], 768, 640),           # H = 768: 6 chunks (a full and a partial window); I = 640: 5
 ]
 
 
@@ -217,7 +220,7 @@ def _run_layer(moe, cfg, inp, tokens=None):
 LAYER_CASES = [
     mi.CONFIGS["tiny"],
     mi.CONFIGS["hy3_decode"].with_(T=8, H=256, E=16, k=4, I=128, I_s=128),        # + shared expert
-    mi.CONFIGS["hy3_decode"].with_(T=6, H=384, E=8, k=2, I=256, I_s=128),         # I_s != I
+    mi.CONFIGS["hy3_decode"].with_(T=6, H=512, E=8, k=2, I=256, I_s=128),         # I_s != I
     mi.CONFIGS["qwen3_decode"].with_(T=300, H=256, E=4, k=2, I=128),              # several token tiles per expert
     mi.CONFIGS["qwen3_decode"].with_(T=1, H=512, E=32, k=8, I=256),
 ]
