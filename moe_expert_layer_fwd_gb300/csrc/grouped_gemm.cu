@@ -492,6 +492,7 @@ __global__ void __launch_bounds__(64 + 32 * (EPI + GW), 1)
       const int ew = warp - 2;
       const int g_rows = min(p.M, s_off[E]);  // rows past offsets[E] are never read
       const int n_chunks = (g_rows + kGatherRows - 1) / kGatherRows;
+      bool bad = false;  // an out-of-range row source, reported once after the loop
       for (int g = 0; g < GW; ++g) {
         const int q = GW * (int)blockIdx.x + g;
         if (q >= n_chunks) break;  // uniform over the epilogue warps
@@ -500,7 +501,7 @@ __global__ void __launch_bounds__(64 + 32 * (EPI + GW), 1)
           const int sp = __ldg(p.g_sp + r0 + i);
           const int t = sp / p.g_k;
           if (sp < 0 || (unsigned)t >= (unsigned)p.g_T) {
-            if (lane == 0) set_status(p.status, DEV_ERR_BOUNDS);
+            bad = true;
             continue;
           }
           const uint4* src = p.g_x + (size_t)t * p.g_H8;
@@ -523,6 +524,7 @@ __global__ void __launch_bounds__(64 + 32 * (EPI + GW), 1)
           st_release_gpu(p.g_flags + q, 1u);
         }
       }
+      if (bad && lane == 0) set_status(p.status, DEV_ERR_BOUNDS);
     }
     int it = 0;
     for (int tile = group; tile < total; tile += ngroups, ++it) {
@@ -624,6 +626,7 @@ __global__ void __launch_bounds__(64 + 32 * (EPI + GW), 1)
     const int n_chunks = (g_rows + kGatherRows - 1) / kGatherRows;
     const int H8 = p.g_H8;
     // the CTA's first GW chunks are gathered by the epilogue warps
+    bool bad = false;  // an out-of-range row source, reported once after the loop
     for (int q = GW * ((int)blockIdx.x + (int)gridDim.x) + gw; q < n_chunks; q += GW * (int)gridDim.x) {
       const int r0 = q * kGatherRows, nrow = min(kGatherRows, g_rows - r0);
       int tl = -1;  // lane i < nrow: source token of row r0 + i
@@ -632,7 +635,7 @@ __global__ void __launch_bounds__(64 + 32 * (EPI + GW), 1)
         tl = sp / p.g_k;
         if (sp < 0 || (unsigned)tl >= (unsigned)p.g_T) {
           tl = -1;
-          set_status(p.status, DEV_ERR_BOUNDS);
+          bad = true;
         }
       }
       for (int i = 0; i < nrow; i += 4) {
@@ -663,6 +666,7 @@ __global__ void __launch_bounds__(64 + 32 * (EPI + GW), 1)
         st_release_gpu(p.g_flags + q, 1u);
       }
     }
+    if (bad) set_status(p.status, DEV_ERR_BOUNDS);
   }
 
   tc_fence_before();

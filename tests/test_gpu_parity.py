@@ -194,20 +194,29 @@ def test_grouped_gemm_swiglu_gathers_its_rows(moe, T, k, E, H, I, skew):
     assert _torch().equal(act.view(_torch().int16), pre.view(_torch().int16))
 
 
-@pytest.mark.parametrize("T,k,E,H,I", [(8, 2, 4, 256, 128), (1000, 4, 8, 256, 128)])
-def test_grouped_gemm_swiglu_flags_bad_row_src(moe, T, k, E, H, I):
-    """A source row outside [0, T*k) is skipped and reported, by the separate gather kernel (the first
-    shape) and by the gather inside the GEMM (the second), without stalling the GEMM."""
+@pytest.mark.parametrize("T,E,bad", [(8, 4, 21), (300, 4, -1), (1200, 4, 2405)],
+                         ids=["decode", "streaming", "compute-bound"])
+def test_grouped_gemm_swiglu_flags_bad_row_src(moe, T, E, bad):
+    """A source row outside [0, T*k) is reported (its row of act is unspecified) on each instance
+    family, by the separate gather kernel (decode, streaming) or the gather inside the GEMM
+    (compute-bound), without stalling the GEMM; every other row is still right."""
     torch = _torch()
+    k, H, I = 2, 256, 128
     idx = np.array([[e % E, (e + 1) % E] for e in range(T)], np.int32)
     _, off, sp, _ = oracle.init_routing(idx, E)
     sp = sp.copy()
-    sp[3] = T * k + 5  # outside [0, T*k)
+    sp[3] = bad  # outside [0, T*k)
     x = mi.normal_bf16(3, 1, (T, H))
     w13 = mi.normal_bf16(3, 2, (E, 2 * I, H), 0.0, 0.02)
     ws = torch.zeros(moe.lib().moe_grouped_gemm_swiglu_workspace_size(T * k, H, 1), dtype=torch.uint8, device="cuda")
-    moe.moe_grouped_gemm_swiglu(dev_bf16(x), moe.moe_prepack_w13(dev_bf16(w13)), dev(off), ws=ws, row_src=dev(sp), k=k)
+    act = moe.moe_grouped_gemm_swiglu(dev_bf16(x), moe.moe_prepack_w13(dev_bf16(w13)), dev(off), ws=ws,
+                                      row_src=dev(sp), k=k)
     assert moe.moe_get_device_status(ws) == moe.MOE_ERR_DEVICE_CHECK
+    sp_ok = sp.copy()
+    sp_ok[3] = 0
+    ref = oracle.grouped_gemm_swiglu(oracle.expand_rows(x, sp_ok, k), w13, off)
+    keep = np.arange(T * k) != 3
+    assert_close(host_bf16_f64(act)[keep], ref[keep], "act rows with a valid source")
 
 
 @pytest.mark.parametrize("counts,H,I", GEMM_CASES)

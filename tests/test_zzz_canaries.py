@@ -71,8 +71,14 @@ def test_guards_around_every_output(moe):
 
     # a3, a4, a6
     act = Guarded((P, I), torch.bfloat16, 7.0)
-    moe.moe_grouped_gemm_swiglu(outs["x_exp"].t, moe.moe_prepack_w13(dev_bf16(inp.w13)), off, act=act.t)
+    w13p = moe.moe_prepack_w13(dev_bf16(inp.w13))
+    moe.moe_grouped_gemm_swiglu(outs["x_exp"].t, w13p, off, act=act.t)
     assert act.intact()
+    # the same GEMM gathering its rows from x: writes only act, and the same bits
+    act_g = Guarded((P, I), torch.bfloat16, 7.0)
+    moe.moe_grouped_gemm_swiglu(x, w13p, off, act=act_g.t, row_src=sp, k=k)
+    assert act_g.intact()
+    assert torch.equal(act_g.t.view(torch.int16), act.t.view(torch.int16))
     yp = Guarded((P, H), torch.bfloat16, 7.0)
     moe.moe_grouped_gemm(act.t, dev_bf16(inp.w2), off, tw.t, sp, out=yp.t)
     assert yp.intact()
