@@ -571,14 +571,15 @@ int layer_forward_impl(const moe_layer_desc* d, const uint16_t* x, const float* 
   auto mark = [&](int i) {
     return events ? cudaEventRecord(reinterpret_cast<cudaEvent_t>(events[i]), st) : cudaSuccess;
   };
+  // Every kernel may start while its predecessor on the stream finishes (programmatic dependent
+  // launch; for gating that is whatever the caller ran before, e.g. the previous layer's
+  // finalize); each waits for its predecessor's completion before touching memory.
+  constexpr bool kPdl = true;
   if (mark(0) != cudaSuccess) return MOE_ERR_CUDA;
   cudaError_t e = moe::launch_gating_topk(logits, bias, T, E, k, d->gate, d->routed_scaling_factor, d->eps,
-                                          topk_w, topk_idx, st);
+                                          topk_w, topk_idx, st, kPdl);
   if (e != cudaSuccess) return MOE_ERR_CUDA;
   if (mark(1) != cudaSuccess) return MOE_ERR_CUDA;
-  // Every kernel after the first may start while its predecessor finishes (programmatic
-  // dependent launch); each waits for its inputs before touching them.
-  constexpr bool kPdl = true;
   // A compute-bound gate/up GEMM gathers the token rows into x_exp itself (overlapping the
   // gather with its matmuls): routing then only sorts, and clears the GEMM's gather flags.
   // Otherwise routing ends with the row gather kernel.
@@ -787,7 +788,7 @@ int layer_forward_w4a8_impl(const moe_layer_desc* d, const uint8_t* x_codes, con
   constexpr bool kPdl = true;
   if (mark(0) != cudaSuccess) return MOE_ERR_CUDA;
   if (moe::launch_gating_topk(logits, bias, T, E, k, d->gate, d->routed_scaling_factor, d->eps, topk_w, topk_idx,
-                              st) != cudaSuccess)
+                              st, kPdl) != cudaSuccess)
     return MOE_ERR_CUDA;
   if (mark(1) != cudaSuccess) return MOE_ERR_CUDA;
   if (moe::launch_init_routing(topk_idx, P, E, k, nullptr, H, nullptr, counts, offsets, sorted_pair, pair_pos,
