@@ -94,6 +94,21 @@ def test_layer_all_tokens_on_one_expert(moe):
     assert_close(host_bf16_f64(layer.y), ref["y"], "y")
 
 
+def test_layer_empty_batch(moe):
+    """T = 0: nothing to compute, no launch, MOE_OK."""
+    import torch
+    cfg = mi.CONFIGS["tiny"]
+    inp = mi.generate(cfg)
+    layer = moe.MoELayer(0, cfg.H, cfg.E, cfg.k, cfg.I, cfg.gate)
+    assert moe.moe_layer_kernel_launches(layer.desc) == 0
+    y = layer.forward(x=torch.empty((0, cfg.H), dtype=torch.bfloat16, device="cuda"),
+                      logits=torch.empty((0, cfg.E), dtype=torch.float32, device="cuda"),
+                      w13=moe.moe_prepack_w13(dev_bf16(inp.w13)), w2=dev_bf16(inp.w2))
+    torch.cuda.synchronize()
+    assert y.shape == (0, cfg.H)
+    assert moe.moe_get_device_status(layer.ws) == moe.MOE_OK
+
+
 def test_layer_is_deterministic(moe):
     cfg = mi.CONFIGS["hy3_decode"]
     inp = mi.generate(cfg)

@@ -223,6 +223,8 @@ LAYER_CASES = [
     mi.CONFIGS["hy3_decode"].with_(T=6, H=512, E=8, k=2, I=256, I_s=128),         # I_s != I
     mi.CONFIGS["qwen3_decode"].with_(T=300, H=256, E=4, k=2, I=128),              # several token tiles per expert
     mi.CONFIGS["qwen3_decode"].with_(T=1, H=512, E=32, k=8, I=256),
+    # the documented limits: E = 1024 experts, k = 32
+    mi.CONFIGS["tiny"].with_(T=64, H=256, E=1024, k=32, I=128),
 ]
 
 
@@ -240,3 +242,31 @@ def test_w4a8_layer_full_size_sampled_tokens(moe, name):
     tokens = np.array([0, cfg.T // 3, 2 * cfg.T // 3, cfg.T - 1])
     got, ref = _run_layer(moe, cfg, mi.generate(cfg), tokens)
     assert_close(got, ref["y"], f"W4A8 layer {name}")
+
+
+def test_w4a8_layer_all_tokens_on_one_expert(moe):
+    """One expert takes every token (300 rows: ten 32-row token tiles of one expert), the rest share the
+    other slot."""
+    cfg = mi.CONFIGS["tiny"].with_(T=300, E=8, k=2)
+    inp = mi.generate(cfg)
+    inp.logits[:, 5] = 50.0  # every token picks expert 5 first
+    got, ref = _run_layer(moe, cfg, inp)
+    assert ref["counts"][5] == cfg.T
+    assert_close(got, ref["y"], "W4A8 layer, one expert")
+
+
+def test_w4a8_layer_empty_batch(moe):
+    """T = 0: nothing to compute, no launch, MOE_OK."""
+    torch = _torch()
+    cfg = mi.CONFIGS["tiny"]
+    layer = moe.W4a8Layer(0, cfg.H, cfg.E, cfg.k, cfg.I, cfg.gate)
+    assert layer.launches == 0
+    inp = mi.generate(cfg)
+    q = lambda w, gu: moe.moe_w4a8_prepack(*moe.moe_mxfp4_quantize(dev_bf16(w)), gate_up=gu)
+    xc = torch.empty((0, cfg.H), dtype=torch.uint8, device="cuda")
+    xs = torch.empty((0, cfg.H // 32), dtype=torch.uint8, device="cuda")
+    lg = torch.empty((0, cfg.E), dtype=torch.float32, device="cuda")
+    y = layer.forward(xc, xs, lg, q(inp.w13, True), q(inp.w2, False))
+    torch.cuda.synchronize()
+    assert y.shape == (0, cfg.H)
+    assert moe.moe_get_device_status(layer.ws) == moe.MOE_OK
