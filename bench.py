@@ -69,7 +69,10 @@ def _args(argv=None):
     ap.add_argument("--profile-w4a8", action="store_true",
                     help="with --profile-steps: the W4A8 layer loop instead (for ncu launch lists and captures)")
     ap.add_argument("--cpu-baseline-child", action="store_true", help=argparse.SUPPRESS)
-    ap.add_argument("--sample-tokens", type=int, default=8)
+    ap.add_argument("--sample-tokens", type=int, default=0,
+                    help="tokens of the CPU-baseline sample (0: as many as fit about --cpu-seconds of oracle time)")
+    ap.add_argument("--cpu-seconds", type=float, default=10.0,
+                    help="target oracle time of the CPU-baseline sample when --sample-tokens is 0")
     ap.add_argument("--profile-steps", action="store_true",
                     help="plain moe_layer_forward loop only (for ncu launch lists)")
     ap.add_argument("--override", default="",
@@ -244,24 +247,46 @@ def oracle_inputs(cfg, tokens):
     return inp
 
 
+def _spread(n, T):
+    """n token indices spread evenly over [0, T)."""
+    import numpy as np
+    return np.unique(np.linspace(0, T - 1, n).round().astype(np.int64))
+
+
 def cpu_baseline_child(args):
-    """Runs in a subprocess with the BLAS thread count fixed: times the oracle on a token sample."""
+    """Runs in a subprocess with the BLAS thread count fixed: times the oracle on a token sample --
+    args.sample_tokens tokens, or (0) a sample grown 4x at a time from 8 tokens until one run takes at
+    least half of args.cpu_seconds or covers the batch (the oracle's time grows with the experts a
+    sample touches, not in proportion to its tokens); tokens spread evenly over the batch.  Input
+    generation is outside the timed region."""
     import numpy as np
     import oracle
     cfg = workload(args)
-    n = min(args.sample_tokens, cfg.T)
-    toks = np.arange(n)
-    inp = oracle_inputs(cfg, toks)
-    t0 = time.perf_counter()
-    oracle.moe_layer_forward_tokens(toks, inp.x, inp.logits, cfg.k, cfg.gate, inp.w13, inp.w2, inp.bias,
-                                    cfg.routed_scaling_factor, cfg.eps, inp.w13_s, inp.w2_s)
-    dt = time.perf_counter() - t0
-    print(json.dumps({"tokens": n, "seconds": dt}))
+
+    def run(toks):
+        inp = oracle_inputs(cfg, toks)
+        t0 = time.perf_counter()
+        oracle.moe_layer_forward_tokens(toks, inp.x, inp.logits, cfg.k, cfg.gate, inp.w13, inp.w2, inp.bias,
+                                        cfg.routed_scaling_factor, cfg.eps, inp.w13_s, inp.w2_s)
+        return time.perf_counter() - t0
+
+    if args.sample_tokens > 0:
+        toks = _spread(min(args.sample_tokens, cfg.T), cfg.T)
+        dt = run(toks)
+    else:
+        n = min(8, cfg.T)
+        while True:
+            toks = _spread(n, cfg.T)
+            dt = run(toks)
+            if dt >= args.cpu_seconds / 2 or n >= cfg.T:
+                break
+            n = min(cfg.T, 4 * n)
+    print(json.dumps({"tokens": int(len(toks)), "seconds": dt}))
 
 
 def cpu_baseline(args, cores=None, workload_name=None, override=None):
-    """The oracle timed on `args.sample_tokens` tokens of a workload, in a child process on `cores`
-    host threads (default: all of this process's affinity set)."""
+    """The oracle timed on a sample of a workload's tokens (cpu_baseline_child), in a child process on
+    `cores` host threads (default: all of this process's affinity set)."""
     workload_name = workload_name or args.workload
     override = args.override if override is None else override
     cores = cores or len(os.sched_getaffinity(0))
@@ -269,16 +294,16 @@ def cpu_baseline(args, cores=None, workload_name=None, override=None):
     for k in ("RANK", "WORLD_SIZE", "LOCAL_RANK", "MASTER_ADDR", "MASTER_PORT"):
         env.pop(k, None)
     cmd = [sys.executable, os.path.join(ROOT, "bench.py"), "--cpu-baseline-child", "--workload", workload_name,
-           "--sample-tokens", str(args.sample_tokens), "--override", override]
+           "--sample-tokens", str(args.sample_tokens), "--cpu-seconds", str(args.cpu_seconds), "--override", override]
     r = subprocess.run(cmd, env=env, capture_output=True, text=True, timeout=900)
     if r.returncode != 0:
         return {"value": None, "unit": "tokens/s", "cores": cores, "kind": "oracle",
                 "error": r.stderr.strip().splitlines()[-1:] }
     d = json.loads(r.stdout.strip().splitlines()[-1])
     return {"value": d["tokens"] / d["seconds"], "unit": "tokens/s", "cores": cores, "kind": "oracle",
-            "sample": f"{d['tokens']} tokens of the {workload_name} workload (routing of all tokens, expert FFNs of the "
-                      f"sampled tokens, float64 numpy with BLAS on {cores} thread{'s' if cores > 1 else ''}): "
-                      f"{d['seconds']:.2f} s"}
+            "sample": f"{d['tokens']} tokens spread over the {workload_name} workload (routing of all tokens, "
+                      f"expert FFNs of the sampled tokens, float64 numpy with BLAS on {cores} "
+                      f"thread{'s' if cores > 1 else ''}): {d['seconds']:.2f} s"}
 
 
 # ------------------------------------------------------------------ reference arm (the oracle)
