@@ -519,7 +519,9 @@ MOE_API int moe_layer_forward(const moe_layer_desc* d, const uint16_t* x, const 
  * per-step device timing: events[0] before gating, [1] before init-routing,
  * [2] before the gate/up grouped GEMM, [3] before the down grouped GEMM(s),
  * [4] before finalize, [5] after finalize.  n_events must be 6; the events
- * stay owned by the caller. */
+ * stay owned by the caller.  A small batch (T*k <= 4096, rows gathered by a separate kernel)
+ * is gated and sorted by one kernel, between events[0] and [1]; between [1] and [2] there is
+ * then only the row gather. */
 MOE_API int moe_layer_forward_events(const moe_layer_desc* d, const uint16_t* x, const float* logits,
                                      const float* bias, const uint16_t* w13, const uint16_t* w2,
                                      const uint16_t* w13_s, const uint16_t* w2_s, uint16_t* y, float* topk_w,
@@ -527,7 +529,10 @@ MOE_API int moe_layer_forward_events(const moe_layer_desc* d, const uint16_t* x,
                                      void* const* events, int n_events);
 
 /* Number of kernel launches one moe_layer_forward call makes for this shape
- * (0 if the shape is invalid). */
+ * (0 if the shape is invalid or T == 0): gating 1 + routing 3 (the four in 1 for T*k <= 4096
+ * when the rows are gathered by a separate kernel) + row gather 1 (unless the compute-bound
+ * gate/up GEMM gathers its rows itself) + gate/up 1 + down 1 (+1 for a shared expert with
+ * I_s != I) + finalize 1. */
 MOE_API int moe_layer_kernel_launches(const moe_layer_desc* d);
 
 /* Byte offsets, inside the moe_layer_forward workspace, of its intermediates

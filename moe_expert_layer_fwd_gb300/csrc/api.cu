@@ -575,18 +575,29 @@ int layer_forward_impl(const moe_layer_desc* d, const uint16_t* x, const float* 
   // launch; for gating that is whatever the caller ran before, e.g. the previous layer's
   // finalize); each waits for its predecessor's completion before touching memory.
   constexpr bool kPdl = true;
-  if (mark(0) != cudaSuccess) return MOE_ERR_CUDA;
-  cudaError_t e = moe::launch_gating_topk(logits, bias, T, E, k, d->gate, d->routed_scaling_factor, d->eps,
-                                          topk_w, topk_idx, st, kPdl);
-  if (e != cudaSuccess) return MOE_ERR_CUDA;
-  if (mark(1) != cudaSuccess) return MOE_ERR_CUDA;
   // A compute-bound gate/up GEMM gathers the token rows into x_exp itself (overlapping the
   // gather with its matmuls): routing then only sorts, and clears the GEMM's gather flags.
-  // Otherwise routing ends with the row gather kernel.
+  // Otherwise routing ends with the row gather kernel.  A small batch (decode) is gated and
+  // sorted by one kernel instead of four.
   const bool inline_gather = moe::grouped_gemm_gathers_inline(P, E, sh, T);
-  e = moe::launch_init_routing(topk_idx, P, E, k, inline_gather ? nullptr : x, H, inline_gather ? nullptr : x_exp,
-                               counts, offsets, sorted_pair, pair_pos, scratch, status, st, kPdl,
-                               inline_gather ? gflags : nullptr, inline_gather ? (P + 15) / 16 : 0);
+  const bool small = !inline_gather && moe::gate_route_small_fits(T, E, k);
+  if (mark(0) != cudaSuccess) return MOE_ERR_CUDA;
+  cudaError_t e;
+  if (small) {
+    e = moe::launch_gate_route_small(logits, bias, T, E, k, d->gate, d->routed_scaling_factor, d->eps, topk_w,
+                                     topk_idx, counts, offsets, sorted_pair, pair_pos, st, kPdl);
+    if (e != cudaSuccess) return MOE_ERR_CUDA;
+    if (mark(1) != cudaSuccess) return MOE_ERR_CUDA;
+    e = moe::launch_expand_rows(x, sorted_pair, P, k, H, x_exp, st, kPdl);
+  } else {
+    e = moe::launch_gating_topk(logits, bias, T, E, k, d->gate, d->routed_scaling_factor, d->eps, topk_w, topk_idx,
+                                st, kPdl);
+    if (e != cudaSuccess) return MOE_ERR_CUDA;
+    if (mark(1) != cudaSuccess) return MOE_ERR_CUDA;
+    e = moe::launch_init_routing(topk_idx, P, E, k, inline_gather ? nullptr : x, H, inline_gather ? nullptr : x_exp,
+                                 counts, offsets, sorted_pair, pair_pos, scratch, status, st, kPdl,
+                                 inline_gather ? gflags : nullptr, inline_gather ? (P + 15) / 16 : 0);
+  }
   if (e != cudaSuccess) return MOE_ERR_CUDA;
 
   moe::GroupedGemmProblem g1{};
@@ -693,12 +704,13 @@ int moe_layer_forward_events(const moe_layer_desc* d, const uint16_t* x, const f
 int moe_layer_kernel_launches(const moe_layer_desc* d) {
   if (check_desc(d)) return 0;
   if (d->T == 0) return 0;
-  // gating 1 + routing (hist, scan, scatter) 3 + row gather 1 (unless the gate/up GEMM gathers
-  // its rows itself) + gate/up GEMM 1 + down GEMM 1 (+1 when the shared expert's intermediate
-  // size differs) + finalize 1
+  // gating 1 + routing (hist, scan, scatter) 3, or both in 1 for a small batch + row gather 1
+  // (unless the gate/up GEMM gathers its rows itself) + gate/up GEMM 1 + down GEMM 1 (+1 when the
+  // shared expert's intermediate size differs) + finalize 1
   const bool sh = d->n_shared > 0;
   const bool gather_kernel = !moe::grouped_gemm_gathers_inline(d->T * d->k, d->E, sh, d->T);
-  return 7 + (gather_kernel ? 1 : 0) + ((sh && d->I_s != d->I) ? 1 : 0);
+  const bool small = gather_kernel && moe::gate_route_small_fits(d->T, d->E, d->k);
+  return (small ? 1 : 4) + 3 + (gather_kernel ? 1 : 0) + ((sh && d->I_s != d->I) ? 1 : 0);
 }
 
 }  // extern "C"
@@ -787,13 +799,20 @@ int layer_forward_w4a8_impl(const moe_layer_desc* d, const uint8_t* x_codes, con
   };
   constexpr bool kPdl = true;
   if (mark(0) != cudaSuccess) return MOE_ERR_CUDA;
-  if (moe::launch_gating_topk(logits, bias, T, E, k, d->gate, d->routed_scaling_factor, d->eps, topk_w, topk_idx,
-                              st, kPdl) != cudaSuccess)
-    return MOE_ERR_CUDA;
-  if (mark(1) != cudaSuccess) return MOE_ERR_CUDA;
-  if (moe::launch_init_routing(topk_idx, P, E, k, nullptr, H, nullptr, counts, offsets, sorted_pair, pair_pos,
-                               scratch, status, st, kPdl) != cudaSuccess)
-    return MOE_ERR_CUDA;
+  if (moe::gate_route_small_fits(T, E, k)) {  // a small batch (decode): gated and sorted by one kernel
+    if (moe::launch_gate_route_small(logits, bias, T, E, k, d->gate, d->routed_scaling_factor, d->eps, topk_w,
+                                     topk_idx, counts, offsets, sorted_pair, pair_pos, st, kPdl) != cudaSuccess)
+      return MOE_ERR_CUDA;
+    if (mark(1) != cudaSuccess) return MOE_ERR_CUDA;
+  } else {
+    if (moe::launch_gating_topk(logits, bias, T, E, k, d->gate, d->routed_scaling_factor, d->eps, topk_w, topk_idx,
+                                st, kPdl) != cudaSuccess)
+      return MOE_ERR_CUDA;
+    if (mark(1) != cudaSuccess) return MOE_ERR_CUDA;
+    if (moe::launch_init_routing(topk_idx, P, E, k, nullptr, H, nullptr, counts, offsets, sorted_pair, pair_pos,
+                                 scratch, status, st, kPdl) != cudaSuccess)
+      return MOE_ERR_CUDA;
+  }
   // the routed MXFP8 rows in expert order, and (shared expert) the padded scale rows of x itself
   if (moe::launch_gather_rows_mx(x_codes, x_scales, sorted_pair, P, k, T, H, x8, x8_sf, nullptr, status, st,
                                  kPdl) != cudaSuccess)
@@ -912,10 +931,11 @@ int moe_layer_forward_w4a8_events(const moe_layer_desc* d, const uint8_t* x_code
 
 int moe_w4a8_layer_kernel_launches(const moe_layer_desc* d) {
   if (check_desc_w4a8(d) || d->T == 0) return 0;
-  // gating 1 + routing 3 + MXFP8 row gather 1 (+1 for the shared expert's scale rows) + gate/up GEMM 1
-  // + down GEMM 1 (+1 when I_s != I) + finalize 1
+  // gating 1 + routing 3 (both in 1 for a small batch) + MXFP8 row gather 1 (+1 for the shared
+  // expert's scale rows) + gate/up GEMM 1 + down GEMM 1 (+1 when I_s != I) + finalize 1
   const bool sh = d->n_shared > 0;
-  return 8 + (sh ? 1 : 0) + ((sh && d->I_s != d->I) ? 1 : 0);
+  const bool small = moe::gate_route_small_fits(d->T, d->E, d->k);
+  return (small ? 1 : 4) + 4 + (sh ? 1 : 0) + ((sh && d->I_s != d->I) ? 1 : 0);
 }
 
 }  // extern "C"

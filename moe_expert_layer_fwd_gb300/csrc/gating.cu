@@ -60,18 +60,12 @@ __device__ __forceinline__ float warp_sum(float v) {
   return v;
 }
 
-// VPL = keys held per lane (E <= 32 * VPL); a compile-time bound keeps them in registers.
+// Top-k of token t by one warp.  VPL = keys held per lane (E <= 32 * VPL); a compile-time bound
+// keeps them in registers.  Lane j < k writes the j-th choice; returns it (-1 on lanes >= k).
 template <int VPL>
-__global__ void __launch_bounds__(256) gating_topk_kernel(const float* __restrict__ logits,
-                                                          const float* __restrict__ bias, int T, int E, int k,
-                                                          int gate, float rsf, float eps,
-                                                          float* __restrict__ topk_w,
-                                                          int32_t* __restrict__ topk_idx) {
-  pdl_wait();
-  pdl_launch_dependents();
-  const int lane = threadIdx.x & 31;
-  const int t = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
-  if (t >= T) return;
+__device__ __forceinline__ int gate_token(const float* __restrict__ logits, const float* __restrict__ bias, int t,
+                                          int E, int k, int gate, float rsf, float eps, float* __restrict__ topk_w,
+                                          int32_t* __restrict__ topk_idx, int lane) {
   const float* row = logits + (size_t)t * E;
   uint32_t keys[VPL];
 #pragma unroll
@@ -122,6 +116,113 @@ __global__ void __launch_bounds__(256) gating_topk_kernel(const float* __restric
     topk_w[(size_t)t * k + lane] = w;
     topk_idx[(size_t)t * k + lane] = my_e;
   }
+  return lane < k ? my_e : -1;
+}
+
+template <int VPL>
+__global__ void __launch_bounds__(256) gating_topk_kernel(const float* __restrict__ logits,
+                                                          const float* __restrict__ bias, int T, int E, int k,
+                                                          int gate, float rsf, float eps,
+                                                          float* __restrict__ topk_w,
+                                                          int32_t* __restrict__ topk_idx) {
+  pdl_wait();
+  pdl_launch_dependents();
+  const int lane = threadIdx.x & 31;
+  const int t = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+  if (t >= T) return;
+  gate_token<VPL>(logits, bias, t, E, k, gate, rsf, eps, topk_w, topk_idx, lane);
+}
+
+// Gating and init-routing of a small batch (P = T*k <= kSmallPairs) in one CTA of 32 warps: the
+// four launches of gating, histogram, scan and scatter become one (decode: their launch and
+// hand-over latencies are most of their time).  Same results, bit for bit:
+//   1. warp w gates tokens w, w + 32, ...; the choices also go to shared memory (pair order);
+//   2. warp w takes pairs [w*CH, (w+1)*CH) and counts them per expert (shared-memory atomics:
+//      counts do not depend on order);
+//   3. thread e sums expert e over the warps (counts), a block scan gives offsets, and thread e
+//      turns the per-warp counts into each warp's first position for expert e;
+//   4. warp w walks its pairs in ascending order, 32 at a time: lanes with the same expert are
+//      grouped by __match_any_sync and ranked by the lower lanes of their group, so positions
+//      follow pair order (the stable sort) with no atomics deciding the order.
+constexpr int kSmallPairs = 4096;
+constexpr int kSmallWarps = 32;
+
+template <int VPL>
+__global__ void __launch_bounds__(kSmallWarps * 32) gate_route_small_kernel(
+    const float* __restrict__ logits, const float* __restrict__ bias, int T, int E, int k, int gate, float rsf,
+    float eps, float* __restrict__ topk_w, int32_t* __restrict__ topk_idx, int32_t* __restrict__ counts,
+    int32_t* __restrict__ offsets, int32_t* __restrict__ sorted_pair, int32_t* __restrict__ pair_pos) {
+  extern __shared__ int sh[];
+  const int P = T * k;
+  int* idx_s = sh;                               // [P] the chosen expert of every pair
+  int* hist = sh + kSmallPairs;                  // [kSmallWarps][E] counts, then first positions
+  __shared__ int wsum[kSmallWarps];
+  pdl_wait();
+  pdl_launch_dependents();
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, tid = threadIdx.x;
+  for (int i = tid; i < kSmallWarps * E; i += blockDim.x) hist[i] = 0;
+  for (int t = warp; t < T; t += kSmallWarps) {
+    const int e = gate_token<VPL>(logits, bias, t, E, k, gate, rsf, eps, topk_w, topk_idx, lane);
+    if (lane < k) idx_s[t * k + lane] = e;
+  }
+  __syncthreads();
+  const int CH = ((P + kSmallWarps - 1) / kSmallWarps + 31) & ~31;  // pairs per warp, whole steps
+  const int p0 = min(P, warp * CH), p1 = min(P, p0 + CH);
+  int* h = hist + warp * E;
+  for (int p = p0 + lane; p < p1; p += 32) atomicAdd(&h[idx_s[p]], 1);
+  __syncthreads();
+  // per expert: total, then (after the scan) each warp's first position
+  int v = 0;
+  for (int e = tid; e < E; e += blockDim.x)  // E <= 1024 = blockDim.x: at most one expert per thread
+    for (int w = 0; w < kSmallWarps; ++w) v += hist[w * E + e];
+  if (tid < E) counts[tid] = v;
+  int x = v;  // block-wide exclusive scan of v over tid
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int y = __shfl_up_sync(0xffffffffu, x, o);
+    if (lane >= o) x += y;
+  }
+  if (lane == 31) wsum[warp] = x;
+  __syncthreads();
+  if (warp == 0) {
+    int ws = wsum[lane];
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, ws, o);
+      if (lane >= o) ws += y;
+    }
+    wsum[lane] = ws;
+  }
+  __syncthreads();
+  const int excl = x + (warp > 0 ? wsum[warp - 1] : 0) - v;
+  if (tid < E) {
+    offsets[tid] = excl;
+    if (tid == E - 1) offsets[E] = excl + v;
+    int run = excl;
+    for (int w = 0; w < kSmallWarps; ++w) {
+      const int c = hist[w * E + tid];
+      hist[w * E + tid] = run;
+      run += c;
+    }
+  }
+  __syncthreads();
+  const unsigned lower = (1u << lane) - 1u;
+  for (int pg = p0; pg < p1; pg += 32) {  // warp-uniform
+    const int p = pg + lane;
+    const bool ok = p < p1;
+    const int e = ok ? idx_s[p] : -1;
+    const unsigned peers = __match_any_sync(0xffffffffu, ok ? e : -1 - lane);
+    const int rank = __popc(peers & lower);
+    const int bs = ok ? h[e] : 0;
+    __syncwarp();
+    if (ok) {
+      const int pos = bs + rank;
+      sorted_pair[pos] = p;
+      pair_pos[p] = pos;
+      if ((peers >> lane) == 1u) h[e] = bs + __popc(peers);  // highest lane of the group
+    }
+    __syncwarp();
+  }
 }
 
 }  // namespace
@@ -142,6 +243,34 @@ cudaError_t launch_gating_topk(const float* logits, const float* bias, int T, in
   if (vpl <= 16) return MOE_GATING_LAUNCH(16);
   return MOE_GATING_LAUNCH(32);
 #undef MOE_GATING_LAUNCH
+}
+
+bool gate_route_small_fits(int T, int E, int k) {
+  return (long long)T * k <= kSmallPairs && E <= 1024 && k <= 32;
+}
+
+cudaError_t launch_gate_route_small(const float* logits, const float* bias, int T, int E, int k, int gate, float rsf,
+                                    float eps, float* topk_w, int32_t* topk_idx, int32_t* counts, int32_t* offsets,
+                                    int32_t* sorted_pair, int32_t* pair_pos, cudaStream_t stream, bool pdl) {
+  if (T == 0) return cudaSuccess;
+  if (!gate_route_small_fits(T, E, k)) return cudaErrorInvalidValue;
+  const size_t smem = (size_t)(kSmallPairs + kSmallWarps * E) * sizeof(int);
+  const int vpl = (E + 31) / 32;
+#define MOE_SMALL_LAUNCH(V)                                                                                        \
+  do {                                                                                                             \
+    cudaError_t err = cudaFuncSetAttribute(gate_route_small_kernel<V>, cudaFuncAttributeMaxDynamicSharedMemorySize, \
+                                           (int)smem);                                                             \
+    if (err != cudaSuccess) return err;                                                                            \
+    return launch_kernel(gate_route_small_kernel<V>, dim3(1), dim3(kSmallWarps * 32), smem, stream, pdl, logits,    \
+                         bias, T, E, k, gate, rsf, eps, topk_w, topk_idx, counts, offsets, sorted_pair, pair_pos);  \
+  } while (0)
+  if (vpl <= 1) MOE_SMALL_LAUNCH(1);
+  if (vpl <= 2) MOE_SMALL_LAUNCH(2);
+  if (vpl <= 4) MOE_SMALL_LAUNCH(4);
+  if (vpl <= 8) MOE_SMALL_LAUNCH(8);
+  if (vpl <= 16) MOE_SMALL_LAUNCH(16);
+  MOE_SMALL_LAUNCH(32);
+#undef MOE_SMALL_LAUNCH
 }
 
 }  // namespace moe

@@ -11,6 +11,13 @@ namespace moe {
 // between the library's own kernels inside moe_layer_forward).
 cudaError_t launch_gating_topk(const float* logits, const float* bias, int T, int E, int k, int gate, float rsf,
                                float eps, float* topk_w, int32_t* topk_idx, cudaStream_t stream, bool pdl = false);
+// Gating and init-routing of a small batch in one CTA (one launch instead of four), with the
+// results of launch_gating_topk followed by launch_init_routing (no row gather): T*k <= 4096,
+// E <= 1024, k <= 32 (gate_route_small_fits).
+bool gate_route_small_fits(int T, int E, int k);
+cudaError_t launch_gate_route_small(const float* logits, const float* bias, int T, int E, int k, int gate, float rsf,
+                                    float eps, float* topk_w, int32_t* topk_idx, int32_t* counts, int32_t* offsets,
+                                    int32_t* sorted_pair, int32_t* pair_pos, cudaStream_t stream, bool pdl = false);
 
 // Init-routing scratch: per-chunk expert histograms and bases.
 int routing_chunk_pairs(int P);

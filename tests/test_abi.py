@@ -63,6 +63,19 @@ def test_workspace_sizes(L, name):
     assert L.moe_init_routing_workspace_size(c.T, c.E, c.k) >= 256
 
 
+def test_layer_kernel_launches(L):
+    # decode-sized (T*k <= 4096): gating + routing in one kernel, row gather, two GEMMs, finalize
+    assert L.moe_layer_kernel_launches(ctypes.byref(moe.make_desc(64, 4096, 128, 8, 1536))) == 5
+    # larger: gating, routing (3), row gather, two GEMMs, finalize
+    assert L.moe_layer_kernel_launches(ctypes.byref(moe.make_desc(4096, 4096, 192, 8, 1536))) == 8
+    # compute-bound (>= 256 rows per expert): the gate/up GEMM gathers its own rows
+    assert L.moe_layer_kernel_launches(ctypes.byref(moe.make_desc(16384, 2048, 128, 8, 768))) == 7
+    assert L.moe_layer_kernel_launches(ctypes.byref(moe.make_desc(1024, 256, 8, 4, 128))) == 7
+    # shared expert with I_s != I: one more down GEMM launch
+    d = moe.make_desc(16, 4096, 192, 8, 1536, gate="sigmoid", n_shared=1, I_s=1024)
+    assert L.moe_layer_kernel_launches(ctypes.byref(d)) == 6
+
+
 def test_desc_validation(L):
     bad = [moe.make_desc(16, 100, 8, 2, 128),      # H % 64
            moe.make_desc(16, 256, 8, 9, 128),      # k > E
@@ -238,7 +251,10 @@ def test_w4a8_validation_returns_before_launch(L):
     d = moe.make_desc(16, 256, 8, 2, 128, gate="sigmoid", n_shared=1, I_s=128)
     need = L.moe_w4a8_layer_workspace_size(ctypes.byref(d))
     assert need > 16 * 2 * (256 + 128 + 512)
-    assert L.moe_w4a8_layer_kernel_launches(ctypes.byref(d)) == 9
+    # a small batch is gated and sorted by one kernel: 1 + row gathers 2 + GEMMs 2 + finalize 1
+    assert L.moe_w4a8_layer_kernel_launches(ctypes.byref(d)) == 6
+    big = moe.make_desc(4096, 256, 8, 2, 128, gate="sigmoid", n_shared=1, I_s=128)
+    assert L.moe_w4a8_layer_kernel_launches(ctypes.byref(big)) == 9
     args = [P16] * 16  # x_codes ... counts (the workspace pointer follows)
     args[3] = None  # no bias
     assert L.moe_layer_forward_w4a8(ctypes.byref(d), *args, P16, need - 1, None) == moe.MOE_ERR_WORKSPACE
