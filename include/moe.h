@@ -320,8 +320,8 @@ MOE_API int moe_prepack_w13(const uint16_t* w13, int E, int I, int H, uint16_t* 
  *           bytes: the status header, and with row_src the gathered rows (M*H*2 bytes)
  *           and one flag per 16 of them.
  *  The gather runs as moe_layer_forward runs it: inside the GEMM (two extra warps per
- *  CTA, overlapping the matmuls) when the problem is compute-bound (>= 256 rows per
- *  expert on average), else as a separate kernel before it.
+ *  CTA, overlapping the matmuls) when the problem takes the CTA-pair instances (more than
+ *  32 rows per expert on average), else as a separate kernel before it.
  */
 MOE_API size_t moe_grouped_gemm_workspace_size(void);
 MOE_API size_t moe_grouped_gemm_swiglu_workspace_size(int M, int H, int gather);

@@ -829,9 +829,11 @@ bool grouped_gemm_streaming(int M, int E) {
 }
 
 bool grouped_gemm_gathers_inline(int M, int E, bool has_shared, int T_s) {
-  // Only a compute-bound gate/up GEMM hides the row gather's HBM traffic behind its matmuls; a
-  // weight-streaming one would only share its bandwidth with it.
-  return !grouped_gemm_narrow(M, E, has_shared, T_s) && !grouped_gemm_streaming(M, E);
+  // The CTA-pair gate/up GEMMs gather their rows themselves: the compute-bound one hides the
+  // gather's HBM traffic behind its matmuls; the weight-streaming one is bound by the latency of
+  // its loads, not by HBM bandwidth, and overlapping the gather saves the separate kernel's time
+  // (hy3_prefill: routing 0.080 -> 0.019 ms, the GEMM 0.960 -> 1.010 ms).
+  return !grouped_gemm_narrow(M, E, has_shared, T_s);
 }
 
 cudaError_t launch_grouped_gemm(const GroupedGemmProblem& pr, cudaStream_t stream, bool pdl) {
@@ -865,9 +867,8 @@ cudaError_t launch_grouped_gemm(const GroupedGemmProblem& pr, cudaStream_t strea
   // they stream weights, and six 64-deep stages keep more weight bytes in flight.
   // Longer segments are compute-bound and take three 128-deep stages, which let the
   // MMA thread issue 8 MMAs between two waits (the tensor pipe idles otherwise).
-  // The compute-bound 256-wide gate/up instance runs 2 extra warps that gather the token rows
-  // while the GEMM runs (when asked to); the other instances have the rows gathered by a
-  // separate kernel first.
+  // The CTA-pair gate/up instances run 2 extra warps that gather the token rows while the GEMM
+  // runs (when asked to); the decode instance has the rows gathered by a separate kernel first.
   if (gather && !grouped_gemm_gathers_inline(pr.M, pr.E, has_shared, pr.T_s)) {
     // rows past offsets[E] are never read by the GEMM: gather only the routed ones
     cudaError_t e = launch_expand_rows(pr.g_x, pr.g_sorted_pair, pr.M, pr.g_k, pr.K, const_cast<uint16_t*>(pr.a_rows),
@@ -877,11 +878,6 @@ cudaError_t launch_grouped_gemm(const GroupedGemmProblem& pr, cudaStream_t strea
   if (grouped_gemm_narrow(pr.M, pr.E, has_shared, pr.T_s))
     return pr.mode == 0 ? launch_instance<32, 5, 0, 16, 8, 2, 1, 1, 0>(pr, gp, stream, pdl)
                         : launch_instance<32, 10, 1, 16, 8, 1, 1, 1, 0>(pr, gp, stream, pdl);
-  // Eight epilogue warps except in the compute-bound gate/up instance, whose epilogue warps also
-  // gather the first row chunks (with sixteen the others measured 2-5 % slower).
-  if (grouped_gemm_streaming(pr.M, pr.E))
-    return pr.mode == 0 ? launch_instance<256, 6, 0, 64, 8, 1, 2, 1, 0>(pr, gp, stream, pdl)
-                        : launch_instance<256, 6, 1, 64, 8, 1, 2, 1, 0>(pr, gp, stream, pdl);
   if (gather) {
     gp.g_x = reinterpret_cast<const uint4*>(pr.g_x);
     gp.g_sp = pr.g_sorted_pair;
@@ -891,6 +887,11 @@ cudaError_t launch_grouped_gemm(const GroupedGemmProblem& pr, cudaStream_t strea
     gp.g_H8 = pr.K / 8;
     gp.g_flags = pr.g_flags;
   }
+  // Eight epilogue warps except in the compute-bound gate/up instance, whose epilogue warps also
+  // gather the first row chunks (with sixteen the others measured 2-5 % slower).
+  if (grouped_gemm_streaming(pr.M, pr.E))
+    return pr.mode == 0 ? launch_instance<256, 6, 0, 64, 8, 1, 2, 1, 2>(pr, gp, stream, pdl)
+                        : launch_instance<256, 6, 1, 64, 8, 1, 2, 1, 0>(pr, gp, stream, pdl);
   return pr.mode == 0 ? launch_instance<256, 3, 0, 64, 16, 1, 2, 2, 2>(pr, gp, stream, pdl)
                       : launch_instance<256, 3, 1, 64, 8, 1, 2, 2, 0>(pr, gp, stream, pdl);
 }

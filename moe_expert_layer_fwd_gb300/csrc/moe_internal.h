@@ -72,7 +72,7 @@ int grouped_gemm_debug_set(int what, unsigned long long value);
 
 // Whether the problem takes the 32-column (decode) instances; whether its CTA-pair instance
 // streams weights (under 256 rows per expert); whether a gate/up GEMM asked to gather its rows
-// does so inside the GEMM (else a separate gather kernel runs first).
+// does so inside the GEMM (the CTA-pair instances; else a separate gather kernel runs first).
 bool grouped_gemm_narrow(int M, int E, bool has_shared, int T_s);
 bool grouped_gemm_streaming(int M, int E);
 bool grouped_gemm_gathers_inline(int M, int E, bool has_shared, int T_s);

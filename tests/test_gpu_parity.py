@@ -163,8 +163,8 @@ def test_grouped_gemm_swiglu_parity(moe, counts, H, I):
 
 
 # (T, k, E, H, I, zipf-like skew): the gate/up GEMM gathering its own rows through row_src, on
-# each instance family: decode (<= 32 rows per expert), weight-streaming CTA pairs (< 256 rows per
-# expert, a separate gather kernel first) and compute-bound CTA pairs (the gather inside the GEMM)
+# each instance family: decode (<= 32 rows per expert, a separate gather kernel first),
+# weight-streaming and compute-bound CTA pairs (< / >= 256 rows per expert, the gather inside the GEMM)
 GATHER_CASES = [(16, 2, 8, 256, 128, 0.0), (300, 4, 16, 512, 128, 0.0), (1000, 4, 8, 512, 256, 0.3),
                 (3000, 2, 6, 256, 128, 0.0), (37, 8, 64, 4096, 1536, 0.0)]
 
@@ -198,8 +198,8 @@ def test_grouped_gemm_swiglu_gathers_its_rows(moe, T, k, E, H, I, skew):
                          ids=["decode", "streaming", "compute-bound"])
 def test_grouped_gemm_swiglu_flags_bad_row_src(moe, T, E, bad):
     """A source row outside [0, T*k) is reported (its row of act is unspecified) on each instance
-    family, by the separate gather kernel (decode, streaming) or the gather inside the GEMM
-    (compute-bound), without stalling the GEMM; every other row is still right."""
+    family, by the separate gather kernel (decode) or the gather inside the GEMM (CTA pairs),
+    without stalling the GEMM; every other row is still right."""
     torch = _torch()
     k, H, I = 2, 256, 128
     idx = np.array([[e % E, (e + 1) % E] for e in range(T)], np.int32)
