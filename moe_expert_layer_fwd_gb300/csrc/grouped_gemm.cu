@@ -263,6 +263,11 @@ __global__ void __launch_bounds__(64 + 32 * (EPI + GW), 1)
     if (PAIR == 2) tmem_alloc_pair(tmem_slot, L::kTmemCols);
     else tmem_alloc(tmem_slot, L::kTmemCols);
   }
+  // The routing offsets are read before griddepcontrol.wait: every launch sequence that chains
+  // this kernel (moe_layer_forward) writes them two or more launches earlier (routing's scan or the
+  // fused small-batch kernel, then at least the scatter or the row gather), and a kernel starts only
+  // after its predecessor has waited for the one before.  Waiting here instead measured ~3 us more
+  // per decode layer.
   for (int i = threadIdx.x; i <= E; i += L::kThreads) s_off[i] = p.offsets ? __ldg(p.offsets + i) : 0;
   __syncthreads();
   if (warp == 2) {

@@ -308,6 +308,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (p.has_shared) tma_prefetch_desc(&tmAs);
   }
   if (warp == 1) tmem_alloc(tmem_slot, L::kTmemCols);
+  // The routing offsets are read before griddepcontrol.wait: moe_layer_forward_w4a8 writes them two
+  // or more launches earlier (then at least the MXFP8 row gather runs), and a kernel starts only
+  // after its predecessor has waited for the one before.  Waiting here instead measured ~3 us more
+  // per decode layer.
   for (int i = threadIdx.x; i <= E; i += kThreads) s_off[i] = p.offsets ? __ldg(p.offsets + i) : 0;
   __syncthreads();
   if (warp == 2) {
