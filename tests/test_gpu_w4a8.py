@@ -225,6 +225,9 @@ LAYER_CASES = [
     mi.CONFIGS["qwen3_decode"].with_(T=1, H=512, E=32, k=8, I=256),
     # the documented limits: E = 1024 experts, k = 32
     mi.CONFIGS["tiny"].with_(T=64, H=256, E=1024, k=32, I=128),
+    # gating and routing in one kernel up to T*k = 4096, four kernels above
+    mi.CONFIGS["qwen3_decode"].with_(T=512, H=256, I=128),
+    mi.CONFIGS["qwen3_decode"].with_(T=513, H=256, I=128),
 ]
 
 
