@@ -575,10 +575,10 @@ int layer_forward_impl(const moe_layer_desc* d, const uint16_t* x, const float* 
   // launch; for gating that is whatever the caller ran before, e.g. the previous layer's
   // finalize); each waits for its predecessor's completion before touching memory.
   constexpr bool kPdl = true;
-  // A compute-bound gate/up GEMM gathers the token rows into x_exp itself (overlapping the
-  // gather with its matmuls): routing then only sorts, and clears the GEMM's gather flags.
-  // Otherwise routing ends with the row gather kernel.  A small batch (decode) is gated and
-  // sorted by one kernel instead of four.
+  // A gate/up GEMM on CTA pairs (prefill sizes) gathers the token rows into x_exp itself
+  // (overlapping the gather with its matmuls): routing then only sorts, and clears the GEMM's
+  // gather flags.  Otherwise (decode) a row gather kernel follows routing, and a small batch is
+  // gated and sorted by one kernel instead of four.
   const bool inline_gather = moe::grouped_gemm_gathers_inline(P, E, sh, T);
   const bool small = !inline_gather && moe::gate_route_small_fits(T, E, k);
   if (mark(0) != cudaSuccess) return MOE_ERR_CUDA;

@@ -45,7 +45,7 @@
 //     The leader CTA (rank 0) issues the MMAs; both CTAs' TMA loads complete on
 //     the leader's barriers; MMA commits are multicast to both CTAs.
 //
-// Warp roles (64 + 32*EPI threads per CTA, 1 CTA/SM, static round-robin tiles):
+// Warp roles (64 + 32*(EPI + GW) threads per CTA, 1 CTA/SM, static round-robin tiles):
 //   warp 0      TMA producer (one lane per box).
 //   warp 1      TMEM allocator + single-thread tcgen05.mma issuer (the leader's
 //               only, when PAIR = 2), double-buffered accumulator.
@@ -53,6 +53,9 @@
 //               32-column chunks: tcgen05.ld 32 lanes x 32 columns, then
 //               mode 0 (w13): SwiGLU = SiLU(gate) * up in fp32;
 //               mode 1 (down): multiply by the routing weight of the row.
+//   warps 2+EPI.. GW row-gather warps (the CTA-pair gate/up instances): copy the
+//               routed token rows x[sorted_pair / k] into x_exp while the GEMM
+//               runs, publishing one flag per 16 rows that the producer waits on.
 // Every wait is bounded (default 2 s); on expiry the CTA raises an abort flag,
 // records DEV_ERR_TIMEOUT, drains its in-flight copies and MMAs and frees TMEM.
 #include "moe_common.cuh"
