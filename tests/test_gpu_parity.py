@@ -127,6 +127,8 @@ GEMM_CASES = [
     # >= 256 rows per expert: compute-bound instance with 128-deep stages; K = 320 and 192
     # leave a last stage holding a single 64-deep chunk
     ([600, 0, 900, 257], 320, 192),
+    # 240 experts: too many for the expert tables beside seven weight-streaming stages, so six
+    ([40] * 120 + [37] * 100 + [0] * 20, 256, 128),
 ]
 
 
@@ -166,7 +168,7 @@ def test_grouped_gemm_swiglu_parity(moe, counts, H, I):
 # each instance family: decode (<= 32 rows per expert, a separate gather kernel first),
 # weight-streaming and compute-bound CTA pairs (< / >= 256 rows per expert, the gather inside the GEMM)
 GATHER_CASES = [(16, 2, 8, 256, 128, 0.0), (300, 4, 16, 512, 128, 0.0), (1000, 4, 8, 512, 256, 0.3),
-                (3000, 2, 6, 256, 128, 0.0), (37, 8, 64, 4096, 1536, 0.0)]
+                (3000, 2, 6, 256, 128, 0.0), (37, 8, 64, 4096, 1536, 0.0), (1100, 8, 240, 256, 128, 0.0)]
 
 
 @pytest.mark.parametrize("T,k,E,H,I,skew", GATHER_CASES)
