@@ -461,22 +461,46 @@ def mxfp4_leg(args, cfg, K, W, moe, inp, t, d16, peaks, peak_src, y_bf16):
 
 
 # ------------------------------------------------------------------ the W4A8 layer (MXFP8 x MXFP4)
+class W4a8Weights:
+    """The MXFP4-quantised, prepacked expert weights, kept for the next workload with the same weights."""
+
+    def __init__(self):
+        self.key = None
+        self.w = None
+
+    def get(self, cfg, moe, mi, d16, t):
+        import torch
+        key = (cfg.seed, cfg.E, cfg.H, cfg.I, cfg.w_std, cfg.n_shared, cfg.I_s)
+        if key != self.key:
+            self.w = None
+            torch.cuda.empty_cache()
+            w13_raw = d16(mi.normal_bf16(cfg.seed, mi.TID_W13, (cfg.E, 2 * cfg.I, cfg.H), 0.0, cfg.w_std))
+            w13 = moe.moe_w4a8_prepack(*moe.moe_mxfp4_quantize(w13_raw), gate_up=True)
+            del w13_raw
+            w2 = moe.moe_w4a8_prepack(*moe.moe_mxfp4_quantize(t["w2"]), gate_up=False)
+            w13_s = w2_s = None
+            if cfg.n_shared:
+                sh = mi.generate(cfg.with_(E=1, T=1))
+                w13_s = moe.moe_w4a8_prepack(*moe.moe_mxfp4_quantize(d16(sh.w13_s)), gate_up=True)
+                w2_s = moe.moe_w4a8_prepack(*moe.moe_mxfp4_quantize(d16(sh.w2_s)), gate_up=False)
+            torch.cuda.empty_cache()
+            self.w = (w13, w2, w13_s, w2_s)
+            self.key = key
+        return self.w
+
+
+W4A8_WEIGHTS = W4a8Weights()
+# dense tensor rate of the block-scaled MXFP8 x MXFP4 MMA over bf16 (nominal 4.5 / 2.25 PFLOP/s)
+FP8_OVER_BF16 = 2.0
+
+
 def w4a8_leg(args, cfg, K, W, moe, mi, d16, t, peaks, peak_src, y_bf16):
     """Times moe_layer_forward_w4a8 (gating, routing, MXFP8 row gather, the two block-scaled W4A8 GEMMs,
     finalize; the shared expert as one more GEMM segment) on the workload: the expert weights quantised
     to MXFP4 on the GPU and the hidden state to MXFP8 by the fused RMSNorm + MX quantisation (both
     one-time, not timed).  Reported beside the bf16 layer (a lower precision), not part of its value."""
     import torch
-    w13_raw = d16(mi.normal_bf16(cfg.seed, mi.TID_W13, (cfg.E, 2 * cfg.I, cfg.H), 0.0, cfg.w_std))
-    w13 = moe.moe_w4a8_prepack(*moe.moe_mxfp4_quantize(w13_raw), gate_up=True)
-    del w13_raw
-    w2 = moe.moe_w4a8_prepack(*moe.moe_mxfp4_quantize(t["w2"]), gate_up=False)
-    w13_s = w2_s = None
-    if cfg.n_shared:
-        sh = mi.generate(cfg.with_(E=1, T=1))
-        w13_s = moe.moe_w4a8_prepack(*moe.moe_mxfp4_quantize(d16(sh.w13_s)), gate_up=True)
-        w2_s = moe.moe_w4a8_prepack(*moe.moe_mxfp4_quantize(d16(sh.w2_s)), gate_up=False)
-    torch.cuda.empty_cache()
+    w13, w2, w13_s, w2_s = W4A8_WEIGHTS.get(cfg, moe, mi, d16, t)
     ones = torch.ones(cfg.H, dtype=torch.bfloat16, device="cuda")
     xc, xs, _, _ = moe.moe_add_rms_norm_mxfp8(t["x"], None, ones, 1e-6, with_fp32=False)
     layer = moe.W4a8Layer(cfg.T, cfg.H, cfg.E, cfg.k, cfg.I, cfg.gate, cfg.routed_scaling_factor, cfg.eps,
@@ -506,23 +530,36 @@ def w4a8_leg(args, cfg, K, W, moe, mi, d16, t, peaks, peak_src, y_bf16):
     n_units = A + (1 if cfg.n_shared else 0)
     b1 = n_units * 2 * cfg.I * cfg.H * per_w
     b2 = n_units * cfg.H * cfg.I * per_w
+    f1 = 2.0 * cfg.T * cfg.k * cfg.H * 2 * cfg.I + (2.0 * cfg.T * cfg.H * 2 * cfg.I_s if cfg.n_shared else 0.0)
+    f2 = f1 / 2  # down: the same rows times I instead of 2I columns
     t1 = kern["gemm_w13_swiglu_w4a8"] * 1e-3
     t2 = kern["gemm_down_w4a8"] * 1e-3
     y = layer.y.float()
+    # bound of the gate/up GEMM: HBM below the ridge of the fp8-rate tensor peak and HBM, tensor above
+    tc_peak = peaks["bf16_tflops"] * FP8_OVER_BF16
+    if f1 / b1 < tc_peak * 1e12 / (peaks["hbm_gbs"] * 1e9):
+        roof = {"bound": "hbm", "kernel": "gemm_w13_swiglu_w4a8", "achieved": b1 / t1 / 1e9,
+                "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": b1 / t1 / 1e9 / peaks["hbm_gbs"],
+                "peak_source": f"{peak_src} (hbm_gbs)"}
+    else:
+        roof = {"bound": "tensor", "kernel": "gemm_w13_swiglu_w4a8", "achieved": f1 / t1 / 1e12,
+                "peak": tc_peak, "unit": "TFLOP/s", "frac": f1 / t1 / 1e12 / tc_peak,
+                "peak_source": f"{peak_src} (bf16_tflops) x {FP8_OVER_BF16} (nominal fp8 / bf16 dense ratio)"}
+    roof.update(algorithmic_bytes_per_launch=b1, flops_per_launch=f1,
+                per_unit=f"{2 * cfg.I * cfg.H} weights x {per_w} B per streamed expert (x {A} active"
+                         + (" + the shared expert)" if cfg.n_shared else ")"),
+                traffic=_traffic(cfg.name, "gemm_w13_swiglu_w4a8", "grouped_gemm_w4a8.cu"))
     return {
         "value": cfg.T / (ms * 1e-3), "unit": "tokens/s", "ms_per_step": ms, "kernels_ms": kern,
         "gpu_launches": layer.launches * K,
         "precision": "W4A8: MXFP8 hidden state and act (E4M3, E8M0 scale per 32), MXFP4 expert weights (E2M1, E8M0 "
                      "scale per 32) quantised on the GPU from the bf16 weights; block-scaled tcgen05 MMA "
                      "(kind::mxf8f6f4), fp32 accumulation",
-        "roofline": {"bound": "hbm", "kernel": "gemm_w13_swiglu_w4a8", "achieved": b1 / t1 / 1e9,
-                     "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": b1 / t1 / 1e9 / peaks["hbm_gbs"],
-                     "peak_source": f"{peak_src} (hbm_gbs)", "algorithmic_bytes_per_launch": b1,
-                     "per_unit": f"{2 * cfg.I * cfg.H} weights x {per_w} B per streamed expert (x {A} active"
-                                 + (" + the shared expert)" if cfg.n_shared else ")"),
-                     "traffic": _traffic(cfg.name, "gemm_w13_swiglu_w4a8", "grouped_gemm_w4a8.cu")},
-        "gemm_down_w4a8": {"achieved_gbs": b2 / t2 / 1e9, "frac": b2 / t2 / 1e9 / peaks["hbm_gbs"]},
+        "roofline": roof,
+        "gemm_down_w4a8": {"achieved_gbs": b2 / t2 / 1e9, "frac": b2 / t2 / 1e9 / peaks["hbm_gbs"],
+                           "achieved_tflops": f2 / t2 / 1e12, "tc_frac": f2 / t2 / 1e12 / tc_peak},
         "layer_hbm_frac_of_measured": (b1 + b2) / (ms * 1e-3) / 1e9 / peaks["hbm_gbs"],
+        "layer_tc_frac_of_fp8_peak": (f1 + f2) / (ms * 1e-3) / 1e12 / tc_peak,
         "max_rel_diff_vs_bf16_layer": float((y - y_bf16).abs().max() / y_bf16.abs().max()),
     }
 
@@ -530,6 +567,11 @@ def w4a8_leg(args, cfg, K, W, moe, mi, d16, t, peaks, peak_src, y_bf16):
 # ------------------------------------------------------------------ GB300 arm
 # the workloads measured beside the default one (hy3_decode and hy3_prefill share their weights)
 OTHER_WORKLOADS = ["tiny", "hy3_decode", "hy3_prefill", "long_prefill"]
+
+
+def _w4a8_fits(cfg):
+    """The W4A8 layer's shape limits: H a multiple of 256, I and I_s of 128."""
+    return cfg.H % 256 == 0 and cfg.I % 128 == 0 and (not cfg.n_shared or cfg.I_s % 128 == 0)
 
 
 def _decode_sized(cfg):
@@ -836,9 +878,9 @@ def run_gb300(args, rank, world, local):
     y_bf16, t, inp = rec.pop("_y"), rec.pop("_t"), rec.pop("_inp")
 
     front = None if args.no_front_end else front_end(args, cfg, K, W, moe, mi, d16)
-    # the W4A8 layer on decode-sized workloads (its GEMMs walk 32 token columns per tile)
+    # the W4A8 layer (its GEMMs walk 32 token columns per tile at decode sizes, 112 at prefill sizes)
     w8 = None
-    if not args.no_mxfp4 and _decode_sized(cfg):
+    if not args.no_mxfp4 and _w4a8_fits(cfg):
         w8 = w4a8_leg(args, cfg, K, W, moe, mi, d16, t, peaks, src, y_bf16)
     # the 4-bit-weight layer on f16 operands (routed experts only), on request
     w4 = None
@@ -854,12 +896,13 @@ def run_gb300(args, rank, world, local):
         r = measure(args, c, K, W, world, rank, local, moe, mi, d16, weights, peaks, src, dev_id)
         y_c, t_c = r.pop("_y"), r.pop("_t")
         r.pop("_inp")
-        if not args.no_mxfp4 and _decode_sized(c):
+        if not args.no_mxfp4 and _w4a8_fits(c):
             r["w4a8"] = w4a8_leg(args, c, K, W, moe, mi, d16, t_c, peaks, src, y_c)
         del y_c, t_c
         r["config"] = _config(c, world)
         others[name] = r
     weights.t = None
+    W4A8_WEIGHTS.w = None
     torch.cuda.empty_cache()
 
     if rank != 0:

@@ -134,7 +134,8 @@ struct Layout {
   static constexpr int kBarOff = STAGES * kStageBytes;
   static constexpr int kNumBars = 2 * STAGES + 5;
   static constexpr int kMiscOff = kBarOff + kNumBars * 8;
-  static constexpr int kTabOff = kMiscOff + 16;                  // offsets and tile starts: 2 x (E + 1) ints
+  static constexpr int kScaleOff = kMiscOff + 16;                // mode 1: per-epilogue-warp row scales
+  static constexpr int kTabOff = kScaleOff + (MODE == 1 ? EPI * NTMAX * 4 : 0);  // then offsets, tile starts
   static constexpr int kAccCols = APARTS * NTMAX;                // TMEM columns of one accumulator buffer
   static constexpr uint32_t kTmemCols = (2 * kAccCols <= 32) ? 32 : (2 * kAccCols <= 64 ? 64 : (2 * kAccCols <= 128 ? 128 : (2 * kAccCols <= 256 ? 256 : 512)));
   static constexpr int kFeatPerBox = MODE == 0 ? 64 : 128;       // output features of one weight box
@@ -229,6 +230,7 @@ __global__ void __launch_bounds__(64 + 32 * (EPI + GW), 1)
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::kMiscOff + 4);
   volatile int* cfg_bad = reinterpret_cast<volatile int*>(smem + L::kMiscOff + 8);
   volatile uint32_t* peer_issued = reinterpret_cast<volatile uint32_t*>(smem + L::kMiscOff + 12);
+  float* s_scale = reinterpret_cast<float*>(smem + L::kScaleOff);
   int* s_off = reinterpret_cast<int*>(smem + L::kTabOff);
   int* s_tt = s_off + (p.E + 1);
 
@@ -539,10 +541,11 @@ __global__ void __launch_bounds__(64 + 32 * (EPI + GW), 1)
       const int buf = it & 1;
       const uint32_t aph = (uint32_t)(it >> 1) & 1u;
       // Mode 1: fetch the routing weights of the tile's rows before waiting for
-      // the accumulator, so their latency overlaps the mainloop.  Lane j holds the weight of
-      // column 32 c + j of this warp's r-th chunk c = half_c + kPerQ r (in registers).
+      // the accumulator, so their latency overlaps the mainloop.  They are kept in shared memory,
+      // where the epilogue reads them as broadcast vector loads (in registers, one shuffle per
+      // column made the compute-bound down GEMM ~18 % slower).
+      float* wsc = s_scale + (warp - 2) * NTMAX;
       constexpr int kMine = (NTMAX / 32 + kPerQ - 1) / kPerQ;  // chunks of 32 columns this warp handles
-      float wsc[kMine];
       const bool scale = MODE == 1 && !t.shared && p.topk_w != nullptr;
       if (scale) {
         int pr[kMine];
@@ -552,7 +555,11 @@ __global__ void __launch_bounds__(64 + 32 * (EPI + GW), 1)
           pr[r] = (col < t.rows && col < NTMAX) ? __ldg(p.sorted_pair + t.row_base + col) : -1;
         }
 #pragma unroll
-        for (int r = 0; r < kMine; ++r) wsc[r] = pr[r] >= 0 ? __ldg(p.topk_w + pr[r]) : 0.0f;
+        for (int r = 0; r < kMine; ++r) {
+          const int col = (kPerQ * r + half_c) * 32 + lane;
+          if (col < NTMAX) wsc[col] = pr[r] >= 0 ? __ldg(p.topk_w + pr[r]) : 0.0f;
+        }
+        __syncwarp();
       }
       // The epilogue has slack: it sleeps in the barrier instead of polling.
       bool w = (lane == 0) ? mbar_wait_sleep(&tfull[buf], aph, abort_flag, p.timeout_ns, p.status) : false;
@@ -599,21 +606,18 @@ __global__ void __launch_bounds__(64 + 32 * (EPI + GW), 1)
           const int feat = t.f * L::kFeatPerTile + ((int)rank * APARTS + part) * kBM + qw * 32 + lane;
           const bool feat_ok = feat < n_feat;
           uint16_t* orow = out + (size_t)t.row_base * ld + feat;
-#pragma unroll
-          for (int r = 0; r < kMine; ++r) {
-            const int c = half_c + kPerQ * r;
-            if (c >= nch) break;
+          for (int c = half_c; c < nch; c += kPerQ) {
             uint32_t v[32];
             tmem_ld32_async(tb + (uint32_t)(part * NTMAX + c * 32), v);
             tmem_wait_ld();
             float o[32];
 #pragma unroll
-            for (int i = 0; i < 32; ++i)
-              o[i] = __uint_as_float(v[i]) * (scale ? __shfl_sync(0xffffffffu, wsc[r], i) : 1.0f);
+            for (int i = 0; i < 32; ++i) o[i] = __uint_as_float(v[i]) * (scale ? wsc[c * 32 + i] : 1.0f);
             store_pairs16(o, lane, orow, ld, c * 32, t.rows, feat_ok);
             store_pairs16(o + 16, lane, orow, ld, c * 32 + 16, t.rows, feat_ok);
           }
         }
+        __syncwarp();  // the next tile rewrites this warp's scales
       }
       tc_fence_before();
       __syncwarp();
@@ -872,8 +876,7 @@ cudaError_t launch_grouped_gemm(const GroupedGemmProblem& pr, cudaStream_t strea
   const bool gather = pr.mode == 0 && pr.g_x != nullptr && pr.M > 0;
   // Among the CTA-pair instances, segments averaging fewer than 256 rows do fewer than
   // 256 FLOPs per weight byte, below the GPU's ratio of tensor rate to HBM bandwidth:
-  // they stream weights, and seven 64-deep stages (six when more than 234 experts' tables take
-  // the room) keep more weight bytes in flight.
+  // they stream weights, and six or seven 64-deep stages keep more weight bytes in flight.
   // Longer segments are compute-bound and take three 128-deep stages, which let the
   // MMA thread issue 8 MMAs between two waits (the tensor pipe idles otherwise).
   // The CTA-pair gate/up instances run 2 extra warps that gather the token rows while the GEMM
@@ -899,12 +902,12 @@ cudaError_t launch_grouped_gemm(const GroupedGemmProblem& pr, cudaStream_t strea
   // Eight epilogue warps except in the compute-bound gate/up instance, whose epilogue warps also
   // gather the first row chunks (with sixteen the others measured 2-5 % slower).
   if (grouped_gemm_streaming(pr.M, pr.E)) {
-    // seven stages where the expert tables leave room for them, else six
+    // gate/up: seven stages where the expert tables leave room for them, else six; down: six (its
+    // routing weights take the room of a seventh)
+    if (pr.mode == 1) return launch_instance<256, 6, 1, 64, 8, 1, 2, 1, 0>(pr, gp, stream, pdl);
     if (pr.E <= Layout<256, 7, 0, 64, 8, 1, 2, 1, 2>::kMaxE)
-      return pr.mode == 0 ? launch_instance<256, 7, 0, 64, 8, 1, 2, 1, 2>(pr, gp, stream, pdl)
-                          : launch_instance<256, 7, 1, 64, 8, 1, 2, 1, 0>(pr, gp, stream, pdl);
-    return pr.mode == 0 ? launch_instance<256, 6, 0, 64, 8, 1, 2, 1, 2>(pr, gp, stream, pdl)
-                        : launch_instance<256, 6, 1, 64, 8, 1, 2, 1, 0>(pr, gp, stream, pdl);
+      return launch_instance<256, 7, 0, 64, 8, 1, 2, 1, 2>(pr, gp, stream, pdl);
+    return launch_instance<256, 6, 0, 64, 8, 1, 2, 1, 2>(pr, gp, stream, pdl);
   }
   return pr.mode == 0 ? launch_instance<256, 3, 0, 64, 16, 1, 2, 2, 2>(pr, gp, stream, pdl)
                       : launch_instance<256, 3, 1, 64, 8, 1, 2, 2, 0>(pr, gp, stream, pdl);

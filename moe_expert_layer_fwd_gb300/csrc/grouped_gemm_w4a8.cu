@@ -49,7 +49,17 @@
 // Warp roles (288 threads, one persistent CTA per SM, static round-robin tiles; an expert's token
 // tiles that reuse a weight tile run next to each other): warp 0 TMA producer, warp 1 TMEM allocator +
 // MMA issuer of weight half 0, warps 2-5 epilogue (one per TMEM lane quarter), warp 6 MMA issuer of
-// half 1, warps 7-8 token loaders.  Every wait is bounded
+// half 1, warps 7-8 token loaders.
+//
+// Prefill-sized problems (more than 32 rows per expert on average) take a wide instance of the same
+// kernel: tiles of 112 token columns (MMA N = the tile's rows rounded up to 16), so a weight tile is
+// read once per 112 rows instead of once per 32.  Its token rows come by TMA (one 112-row box per
+// 128-K chunk, completing on the window's barrier by byte count); its single loader warp only places
+// each token's four block scales at byte (r % 32) * 16 + (r / 32) * 4 of the chunk's 512-byte block,
+// the tensor-memory scale-factor layout of an operand of up to 128 rows (token r at lane r % 32,
+// column r / 32, as for the weights), then fences and arrives.  Eight epilogue warps, two per lane
+// quarter, split a tile's four 32-column chunks (with four, the epilogue bounded the GEMMs).  Windows
+// of two chunks, three of them in flight where the expert tables leave room.  Every wait is bounded
 // (2 s): on expiry the CTA raises its abort flag, records DEV_ERR_TIMEOUT, lets its copies land,
 // drains its MMAs and frees TMEM.
 #include "moe_common.cuh"
@@ -65,44 +75,60 @@ namespace {
 
 constexpr int kBM = 128;                  // weight rows per MMA (M), one half of a tile
 constexpr int kTR = 256;                  // weight rows per tile and per A copy
-constexpr int kNT = 32;                   // token columns per tile (MMA N)
 constexpr int kKC = 128;                  // K per chunk: 4 MMAs of K = 32 per half
-constexpr int kWin = 4;                   // chunks per T-ring window (512 K)
 constexpr int kABox = kTR * 128;          // shared-memory bytes of one A copy (padded codes): 32 KB
 constexpr int kATx = kTR * kKC / 2;       // bytes the A copy moves (and counts on the barrier): 16 KB
 constexpr int kSF = 512;                  // one scale-factor atom (128 rows) / 32 token scale rows
-constexpr int kTB = kWin * kNT * kKC;     // token rows of a window: 16 KB
-constexpr int kTSB = kWin * kSF;          // their padded scale rows: 2 KB
-constexpr int kTSA = kWin * 2 * kSF;      // the window's weight scale atoms: 4 KB
-constexpr int kTSlot = kTB + kTSB + kTSA; // 22 KB
-constexpr int kEPI = 4;                   // epilogue warps (2-5), one per TMEM lane quarter
-constexpr int kMMA2 = 2 + kEPI;           // warp of the second MMA issuer (weight half 1)
-constexpr int kLD0 = kMMA2 + 1;           // first of the two token-loader warps
-constexpr int kLoaders = 64;              // token-loader threads
-constexpr int kThreads = 32 * (kLD0 + 2);
+// Warp roles of an instance with NT token columns per tile: warp 0 producer, warp 1 MMA issuer of weight
+// half 0, kEPI epilogue warps, the MMA issuer of half 1, kLW loader warps.  The decode instance has one
+// epilogue warp per TMEM lane quarter and two loader warps (token rows and scales by cp.async); the wide
+// one two epilogue warps per quarter (its tiles have up to four 32-column chunks) and one loader warp
+// (the token rows come by TMA, the loader only places their scales).
+template <int NT>
+struct W8Roles {
+  static constexpr int kEPI = NT > 32 ? 8 : 4;
+  static constexpr int kPerQ = kEPI / 4;      // epilogue warps sharing a TMEM lane quarter
+  static constexpr int kMMA2 = 2 + kEPI;
+  static constexpr int kLD0 = kMMA2 + 1;
+  static constexpr int kLW = NT > 32 ? 1 : 2;
+  static constexpr int kLoaders = 32 * kLW;
+  static constexpr int kThreads = 32 * (kLD0 + kLW);
+};
 constexpr int kMaxDynSmem = 232448;
 constexpr unsigned long long kTimeoutNs = 2000000000ull;
 
-template <int MODE, int STAGES, int TSLOTS>
+// NT token columns per tile (MMA N at most), WIN 128-K chunks per token window.
+template <int MODE, int STAGES, int TSLOTS, int NT, int WIN>
 struct W8Layout {
+  static constexpr int kNTPad = (NT + 31) / 32 * 32;               // epilogue: 32-column chunks
+  static constexpr int kTB = WIN * NT * kKC;                       // token rows of a window
+  static constexpr int kTSB = WIN * kSF;                           // their scales: one 512-byte block per chunk
+  static constexpr int kTSA = WIN * 2 * kSF;                       // the window's weight scale atoms
+  static constexpr int kTSlot = kTB + kTSB + kTSA;
   static constexpr int kAOff = 0;                                  // STAGES x 32 KB
-  static constexpr int kTOff = STAGES * kABox;                     // TSLOTS x 22 KB
+  static constexpr int kTOff = STAGES * kABox;                     // TSLOTS x kTSlot
   static constexpr int kBarOff = kTOff + TSLOTS * kTSlot;
   static constexpr int kNumBars = 2 * STAGES + 2 * TSLOTS + 6;
   static constexpr int kMiscOff = kBarOff + kNumBars * 8;
-  static constexpr int kScaleOff = kMiscOff + 16;                  // mode 1: routing weights per epilogue warp
-  static constexpr int kTabOff = kScaleOff + kEPI * kNT * 4;
-  // tensor memory: two accumulator buffers of 2 x 32 columns, then a scale-factor slot per A stage:
+  // mode 1: the routing weights of each epilogue warp's columns (kMine 32-column chunks per warp)
+  static constexpr int kMine = (kNTPad / 32 + W8Roles<NT>::kPerQ - 1) / W8Roles<NT>::kPerQ;
+  static constexpr int kScaleOff = kMiscOff + 16;
+  static constexpr int kTabOff = kScaleOff + (MODE == 1 ? W8Roles<NT>::kEPI * kMine * 32 * 4 : 0);
+  // tensor memory: two accumulator buffers of 2 x NT columns, then a scale-factor slot per A stage:
   // per weight half (one per MMA issuer) 4 columns of weight scales and 4 of token scales
-  static constexpr int kAccCols = 2 * kNT;
+  static constexpr int kAccCols = 2 * NT;
   static constexpr int kSFCol0 = 2 * kAccCols;
   static constexpr int kSFColsPerStage = 16;
   static constexpr int kColsNeeded = kSFCol0 + STAGES * kSFColsPerStage;
   static constexpr uint32_t kTmemCols = kColsNeeded <= 64 ? 64 : (kColsNeeded <= 128 ? 128 : (kColsNeeded <= 256 ? 256 : 512));
   static constexpr int kFeatPerTile = MODE == 0 ? 128 : 256;
   static_assert(kColsNeeded <= 512, "TMEM");
-  static_assert(kABox % 1024 == 0 && kTOff % 1024 == 0 && kTSlot % 1024 == 0 && kTB % 1024 == 0, "alignment");
-  static_assert(1024 + kTabOff + 2 * 1025 * 4 <= kMaxDynSmem, "shared memory");
+  // the epilogue reads whole 32-column chunks: the last one may run past NT, never past TMEM
+  static_assert(kAccCols + NT + kNTPad <= (int)kTmemCols, "TMEM reads");
+  static_assert(NT % 16 == 0 && NT >= 32 && NT <= 128, "token tile");
+  static_assert(kABox % 1024 == 0 && kTOff % 1024 == 0 && kTSlot % 1024 == 0 && (NT * kKC) % 1024 == 0, "alignment");
+  static constexpr int kMaxE = (kMaxDynSmem - 1024 - kTabOff) / 8 - 1;  // experts whose tables fit
+  static_assert(kMaxE >= 64, "shared memory");
   static size_t bytes(int E) { return 1024 + kTabOff + 2 * (size_t)(E + 1) * 4; }
 };
 
@@ -134,6 +160,7 @@ struct W8Tile {
   int nt;  // token tiles of this segment (> 1: the weight tile is read again)
 };
 
+template <int NT>
 __device__ __forceinline__ W8Tile w8_tile(int tile, int routed_total, const int* s_off, const int* s_tt,
                                           const W8Params& p) {
   W8Tile t;
@@ -153,32 +180,32 @@ __device__ __forceinline__ W8Tile w8_tile(int tile, int routed_total, const int*
     t.e = lo;
     t.nt = nt;
     t.f = m_major ? local - m * p.n_ftiles : local / nt;
-    t.row_base = s_off[lo] + m * kNT;
-    t.rows = min(kNT, s_off[lo + 1] - t.row_base);
+    t.row_base = s_off[lo] + m * NT;
+    t.rows = min(NT, s_off[lo + 1] - t.row_base);
   } else {
     const int local = tile - routed_total;
-    const int nt = (p.T_s + kNT - 1) / kNT;
+    const int nt = (p.T_s + NT - 1) / NT;
     const bool m_major = p.T_s > p.n_out_s;
     const int m = m_major ? local / p.n_ftiles_s : local % nt;
     t.shared = 1;
     t.e = -1;
     t.nt = nt;
     t.f = m_major ? local - m * p.n_ftiles_s : local / nt;
-    t.row_base = m * kNT;
-    t.rows = min(kNT, p.T_s - t.row_base);
+    t.row_base = m * NT;
+    t.rows = min(NT, p.T_s - t.row_base);
   }
   return t;
 }
 
 // Instruction descriptor of tcgen05.mma kind::mxf8f6f4 .block_scale: A E2M1 (5), B E4M3 (0), both
-// K-major, E8M0 scale factors, M = 128, N = 32; the scale-factor ids of A (bits 29-30) and B
-// (bits 4-5) select the byte of each 32-bit tensor-memory scale column, i.e. the K block.
-__device__ __forceinline__ uint32_t w4a8_idesc(uint32_t sf_id) {
+// K-major, E8M0 scale factors, M = 128, N = n (a multiple of 16); the scale-factor ids of A (bits 29-30)
+// and B (bits 4-5) select the byte of each 32-bit tensor-memory scale column, i.e. the K block.
+__device__ __forceinline__ uint32_t w4a8_idesc(uint32_t sf_id, int n) {
   uint32_t d = 0;
   d |= sf_id << 4;                 // B scale-factor id
   d |= 5u << 7;                    // A format: E2M1
   d |= 0u << 10;                   // B format: E4M3
-  d |= (uint32_t)(kNT >> 3) << 17; // N / 8
+  d |= (uint32_t)(n >> 3) << 17;   // N / 8
   d |= 1u << 23;                   // scale-factor type: UE8M0
   d |= (uint32_t)(kBM >> 4) << 24; // M / 16
   d |= sf_id << 29;                // A scale-factor id
@@ -230,6 +257,13 @@ __device__ __forceinline__ void cp_async16(void* smem_dst, const void* src, uint
                : "memory");
 }
 
+// cp.async of 4 bytes global -> shared (zero-filled when src_bytes is 0).
+__device__ __forceinline__ void cp_async4(void* smem_dst, const void* src, uint32_t src_bytes) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;" ::"r"(smem_u32(smem_dst)),
+               "l"(reinterpret_cast<uint64_t>(src)), "r"(src_bytes)
+               : "memory");
+}
+
 // floor(log2 m) - 8 clamped to the E8M0 range (m == 0 -> -127): the block's shared exponent.
 __device__ __forceinline__ int mx_shared_exponent(float m) {
   const uint32_t b = __float_as_uint(m);
@@ -260,11 +294,14 @@ __device__ __forceinline__ void store_pairs16_bf16(const float* v, int lane, uin
   }
 }
 
-template <int MODE, int STAGES, int TSLOTS>
-__global__ void __launch_bounds__(kThreads, 1)
+template <int MODE, int STAGES, int TSLOTS, int NT, int WIN>
+__global__ void __launch_bounds__(W8Roles<NT>::kThreads, 1)
     grouped_gemm_w4a8_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmAs,
+                             const __grid_constant__ CUtensorMap tmB, const __grid_constant__ CUtensorMap tmBs,
                              const W8Params p) {
-  using L = W8Layout<MODE, STAGES, TSLOTS>;
+  using L = W8Layout<MODE, STAGES, TSLOTS, NT, WIN>;
+  using R = W8Roles<NT>;
+  constexpr int kEPI = R::kEPI, kMMA2 = R::kMMA2, kLD0 = R::kLD0, kLoaders = R::kLoaders, kThreads = R::kThreads;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint64_t* afull = reinterpret_cast<uint64_t*>(smem + L::kBarOff);
@@ -306,6 +343,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == 0 && lane == 0) {
     tma_prefetch_desc(&tmA);
     if (p.has_shared) tma_prefetch_desc(&tmAs);
+    if (NT > 32) {
+      tma_prefetch_desc(&tmB);
+      if (p.has_shared) tma_prefetch_desc(&tmBs);
+    }
   }
   if (warp == 1) tmem_alloc(tmem_slot, L::kTmemCols);
   // The routing offsets are read before griddepcontrol.wait: moe_layer_forward_w4a8 writes them two
@@ -323,7 +364,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int e = e0; e < e1; ++e) {
       const int n = s_off[e + 1] - s_off[e];
       if (n < 0) bad = true;
-      else sum += (n + kNT - 1) / kNT;
+      else sum += (n + NT - 1) / NT;
     }
     int x = sum;
 #pragma unroll
@@ -335,7 +376,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int e = e0; e < e1; ++e) {
       s_tt[e] = run;
       const int n = s_off[e + 1] - s_off[e];
-      run += n > 0 ? (n + kNT - 1) / kNT : 0;
+      run += n > 0 ? (n + NT - 1) / NT : 0;
     }
     if (lane == 31) s_tt[E] = x;
     if (__any_sync(0xffffffffu, bad) && lane == 0) {
@@ -349,7 +390,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t tmem_base = *tmem_slot;
 
   const int routed_total = *cfg_bad ? 0 : s_tt[E] * p.n_ftiles;
-  const int shared_total = (*cfg_bad || !p.has_shared) ? 0 : ((p.T_s + kNT - 1) / kNT) * p.n_ftiles_s;
+  const int shared_total = (*cfg_bad || !p.has_shared) ? 0 : ((p.T_s + NT - 1) / NT) * p.n_ftiles_s;
   const int total = routed_total + shared_total;
   const int KB = p.K / kKC;  // chunks per tile (K is a multiple of 128)
 
@@ -367,23 +408,31 @@ __global__ void __launch_bounds__(kThreads, 1)
       pdl_wait();
       pdl_launch_dependents();
       for (int tile = blockIdx.x; ok && tile < total; tile += gridDim.x) {
-        const W8Tile t = w8_tile(tile, routed_total, s_off, s_tt, p);
+        const W8Tile t = w8_tile<NT>(tile, routed_total, s_off, s_tt, p);
         const CUtensorMap* mA = t.shared ? &tmAs : &tmA;
+        const CUtensorMap* mB = t.shared ? &tmBs : &tmB;
         const int n_out = t.shared ? p.n_out_s : p.n_out;
         const int a_tile = ((t.shared ? 0 : t.e * n_out) + t.f * kTR) / kTR;  // 256-row tile of the weights
         const uint8_t* sfa = (t.shared ? p.sfa_s : p.sfa) + (size_t)a_tile * KB * 2 * kSF;
         const uint64_t pol_a = t.nt > 1 ? pol_last : pol_first;  // weight tiles read again stay in L2
         for (int kb = 0; kb < KB && ok; ++kb) {
-          if (kb % kWin == 0) {
+          if (kb % WIN == 0) {
             // the window's weight scale atoms (the loader warps copy its token rows and their scales)
             if (!mbar_wait_bounded(&wempty[ws], wph ^ 1u, abort_flag, p.timeout_ns, p.status)) {
               ok = false;
               break;
             }
-            const int nch = min(kWin, KB - kb);
-            uint8_t* slot = smem + L::kTOff + ws * kTSlot;
-            mbar_arrive_expect_tx(&wfull[ws], (uint32_t)(nch * 2 * kSF));
-            bulk_load(slot + kTB + kTSB, sfa + (size_t)kb * 2 * kSF, (uint32_t)(nch * 2 * kSF), &wfull[ws], pol_a);
+            const int nch = min(WIN, KB - kb);
+            uint8_t* slot = smem + L::kTOff + ws * L::kTSlot;
+            // the wide instance's token rows come by TMA too: one NT-row box per chunk (rows past the
+            // end of the matrix read as zeros)
+            const uint32_t tx = (uint32_t)(nch * 2 * kSF) + (NT > 32 ? (uint32_t)(nch * NT * kKC) : 0u);
+            mbar_arrive_expect_tx(&wfull[ws], tx);
+            bulk_load(slot + L::kTB + L::kTSB, sfa + (size_t)kb * 2 * kSF, (uint32_t)(nch * 2 * kSF), &wfull[ws],
+                      pol_a);
+            if (NT > 32)
+              for (int c = 0; c < nch; ++c)
+                tma_load_2d(slot + c * (NT * kKC), mB, (kb + c) * kKC, t.row_base, &wfull[ws], pol_last);
             ++w_issued;
             if (++ws == TSLOTS) {
               ws = 0;
@@ -433,11 +482,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int tile = blockIdx.x; ok && tile < total; tile += gridDim.x, ++it) {
         const int buf = it & 1;
         const uint32_t acc_ph = (uint32_t)(it >> 1) & 1u;
+        // MMA N: the tile's rows rounded up to 16 (the narrow instance always takes its 32 columns)
+        const int nmma = NT == 32 ? 32 : ((w8_tile<NT>(tile, routed_total, s_off, s_tt, p).rows + 15) & ~15);
         if (!mbar_wait_bounded(&tempty[buf], acc_ph ^ 1u, abort_flag, p.timeout_ns, p.status)) break;
         tc_fence_after();
-        const uint32_t d = tmem_base + (uint32_t)(buf * L::kAccCols + half * kNT);
+        const uint32_t d = tmem_base + (uint32_t)(buf * L::kAccCols + half * NT);
         for (int kb = 0; kb < KB; ++kb) {
-          const int ci = kb % kWin;  // chunk inside the window
+          const int ci = kb % WIN;  // chunk inside the window
           if (ci == 0) {
             if (!mbar_wait_bounded(&wfull[ws], wph, abort_flag, p.timeout_ns, p.status)) {
               ok = false;
@@ -449,23 +500,23 @@ __global__ void __launch_bounds__(kThreads, 1)
             break;
           }
           tc_fence_after();
-          const uint32_t woff = (uint32_t)(L::kTOff + ws * kTSlot);
+          const uint32_t woff = (uint32_t)(L::kTOff + ws * L::kTSlot);
           const uint32_t sfa_t = tmem_base + (uint32_t)(L::kSFCol0 + as * L::kSFColsPerStage + 8 * half);
           const uint32_t sfb_t = sfa_t + 4u;
-          tmem_cp_32x128_x4(sfa_t, sfd0 + (uint64_t)((woff + kTB + kTSB + (ci * 2 + half) * kSF) >> 4));
-          tmem_cp_32x128_x4(sfb_t, sfd0 + (uint64_t)((woff + kTB + ci * kSF) >> 4));
+          tmem_cp_32x128_x4(sfa_t, sfd0 + (uint64_t)((woff + L::kTB + L::kTSB + (ci * 2 + half) * kSF) >> 4));
+          tmem_cp_32x128_x4(sfb_t, sfd0 + (uint64_t)((woff + L::kTB + ci * kSF) >> 4));
           const uint64_t ad0 = desc0 + (uint64_t)((L::kAOff + as * kABox + half * kBM * 128) >> 4);
-          const uint64_t bd0 = desc0 + (uint64_t)((woff + ci * kNT * kKC) >> 4);
+          const uint64_t bd0 = desc0 + (uint64_t)((woff + ci * NT * kKC) >> 4);
 #pragma unroll
           for (int kk = 0; kk < kKC / 32; ++kk)
-            umma_w4a8(d, ad0 + (uint64_t)((kk * 32) >> 4), bd0 + (uint64_t)((kk * 32) >> 4), w4a8_idesc((uint32_t)kk),
-                      sfa_t, sfb_t, (kb | kk) != 0);
+            umma_w4a8(d, ad0 + (uint64_t)((kk * 32) >> 4), bd0 + (uint64_t)((kk * 32) >> 4),
+                      w4a8_idesc((uint32_t)kk, nmma), sfa_t, sfb_t, (kb | kk) != 0);
           umma_commit(&aempty[as]);
           if (++as == STAGES) {
             as = 0;
             aph ^= 1u;
           }
-          if (ci == kWin - 1 || kb == KB - 1) {
+          if (ci == WIN - 1 || kb == KB - 1) {
             umma_commit(&wempty[ws]);  // the window's token rows and scales are no longer read
             if (++ws == TSLOTS) {
               ws = 0;
@@ -489,39 +540,89 @@ __global__ void __launch_bounds__(kThreads, 1)
     // them to the async proxy before arriving, one window behind the copies it issues.
     const int lt = (warp - kLD0) * 32 + lane;
     pdl_wait();  // the token rows come from the previous kernel
+    if constexpr (NT > 32) {
+      // Wide instance: the producer's TMA brings the token rows; the loaders only put each token's four
+      // block scales (the first 4 bytes of its padded scale row) at byte (r % 32) * 16 + (r / 32) * 4 of
+      // the chunk's 512-byte block -- the scale-factor layout of an operand of up to 128 rows, as for
+      // the weights: token r at lane r % 32, column r / 32 -- then fence them to the async proxy and
+      // arrive.
+      constexpr int kPer = (WIN * NT + kLoaders - 1) / kLoaders;
+      int ws = 0;
+      uint32_t wph = 0;
+      for (int tile = blockIdx.x; tile < total; tile += gridDim.x) {
+        const W8Tile t = w8_tile<NT>(tile, routed_total, s_off, s_tt, p);
+        const uint8_t* sfr = t.shared ? p.bs_sf : p.b_sf;
+        const int nrows = t.shared ? p.T_s : p.M;
+        const int nmma = (t.rows + 15) & ~15;  // token rows the tile's MMAs read
+        bool ok = true;
+        for (int kb0 = 0; kb0 < KB; kb0 += WIN) {
+          uint32_t wv[kPer];
+#pragma unroll
+          for (int i = 0; i < kPer; ++i) {
+            const int piece = lt + i * kLoaders;  // (chunk, row)
+            const int c = piece / NT, r = piece - c * NT;
+            const int row = t.row_base + r, kc = kb0 + c;
+            const bool valid = piece < WIN * NT && r < nmma && row < nrows && kc < KB;
+            wv[i] = valid ? __ldg(reinterpret_cast<const uint32_t*>(sfr + ((size_t)row * KB + kc) * 16)) : 0u;
+          }
+          bool w = (lane == 0) ? mbar_wait_bounded(&wempty[ws], wph ^ 1u, abort_flag, p.timeout_ns, p.status) : false;
+          w = __shfl_sync(0xffffffffu, w, 0);
+          if (!w) {
+            ok = false;
+            break;
+          }
+          uint8_t* blk = smem + L::kTOff + ws * L::kTSlot + L::kTB;
+#pragma unroll
+          for (int i = 0; i < kPer; ++i) {
+            const int piece = lt + i * kLoaders;
+            const int c = piece / NT, r = piece - c * NT;
+            if (piece < WIN * NT && r < nmma)
+              *reinterpret_cast<uint32_t*>(blk + c * kSF + (r & 31) * 16 + (r >> 5) * 4) = wv[i];
+          }
+          asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+          mbar_arrive(&wfull[ws]);
+          if (++ws == TSLOTS) {
+            ws = 0;
+            wph ^= 1u;
+          }
+        }
+        if (!ok) break;
+      }
+    } else {
     int ws = 0, prev = -1;
     uint32_t wph = 0;
     bool ok = true;
     for (int tile = blockIdx.x; ok && tile < total; tile += gridDim.x) {
-      const W8Tile t = w8_tile(tile, routed_total, s_off, s_tt, p);
+      const W8Tile t = w8_tile<NT>(tile, routed_total, s_off, s_tt, p);
       const uint8_t* rows = t.shared ? p.bs_rows : p.b_rows;
       const uint8_t* sfr = t.shared ? p.bs_sf : p.b_sf;
       const int nrows = t.shared ? p.T_s : p.M;
-      for (int kb0 = 0; kb0 < KB; kb0 += kWin) {
+      for (int kb0 = 0; kb0 < KB; kb0 += WIN) {
         bool w = (lane == 0) ? mbar_wait_bounded(&wempty[ws], wph ^ 1u, abort_flag, p.timeout_ns, p.status) : false;
         w = __shfl_sync(0xffffffffu, w, 0);
         if (!w) {
           ok = false;
           break;
         }
-        uint8_t* slot = smem + L::kTOff + ws * kTSlot;
+        uint8_t* slot = smem + L::kTOff + ws * L::kTSlot;
 #pragma unroll 4
-        for (int i = 0; i < kTB / 16 / kLoaders; ++i) {
+        for (int i = 0; i < L::kTB / 16 / kLoaders; ++i) {
           const int piece = lt + i * kLoaders;  // (chunk, row, 16-byte unit)
           const int c = piece >> 8, r = (piece >> 3) & 31, j = piece & 7;
           const int row = t.row_base + r, kc = kb0 + c;
           const bool valid = row < nrows && kc < KB;
           const uint8_t* src = valid ? rows + (size_t)row * p.K + kc * kKC + j * 16 : rows;
-          cp_async16(slot + c * (kNT * kKC) + r * kKC + ((j ^ (r & 7)) << 4), src, valid ? 16u : 0u);
+          cp_async16(slot + c * (NT * kKC) + r * kKC + ((j ^ (r & 7)) << 4), src, valid ? 16u : 0u);
         }
+        // the 32 padded scale rows of each chunk as they are: token r lands at lane r, column 0
 #pragma unroll
-        for (int i = 0; i < kTSB / 16 / kLoaders; ++i) {
+        for (int i = 0; i < L::kTSB / 16 / kLoaders; ++i) {
           const int piece = lt + i * kLoaders;  // (chunk, row)
           const int c = piece >> 5, r = piece & 31;
           const int row = t.row_base + r, kc = kb0 + c;
           const bool valid = row < nrows && kc < KB;
           const uint8_t* src = valid ? sfr + ((size_t)row * KB + kc) * 16 : sfr;
-          cp_async16(slot + kTB + c * kSF + r * 16, src, valid ? 16u : 0u);
+          cp_async16(slot + L::kTB + c * kSF + r * 16, src, valid ? 16u : 0u);
         }
         asm volatile("cp.async.commit_group;" ::: "memory");
         if (prev >= 0) {
@@ -539,20 +640,31 @@ __global__ void __launch_bounds__(kThreads, 1)
     asm volatile("cp.async.wait_group 0;" ::: "memory");
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
     if (prev >= 0) mbar_arrive(&wfull[prev]);
+    }
   } else {
     // ------------------------------------------------------------ epilogue (warps 2-5)
-    const int qw = warp & 3;  // TMEM lane quarter this warp may access
+    const int qw = warp & 3;             // TMEM lane quarter this warp may access
+    const int half_c = (warp - 2) >> 2;  // which of the quarter's warps this is
     int it = 0;
     for (int tile = blockIdx.x; tile < total; tile += gridDim.x, ++it) {
-      const W8Tile t = w8_tile(tile, routed_total, s_off, s_tt, p);
+      const W8Tile t = w8_tile<NT>(tile, routed_total, s_off, s_tt, p);
       const int buf = it & 1;
       const uint32_t acc_ph = (uint32_t)(it >> 1) & 1u;
-      float* wsc = s_scale + (warp - 2) * kNT;
+      // Mode 1: the routing weights of the tile's rows, fetched before the accumulator wait, in shared
+      // memory (read back as broadcast vector loads): wsc[32 r + j] is the weight of column 32 cc + j of
+      // this warp's r-th chunk cc = half_c + kPerQ r.
+      constexpr int kMine = L::kMine;
+      float* wsc = s_scale + (warp - 2) * kMine * 32;
       const bool scale = MODE == 1 && !t.shared && p.topk_w != nullptr;
       if (scale) {
-        // routing weights of the tile's rows, fetched before the accumulator wait
-        const int pr = lane < t.rows ? __ldg(p.sorted_pair + t.row_base + lane) : -1;
-        wsc[lane] = pr >= 0 ? __ldg(p.topk_w + pr) : 0.0f;
+        int pr[kMine];
+#pragma unroll
+        for (int r = 0; r < kMine; ++r) {
+          const int col = (half_c + R::kPerQ * r) * 32 + lane;
+          pr[r] = col < t.rows ? __ldg(p.sorted_pair + t.row_base + col) : -1;
+        }
+#pragma unroll
+        for (int r = 0; r < kMine; ++r) wsc[32 * r + lane] = pr[r] >= 0 ? __ldg(p.topk_w + pr[r]) : 0.0f;
         __syncwarp();
       }
       bool w = (lane == 0) ? mbar_wait_sleep(&tfull[buf], acc_ph, abort_flag, p.timeout_ns, p.status) : false;
@@ -560,14 +672,30 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!w) break;
       tc_fence_after();
       const uint32_t tb = tmem_base + ((uint32_t)(qw * 32) << 16) + (uint32_t)(buf * L::kAccCols);
+      // 32 token columns at a time (the last chunk may read past the tile's columns: not stored); the
+      // kPerQ warps of a lane quarter take chunks half_c, half_c + kPerQ, ...
+      const int nch = (t.rows + 31) >> 5;
+      const int last = nch > half_c ? half_c + (nch - 1 - half_c) / R::kPerQ * R::kPerQ : -1;  // this warp's last
+      if (last < 0) {
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&tempty[buf]);
+      }
+#pragma unroll
+      for (int r = 0; r < kMine; ++r) {
+      const int cc = half_c + R::kPerQ * r;
+      if (cc >= nch) break;
+      const int c0 = cc * 32;
       uint32_t v[2][32];
-      tmem_ld32_async(tb, v[0]);
-      tmem_ld32_async(tb + kNT, v[1]);
+      tmem_ld32_async(tb + (uint32_t)c0, v[0]);
+      tmem_ld32_async(tb + (uint32_t)(NT + c0), v[1]);
       tmem_wait_ld();
-      // release the accumulator at once: everything below works on registers
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&tempty[buf]);
+      if (cc == last) {
+        // release the accumulator after this warp's last load: everything below works on registers
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&tempty[buf]);
+      }
       if (MODE == 0) {
         // SwiGLU: lanes 0-15 hold gate rows, lanes 16-31 the up rows of the same features; the gate
         // lanes finish token columns 0-15, the up lanes columns 16-31
@@ -600,7 +728,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           const int sh = mx_shared_exponent(m);
           if ((lane & 15) == i) my_shared = sh;
           const float inv = pow2_neg(sh);
-          const int col = col_half + i;
+          const int col = c0 + col_half + i;
           if (col < t.rows) {
             const __nv_fp8x2_storage_t c2 =
                 __nv_cvt_float2_to_fp8x2(make_float2(a[0][i] * inv, a[1][i] * inv), __NV_SATFINITE, __NV_E4M3);
@@ -611,7 +739,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         // lane j of each half writes the scale byte of token column (half + j); the quarter-0 warp
         // also clears the entry's 12 padding bytes
-        const int col = col_half + (lane & 15);
+        const int col = c0 + col_half + (lane & 15);
         if (col < t.rows) {
           uint8_t* e = act_sf + ((size_t)(t.row_base + col) * (n_feat / 128) + t.f) * 16;
           e[qw] = (uint8_t)(my_shared + 127);
@@ -629,13 +757,14 @@ __global__ void __launch_bounds__(kThreads, 1)
           const int feat = t.f * L::kFeatPerTile + half * kBM + qw * 32 + lane;
           float o[32];
 #pragma unroll
-          for (int i = 0; i < 32; ++i) o[i] = __uint_as_float(v[half][i]) * (scale ? wsc[i] : 1.0f);
+          for (int i = 0; i < 32; ++i) o[i] = __uint_as_float(v[half][i]) * (scale ? wsc[32 * r + i] : 1.0f);
           uint16_t* orow = out + (size_t)t.row_base * n_feat + feat;
-          store_pairs16_bf16(o, lane, orow, (size_t)n_feat, 0, t.rows, feat < n_feat);
-          store_pairs16_bf16(o + 16, lane, orow, (size_t)n_feat, 16, t.rows, feat < n_feat);
+          store_pairs16_bf16(o, lane, orow, (size_t)n_feat, c0, t.rows, feat < n_feat);
+          store_pairs16_bf16(o + 16, lane, orow, (size_t)n_feat, c0 + 16, t.rows, feat < n_feat);
         }
-        __syncwarp();  // the next tile rewrites this warp's routing weights
       }
+      }
+      if (MODE == 1) __syncwarp();  // the next tile rewrites this warp's routing weights
     }
   }
 
@@ -692,36 +821,63 @@ __global__ void __launch_bounds__(256) w4a8_prepack_kernel(const uint8_t* __rest
 // MXFP8 token rows for the W4A8 GEMMs: out_codes[pos] = x_codes[t] and the padded scale row
 // out_sf[pos] = (x_scales[t][4c .. 4c+3], 0 x 12) per 128-K chunk c, with t = sorted_pair[pos] / k
 // (sorted_pair NULL: t = pos, and no codes are written -- the scale rows of the token rows
-// themselves, for the shared expert).  One block per row; n_rows: optional device bound on the
-// rows (rows past it are left alone).
-__global__ void __launch_bounds__(128) gather_rows_mx_kernel(const uint8_t* __restrict__ x_codes,
+// themselves, for the shared expert).  A block moves kMxRows consecutive rows; each thread loads its
+// 16-byte piece of every one of them before storing any, so kMxRows independent loads are in flight.
+// n_rows: optional device bound on the rows (rows past it are left alone); a row whose pair index is
+// out of range is skipped and reported.
+constexpr int kMxRows = 8;
+
+__global__ void __launch_bounds__(256) gather_rows_mx_kernel(const uint8_t* __restrict__ x_codes,
                                                              const uint8_t* __restrict__ x_scales,
                                                              const int32_t* __restrict__ sorted_pair, int M, int k,
                                                              int T, int H, uint8_t* __restrict__ out_codes,
                                                              uint8_t* __restrict__ out_sf,
                                                              const int32_t* __restrict__ n_rows, unsigned* status) {
+  __shared__ int s_t[kMxRows];  // source token of each row of the block, -1: left alone
   pdl_wait();
   pdl_launch_dependents();
-  const int pos = blockIdx.x;
-  if (pos >= M) return;
-  if (n_rows && pos >= __ldg(n_rows)) return;
-  int t = pos;
-  if (sorted_pair) {
-    const int sp = __ldg(sorted_pair + pos);
-    if (sp < 0 || (long long)sp >= (long long)T * k) {
-      if (threadIdx.x == 0) set_status(status, DEV_ERR_BOUNDS);
-      return;
+  const int r0 = blockIdx.x * kMxRows;
+  if (threadIdx.x < kMxRows) {
+    const int pos = r0 + threadIdx.x;
+    int t = -1;
+    if (pos < M && (!n_rows || pos < __ldg(n_rows))) {
+      t = pos;
+      if (sorted_pair) {
+        const int sp = __ldg(sorted_pair + pos);
+        if (sp < 0 || (long long)sp >= (long long)T * k) {
+          set_status(status, DEV_ERR_BOUNDS);
+          t = -1;
+        } else {
+          t = sp / k;
+        }
+      }
     }
-    t = sp / k;
+    s_t[threadIdx.x] = t;
   }
+  __syncthreads();
+  int src[kMxRows];
+#pragma unroll
+  for (int u = 0; u < kMxRows; ++u) src[u] = s_t[u];
   if (out_codes) {
-    const uint4* src = reinterpret_cast<const uint4*>(x_codes + (size_t)t * H);
-    uint4* dst = reinterpret_cast<uint4*>(out_codes + (size_t)pos * H);
-    for (int c = threadIdx.x; c < H / 16; c += blockDim.x) dst[c] = __ldg(src + c);
+    const int H16 = H / 16;
+    for (int c = threadIdx.x; c < H16; c += blockDim.x) {
+      uint4 v[kMxRows];
+#pragma unroll
+      for (int u = 0; u < kMxRows; ++u)
+        if (src[u] >= 0) v[u] = __ldg(reinterpret_cast<const uint4*>(x_codes + (size_t)src[u] * H) + c);
+#pragma unroll
+      for (int u = 0; u < kMxRows; ++u)
+        if (src[u] >= 0) reinterpret_cast<uint4*>(out_codes + (size_t)(r0 + u) * H)[c] = v[u];
+    }
   }
-  const uint32_t* ssrc = reinterpret_cast<const uint32_t*>(x_scales + (size_t)t * (H / 32));
-  uint4* sdst = reinterpret_cast<uint4*>(out_sf + (size_t)pos * (H / kKC) * 16);
-  for (int c = threadIdx.x; c < H / kKC; c += blockDim.x) sdst[c] = make_uint4(__ldg(ssrc + c), 0u, 0u, 0u);
+  const int nc = H / kKC;  // padded scale entries per row
+  for (int i = threadIdx.x; i < kMxRows * nc; i += blockDim.x) {
+    const int u = i / nc, c = i - u * nc;
+    const int t = s_t[u];
+    if (t < 0) continue;
+    const uint32_t w = __ldg(reinterpret_cast<const uint32_t*>(x_scales + (size_t)t * (H / 32)) + c);
+    reinterpret_cast<uint4*>(out_sf + (size_t)(r0 + u) * nc * 16)[c] = make_uint4(w, 0u, 0u, 0u);
+  }
 }
 
 // ---------------------------------------------------------------- host side
@@ -743,6 +899,19 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn_w8() {
 // (the operand layout of the block-scaled MMA for 4-bit A), 128-byte swizzle.
 // The prepacked codes are seen as one matrix of (rows * K/128) rows of 128 codes (the chunk-major
 // blocks stacked): block (tile, chunk) starts at row (tile * K/128 + chunk) * 256.
+// E4M3 token rows [rows, K] in NT-row x 128-byte boxes, 128-byte swizzle (the wide instance's operand B).
+bool make_map_rows_e4m3(CUtensorMap* m, const void* base, int K, long long rows, int box_rows) {
+  auto fn = encode_fn_w8();
+  if (!fn) return false;
+  cuuint64_t dims[2] = {(cuuint64_t)K, (cuuint64_t)rows};
+  cuuint64_t strides[1] = {(cuuint64_t)K};
+  cuuint32_t box[2] = {(cuuint32_t)kKC, (cuuint32_t)box_rows};
+  cuuint32_t estr[2] = {1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 bool make_map_e2m1(CUtensorMap* m, const void* base, int K, long long rows) {
   auto fn = encode_fn_w8();
   if (!fn) return false;
@@ -755,24 +924,38 @@ bool make_map_e2m1(CUtensorMap* m, const void* base, int K, long long rows) {
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <int MODE, int STAGES, int TSLOTS>
+template <int MODE, int STAGES, int TSLOTS, int NT, int WIN>
 cudaError_t launch_w8(const W4a8GemmProblem& pr, W8Params gp, cudaStream_t stream, bool pdl) {
-  using L = W8Layout<MODE, STAGES, TSLOTS>;
+  using L = W8Layout<MODE, STAGES, TSLOTS, NT, WIN>;
   const bool has_shared = gp.has_shared != 0;
-  CUtensorMap ta, tas;
+  CUtensorMap ta, tas, tb, tbs;
   if (pr.M > 0 && !make_map_e2m1(&ta, pr.codes, pr.K, (long long)pr.E * pr.n_out)) return cudaErrorInvalidValue;
   if (has_shared && !make_map_e2m1(&tas, pr.s_codes, pr.K, pr.n_out_s)) return cudaErrorInvalidValue;
-  // with no routed rows the routed map is never read (and vice versa): alias them
-  if (pr.M <= 0) ta = tas;
-  else if (!has_shared) tas = ta;
-  auto kern = grouped_gemm_w4a8_kernel<MODE, STAGES, TSLOTS>;
+  if (NT > 32) {
+    if (pr.M > 0 && !make_map_rows_e4m3(&tb, pr.a_rows, pr.K, pr.M, NT)) return cudaErrorInvalidValue;
+    if (has_shared && !make_map_rows_e4m3(&tbs, pr.s_rows, pr.K, pr.T_s, NT)) return cudaErrorInvalidValue;
+  }
+  // with no routed rows the routed maps are never read (and vice versa): alias them
+  if (pr.M <= 0) {
+    ta = tas;
+    tb = tbs;
+  } else if (!has_shared) {
+    tas = ta;
+    tbs = tb;
+  }
+  if (NT == 32) {  // the token rows come by cp.async: the maps are not read
+    tb = ta;
+    tbs = ta;
+  }
+  auto kern = grouped_gemm_w4a8_kernel<MODE, STAGES, TSLOTS, NT, WIN>;
+  if (gp.E > L::kMaxE) return cudaErrorInvalidValue;
   const size_t smem = L::bytes(gp.E);
   cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (err != cudaSuccess) return err;
   int dev = 0, n_sms = 0;
   cudaGetDevice(&dev);
   cudaDeviceGetAttribute(&n_sms, cudaDevAttrMultiProcessorCount, dev);
-  return launch_kernel(kern, dim3(n_sms > 0 ? n_sms : 1), dim3(kThreads), smem, stream, pdl, ta, tas, gp);
+  return launch_kernel(kern, dim3(n_sms > 0 ? n_sms : 1), dim3(W8Roles<NT>::kThreads), smem, stream, pdl, ta, tas, tb, tbs, gp);
 }
 
 }  // namespace
@@ -811,7 +994,21 @@ cudaError_t launch_grouped_gemm_w4a8(const W4a8GemmProblem& pr, cudaStream_t str
   }
   gp.status = pr.status;
   gp.timeout_ns = kTimeoutNs;
-  return pr.mode == 0 ? launch_w8<0, 4, 3>(pr, gp, stream, pdl) : launch_w8<1, 4, 3>(pr, gp, stream, pdl);
+  // Decode-like problems (a few rows per expert) walk 32 token columns per tile behind a deep weight
+  // ring; prefill-like ones take 112 columns per tile, so each weight tile is read once per 112 rows.
+  if (w4a8_narrow(pr.M, pr.E, has_shared, pr.T_s))
+    return pr.mode == 0 ? launch_w8<0, 4, 3, 32, 4>(pr, gp, stream, pdl) : launch_w8<1, 4, 3, 32, 4>(pr, gp, stream, pdl);
+  // three token windows where the expert tables (and the down GEMM's routing weights) leave room for
+  // them, else two
+  if (pr.mode == 0)
+    return pr.E <= W8Layout<0, 4, 3, 112, 2>::kMaxE ? launch_w8<0, 4, 3, 112, 2>(pr, gp, stream, pdl)
+                                                    : launch_w8<0, 4, 2, 112, 2>(pr, gp, stream, pdl);
+  return pr.E <= W8Layout<1, 4, 3, 112, 2>::kMaxE ? launch_w8<1, 4, 3, 112, 2>(pr, gp, stream, pdl)
+                                                  : launch_w8<1, 4, 2, 112, 2>(pr, gp, stream, pdl);
+}
+
+bool w4a8_narrow(int M, int E, bool has_shared, int T_s) {
+  return (long long)M <= 32LL * E && (!has_shared || T_s <= 32);
 }
 
 cudaError_t launch_w4a8_prepack(const uint8_t* codes, const uint8_t* scales, int E, int n_out, int K, int gate_up,
@@ -827,8 +1024,9 @@ cudaError_t launch_gather_rows_mx(const uint8_t* x_codes, const uint8_t* x_scale
                                   int k, int T, int H, uint8_t* out_codes, uint8_t* out_sf, const int32_t* n_rows,
                                   unsigned* status, cudaStream_t stream, bool pdl) {
   if (M <= 0) return cudaSuccess;
-  return launch_kernel(gather_rows_mx_kernel, dim3(M), dim3(128), 0, stream, pdl, x_codes, x_scales, sorted_pair, M,
-                       k, T, H, out_codes, out_sf, n_rows, status);
+  const int threads = H / 16 >= 256 ? 256 : ((H / 16 + 31) / 32 * 32);
+  return launch_kernel(gather_rows_mx_kernel, dim3((unsigned)((M + kMxRows - 1) / kMxRows)), dim3(threads), 0, stream,
+                       pdl, x_codes, x_scales, sorted_pair, M, k, T, H, out_codes, out_sf, n_rows, status);
 }
 
 }  // namespace moe

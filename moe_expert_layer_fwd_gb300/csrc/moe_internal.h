@@ -149,6 +149,8 @@ struct W4a8GemmProblem {
   unsigned* status;
 };
 cudaError_t launch_grouped_gemm_w4a8(const W4a8GemmProblem& p, cudaStream_t stream, bool pdl = false);
+// True when the W4A8 GEMMs take the 32-column (decode) instance, else the 112-column one.
+bool w4a8_narrow(int M, int E, bool has_shared, int T_s);
 cudaError_t launch_w4a8_prepack(const uint8_t* codes, const uint8_t* scales, int E, int n_out, int K, int gate_up,
                                 uint8_t* codes_p, uint8_t* sf_p, cudaStream_t stream);
 // sorted_pair NULL: identity rows and no codes written (the padded scale rows of x itself).

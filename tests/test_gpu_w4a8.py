@@ -117,6 +117,15 @@ GEMM_CASES = [
     ([1] * 12 + [0] * 4, 512, 256),
     ([40, 2, 0, 9], 1024, 384),          # I = 384: a window of 3 chunks in the down GEMM
     ([2, 0, 65, 7], 768, 640),           # H = 768: 6 chunks (a full and a partial window); I = 640: 5
+    # more than 32 rows per expert on average: the 112-column instance (tiles of 112 token rows, MMA N
+    # the tile's rows rounded up to 16), ragged tails of 1, 52 and 76 rows, exact multiples of 112
+    ([300, 0, 1, 111, 112, 113, 224, 500], 256, 128),
+    ([200, 150, 0, 90], 768, 640),       # 6 and 5 chunks: full and partial 2-chunk windows
+    ([120] * 6 + [0] * 2, 512, 256),
+    # 400 experts: three token windows for the gate/up GEMM, two for the down GEMM (its routing weights
+    # take the room); 620: two for both
+    ([34] * 400, 256, 128),
+    ([34] * 620, 256, 128),
 ]
 
 
@@ -228,6 +237,9 @@ LAYER_CASES = [
     # gating and routing in one kernel up to T*k = 4096, four kernels above
     mi.CONFIGS["qwen3_decode"].with_(T=512, H=256, I=128),
     mi.CONFIGS["qwen3_decode"].with_(T=513, H=256, I=128),
+    # prefill-like: the 112-column instance, with and without the shared expert
+    mi.CONFIGS["hy3_prefill"].with_(T=300, H=256, E=16, k=4, I=128, I_s=256, zipf_beta=0.3, n_dead=2),
+    mi.CONFIGS["long_prefill"].with_(T=1000, H=512, E=16, k=4, I=256, zipf_beta=0.5, n_dead=3),
 ]
 
 
@@ -237,10 +249,11 @@ def test_w4a8_layer_parity(moe, cfg):
     assert_close(got, ref["y"], f"W4A8 layer {cfg.name}")
 
 
-@pytest.mark.parametrize("name", ["qwen3_decode", "hy3_decode"])
+@pytest.mark.parametrize("name", ["qwen3_decode", "hy3_decode", "hy3_prefill", "long_prefill"])
 def test_w4a8_layer_full_size_sampled_tokens(moe, name):
-    """The full decode sizes, launched as the bench launches them: routing of every token bit-exact, y of
-    four tokens (first, last and two between) against the oracle, which quantises each needed expert."""
+    """The full sizes (decode: the 32-column GEMMs; prefill: the 112-column ones), launched as the bench
+    launches them: routing of every token bit-exact, y of four tokens (first, last and two between)
+    against the oracle, which quantises each needed expert."""
     cfg = mi.CONFIGS[name]
     tokens = np.array([0, cfg.T // 3, 2 * cfg.T // 3, cfg.T - 1])
     got, ref = _run_layer(moe, cfg, mi.generate(cfg), tokens)
@@ -248,8 +261,8 @@ def test_w4a8_layer_full_size_sampled_tokens(moe, name):
 
 
 def test_w4a8_layer_all_tokens_on_one_expert(moe):
-    """One expert takes every token (300 rows: ten 32-row token tiles of one expert), the rest share the
-    other slot."""
+    """One expert takes every token (300 rows: three 112-row token tiles of one expert, the last one
+    ragged), the rest share the other slot."""
     cfg = mi.CONFIGS["tiny"].with_(T=300, E=8, k=2)
     inp = mi.generate(cfg)
     inp.logits[:, 5] = 50.0  # every token picks expert 5 first
