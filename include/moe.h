@@ -438,8 +438,9 @@ MOE_API int moe_grouped_gemm_mxfp4(const uint16_t* a16, const uint8_t* w_codes, 
  * moe_grouped_gemm_w4a8: out [M,N] bf16 = topk_w[sorted_pair[pos]] (optional) *
  *   (a[pos] . w[e]^T), a [M,K] E4M3 with a_sf [M,K/128,16], w prepacked with gate_up = 0;
  *   N % 256 == 0, K % 128 == 0.
- * Both walk 32 token columns per tile (a decode-shaped instance; correct for any M).  ws: at least
- * moe_grouped_gemm_workspace_size() bytes.
+ * Both walk 32 token columns per tile when M <= 32*E (decode: a few rows per expert), else 112 (prefill:
+ * each weight tile read once per 112 rows); the same results either way, within the stated rounding.
+ * ws: at least moe_grouped_gemm_workspace_size() bytes.
  *
  * moe_layer_forward_w4a8: the whole layer a1 -> a6 on MXFP8 x (x_codes [T,H], x_scales [T,H/32],
  *   e.g. from moe_add_rms_norm_mxfp8): gating, routing, the MXFP8 row gather, the W4A8 gate/up GEMM
