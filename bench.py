@@ -838,15 +838,7 @@ def run_gb300(args, rank, world, local):
         t.update(x=d16(inp.x), logits=torch.from_numpy(inp.logits).cuda(),
                  bias=torch.from_numpy(inp.bias).cuda() if inp.bias is not None else None)
         if args.profile_w4a8:
-            w13_raw = d16(mi.normal_bf16(cfg.seed, mi.TID_W13, (cfg.E, 2 * cfg.I, cfg.H), 0.0, cfg.w_std))
-            w13 = moe.moe_w4a8_prepack(*moe.moe_mxfp4_quantize(w13_raw), gate_up=True)
-            del w13_raw
-            w2 = moe.moe_w4a8_prepack(*moe.moe_mxfp4_quantize(t["w2"]), gate_up=False)
-            w13_s = w2_s = None
-            if cfg.n_shared:
-                sh = mi.generate(cfg.with_(E=1, T=1))
-                w13_s = moe.moe_w4a8_prepack(*moe.moe_mxfp4_quantize(d16(sh.w13_s)), gate_up=True)
-                w2_s = moe.moe_w4a8_prepack(*moe.moe_mxfp4_quantize(d16(sh.w2_s)), gate_up=False)
+            w13, w2, w13_s, w2_s = W4A8_WEIGHTS.get(cfg, moe, mi, d16, t)
             ones = torch.ones(cfg.H, dtype=torch.bfloat16, device="cuda")
             xc, xs, _, _ = moe.moe_add_rms_norm_mxfp8(t["x"], None, ones, 1e-6, with_fp32=False)
             l8 = moe.W4a8Layer(cfg.T, cfg.H, cfg.E, cfg.k, cfg.I, cfg.gate, cfg.routed_scaling_factor, cfg.eps,
