@@ -37,6 +37,10 @@ __global__ void __launch_bounds__(512) finalize_kernel(const uint4* __restrict__
   const int32_t* pp = pair_pos + (size_t)t * k;
   for (int c = threadIdx.x; c < H8; c += blockDim.x) {
     float a[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+    const size_t o_idx = (size_t)t * H8 + c;
+    // the shared expert's word is loaded with the routed rows (it is still added last)
+    uint4 sv = make_uint4(0u, 0u, 0u, 0u);
+    if (shared) sv = __ldg(shared + o_idx);
     for (int j0 = 0; j0 < k; j0 += kSlotBatch) {
       const uint4* row[kSlotBatch];
 #pragma unroll
@@ -52,8 +56,7 @@ __global__ void __launch_bounds__(512) finalize_kernel(const uint4* __restrict__
       for (int j = 0; j < kSlotBatch; ++j)
         if (row[j]) acc8(a, v[j]);
     }
-    const size_t o_idx = (size_t)t * H8 + c;
-    if (shared) acc8(a, __ldg(shared + o_idx));
+    if (shared) acc8(a, sv);
     uint4 o;
     o.x = pack_bf16x2(a[0], a[1]);
     o.y = pack_bf16x2(a[2], a[3]);

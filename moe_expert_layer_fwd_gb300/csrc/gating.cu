@@ -60,12 +60,22 @@ __device__ __forceinline__ float warp_sum(float v) {
   return v;
 }
 
-// Top-k of token t by one warp.  VPL = keys held per lane (E <= 32 * VPL); a compile-time bound
-// keeps them in registers.  Lane j < k writes the j-th choice; returns it (-1 on lanes >= k).
+// This lane's logits of token t (experts lane + 32 i), 0 past E.
 template <int VPL>
-__device__ __forceinline__ int gate_token(const float* __restrict__ logits, const float* __restrict__ bias, int t,
-                                          int E, int k, int gate, float rsf, float eps, float* __restrict__ topk_w,
-                                          int32_t* __restrict__ topk_idx, int lane) {
+__device__ __forceinline__ void load_logits(const float* __restrict__ logits, int t, int E, int lane, float (&raw)[VPL]) {
+  const float* row = logits + (size_t)t * E;
+#pragma unroll
+  for (int i = 0; i < VPL; ++i) raw[i] = lane + 32 * i < E ? __ldg(row + lane + 32 * i) : 0.0f;
+}
+
+// Top-k of token t by one warp from its logits already in registers (raw, as load_logits gives them).
+// VPL = keys held per lane (E <= 32 * VPL); a compile-time bound keeps them in registers.  Lane j < k
+// writes the j-th choice; returns it (-1 on lanes >= k).
+template <int VPL>
+__device__ __forceinline__ int gate_token_from(const float (&raw)[VPL], const float* __restrict__ logits,
+                                               const float* __restrict__ bias, int t, int E, int k, int gate,
+                                               float rsf, float eps, float* __restrict__ topk_w,
+                                               int32_t* __restrict__ topk_idx, int lane) {
   const float* row = logits + (size_t)t * E;
   uint32_t keys[VPL];
 #pragma unroll
@@ -73,7 +83,7 @@ __device__ __forceinline__ int gate_token(const float* __restrict__ logits, cons
     keys[i] = 0u;  // below every real key: never chosen
     const int e = lane + 32 * i;
     if (e < E) {
-      const float l = __ldg(row + e);
+      const float l = raw[i];
       float key = l;
       if (gate == MOE_GATE_SIGMOID) {
         key = sigmoid_fixed_f32(l);
@@ -120,6 +130,19 @@ __device__ __forceinline__ int gate_token(const float* __restrict__ logits, cons
 }
 
 template <int VPL>
+__device__ __forceinline__ int gate_token(const float* __restrict__ logits, const float* __restrict__ bias, int t,
+                                          int E, int k, int gate, float rsf, float eps, float* __restrict__ topk_w,
+                                          int32_t* __restrict__ topk_idx, int lane) {
+  float raw[VPL];
+  load_logits<VPL>(logits, t, E, lane, raw);
+  return gate_token_from<VPL>(raw, logits, bias, t, E, k, gate, rsf, eps, topk_w, topk_idx, lane);
+}
+
+// kTPW tokens per warp: all their logits are loaded before the first is gated, so a large batch
+// takes one wave of warps with one load latency instead of two.
+constexpr int kTPW = 2;
+
+template <int VPL>
 __global__ void __launch_bounds__(256) gating_topk_kernel(const float* __restrict__ logits,
                                                           const float* __restrict__ bias, int T, int E, int k,
                                                           int gate, float rsf, float eps,
@@ -128,9 +151,15 @@ __global__ void __launch_bounds__(256) gating_topk_kernel(const float* __restric
   pdl_wait();
   pdl_launch_dependents();
   const int lane = threadIdx.x & 31;
-  const int t = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
-  if (t >= T) return;
-  gate_token<VPL>(logits, bias, t, E, k, gate, rsf, eps, topk_w, topk_idx, lane);
+  const int t0 = (blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5)) * kTPW;
+  if (t0 >= T) return;
+  float raw[kTPW][VPL];
+#pragma unroll
+  for (int u = 0; u < kTPW; ++u)
+    if (t0 + u < T) load_logits<VPL>(logits, t0 + u, E, lane, raw[u]);
+#pragma unroll
+  for (int u = 0; u < kTPW; ++u)
+    if (t0 + u < T) gate_token_from<VPL>(raw[u], logits, bias, t0 + u, E, k, gate, rsf, eps, topk_w, topk_idx, lane);
 }
 
 // Gating and init-routing of a small batch (P = T*k <= kSmallPairs) in one CTA of 32 warps: the
@@ -231,7 +260,7 @@ cudaError_t launch_gating_topk(const float* logits, const float* bias, int T, in
                                float eps, float* topk_w, int32_t* topk_idx, cudaStream_t stream, bool pdl) {
   if (T == 0) return cudaSuccess;
   const int warps = 8;
-  dim3 grid((T + warps - 1) / warps);
+  dim3 grid((T + warps * kTPW - 1) / (warps * kTPW));
   const int vpl = (E + 31) / 32;
 #define MOE_GATING_LAUNCH(V)                                                                                 \
   launch_kernel(gating_topk_kernel<V>, grid, dim3(warps * 32), 0, stream, pdl, logits, bias, T, E, k, gate, rsf, \

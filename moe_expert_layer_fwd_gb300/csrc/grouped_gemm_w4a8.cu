@@ -25,14 +25,14 @@
 // Product (swap-AB, as the bf16 decode instances): weight rows are the MMA's operand A, two M = 128
 // halves of a 256-row tile into two accumulators, read from shared memory in the padded E2M1 layout
 // that TMA writes for CU_TENSOR_MAP_DATA_TYPE_16U4_ALIGN16B (each 16 codes = 8 bytes followed by 8
-// zero bytes, so a 128-code row is a 128-byte swizzled row); the expert's token rows are the N = 32
-// operand B (E4M3, 128-byte swizzled rows).  One 128-K chunk = 4 MMAs of K = 32 per half, each
+// zero bytes, so a 128-code row is a 128-byte swizzled row); the expert's token rows are the operand B
+// (E4M3, 128-byte swizzled rows; N = 32 in the decode instance, below).  One 128-K chunk = 4 MMAs of K = 32 per half, each
 // naming its block with the scale-factor ids of the instruction descriptor; the scale factors are
 // copied into a per-stage tensor-memory slot by the MMA thread (tcgen05.cp, which the MMAs issued
 // after it by the same thread are ordered behind).
 //
-// Loads.  Each SM's TMA engine works through its copies one after another (about 0.33 us per 16 KB),
-// so it carries only the weights: one 16-KB copy per 128-K chunk of the tile's 256 weight rows (A ring,
+// Loads (decode instance).  Each SM's TMA engine works through its copies one after another (about
+// 0.33 us per 16 KB), so it carries only the weights: one 16-KB copy per 128-K chunk of the tile's 256 weight rows (A ring,
 // 32 KB in shared memory in the padded layout; the prepacked codes of a (tile, chunk) are one contiguous
 // block) and one bulk copy of the weight scale atoms per 512-K window (4 chunks).  The window's 32 token
 // rows and their scale rows, read from L2 again by every feature tile of an expert, are copied by two
@@ -46,8 +46,8 @@
 // writes the E4M3 codes and the E8M0 scale byte of that block for the down GEMM.
 // Mode 1 (down + routing weight): 256 output features per tile, bf16 times topk_w[sorted_pair[pos]].
 //
-// Warp roles (288 threads, one persistent CTA per SM, static round-robin tiles; an expert's token
-// tiles that reuse a weight tile run next to each other): warp 0 TMA producer, warp 1 TMEM allocator +
+// Warp roles of the decode instance (288 threads, one persistent CTA per SM, static round-robin tiles;
+// an expert's token tiles that reuse a weight tile run next to each other): warp 0 TMA producer, warp 1 TMEM allocator +
 // MMA issuer of weight half 0, warps 2-5 epilogue (one per TMEM lane quarter), warp 6 MMA issuer of
 // half 1, warps 7-8 token loaders.
 //
@@ -78,7 +78,7 @@ constexpr int kTR = 256;                  // weight rows per tile and per A copy
 constexpr int kKC = 128;                  // K per chunk: 4 MMAs of K = 32 per half
 constexpr int kABox = kTR * 128;          // shared-memory bytes of one A copy (padded codes): 32 KB
 constexpr int kATx = kTR * kKC / 2;       // bytes the A copy moves (and counts on the barrier): 16 KB
-constexpr int kSF = 512;                  // one scale-factor atom (128 rows) / 32 token scale rows
+constexpr int kSF = 512;                  // one scale-factor block: 128 rows' atom, or 32 padded token scale rows
 // Warp roles of an instance with NT token columns per tile: warp 0 producer, warp 1 MMA issuer of weight
 // half 0, kEPI epilogue warps, the MMA issuer of half 1, kLW loader warps.  The decode instance has one
 // epilogue warp per TMEM lane quarter and two loader warps (token rows and scales by cp.async); the wide
@@ -533,11 +533,12 @@ __global__ void __launch_bounds__(W8Roles<NT>::kThreads, 1)
     }
     __syncwarp();
   } else if (warp >= kLD0) {
-    // ------------------------------------------------------------ token loaders (cp.async)
-    // The window's 32 token rows x 4 chunks (128 bytes each, written in the 128-byte swizzle the MMA's
-    // operand descriptor expects: 16-byte unit j of row r at j ^ (r % 8)) and their padded scale rows;
-    // rows and chunks past the end are zero-filled.  Each thread waits for its own copies and fences
-    // them to the async proxy before arriving, one window behind the copies it issues.
+    // ------------------------------------------------------------ token loaders
+    // Decode instance (cp.async): the window's 32 token rows x 4 chunks (128 bytes each, written in the
+    // 128-byte swizzle the MMA's operand descriptor expects: 16-byte unit j of row r at j ^ (r % 8)) and
+    // their padded scale rows; rows and chunks past the end are zero-filled.  Each thread waits for its
+    // own copies and fences them to the async proxy before arriving, one window behind the copies it
+    // issues.
     const int lt = (warp - kLD0) * 32 + lane;
     pdl_wait();  // the token rows come from the previous kernel
     if constexpr (NT > 32) {

@@ -80,19 +80,30 @@ __global__ void __launch_bounds__(1024) route_scan_kernel(const int32_t* __restr
   const bool active = seg < S;
   const int cps = (n_chunks + S - 1) / S;
   const int c0 = min(n_chunks, seg * cps), c1 = min(n_chunks, c0 + cps);
-  // chunk histograms are read 8 at a time so that their loads overlap
-  constexpr int kU = 8;
+  // A thread's chunk histograms are all loaded at once and kept in registers for the second pass when
+  // there are at most kReg of them (one load latency instead of four); otherwise they are read kU at a
+  // time, twice.
+  constexpr int kReg = 32, kU = 16;
+  const bool in_regs = c1 - c0 <= kReg;
+  int hv[kReg];
   if (active) {
     int s = 0;
-    int c = c0;
-    for (; c + kU <= c1; c += kU) {
-      int v[kU];
+    if (in_regs) {
 #pragma unroll
-      for (int u = 0; u < kU; ++u) v[u] = __ldg(hist + (size_t)(c + u) * E + e);
+      for (int u = 0; u < kReg; ++u) hv[u] = c0 + u < c1 ? __ldg(hist + (size_t)(c0 + u) * E + e) : 0;
 #pragma unroll
-      for (int u = 0; u < kU; ++u) s += v[u];
+      for (int u = 0; u < kReg; ++u) s += hv[u];
+    } else {
+      int c = c0;
+      for (; c + kU <= c1; c += kU) {
+        int v[kU];
+#pragma unroll
+        for (int u = 0; u < kU; ++u) v[u] = __ldg(hist + (size_t)(c + u) * E + e);
+#pragma unroll
+        for (int u = 0; u < kU; ++u) s += v[u];
+      }
+      for (; c < c1; ++c) s += __ldg(hist + (size_t)c * E + e);
     }
-    for (; c < c1; ++c) s += __ldg(hist + (size_t)c * E + e);
     part[seg * E + e] = s;
   }
   __syncthreads();
@@ -127,7 +138,16 @@ __global__ void __launch_bounds__(1024) route_scan_kernel(const int32_t* __restr
     if (tid == E - 1) offsets[E] = incl;
   }
   __syncthreads();
-  if (active) {
+  if (active && in_regs) {
+    int run = excl_s[e];
+    for (int g = 0; g < seg; ++g) run += part[g * E + e];
+#pragma unroll
+    for (int u = 0; u < kReg; ++u)
+      if (c0 + u < c1) {
+        base[(size_t)(c0 + u) * E + e] = run;
+        run += hv[u];
+      }
+  } else if (active) {
     int run = excl_s[e];
     for (int g = 0; g < seg; ++g) run += part[g * E + e];
     int c = c0;
