@@ -104,3 +104,41 @@ def test_guards_around_every_output(moe):
     assert y4.intact()
     ref4 = oracle.moe_layer_forward_tokens_mxfp4(np.arange(T), inp.x, inp.logits, k, cfg.gate, inp.w13, inp.w2)
     assert_close(host_bf16_f64(y4.t), ref4["y"], "y (4-bit path)")
+
+
+@pytest.mark.parametrize("T,E,k", [(24, 16, 8), (300, 8, 2)], ids=["32-column", "112-column"])
+def test_guards_around_w4a8_outputs(moe, T, E, k):
+    """The W4A8 outputs (MXFP8 row gather, gate/up codes and scales, down rows) inside guard regions,
+    on the decode (32-column) and prefill (112-column) GEMM instances: guards unchanged, and each
+    output bit-equal to the same call into a plain buffer."""
+    import torch
+    from oracle.mx import mx_quantize_e4m3
+    cfg = mi.CONFIGS["qwen3_decode"].with_(T=T, H=512, E=E, k=k, I=256)
+    H, I, P = cfg.H, cfg.I, T * k
+    inp = mi.generate(cfg)
+    _, idx = oracle.gating_topk(inp.logits, k, cfg.gate)
+    counts, off, sp, _ = oracle.init_routing(idx, E)
+    assert (P > 32 * E) == (T == 300)  # which instance the GEMMs take
+    xc, xs = mx_quantize_e4m3(oracle.bf16_to_f64(inp.x))
+    q = lambda w, gu: moe.moe_w4a8_prepack(*moe.moe_mxfp4_quantize(dev_bf16(w)), gate_up=gu)
+    w13, w2 = q(inp.w13, True), q(inp.w2, False)
+    d_off, d_sp = dev(off), dev(sp)
+    topk_w = torch.rand(P, dtype=torch.float32, device="cuda") + 0.1
+
+    gc, gs = Guarded((P, H), torch.uint8, 0x5A), Guarded((P, H // 128, 16), torch.uint8, 0x5A)
+    moe.moe_gather_rows_mx(dev(xc), dev(xs), d_sp, k, out_codes=gc.t, out_sf=gs.t)
+    assert gc.intact() and gs.intact()
+    pc, ps = moe.moe_gather_rows_mx(dev(xc), dev(xs), d_sp, k)
+    assert torch.equal(gc.t, pc) and torch.equal(gs.t, ps)
+
+    ac, asf = Guarded((P, I), torch.uint8, 0x5A), Guarded((P, I // 128, 16), torch.uint8, 0x5A)
+    moe.moe_grouped_gemm_swiglu_w4a8(gc.t, gs.t, w13, d_off, act=ac.t, act_sf=asf.t)
+    assert ac.intact() and asf.intact()
+    pa, pas = moe.moe_grouped_gemm_swiglu_w4a8(pc, ps, w13, d_off)
+    assert torch.equal(ac.t, pa) and torch.equal(asf.t, pas)
+
+    yp = Guarded((P, H), torch.bfloat16, 7.0)
+    moe.moe_grouped_gemm_w4a8(ac.t, asf.t, w2, d_off, topk_w, d_sp, out=yp.t)
+    assert yp.intact()
+    py = moe.moe_grouped_gemm_w4a8(pa, pas, w2, d_off, topk_w, d_sp)
+    assert torch.equal(yp.t.view(torch.int16), py.view(torch.int16))
