@@ -107,3 +107,19 @@ def test_oracle_inputs_generate_exactly_the_needed_experts():
     b = oracle.moe_layer_forward_tokens(toks, lazy.x, lazy.logits, *args, lazy.w13, lazy.w2, lazy.bias,
                                         w13_s=lazy.w13_s, w2_s=lazy.w2_s, **kw)
     assert (a["y"] == b["y"]).all()
+
+
+def test_w4a8_leg_shapes_and_bound():
+    """Every workload fits the W4A8 layer's shape limits; its gate/up GEMM is HBM-bound at decode
+    sizes and tensor-bound (against the fp8-rate peak) at prefill sizes, by arithmetic intensity."""
+    assert all(bench._w4a8_fits(c) for c in mi.CONFIGS.values())
+    assert not bench._w4a8_fits(mi.CONFIGS["tiny"].with_(H=192))
+    assert not bench._w4a8_fits(mi.CONFIGS["hy3_decode"].with_(I_s=192))
+    peaks = {"hbm_gbs": 6788.6, "bf16_tflops": 1855.6}
+    ridge = peaks["bf16_tflops"] * bench.FP8_OVER_BF16 * 1e12 / (peaks["hbm_gbs"] * 1e9)
+    per_w = 0.5 + 1.0 / 32
+    for name, tensor in [("qwen3_decode", False), ("hy3_decode", False), ("hy3_prefill", True), ("long_prefill", True)]:
+        c = mi.CONFIGS[name]
+        f1 = 2.0 * c.T * c.k * c.H * 2 * c.I + (2.0 * c.T * c.H * 2 * c.I_s if c.n_shared else 0.0)
+        b1 = (c.E + (1 if c.n_shared else 0)) * 2 * c.I * c.H * per_w  # every expert active: the lowest intensity
+        assert (f1 / b1 >= ridge) == tensor, name
