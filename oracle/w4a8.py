@@ -22,7 +22,7 @@ Readings (the pages name the formats and the ops, not their arithmetic):
   round-half-to-even saturating at 448); the down projection sees the quantised act.  The
   quantisation of act is an integer decision the GPU takes on its fp32 act: where the fp32 and the
   float64 values fall on two sides of a rounding boundary the two act codes differ by one E4M3 step
-  -- a difference far inside the layer tolerance, which is how the GPU path is judged.
+  -- a difference far inside the layer tolerance, against which the GPU path is checked.
 * The routing weight multiplies the down projection's result (the bf16 layer's order); the shared
   expert is the same quantised FFN with its own MXFP4 weights, weight 1.
 """
