@@ -11,7 +11,9 @@ through the C ABI.
   then one E4M3 step apart;
 * the whole W4A8 layer (moe_layer_forward_w4a8) against oracle.moe_layer_forward_w4a8: routing
   bit-exact, y within max-rel 2e-2 and mean-rel 5e-3, with and without a shared expert, several
-  token tiles in one expert, I_s != I, and at the full decode sizes on sampled tokens.
+  token tiles in one expert, I_s != I, and at the full decode and prefill sizes on sampled tokens.
+Both GEMM instances are covered: 32 token columns per tile (at most 32 rows per expert on average)
+and 112 (more), including ragged tails, 400 and 620 experts.
 """
 import numpy as np
 import pytest
