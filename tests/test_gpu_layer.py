@@ -63,6 +63,8 @@ SMALL = [
     mi.CONFIGS["hy3_decode"].with_(T=24, H=256, E=32, k=8, I=128, I_s=128, gate="sigmoid_inner_bias", bias_std=0.5),
     # the documented limits: E = 1024 experts, k = 32
     mi.CONFIGS["tiny"].with_(T=64, H=256, E=1024, k=32, I=128),
+    # a few rows per routed expert, but a shared expert over 40 tokens: the CTA-pair instances
+    mi.CONFIGS["hy3_decode"].with_(T=40, H=256, E=64, k=4, I=128, I_s=128),
     # gating and routing in one kernel up to T*k = 4096 (decode instances), four kernels above
     mi.CONFIGS["qwen3_decode"].with_(T=512, H=256, I=128),
     mi.CONFIGS["qwen3_decode"].with_(T=513, H=256, I=128),

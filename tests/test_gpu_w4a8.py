@@ -239,6 +239,8 @@ LAYER_CASES = [
     # gating and routing in one kernel up to T*k = 4096, four kernels above
     mi.CONFIGS["qwen3_decode"].with_(T=512, H=256, I=128),
     mi.CONFIGS["qwen3_decode"].with_(T=513, H=256, I=128),
+    # a few rows per routed expert, but a shared expert over 40 tokens: the 112-column instance
+    mi.CONFIGS["hy3_decode"].with_(T=40, H=256, E=64, k=4, I=128, I_s=128),
     # prefill-like: the 112-column instance, with and without the shared expert
     mi.CONFIGS["hy3_prefill"].with_(T=300, H=256, E=16, k=4, I=128, I_s=256, zipf_beta=0.3, n_dead=2),
     mi.CONFIGS["long_prefill"].with_(T=1000, H=512, E=16, k=4, I=256, zipf_beta=0.5, n_dead=3),
