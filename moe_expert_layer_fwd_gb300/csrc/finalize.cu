@@ -72,9 +72,11 @@ cudaError_t launch_finalize(const uint16_t* y_perm, const int32_t* pair_pos, con
                             int H, uint16_t* y, cudaStream_t stream, bool pdl) {
   if (T == 0 || H == 0) return cudaSuccess;
   const int H8 = H / 8;
-  // 128 threads per token, each taking every 128th column word (0.099 -> 0.095 ms at long_prefill
-  // against one word per thread in blocks of up to 512)
-  const int threads = H8 >= 128 ? 128 : (H8 + 31) / 32 * 32;
+  // Large batches: 128 threads per token, each taking every 128th column word (long_prefill 0.099 ->
+  // 0.095 ms against one word per thread in blocks of up to 512).  Small batches keep the wide blocks:
+  // with a few dozen tokens, 128-thread blocks leave most of the GPU idle (qwen3_decode 0.007 -> 0.011 ms).
+  const int cap = T >= 1024 ? 128 : 512;
+  const int threads = H8 >= cap ? cap : (H8 + 31) / 32 * 32;
   return launch_kernel(finalize_kernel, dim3((unsigned)T), dim3(threads), 0, stream, pdl,
                        reinterpret_cast<const uint4*>(y_perm), pair_pos, reinterpret_cast<const uint4*>(shared), T, k,
                        H8, reinterpret_cast<uint4*>(y));
