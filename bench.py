@@ -576,7 +576,7 @@ def _w4a8_fits(cfg):
 
 def _decode_sized(cfg):
     """Decode-shaped problems (at most 32 token rows per expert on average, no more than 32 tokens for a
-    shared expert), the shapes the 4-bit layers' 32-column tiles are built for."""
+    shared expert), the shapes the f16-operand 4-bit layer's 32-column tiles are built for."""
     return cfg.T * cfg.k <= 32 * cfg.E and cfg.T <= 64 and cfg.E >= 16
 
 
